@@ -1,0 +1,430 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged-KV decode step (append + GQA decode) on GB300.
+
+Default workload: the Qwen2.5-7B-shaped batch (128 sequences, 28 q / 4 kv
+heads, head_dim 128, fp16, lognormal context lengths with median 1024 clipped
+to [1, 8192]; seeded synthetic data).  A step is the whole hot path for one
+batch: pa_cache_append of the new token, then pa_decode (split-K attention
+and the log-sum-exp merge).  L2 is flushed (a 2x-L2 buffer is rewritten)
+before every timed step, outside the timed region.
+
+Prints one JSON line.  ``value`` is attended KV tokens/s of the whole job
+(sum of context lengths over all ranks / max-over-ranks step time); the line
+also carries the decode call's HBM roofline, an end-to-end figure through
+pinned host buffers, the fp64 CPU oracle's throughput as a reported baseline,
+the number of this library's kernel launches and the SM clocks seen.
+
+``--impl reference`` times the oracle (the only reference that exists for
+this path) on the host cores instead, on a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "paged GQA decode: attended KV tokens/s and HBM GB/s (% of GB300 peak)"
+UNIT = "tokens/s"
+DEFAULT_CONFIG = "qwen2_5_7b"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(w, lens: np.ndarray) -> dict:
+    """Bytes one decode call must move: K+V of every attended token, q, out,
+    the block-table entries and context lengths read (plus page scales for an
+    E4M3 pool).  Workspace traffic and the padding rows of each sequence's
+    last block are overhead, not counted."""
+    e_kv = 1 if w.kv == "fp8" else 2
+    L = lens.astype(np.int64)
+    nblk = (L + w.block_size - 1) // w.block_size
+    kv = int(L.sum()) * w.Hkv * 2 * w.D * e_kv
+    qo = 2 * w.B * w.Hq * w.D * 2
+    meta = int(nblk.sum()) * 4 + w.B * 4
+    scales = int(nblk.sum()) * w.Hkv * 2 * 4 if w.kv == "fp8" else 0
+    return {"kv": kv, "q_out": qo, "meta": meta, "scales": scales,
+            "total": kv + qo + meta + scales}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 20):
+        self.index = index
+        self.period_ms = period_ms
+        self.proc = None
+        self.file = None
+        self.marks = {}
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period_ms}"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, name):
+        self.marks[name] = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = []
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+            except (ValueError, IndexError):
+                continue
+        os.unlink(self.file.name)
+        t0, t1 = self.marks.get("timed_start", 0), self.marks.get("timed_end", 1e30)
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        window = "timed"
+        if len(inside) < 3:
+            t0w = self.marks.get("warmup_start", t0)
+            inside = [r for r in rows if t0w - 0.05 <= r[0] <= t1 + 0.05]
+            window = "warmup+timed"
+        if not inside:
+            inside, window = rows, "whole run"
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median([r[1] for r in inside]) if inside else None,
+                "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+def oracle_baseline(w, budget_s: float = 10.0) -> dict:
+    """fp64 CPU oracle (as it stands) on a bounded sample of the batch's sequences."""
+    import oracle
+    from paged_kv_cache_179_gb300 import workloads as W
+    lens = w.context_lens.cpu().numpy()
+    tables = w.block_tables.cpu().numpy()
+    q = W.to_numpy16(w.q)
+    if w.kv == "fp8":
+        raise NotImplementedError
+    kp, vp = W.to_numpy16(w.k_cache), W.to_numpy16(w.v_cache)
+    bf16 = w.dtype == "bf16"
+    order = np.random.default_rng(0).permutation(w.B)
+    # calibrate on 4 sequences, then size the sample to ~budget_s
+    probe = order[:4]
+    t = time.perf_counter()
+    oracle.decode(q, kp, vp, tables, lens, w.scale, bf16=bf16, rows=probe)
+    dt = max(time.perf_counter() - t, 1e-3)
+    per_tok = dt / max(1, int(lens[probe].sum()))
+    n, tok = 0, 0
+    for b in order:
+        if (tok + lens[b]) * per_tok > budget_s and n >= 4:
+            break
+        n += 1
+        tok += int(lens[b])
+    rows = order[:n]
+    t = time.perf_counter()
+    oracle.decode(q, kp, vp, tables, lens, w.scale, bf16=bf16, rows=rows)
+    dt = time.perf_counter() - t
+    return {"value": int(lens[rows].sum()) / dt, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} of {w.B} sequences ({int(lens[rows].sum())} attended tokens, "
+                      f"all {w.Hq} q heads), fp64 two-pass softmax, {dt:.2f} s"}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, dev):
+    from paged_kv_cache_179_gb300 import _abi
+    from paged_kv_cache_179_gb300 import workloads as W
+    from paged_kv_cache_179_gb300.step import DecodeStep
+
+    _abi.load()
+    w = W.make_workload(args.config, seed=args.seed + rank, device=dev)
+    lens = w.context_lens.cpu().numpy()
+    tokens = int(lens.sum())
+    if w.kv == "fp8":
+        kc = torch.empty(w.k_cache.shape, dtype=torch.uint8, device=dev)
+        vc = torch.empty_like(kc)
+        ks = torch.empty(w.num_blocks, w.Hkv, dtype=torch.float32, device=dev)
+        vs = torch.empty_like(ks)
+        _abi.pa_quantize_fp8(w.k_cache, w.v_cache, kc, vc, ks, vs)
+        pools = dict(k_cache=kc, v_cache=vc, k_scale=ks, v_scale=vs)
+    else:
+        pools = dict(k_cache=w.k_cache, v_cache=w.v_cache)
+    step = DecodeStep(**pools, block_tables=w.block_tables, context_lens=w.context_lens,
+                      max_context_len=w.max_context_len, scale=w.scale, num_q_heads=w.Hq,
+                      partition_tokens=args.partition or None, total_context_tokens=tokens)
+    out = torch.empty_like(w.q)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
+    flush = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 2 + (1 if step.workspace is not None else 0)
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    if rank == 0:
+        clocks.start()
+    clocks.mark("warmup_start")
+    for _ in range(args.warmup):
+        flush.add_(1)
+        step(w.q, w.k_new, w.v_new, w.slot_mapping, out)
+    rc, bits = _abi.pa_get_status(dev)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} bits {bits}")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.mark("timed_start")
+    for i in range(K):
+        flush.add_(1)
+        ev[i][0].record(stream)
+        step.append(w.k_new, w.v_new, w.slot_mapping)
+        ev[i][1].record(stream)
+        step.decode(w.q, out)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark("timed_end")
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    app_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    total_ms = sum(step_ms)
+
+    # end to end through the public API with pinned host buffers
+    host_in = {k: getattr(w, k).cpu().pin_memory()
+               for k in ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")}
+    dev_in = {k: getattr(w, k) for k in host_in}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for _ in range(max(1, args.warmup)):
+        step.run_from_host(host_in, dev_in, host_out, out)
+    torch.cuda.synchronize(dev)
+    h2d = d2h = 0
+    for i in range(K):
+        flush.add_(1)
+        e2e_ev[i][0].record(stream)
+        h2d, d2h = step.run_from_host(host_in, dev_in, host_out, out)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
+    rc, bits = _abi.pa_get_status(dev)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} bits {bits}")
+    clk = clocks.stop() if rank == 0 else None
+
+    # whole-job aggregation: max time over ranks, tokens summed over ranks
+    t = torch.tensor([total_ms, e2e_ms, float(tokens)], dtype=torch.float64, device=dev)
+    if world > 1:
+        tmax = t.clone()
+        torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
+        tsum = t.clone()
+        torch.distributed.all_reduce(tsum, op=torch.distributed.ReduceOp.SUM)
+        total_ms_max, e2e_ms_max, tokens_all = tmax[0].item(), tmax[1].item(), tsum[2].item()
+    else:
+        total_ms_max, e2e_ms_max, tokens_all = total_ms, e2e_ms, float(tokens)
+    if rank != 0:
+        return None
+
+    ab = algorithmic_bytes(w, lens)
+    dec_mean_s = statistics.mean(dec_ms) / 1e3
+    peak, peak_kind = measured_peaks()
+    achieved = ab["total"] / dec_mean_s / 1e9
+    value = tokens_all * K / (total_ms_max / 1e3)
+    traffic = load_traffic(args.config, step.partition_tokens)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms_max / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3->f32" if w.kv == "fp8" else w.dtype, "data": "synthetic",
+        "config": {
+            "workload": describe(w, tokens), "step": "pa_cache_append + pa_decode",
+            "partition_tokens": step.partition_tokens, "l2": "flushed before every timed step",
+            "seed": args.seed, "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "hbm_gbs": round(achieved, 1), "hbm_frac_of_peak": round(achieved / peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "pa_decode (split-K decode_kernel + merge_kernel)",
+                     "bytes_per_launch": ab["total"], "peak_source": peak_kind},
+        "decode_us": {"mean": round(statistics.mean(dec_ms) * 1e3, 2),
+                      "median": round(statistics.median(dec_ms) * 1e3, 2),
+                      "p20": round(float(np.percentile(dec_ms, 20)) * 1e3, 2),
+                      "p80": round(float(np.percentile(dec_ms, 80)) * 1e3, 2),
+                      "min": round(min(dec_ms) * 1e3, 2)},
+        "append_us": {"mean": round(statistics.mean(app_ms) * 1e3, 2),
+                      "median": round(statistics.median(app_ms) * 1e3, 2)},
+        "e2e": {"value": round(tokens_all * K / (e2e_ms_max / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and w.kv != "fp8":
+        line["cpu_baseline"] = oracle_baseline(w, args.cpu_budget)
+    return line
+
+
+def describe(w, tokens):
+    return (f"{w.name}: {w.B} seqs, {w.Hq} q / {w.Hkv} kv heads, head_dim {w.D}, block 16, "
+            f"{'E4M3 pool, fp16 q' if w.kv == 'fp8' else w.dtype}, "
+            f"{tokens} attended tokens (max {w.max_context_len}), {w.num_blocks}-block pool")
+
+
+def load_traffic(config, part):
+    """DRAM bytes per decode call from the committed ncu summary, when it
+    matches this workload and partition size (else null)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t.get(config)
+        if e and e.get("partition_tokens") == part:
+            return e.get("bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args):
+    import oracle
+    from paged_kv_cache_179_gb300 import workloads as W
+    w = W.make_workload(args.config, seed=args.seed, device="cpu")
+    lens = w.context_lens.numpy()
+    tables = w.block_tables.numpy()
+    q, kp, vp = W.to_numpy16(w.q), W.to_numpy16(w.k_cache), W.to_numpy16(w.v_cache)
+    bf16 = w.dtype == "bf16"
+    kn, vn = W.to_numpy16(w.k_new), W.to_numpy16(w.v_new)
+    slots = w.slot_mapping.numpy()
+    if w.kv == "fp8":
+        kc, ks = oracle.quantize_fp8(kp)
+        vc, vs = oracle.quantize_fp8(vp)
+    order = np.random.default_rng(0).permutation(w.B)
+    # size each step's sample to about args.ref_step_s seconds of host work
+    probe = order[:2]
+    t = time.perf_counter()
+    if w.kv == "fp8":
+        oracle.decode_fp8(q, kc, vc, ks, vs, tables, lens, w.scale, rows=probe)
+    else:
+        oracle.decode(q, kp, vp, tables, lens, w.scale, bf16=bf16, rows=probe)
+    per_tok = max(time.perf_counter() - t, 1e-4) / max(1, int(lens[probe].sum()))
+    n = max(2, min(w.B, int(args.ref_step_s / per_tok / max(1.0, lens.mean()))))
+    rows = order[:n]
+    sample_tokens = int(lens[rows].sum())
+
+    def one_step():
+        if w.kv == "fp8":
+            oracle.cache_append_fp8(kn, vn, kc, vc, ks, vs, slots, 16)
+            oracle.decode_fp8(q, kc, vc, ks, vs, tables, lens, w.scale, rows=rows)
+        else:
+            oracle.cache_append(kn, vn, kp, vp, slots, 16)
+            oracle.decode(q, kp, vp, tables, lens, w.scale, bf16=bf16, rows=rows)
+
+    for _ in range(args.warmup):
+        one_step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    dt = time.perf_counter() - t
+    value = sample_tokens * args.steps / dt
+    sample = (f"{n} of {w.B} sequences per step ({sample_tokens} attended tokens, all {w.Hq} "
+              f"q heads) + the whole batch's append; fp64 oracle")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(w, int(lens.sum())), "step": "oracle append + decode",
+                   "seed": args.seed},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--partition", type=int, default=0, help="tokens per partition (0 = auto)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--ref-step-s", type=float, default=2.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    try:
+        line = run_ours(args, rank, world, dev)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

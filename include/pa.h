@@ -1,0 +1,204 @@
+/*
+ * pa.h -- C ABI of libpa: the decode-step hot path of a paged KV cache on
+ * one GB300 (sm_103a).
+ *
+ * Two operations make up one decode step of a vLLM-style serving engine:
+ *
+ *   1. append: scatter each sequence's new K/V token into a pool of
+ *      fixed-size blocks through a slot mapping
+ *      ("rvLLM: High-performance LLM inference in Rust", CUDA Kernels table,
+ *      "Reshape and Cache"; "rvllm - A Small LLM Inference Engine in Rust",
+ *      How it's put together: write positions computed from the block table);
+ *   2. decode attention: one query token per sequence attends, with grouped-
+ *      query heads, over the blocks its block table lists, with an online
+ *      softmax over context partitions merged by log-sum-exp
+ *      (rvLLM, CUDA Kernels table, "PagedAttention V2"; "LLM Serving Kernels",
+ *      Projects table, row 04 "Paged decode attention").
+ *
+ * An FP8 variant stores the pool as E4M3 codes with one fp32 scale per
+ * (physical block, kv head) and dequantises inside the attention loop (rvLLM,
+ * CUDA Kernels table, "FP8 KV Cache"; feature list "FP8 KV cache (E4M3
+ * quantization with per-head scaling)"; "LLM Serving Kernels", row 05
+ * "E4M3 storage, page scales, fused dequantization").
+ *
+ * Conventions for every entry point
+ *   - Pointers named *_cache, q, out, k_new, v_new, slot_mapping,
+ *     block_tables, context_lens, *_scale and workspace are DEVICE pointers
+ *     owned by the caller; they must be 16-byte aligned.  The library
+ *     allocates nothing and keeps no per-call state.
+ *   - Layouts are dense row-major:
+ *       16-bit pools   [num_blocks][num_kv_heads][block_size][head_dim]
+ *       E4M3 pools     same shape, one byte per element
+ *       page scales    fp32 [num_blocks][num_kv_heads]
+ *       q, out         [num_seqs][num_q_heads][head_dim]
+ *       k_new, v_new   [num_tokens][num_kv_heads][head_dim]
+ *       block_tables   int32 [num_seqs][max_blocks_per_seq]
+ *       context_lens   int32 [num_seqs]  (tokens attended, the new one included)
+ *       slot_mapping   int64 [num_tokens] (slot = block * block_size + row;
+ *                      a negative slot marks a padding token and is skipped)
+ *   - q head hq reads kv head hq / (num_q_heads / num_kv_heads).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on it and never synchronise, except
+ *     pa_get_status.
+ *   - Argument errors are returned before anything is launched.  Index
+ *     errors that only the device can see (a block id outside the pool, a
+ *     context length above its bound, a slot outside the pool) are never
+ *     dereferenced: the kernel skips the access and sets a bit in the
+ *     library's device status word, which pa_get_status reads.
+ *   - Supported now: head_dim 64 or 128, block_size 16, num_q_heads /
+ *     num_kv_heads from 1 to 8.  Other shapes return PA_ERR_UNSUPPORTED.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of 16-bit activations and pools. */
+enum { PA_F16 = 0, PA_BF16 = 1 };
+
+/* Return codes. */
+enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, Hq % Hkv != 0 */
+    PA_ERR_UNSUPPORTED = 2,  /* head_dim, block_size or group size not supported */
+    PA_ERR_WORKSPACE = 3,    /* workspace missing, too small or misaligned */
+    PA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    PA_ERR_BOUNDS = 5,       /* pa_get_status: a kernel skipped an out-of-range index */
+    PA_ERR_TIMEOUT = 6       /* pa_get_status: an asynchronous-copy wait gave up */
+};
+
+/* Bits of the device status word (pa_get_status). */
+#define PA_STATUS_BAD_BLOCK 1u   /* block table entry outside [0, num_blocks) */
+#define PA_STATUS_BAD_LEN 2u     /* context_len < 0, > max_context_len or > max_blocks_per_seq*block_size */
+#define PA_STATUS_BAD_SLOT 4u    /* slot >= num_blocks * block_size */
+#define PA_STATUS_TIMEOUT 8u     /* an mbarrier wait reached its iteration limit */
+
+/*
+ * Append: for each token i with s = slot_mapping[i] >= 0 and each kv head h,
+ * copy k_new[i][h][:] to k_cache[s / block_size][h][s % block_size][:] and
+ * the same for V.  A byte copy: results are bit-exact and no other byte of
+ * the pools changes.  Two tokens with the same slot race.
+ * dtype: PA_F16 or PA_BF16 (only the element size matters).
+ * Source: rvLLM, CUDA Kernels table, "Reshape and Cache"; rvllm (small
+ * engine), How it's put together, write_positions.
+ */
+int pa_cache_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                    const int64_t *slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                    int block_size, int num_blocks, int dtype, void *stream);
+
+/*
+ * FP8 append: like pa_cache_append, but each fp16 row is written as E4M3
+ * codes.  A page that receives its first token (slot % block_size == 0)
+ * gets, per kv head, scale = amax(|row|) / 448 in fp32 (1.0 when amax is 0),
+ * stored to k_scale / v_scale [num_blocks][num_kv_heads]; a later token of
+ * the page reuses the stored scale and saturates at +-448.  Codes are
+ * E4M3(x / scale) with the quotient rounded in fp32 and the code rounded to
+ * nearest even.  Within one call, a page's first token and later tokens of
+ * the same page race: give them in separate calls.
+ * Source: rvLLM, CUDA Kernels table, "FP8 KV Cache"; LLM Serving Kernels,
+ * Projects table, row 05.
+ */
+int pa_cache_append_fp8(const void *k_new, const void *v_new, uint8_t *k_cache, uint8_t *v_cache,
+                        float *k_scale, float *v_scale, const int64_t *slot_mapping,
+                        int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                        int num_blocks, void *stream);
+
+/*
+ * Bulk page quantisation of two fp16 pools (K and V) into E4M3 pools: for
+ * every (block, kv head) tile, amax = max |x| over its block_size x head_dim
+ * values, scale = amax / 448 in fp32 (1.0 when amax is 0), code =
+ * E4M3_RNE_saturating(x / scale) with the quotient rounded in fp32.
+ * k_src may equal NULL to quantise V only, and v_src NULL for K only.
+ * Source: rvLLM, CUDA Kernels table, "FP8 KV Cache"; LLM Serving Kernels,
+ * Projects table, row 05 ("page scales").
+ */
+int pa_quantize_fp8(const void *k_src, const void *v_src, uint8_t *k_cache, uint8_t *v_cache,
+                    float *k_scale, float *v_scale, int num_blocks, int num_kv_heads,
+                    int head_dim, int block_size, void *stream);
+
+/*
+ * The E4M3 encoder on its own: codes[i] = E4M3_RNE_saturating(x[i]) for n
+ * fp32 values (NaN gives a NaN code).  Exposed so the codec can be checked
+ * exhaustively; the quantisers use the same instruction.
+ */
+int pa_e4m3_encode(const float *x, uint8_t *codes, int64_t n, void *stream);
+
+/*
+ * Bytes of device workspace pa_decode / pa_decode_fp8 need for these sizes:
+ * the per-partition partial results that the log-sum-exp merge combines.
+ * 0 when no sequence can span more than one partition.  Returns 0 for
+ * invalid sizes too (pa_decode then reports the argument error).
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
+                                int partition_tokens);
+
+/*
+ * A partition size (tokens, a multiple of 16) that gives this device enough
+ * independent work, from what the host scheduler knows: the batch size, kv
+ * heads, the sum of context lengths and their maximum.
+ */
+int pa_decode_pick_partition(int num_seqs, int num_kv_heads, int64_t total_context_tokens,
+                             int max_context_len);
+
+/*
+ * Paged GQA decode over a 16-bit pool.  For every sequence b and q head hq,
+ *   out[b][hq][:] = sum_t softmax_t(scale * q[b][hq] . K_t) * V_t
+ * over the context_lens[b] tokens of b, token t read from physical block
+ * block_tables[b][t / block_size], row t % block_size, kv head
+ * hq / (num_q_heads / num_kv_heads).  Context tokens are split into
+ * partitions of partition_tokens; each is reduced with an online softmax in
+ * fp32 and, where a sequence spans several, a second kernel merges them by
+ * log-sum-exp.  out is rounded to dtype (round to nearest even).  A sequence
+ * with context_len 0 gets a zero output.
+ *   max_context_len: host-side upper bound of context_lens (no device read);
+ *   partition_tokens: a multiple of 16 in [16, 16384];
+ *   workspace: at least pa_decode_workspace_size(...) bytes (may be NULL when
+ *   that is 0).
+ * Source: rvLLM, CUDA Kernels table, "PagedAttention V2" (block-table
+ * indirection, online softmax); LLM Serving Kernels, Projects table, row 04;
+ * rvllm (small engine), How it's put together (GQA, read_blocks).
+ */
+int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+              int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+              int block_size, int num_blocks, float scale, int dtype, int partition_tokens,
+              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Paged GQA decode over an E4M3 pool: as pa_decode with fp16 q and out, K_t
+ * = e4m3(k_code) * k_scale[block][kv head] and V_t likewise, dequantised in
+ * registers inside the attention loop.
+ * Source: rvLLM, CUDA Kernels table, "FP8 KV Cache" and "PagedAttention V2";
+ * LLM Serving Kernels, Projects table, row 05 ("fused dequantization").
+ */
+int pa_decode_fp8(void *out, const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                  const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                  int max_blocks_per_seq, const int32_t *context_lens, int max_context_len,
+                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                  int num_blocks, float scale, int partition_tokens, void *workspace,
+                  size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word.  Returns PA_OK when it was clear, PA_ERR_TIMEOUT when a wait gave
+ * up, PA_ERR_BOUNDS for index errors, PA_ERR_CUDA when CUDA failed; the raw
+ * bits go to *bits when bits is not NULL.
+ */
+int pa_get_status(void *stream, unsigned *bits);
+
+/* A static string naming a return code. */
+const char *pa_status_string(int code);
+
+/* ABI version: major * 100 + minor. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

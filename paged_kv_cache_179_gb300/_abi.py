@@ -1,0 +1,264 @@
+"""Thin ctypes binding of libpa (include/pa.h): argument marshalling only.
+
+Every function takes torch tensors, checks that they are CUDA, contiguous and
+of the expected dtype and shape, passes their device pointers and the current
+torch stream to the C entry point of the same name, and raises ``PAError`` on a
+non-zero return code.  All arithmetic happens in the CUDA kernels; if
+libpa.so is missing this module raises instead of falling back to anything.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+PA_F16, PA_BF16 = 0, 1
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_BOUNDS, \
+    PA_ERR_TIMEOUT = range(7)
+PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_LEN, PA_STATUS_BAD_SLOT, PA_STATUS_TIMEOUT = 1, 2, 4, 8
+
+# (name, argtypes, restype) of every exported entry point
+_vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "pa_version": ([], _i32),
+    "pa_status_string": ([_i32], ctypes.c_char_p),
+    "pa_cache_append": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp], _i32),
+    "pa_cache_append_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp],
+                            _i32),
+    "pa_quantize_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
+    "pa_e4m3_encode": ([_vp, _vp, _i64, _vp], _i32),
+    "pa_decode_workspace_size": ([_i32, _i32, _i32, _i32, _i32], _sz),
+    "pa_decode_pick_partition": ([_i32, _i32, _i64, _i32], _i32),
+    "pa_decode": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                   _f32, _i32, _i32, _vp, _sz, _vp], _i32),
+    "pa_decode_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                       _i32, _i32, _f32, _i32, _vp, _sz, _vp], _i32),
+    "pa_get_status": ([_vp, ctypes.POINTER(ctypes.c_uint)], _i32),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} (code {code})")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libpa.so (raising if it is absent, unless asked to build it)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB):
+                if not build_if_missing:
+                    raise RuntimeError(f"{_build.LIB} is not built; call __graft_entry__.build() "
+                                       "or python -m paged_kv_cache_179_gb300.build")
+                _build.build()
+            L = ctypes.CDLL(_build.LIB)
+            for name, (args, res) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load().pa_status_string(code).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != PA_OK:
+        raise PAError(rc, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(dev) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _need(t, name, dtype=None, ndim=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, has {t.dim()}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _act_code(dtype) -> int:
+    if dtype == torch.float16:
+        return PA_F16
+    if dtype == torch.bfloat16:
+        return PA_BF16
+    raise TypeError(f"unsupported activation dtype {dtype}")
+
+
+# ---------------------------------------------------------------- entry points
+def pa_version() -> int:
+    return load().pa_version()
+
+
+def pa_cache_append(k_new, v_new, k_cache, v_cache, slot_mapping) -> None:
+    """Scatter k_new/v_new [T][Hkv][D] into the pools [NB][Hkv][bs][D] at slot_mapping [T]."""
+    dev = k_cache.device
+    act = (torch.float16, torch.bfloat16)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, n, act, 3, dev)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, k_new.dtype, 4, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    T, Hkv, D = k_new.shape
+    NB, Hkv2, bs, D2 = k_cache.shape
+    if (Hkv2, D2) != (Hkv, D) or v_new.shape != k_new.shape or v_cache.shape != k_cache.shape \
+            or slot_mapping.shape[0] != T:
+        raise ValueError("shape mismatch")
+    _check(load().pa_cache_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(slot_mapping), T, Hkv, D, bs, NB, _act_code(k_new.dtype),
+                                  _stream(dev)), "pa_cache_append")
+
+
+def pa_cache_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping) -> None:
+    """E4M3-encode fp16 k_new/v_new into uint8 pools; a page's first token sets its scales."""
+    dev = k_cache.device
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, n, torch.float16, 3, dev)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.uint8, 4, dev)
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need(t, n, torch.float32, 2, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    T, Hkv, D = k_new.shape
+    NB, _, bs, _ = k_cache.shape
+    if k_scale.shape != (NB, Hkv) or v_scale.shape != (NB, Hkv) or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch")
+    _check(load().pa_cache_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), T, Hkv,
+                                      D, bs, NB, _stream(dev)), "pa_cache_append_fp8")
+
+
+def pa_quantize_fp8(k_src, v_src, k_cache, v_cache, k_scale, v_scale) -> None:
+    """Quantise fp16 pools [NB][Hkv][bs][D] into E4M3 pools and [NB][Hkv] fp32 scales."""
+    ref = k_src if k_src is not None else v_src
+    dev = ref.device
+    NB, Hkv, bs, D = ref.shape
+    for src, codes, sc, n in ((k_src, k_cache, k_scale, "k"), (v_src, v_cache, v_scale, "v")):
+        if src is None:
+            continue
+        _need(src, n + "_src", torch.float16, 4, dev)
+        _need(codes, n + "_cache", torch.uint8, 4, dev)
+        _need(sc, n + "_scale", torch.float32, 2, dev)
+        if src.shape != ref.shape or codes.shape != ref.shape or sc.shape != (NB, Hkv):
+            raise ValueError("shape mismatch")
+    _check(load().pa_quantize_fp8(_ptr(k_src), _ptr(v_src), _ptr(k_cache if k_src is not None else None),
+                                  _ptr(v_cache if v_src is not None else None),
+                                  _ptr(k_scale if k_src is not None else None),
+                                  _ptr(v_scale if v_src is not None else None), NB, Hkv, D, bs,
+                                  _stream(dev)), "pa_quantize_fp8")
+
+
+def pa_e4m3_encode(x, codes) -> None:
+    _need(x, "x", torch.float32, None)
+    _need(codes, "codes", torch.uint8, None, x.device)
+    if codes.numel() != x.numel():
+        raise ValueError("size mismatch")
+    _check(load().pa_e4m3_encode(_ptr(x), _ptr(codes), x.numel(), _stream(x.device)),
+           "pa_e4m3_encode")
+
+
+def pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len,
+                             partition_tokens) -> int:
+    return int(load().pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len,
+                                               partition_tokens))
+
+
+def pa_decode_pick_partition(num_seqs, num_kv_heads, total_context_tokens, max_context_len) -> int:
+    return int(load().pa_decode_pick_partition(num_seqs, num_kv_heads, int(total_context_tokens),
+                                               max_context_len))
+
+
+def alloc_workspace(num_seqs, num_q_heads, head_dim, max_context_len, partition_tokens, device):
+    """Caller-owned workspace for pa_decode (None when the sizes need none)."""
+    n = pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len, partition_tokens)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def _decode_common(out, q, block_tables, context_lens, dev):
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    B, Hq, D = q.shape
+    if out.shape != q.shape or block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("shape mismatch")
+    return B, Hq, D
+
+
+def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
+              scale: float, partition_tokens: int, workspace=None) -> None:
+    """out[b][hq] = softmax(scale q.K) V over each sequence's blocks (16-bit pools)."""
+    dev = q.device
+    act = (torch.float16, torch.bfloat16)
+    _need(q, "q", act, 3, dev)
+    _need(out, "out", q.dtype, 3, dev)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, q.dtype, 4, dev)
+    B, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
+    NB, Hkv, bs, _ = k_cache.shape
+    ws_bytes = 0
+    if workspace is not None:
+        _need(workspace, "workspace", None, None, dev)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                            block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq,
+                            Hkv, D, bs, NB, float(scale), _act_code(q.dtype),
+                            int(partition_tokens), _ptr(workspace), ws_bytes, _stream(dev)),
+           "pa_decode")
+
+
+def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                  max_context_len: int, scale: float, partition_tokens: int,
+                  workspace=None) -> None:
+    """As pa_decode over E4M3 pools with per-(block, kv head) fp32 scales; q/out fp16."""
+    dev = q.device
+    _need(q, "q", torch.float16, 3, dev)
+    _need(out, "out", torch.float16, 3, dev)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.uint8, 4, dev)
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need(t, n, torch.float32, 2, dev)
+    B, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
+    NB, Hkv, bs, _ = k_cache.shape
+    ws_bytes = 0
+    if workspace is not None:
+        _need(workspace, "workspace", None, None, dev)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().pa_decode_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
+                                _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
+                                float(scale), int(partition_tokens), _ptr(workspace), ws_bytes,
+                                _stream(dev)), "pa_decode_fp8")
+
+
+def pa_get_status(device=None) -> tuple[int, int]:
+    """(return code, raw status bits) after synchronising the current stream."""
+    bits = ctypes.c_uint(0)
+    rc = load().pa_get_status(_stream(device or torch.cuda.current_device()), ctypes.byref(bits))
+    return rc, bits.value

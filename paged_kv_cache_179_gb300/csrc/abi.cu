@@ -1,0 +1,296 @@
+// abi.cu -- the extern "C" entry points declared in include/pa.h.
+//
+// Each entry point checks its arguments on the host (returning an error code
+// before anything is launched), then launches the kernels of append.cu,
+// quantize.cu and decode.cu on the caller's stream.  The only state the
+// library keeps is one device status word per device (index errors and wait
+// timeouts seen by kernels) and a per-device cache of its address and SM
+// count.
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "pa.h"
+#include "pa_launch.h"
+
+__device__ unsigned int g_pa_status_word;
+
+namespace pa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+  bool ready = false;
+  unsigned* status = nullptr;
+  int sm_count = 0;
+};
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+
+// Status word address and SM count of the current device (set up once).
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& d = g_devices[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pa_status_word) != cudaSuccess) return PA_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PA_ERR_CUDA;
+    d.status = static_cast<unsigned*>(p);
+    d.sm_count = sms;
+    d.ready = true;
+  }
+  *out = &d;
+  return PA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+struct DecodeShape {
+  int B, Hq, Hkv, D, bs, NB, mbs, max_ctx, part;
+};
+
+int check_decode_shape(const DecodeShape& s, float scale) {
+  if (s.B < 0 || s.Hq <= 0 || s.Hkv <= 0 || s.Hq % s.Hkv != 0) return PA_ERR_INVALID_ARG;
+  if (s.NB <= 0 || s.mbs <= 0 || s.max_ctx < 0) return PA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(s.max_ctx) > static_cast<int64_t>(s.mbs) * s.bs) return PA_ERR_INVALID_ARG;
+  if (s.part < 16 || s.part > 16384 || s.part % 16 != 0) return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (s.D != 64 && s.D != 128) return PA_ERR_UNSUPPORTED;
+  if (s.bs != 16) return PA_ERR_UNSUPPORTED;
+  if (s.Hq / s.Hkv > 8) return PA_ERR_UNSUPPORTED;
+  if (s.B > 65535 || s.Hkv > 65535) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+int run_decode(const DecodeShape& s, void* out, const void* q, const void* k, const void* v,
+               const float* ks, const float* vs, const int32_t* bt, const int32_t* cl,
+               float scale, bool fp8, bool bf16, void* ws, size_t ws_bytes, void* stream) {
+  if (s.B == 0) return PA_OK;
+  const size_t need = decode_workspace_bytes(s.B, s.Hq, s.D, s.max_ctx, s.part);
+  if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned(ws, 256))) return PA_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  if (int rc = device_state(&dev)) return rc;
+  DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_cache = k;
+  a.v_cache = v;
+  a.k_scale = ks;
+  a.v_scale = vs;
+  a.block_tables = bt;
+  a.context_lens = cl;
+  a.status = dev->status;
+  a.mbs = s.mbs;
+  a.B = s.B;
+  a.Hq = s.Hq;
+  a.Hkv = s.Hkv;
+  a.group = s.Hq / s.Hkv;
+  a.D = s.D;
+  a.num_blocks = s.NB;
+  a.max_context_len = s.max_ctx;
+  a.part_tokens = s.part;
+  const int64_t parts = (static_cast<int64_t>(s.max_ctx) + s.part - 1) / s.part;
+  a.max_parts = static_cast<int>(parts < 1 ? 1 : parts);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  if (need > 0) decode_workspace_split(a, ws, &a.ws_acc, &a.ws_ml);
+  return cuda_status(launch_decode(a, fp8, bf16, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+int device_sm_count() {
+  DeviceState* d = nullptr;
+  return device_state(&d) == PA_OK ? d->sm_count : 148;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_version(void) { return 100; }
+
+const char* pa_status_string(int code) {
+  switch (code) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported shape";
+    case PA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_BOUNDS: return "a kernel skipped an out-of-range index";
+    case PA_ERR_TIMEOUT: return "an asynchronous-copy wait gave up";
+    default: return "unknown status";
+  }
+}
+
+int pa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                    const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                    int block_size, int num_blocks, int dtype, void* stream) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+  if (head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;   // rows move as 16-byte chunks
+  for (const void* p : {k_new, v_new, static_cast<const void*>(k_cache),
+                        static_cast<const void*>(v_cache)})
+    if (!aligned(p, 16)) return PA_ERR_INVALID_ARG;
+  if (!aligned(slot_mapping, 8)) return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (static_cast<int64_t>(num_tokens) * num_kv_heads * (head_dim / 8) > (INT64_C(1) << 40))
+    return PA_ERR_UNSUPPORTED;
+  DeviceState* dev = nullptr;
+  if (int rc = device_state(&dev)) return rc;
+  return cuda_status(launch_append(k_new, v_new, k_cache, v_cache, slot_mapping, num_tokens,
+                                   num_kv_heads, head_dim * 2, block_size, num_blocks,
+                                   dev->status, static_cast<cudaStream_t>(stream)));
+}
+
+int pa_cache_append_fp8(const void* k_new, const void* v_new, uint8_t* k_cache, uint8_t* v_cache,
+                        float* k_scale, float* v_scale, const int64_t* slot_mapping,
+                        int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                        int num_blocks, void* stream) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !k_scale || !v_scale || !slot_mapping)
+    return PA_ERR_INVALID_ARG;
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  for (const void* p : {k_new, v_new, static_cast<const void*>(k_cache),
+                        static_cast<const void*>(v_cache)})
+    if (!aligned(p, 16)) return PA_ERR_INVALID_ARG;
+  if (!aligned(k_scale, 4) || !aligned(v_scale, 4) || !aligned(slot_mapping, 8))
+    return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  DeviceState* dev = nullptr;
+  if (int rc = device_state(&dev)) return rc;
+  return cuda_status(launch_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                                       slot_mapping, num_tokens, num_kv_heads, head_dim,
+                                       block_size, num_blocks, dev->status,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int pa_quantize_fp8(const void* k_src, const void* v_src, uint8_t* k_cache, uint8_t* v_cache,
+                    float* k_scale, float* v_scale, int num_blocks, int num_kv_heads,
+                    int head_dim, int block_size, void* stream) {
+  if (!k_src && !v_src) return PA_ERR_INVALID_ARG;
+  if (k_src && (!k_cache || !k_scale)) return PA_ERR_INVALID_ARG;
+  if (v_src && (!v_cache || !v_scale)) return PA_ERR_INVALID_ARG;
+  if (num_blocks < 0 || num_kv_heads <= 0) return PA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size != 16) return PA_ERR_UNSUPPORTED;
+  for (const void* p : {k_src, v_src, static_cast<const void*>(k_cache),
+                        static_cast<const void*>(v_cache)})
+    if (p && !aligned(p, 16)) return PA_ERR_INVALID_ARG;
+  if ((k_scale && !aligned(k_scale, 4)) || (v_scale && !aligned(v_scale, 4)))
+    return PA_ERR_INVALID_ARG;
+  const int64_t tiles = static_cast<int64_t>(num_blocks) * num_kv_heads;
+  if (tiles == 0) return PA_OK;
+  DeviceState* dev = nullptr;
+  if (int rc = device_state(&dev)) return rc;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int tile_elems = block_size * head_dim;
+  if (k_src)
+    if (cudaError_t e = launch_quantize_fp8(k_src, k_cache, k_scale, tiles, tile_elems, s))
+      return cuda_status(e);
+  if (v_src)
+    if (cudaError_t e = launch_quantize_fp8(v_src, v_cache, v_scale, tiles, tile_elems, s))
+      return cuda_status(e);
+  return PA_OK;
+}
+
+int pa_e4m3_encode(const float* x, uint8_t* codes, int64_t n, void* stream) {
+  if (!x || !codes || n < 0) return PA_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(codes, 16)) return PA_ERR_INVALID_ARG;
+  if (n == 0) return PA_OK;
+  DeviceState* dev = nullptr;
+  if (int rc = device_state(&dev)) return rc;
+  return cuda_status(launch_e4m3_encode(x, codes, n, static_cast<cudaStream_t>(stream)));
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
+                                int partition_tokens) {
+  if (partition_tokens < 16 || partition_tokens % 16 != 0) return 0;
+  return decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len,
+                                partition_tokens);
+}
+
+int pa_decode_pick_partition(int num_seqs, int num_kv_heads, int64_t total_context_tokens,
+                             int max_context_len) {
+  // Aim at ~16 partitions per SM (two resident CTAs per SM, eight waves),
+  // with partitions of 128..4096 tokens in steps of 64.
+  (void)num_seqs;
+  (void)max_context_len;
+  int sms = 148;
+  DeviceState* d = nullptr;
+  if (device_state(&d) == PA_OK) sms = d->sm_count;
+  const int64_t target = static_cast<int64_t>(sms) * 16;
+  int64_t work = total_context_tokens * (num_kv_heads > 0 ? num_kv_heads : 1);
+  int64_t p = (work + target - 1) / target;
+  p = ((p + 63) / 64) * 64;
+  if (p < 128) p = 128;
+  if (p > 4096) p = 4096;
+  return static_cast<int>(p);
+}
+
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+              int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+              int block_size, int num_blocks, float scale, int dtype, int partition_tokens,
+              void* workspace, size_t workspace_bytes, void* stream) {
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return PA_ERR_INVALID_ARG;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+  const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                      num_blocks, max_blocks_per_seq, max_context_len, partition_tokens};
+  if (int rc = check_decode_shape(s, scale)) return rc;
+  for (const void* p : {static_cast<const void*>(out), q, k_cache, v_cache})
+    if (!aligned(p, 16)) return PA_ERR_INVALID_ARG;
+  if (!aligned(block_tables, 4) || !aligned(context_lens, 4)) return PA_ERR_INVALID_ARG;
+  return run_decode(s, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens,
+                    scale, false, dtype == PA_BF16, workspace, workspace_bytes, stream);
+}
+
+int pa_decode_fp8(void* out, const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                  const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                  int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
+                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                  int num_blocks, float scale, int partition_tokens, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  if (!out || !q || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables ||
+      !context_lens)
+    return PA_ERR_INVALID_ARG;
+  const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                      num_blocks, max_blocks_per_seq, max_context_len, partition_tokens};
+  if (int rc = check_decode_shape(s, scale)) return rc;
+  for (const void* p : {static_cast<const void*>(out), q, static_cast<const void*>(k_cache),
+                        static_cast<const void*>(v_cache)})
+    if (!aligned(p, 16)) return PA_ERR_INVALID_ARG;
+  if (!aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(k_scale, 4) ||
+      !aligned(v_scale, 4))
+    return PA_ERR_INVALID_ARG;
+  return run_decode(s, out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                    scale, true, false, workspace, workspace_bytes, stream);
+}
+
+int pa_get_status(void* stream, unsigned* bits) {
+  DeviceState* dev = nullptr;
+  if (int rc = device_state(&dev)) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpy(&v, dev->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaMemcpy(dev->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (bits) *bits = v;
+  if (v & PA_STATUS_TIMEOUT) return PA_ERR_TIMEOUT;
+  if (v) return PA_ERR_BOUNDS;
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,54 @@
+// pa_launch.h -- kernel launchers shared between the translation units of
+// libpa.  The C ABI (abi.cu) validates arguments and then calls these.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pa {
+
+// All pointers are device pointers; sizes were validated by the caller.
+struct DecodeArgs {
+  void* out;                    // [B][Hq][D] f16/bf16
+  const void* q;                // [B][Hq][D] f16/bf16
+  const void* k_cache;          // [NB][Hkv][16][D] f16/bf16 or e4m3
+  const void* v_cache;
+  const float* k_scale;         // [NB][Hkv] (E4M3 pools only)
+  const float* v_scale;
+  const int32_t* block_tables;  // [B][mbs]
+  const int32_t* context_lens;  // [B]
+  float* ws_acc;                // [B][Hq][max_parts][D] partial sums (unnormalised)
+  float* ws_ml;                 // [B][Hq][max_parts][2] partial (max, sum) in log2 units
+  unsigned* status;             // device status word
+  int mbs;                      // max blocks per sequence (block table row stride)
+  int B, Hq, Hkv, group, D;
+  int num_blocks;
+  int max_context_len;
+  int part_tokens;              // tokens per partition, multiple of 16
+  int max_parts;                // ceil(max_context_len / part_tokens)
+  float scale_log2;             // softmax scale * log2(e)
+};
+
+size_t decode_workspace_bytes(int B, int Hq, int D, int max_context_len, int part_tokens);
+void decode_workspace_split(const DecodeArgs& a, void* ws, float** acc, float** ml);
+
+cudaError_t launch_decode(const DecodeArgs& a, bool fp8, bool bf16, cudaStream_t s);
+
+cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                          const int64_t* slots, int T, int Hkv, int row_bytes, int block_size,
+                          int64_t num_blocks, unsigned* status, cudaStream_t s);
+
+cudaError_t launch_append_fp8(const void* k_new, const void* v_new, uint8_t* k_cache,
+                              uint8_t* v_cache, float* k_scale, float* v_scale,
+                              const int64_t* slots, int T, int Hkv, int D, int block_size,
+                              int64_t num_blocks, unsigned* status, cudaStream_t s);
+
+cudaError_t launch_quantize_fp8(const void* src, uint8_t* codes, float* scales,
+                                int64_t num_tiles, int tile_elems, cudaStream_t s);
+
+cudaError_t launch_e4m3_encode(const float* x, uint8_t* codes, int64_t n, cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace pa

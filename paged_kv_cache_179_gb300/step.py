@@ -1,0 +1,80 @@
+"""One decode step over a paged KV cache: append the new token, then attend.
+
+``DecodeStep`` owns nothing but the caller's tensors and a workspace; each
+method is one or two C-ABI calls (see ``_abi``).  ``run_from_host`` is the
+end-to-end form a serving loop uses: the step's per-token inputs arrive in
+pinned host memory, are copied to the device, the step runs, and the
+attention output is copied back.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _abi
+
+
+class DecodeStep:
+    """Append + decode for one batch shape.
+
+    Pools are [NB][Hkv][bs][D]: 16-bit (``kv="f16"|"bf16"``) or E4M3 codes
+    with fp32 [NB][Hkv] scales (``kv="fp8"``, q/out fp16).
+    """
+
+    def __init__(self, *, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
+                 num_q_heads, k_scale=None, v_scale=None, partition_tokens=None,
+                 total_context_tokens=None):
+        self.kv = "fp8" if k_cache.dtype == torch.uint8 else "16"
+        self.k_cache, self.v_cache = k_cache, v_cache
+        self.k_scale, self.v_scale = k_scale, v_scale
+        self.block_tables, self.context_lens = block_tables, context_lens
+        self.max_context_len = int(max_context_len)
+        self.scale = float(scale)
+        self.B = int(block_tables.shape[0])
+        self.Hq = int(num_q_heads)
+        self.NB, self.Hkv, self.bs, self.D = (int(x) for x in k_cache.shape)
+        if partition_tokens is None:
+            total = (int(total_context_tokens) if total_context_tokens is not None
+                     else self.B * self.max_context_len)
+            partition_tokens = _abi.pa_decode_pick_partition(self.B, self.Hkv, total,
+                                                             self.max_context_len)
+        self.partition_tokens = int(partition_tokens)
+        self.workspace = _abi.alloc_workspace(self.B, self.Hq, self.D, self.max_context_len,
+                                              self.partition_tokens, k_cache.device)
+
+    def append(self, k_new, v_new, slot_mapping):
+        if self.kv == "fp8":
+            _abi.pa_cache_append_fp8(k_new, v_new, self.k_cache, self.v_cache, self.k_scale,
+                                     self.v_scale, slot_mapping)
+        else:
+            _abi.pa_cache_append(k_new, v_new, self.k_cache, self.v_cache, slot_mapping)
+
+    def decode(self, q, out):
+        if self.kv == "fp8":
+            _abi.pa_decode_fp8(out, q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
+                               self.block_tables, self.context_lens, self.max_context_len,
+                               self.scale, self.partition_tokens, self.workspace)
+        else:
+            _abi.pa_decode(out, q, self.k_cache, self.v_cache, self.block_tables,
+                           self.context_lens, self.max_context_len, self.scale,
+                           self.partition_tokens, self.workspace)
+
+    def __call__(self, q, k_new, v_new, slot_mapping, out):
+        self.append(k_new, v_new, slot_mapping)
+        self.decode(q, out)
+        return out
+
+    def run_from_host(self, host_in: dict, dev_in: dict, host_out, dev_out):
+        """Copy the step's inputs from pinned host tensors, run it, copy the output back.
+
+        host_in/dev_in map q, k_new, v_new, slot_mapping, block_tables and
+        context_lens to same-shaped pinned-host / device tensors (the device
+        block_tables and context_lens must be the ones this step was built
+        with).  Returns (h2d bytes, d2h bytes).
+        """
+        h2d = 0
+        for k, h in host_in.items():
+            dev_in[k].copy_(h, non_blocking=True)
+            h2d += h.numel() * h.element_size()
+        self(dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["slot_mapping"], dev_out)
+        host_out.copy_(dev_out, non_blocking=True)
+        return h2d, host_out.numel() * host_out.element_size()

@@ -1,0 +1,105 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol that
+include/pa.h declares, and rejects bad arguments on the host before any
+CUDA call (these calls never dereference the pointers they are given)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from paged_kv_cache_179_gb300 import _abi, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+FAKE = 0x10000          # a 16-byte-aligned address that is never dereferenced
+MISALIGNED = 0x10008
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _abi.load()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    names = header_functions()
+    assert len(names) == 11
+    assert sorted(_abi.SIGNATURES) == names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    assert lib.pa_version() == 100
+    assert lib.pa_status_string(0) == b"ok"
+    assert b"workspace" in lib.pa_status_string(3)
+
+
+def _decode(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, mbs=8, cl=FAKE, max_ctx=128, B=2, Hq=8,
+             Hkv=2, D=64, bs=16, NB=32, scale=0.125, dtype=0, part=64, ws=FAKE, ws_bytes=1 << 20)
+    a.update(kw)
+    return lib.pa_decode(a["out"], a["q"], a["k"], a["v"], a["bt"], a["mbs"], a["cl"],
+                         a["max_ctx"], a["B"], a["Hq"], a["Hkv"], a["D"], a["bs"], a["NB"],
+                         a["scale"], a["dtype"], a["part"], a["ws"], a["ws_bytes"], None)
+
+
+def test_decode_argument_errors(lib):
+    assert _decode(lib, q=None) == _abi.PA_ERR_INVALID_ARG
+    assert _decode(lib, Hq=7) == _abi.PA_ERR_INVALID_ARG            # 7 % 2 != 0
+    assert _decode(lib, part=8) == _abi.PA_ERR_INVALID_ARG
+    assert _decode(lib, part=40) == _abi.PA_ERR_INVALID_ARG
+    assert _decode(lib, max_ctx=129) == _abi.PA_ERR_INVALID_ARG     # > mbs * 16
+    assert _decode(lib, scale=float("nan")) == _abi.PA_ERR_INVALID_ARG
+    assert _decode(lib, dtype=3) == _abi.PA_ERR_INVALID_ARG
+    assert _decode(lib, q=MISALIGNED) == _abi.PA_ERR_INVALID_ARG
+    assert _decode(lib, D=96) == _abi.PA_ERR_UNSUPPORTED
+    assert _decode(lib, bs=32, mbs=4) == _abi.PA_ERR_UNSUPPORTED
+    assert _decode(lib, Hq=18, Hkv=2) == _abi.PA_ERR_UNSUPPORTED    # group of 9
+    assert _decode(lib, ws=None) == _abi.PA_ERR_WORKSPACE
+    assert _decode(lib, ws_bytes=16) == _abi.PA_ERR_WORKSPACE
+    assert _decode(lib, ws=FAKE + 16) == _abi.PA_ERR_WORKSPACE      # not 256-aligned
+    assert _decode(lib, B=0) == _abi.PA_OK                          # nothing to do
+
+
+def test_workspace_size_formula(lib):
+    # two partitions of 64 for 128 tokens: [B][Hq][2] rows of D floats, then (m, l)
+    n = lib.pa_decode_workspace_size(2, 8, 64, 128, 64)
+    acc = 2 * 8 * 2 * 64 * 4
+    assert n == ((acc + 255) // 256) * 256 + 2 * 8 * 2 * 2 * 4
+    assert lib.pa_decode_workspace_size(2, 8, 64, 64, 64) == 0     # one partition: no merge
+    assert lib.pa_decode_workspace_size(2, 8, 64, 128, 8) == 0     # invalid partition
+
+
+def test_append_and_quantize_argument_errors(lib):
+    f = lib.pa_cache_append
+    assert f(None, FAKE, FAKE, FAKE, FAKE, 4, 2, 64, 16, 8, 0, None) == _abi.PA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 60, 16, 8, 0, None) == _abi.PA_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, MISALIGNED, FAKE, FAKE, 4, 2, 64, 16, 8, 0, None) == _abi.PA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 2, 64, 16, 8, 0, None) == _abi.PA_OK
+    g = lib.pa_cache_append_fp8
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 96, 16, 8, None) == _abi.PA_ERR_UNSUPPORTED
+    q = lib.pa_quantize_fp8
+    assert q(None, None, FAKE, FAKE, FAKE, FAKE, 8, 2, 64, 16, None) == _abi.PA_ERR_INVALID_ARG
+    assert q(FAKE, None, FAKE, None, FAKE, None, 8, 2, 64, 32, None) == _abi.PA_ERR_UNSUPPORTED
+    assert lib.pa_e4m3_encode(FAKE, MISALIGNED, 10, None) == _abi.PA_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a CUDA device")
+def test_valid_call_without_device_reports_cuda_error(lib):
+    assert _decode(lib) == _abi.PA_ERR_CUDA
+
+
+def test_binding_refuses_cpu_tensors():
+    t = torch.zeros(2, 8, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        _abi.pa_decode(t, t, t, t, torch.zeros(2, 4, dtype=torch.int32),
+                       torch.zeros(2, dtype=torch.int32), 64, 0.125, 64)
