@@ -22,6 +22,8 @@
  * "E4M3 storage, page scales, fused dequantization").
  *
  * Conventions for every entry point
+ *   - A call with zero tokens or zero sequences returns PA_OK at once,
+ *     whatever its pointers (empty tensors may have NULL data).
  *   - Pointers named *_cache, q, out, k_new, v_new, slot_mapping,
  *     block_tables, context_lens, *_scale and workspace are DEVICE pointers
  *     owned by the caller; they must be 16-byte aligned.  The library

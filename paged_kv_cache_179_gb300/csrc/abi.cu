@@ -133,6 +133,7 @@ const char* pa_status_string(int code) {
 int pa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                     const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
                     int block_size, int num_blocks, int dtype, void* stream) {
+  if (num_tokens == 0) return PA_OK;   // nothing to move (empty tensors may have null data)
   if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
     return PA_ERR_INVALID_ARG;
@@ -156,6 +157,7 @@ int pa_cache_append_fp8(const void* k_new, const void* v_new, uint8_t* k_cache, 
                         float* k_scale, float* v_scale, const int64_t* slot_mapping,
                         int num_tokens, int num_kv_heads, int head_dim, int block_size,
                         int num_blocks, void* stream) {
+  if (num_tokens == 0) return PA_OK;
   if (!k_new || !v_new || !k_cache || !v_cache || !k_scale || !v_scale || !slot_mapping)
     return PA_ERR_INVALID_ARG;
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
@@ -243,6 +245,7 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
               int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
               int block_size, int num_blocks, float scale, int dtype, int partition_tokens,
               void* workspace, size_t workspace_bytes, void* stream) {
+  if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
     return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
@@ -262,6 +265,7 @@ int pa_decode_fp8(void* out, const void* q, const uint8_t* k_cache, const uint8_
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                   int num_blocks, float scale, int partition_tokens, void* workspace,
                   size_t workspace_bytes, void* stream) {
+  if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables ||
       !context_lens)
     return PA_ERR_INVALID_ARG;

@@ -85,6 +85,7 @@ def test_append_and_quantize_argument_errors(lib):
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 60, 16, 8, 0, None) == _abi.PA_ERR_UNSUPPORTED
     assert f(FAKE, FAKE, MISALIGNED, FAKE, FAKE, 4, 2, 64, 16, 8, 0, None) == _abi.PA_ERR_INVALID_ARG
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 2, 64, 16, 8, 0, None) == _abi.PA_OK
+    assert f(None, None, None, None, None, 0, 2, 64, 16, 8, 0, None) == _abi.PA_OK   # empty batch
     g = lib.pa_cache_append_fp8
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 96, 16, 8, None) == _abi.PA_ERR_UNSUPPORTED
     q = lib.pa_quantize_fp8
