@@ -195,12 +195,12 @@ def run_ours(args, rank, world, dev):
         pools = dict(k_cache=w.k_cache, v_cache=w.v_cache)
     step = DecodeStep(**pools, block_tables=w.block_tables, context_lens=w.context_lens,
                       max_context_len=w.max_context_len, scale=w.scale, num_q_heads=w.Hq,
-                      partition_tokens=args.partition or None, total_context_tokens=tokens)
+                      split_ctas=args.splits)
     out = torch.empty_like(w.q)
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
     flush = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 2 + (1 if step.workspace is not None else 0)
+    launches_per_step = 2   # append_kernel + decode_kernel
 
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     if rank == 0:
@@ -275,7 +275,7 @@ def run_ours(args, rank, world, dev):
     peak, peak_kind = measured_peaks()
     achieved = ab["total"] / dec_mean_s / 1e9
     value = tokens_all * K / (total_ms_max / 1e3)
-    traffic = load_traffic(args.config, step.partition_tokens)
+    traffic = load_traffic(args.config, step.split_ctas)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms_max / K, 5),
@@ -283,13 +283,13 @@ def run_ours(args, rank, world, dev):
         "dtype": "e4m3->f32" if w.kv == "fp8" else w.dtype, "data": "synthetic",
         "config": {
             "workload": describe(w, tokens), "step": "pa_cache_append + pa_decode",
-            "partition_tokens": step.partition_tokens, "l2": "flushed before every timed step",
+            "split_ctas": step.split_ctas, "l2": "flushed before every timed step",
             "seed": args.seed, "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "hbm_gbs": round(achieved, 1), "hbm_frac_of_peak": round(achieved / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "pa_decode (split-K decode_kernel + merge_kernel)",
+                     "kernel": "pa_decode (decode_kernel, split-K merge fused)",
                      "bytes_per_launch": ab["total"], "peak_source": peak_kind},
         "decode_us": {"mean": round(statistics.mean(dec_ms) * 1e3, 2),
                       "median": round(statistics.median(dec_ms) * 1e3, 2),
@@ -314,15 +314,15 @@ def describe(w, tokens):
             f"{tokens} attended tokens (max {w.max_context_len}), {w.num_blocks}-block pool")
 
 
-def load_traffic(config, part):
+def load_traffic(config, splits):
     """DRAM bytes per decode call from the committed ncu summary, when it
-    matches this workload and partition size (else null)."""
+    matches this workload and CTA split (else null)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
         e = t.get(config)
-        if e and e.get("partition_tokens") == part:
+        if e and e.get("split_ctas") == splits:
             return e.get("bytes_per_launch")
     except (OSError, ValueError):
         pass
@@ -395,7 +395,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--partition", type=int, default=0, help="tokens per partition (0 = auto)")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="CTAs the batch is divided among (0 = two per SM)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-step-s", type=float, default=2.0)

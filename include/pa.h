@@ -131,36 +131,43 @@ int pa_quantize_fp8(const void *k_src, const void *v_src, uint8_t *k_cache, uint
 int pa_e4m3_encode(const float *x, uint8_t *codes, int64_t n, void *stream);
 
 /*
- * Bytes of device workspace pa_decode / pa_decode_fp8 need for these sizes:
- * the per-partition partial results that the log-sum-exp merge combines.
- * 0 when no sequence can span more than one partition.  Returns 0 for
- * invalid sizes too (pa_decode then reports the argument error).
+ * Number of CTAs pa_decode divides a batch among when split_ctas is 0: two
+ * per SM of the current device, the count that is resident at once.
  */
-size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
-                                int partition_tokens);
+int pa_decode_default_splits(void);
 
 /*
- * A partition size (tokens, a multiple of 16) that gives this device enough
- * independent work, from what the host scheduler knows: the batch size, kv
- * heads, the sum of context lengths and their maximum.
+ * Bytes of device workspace pa_decode / pa_decode_fp8 need: room for the
+ * partial results of the context partitions that cross CTA boundaries (at
+ * most two per CTA) and one counter per (sequence, kv head).  split_ctas 0
+ * means pa_decode_default_splits() of the current device; 1 needs no
+ * workspace (0 is returned).
+ *
+ * The caller allocates the workspace and must zero-fill it once before its
+ * first use; every call that completes leaves the counters at zero again,
+ * so the same workspace serves call after call.  After a call whose status
+ * reports PA_ERR_TIMEOUT, zero it again.  Calls that share a workspace must
+ * not overlap on the device.
  */
-int pa_decode_pick_partition(int num_seqs, int num_kv_heads, int64_t total_context_tokens,
-                             int max_context_len);
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int split_ctas);
 
 /*
  * Paged GQA decode over a 16-bit pool.  For every sequence b and q head hq,
  *   out[b][hq][:] = sum_t softmax_t(scale * q[b][hq] . K_t) * V_t
  * over the context_lens[b] tokens of b, token t read from physical block
  * block_tables[b][t / block_size], row t % block_size, kv head
- * hq / (num_q_heads / num_kv_heads).  Context tokens are split into
- * partitions of partition_tokens; each is reduced with an online softmax in
- * fp32 and, where a sequence spans several, a second kernel merges them by
- * log-sum-exp.  out is rounded to dtype (round to nearest even).  A sequence
- * with context_len 0 gets a zero output.
+ * hq / (num_q_heads / num_kv_heads).  out is rounded to dtype (round to
+ * nearest even); a sequence with context_len 0 gets a zero output.
+ *
+ * The batch's (sequence, kv head, block) units are divided evenly among
+ * split_ctas CTAs (0: pa_decode_default_splits()).  A CTA's share of one
+ * sequence is a context partition, reduced with an online softmax in fp32;
+ * a sequence split across CTAs has its partitions merged by log-sum-exp in
+ * the same launch.  Results do not depend on split_ctas beyond fp32
+ * rounding, and a given split_ctas is deterministic.
  *   max_context_len: host-side upper bound of context_lens (no device read);
- *   partition_tokens: a multiple of 16 in [16, 16384];
- *   workspace: at least pa_decode_workspace_size(...) bytes (may be NULL when
- *   that is 0).
+ *   workspace: at least pa_decode_workspace_size(...) bytes, 256-byte
+ *   aligned, zero-filled before first use (may be NULL when that size is 0).
  * Source: rvLLM, CUDA Kernels table, "PagedAttention V2" (block-table
  * indirection, online softmax); LLM Serving Kernels, Projects table, row 04;
  * rvllm (small engine), How it's put together (GQA, read_blocks).
@@ -168,7 +175,7 @@ int pa_decode_pick_partition(int num_seqs, int num_kv_heads, int64_t total_conte
 int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
               const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
               int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-              int block_size, int num_blocks, float scale, int dtype, int partition_tokens,
+              int block_size, int num_blocks, float scale, int dtype, int split_ctas,
               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -182,7 +189,7 @@ int pa_decode_fp8(void *out, const void *q, const uint8_t *k_cache, const uint8_
                   const float *k_scale, const float *v_scale, const int32_t *block_tables,
                   int max_blocks_per_seq, const int32_t *context_lens, int max_context_len,
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                  int num_blocks, float scale, int partition_tokens, void *workspace,
+                  int num_blocks, float scale, int split_ctas, void *workspace,
                   size_t workspace_bytes, void *stream);
 
 /*

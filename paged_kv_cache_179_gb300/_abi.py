@@ -31,8 +31,8 @@ SIGNATURES = {
                             _i32),
     "pa_quantize_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
     "pa_e4m3_encode": ([_vp, _vp, _i64, _vp], _i32),
-    "pa_decode_workspace_size": ([_i32, _i32, _i32, _i32, _i32], _sz),
-    "pa_decode_pick_partition": ([_i32, _i32, _i64, _i32], _i32),
+    "pa_decode_workspace_size": ([_i32, _i32, _i32, _i32], _sz),
+    "pa_decode_default_splits": ([], _i32),
     "pa_decode": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                    _f32, _i32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
@@ -185,21 +185,18 @@ def pa_e4m3_encode(x, codes) -> None:
            "pa_e4m3_encode")
 
 
-def pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len,
-                             partition_tokens) -> int:
-    return int(load().pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len,
-                                               partition_tokens))
+def pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, split_ctas=0) -> int:
+    return int(load().pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, split_ctas))
 
 
-def pa_decode_pick_partition(num_seqs, num_kv_heads, total_context_tokens, max_context_len) -> int:
-    return int(load().pa_decode_pick_partition(num_seqs, num_kv_heads, int(total_context_tokens),
-                                               max_context_len))
+def pa_decode_default_splits() -> int:
+    return int(load().pa_decode_default_splits())
 
 
-def alloc_workspace(num_seqs, num_q_heads, head_dim, max_context_len, partition_tokens, device):
-    """Caller-owned workspace for pa_decode (None when the sizes need none)."""
-    n = pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len, partition_tokens)
-    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+def alloc_workspace(num_seqs, num_q_heads, head_dim, split_ctas, device):
+    """Caller-owned, zero-filled workspace for pa_decode (None when the sizes need none)."""
+    n = pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, split_ctas)
+    return torch.zeros(n, dtype=torch.uint8, device=device) if n else None
 
 
 def _decode_common(out, q, block_tables, context_lens, dev):
@@ -212,7 +209,7 @@ def _decode_common(out, q, block_tables, context_lens, dev):
 
 
 def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
-              scale: float, partition_tokens: int, workspace=None) -> None:
+              scale: float, split_ctas: int = 0, workspace=None) -> None:
     """out[b][hq] = softmax(scale q.K) V over each sequence's blocks (16-bit pools)."""
     dev = q.device
     act = (torch.float16, torch.bfloat16)
@@ -229,12 +226,12 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_
     _check(load().pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                             block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq,
                             Hkv, D, bs, NB, float(scale), _act_code(q.dtype),
-                            int(partition_tokens), _ptr(workspace), ws_bytes, _stream(dev)),
+                            int(split_ctas), _ptr(workspace), ws_bytes, _stream(dev)),
            "pa_decode")
 
 
 def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
-                  max_context_len: int, scale: float, partition_tokens: int,
+                  max_context_len: int, scale: float, split_ctas: int = 0,
                   workspace=None) -> None:
     """As pa_decode over E4M3 pools with per-(block, kv head) fp32 scales; q/out fp16."""
     dev = q.device
@@ -253,7 +250,7 @@ def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, cont
     _check(load().pa_decode_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                 _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
                                 _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
-                                float(scale), int(partition_tokens), _ptr(workspace), ws_bytes,
+                                float(scale), int(split_ctas), _ptr(workspace), ws_bytes,
                                 _stream(dev)), "pa_decode_fp8")
 
 

@@ -52,14 +52,14 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
 
 struct DecodeShape {
-  int B, Hq, Hkv, D, bs, NB, mbs, max_ctx, part;
+  int B, Hq, Hkv, D, bs, NB, mbs, max_ctx, splits;
 };
 
 int check_decode_shape(const DecodeShape& s, float scale) {
   if (s.B < 0 || s.Hq <= 0 || s.Hkv <= 0 || s.Hq % s.Hkv != 0) return PA_ERR_INVALID_ARG;
   if (s.NB <= 0 || s.mbs <= 0 || s.max_ctx < 0) return PA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(s.max_ctx) > static_cast<int64_t>(s.mbs) * s.bs) return PA_ERR_INVALID_ARG;
-  if (s.part < 16 || s.part > 16384 || s.part % 16 != 0) return PA_ERR_INVALID_ARG;
+  if (s.splits < 0) return PA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
   if (s.D != 64 && s.D != 128) return PA_ERR_UNSUPPORTED;
   if (s.bs != 16) return PA_ERR_UNSUPPORTED;
@@ -68,38 +68,52 @@ int check_decode_shape(const DecodeShape& s, float scale) {
   return PA_OK;
 }
 
-int run_decode(const DecodeShape& s, void* out, const void* q, const void* k, const void* v,
+int run_decode(DecodeShape s, void* out, const void* q, const void* k, const void* v,
                const float* ks, const float* vs, const int32_t* bt, const int32_t* cl,
                float scale, bool fp8, bool bf16, void* ws, size_t ws_bytes, void* stream) {
   if (s.B == 0) return PA_OK;
-  const size_t need = decode_workspace_bytes(s.B, s.Hq, s.D, s.max_ctx, s.part);
-  if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned(ws, 256))) return PA_ERR_WORKSPACE;
+  auto ws_ok = [&]() {
+    const size_t need = decode_workspace_bytes(s.B, s.Hq, s.D, s.splits);
+    return s.splits <= 1 || (ws != nullptr && ws_bytes >= need && aligned(ws, 256));
+  };
+  if (s.splits > 0 && !ws_ok()) return PA_ERR_WORKSPACE;   // checked before touching CUDA
   DeviceState* dev = nullptr;
   if (int rc = device_state(&dev)) return rc;
+  if (s.splits == 0) {
+    s.splits = decode_default_ctas();
+    if (!ws_ok()) return PA_ERR_WORKSPACE;
+  }
   DecodeArgs a{};
-  a.out = out;
-  a.q = q;
   a.k_cache = k;
   a.v_cache = v;
   a.k_scale = ks;
   a.v_scale = vs;
-  a.block_tables = bt;
-  a.context_lens = cl;
   a.status = dev->status;
   a.mbs = s.mbs;
-  a.B = s.B;
   a.Hq = s.Hq;
   a.Hkv = s.Hkv;
   a.group = s.Hq / s.Hkv;
   a.D = s.D;
   a.num_blocks = s.NB;
   a.max_context_len = s.max_ctx;
-  a.part_tokens = s.part;
-  const int64_t parts = (static_cast<int64_t>(s.max_ctx) + s.part - 1) / s.part;
-  a.max_parts = static_cast<int>(parts < 1 ? 1 : parts);
+  a.split_ctas = s.splits;
   a.scale_log2 = scale * 1.4426950408889634f;
-  if (need > 0) decode_workspace_split(a, ws, &a.ws_acc, &a.ws_ml);
-  return cuda_status(launch_decode(a, fp8, bf16, static_cast<cudaStream_t>(stream)));
+  // Batches above kMaxBatchPerLaunch run as consecutive launches on the
+  // stream; each reuses the workspace (its counters are back to zero when
+  // a launch ends).
+  const size_t out_row = static_cast<size_t>(s.Hq) * s.D * 2;   // q and out are 16-bit
+  for (int b0 = 0; b0 < s.B; b0 += kMaxBatchPerLaunch) {
+    DecodeArgs c = a;
+    c.B = s.B - b0 < kMaxBatchPerLaunch ? s.B - b0 : kMaxBatchPerLaunch;
+    c.out = static_cast<uint8_t*>(out) + b0 * out_row;
+    c.q = static_cast<const uint8_t*>(q) + b0 * out_row;
+    c.block_tables = bt + static_cast<int64_t>(b0) * s.mbs;
+    c.context_lens = cl + b0;
+    if (s.splits > 1) decode_workspace_split(c, ws, &c.ws_acc, &c.ws_ml, &c.counters);
+    if (cudaError_t e = launch_decode(c, fp8, bf16, static_cast<cudaStream_t>(stream)))
+      return cuda_status(e);
+  }
+  return PA_OK;
 }
 
 }  // namespace
@@ -215,42 +229,26 @@ int pa_e4m3_encode(const float* x, uint8_t* codes, int64_t n, void* stream) {
   return cuda_status(launch_e4m3_encode(x, codes, n, static_cast<cudaStream_t>(stream)));
 }
 
-size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
-                                int partition_tokens) {
-  if (partition_tokens < 16 || partition_tokens % 16 != 0) return 0;
-  return decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len,
-                                partition_tokens);
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int split_ctas) {
+  if (split_ctas < 0) return 0;
+  if (split_ctas == 0) split_ctas = decode_default_ctas();
+  if (split_ctas <= 1) return 0;
+  return decode_workspace_bytes(num_seqs, num_q_heads, head_dim, split_ctas);
 }
 
-int pa_decode_pick_partition(int num_seqs, int num_kv_heads, int64_t total_context_tokens,
-                             int max_context_len) {
-  // Aim at ~16 partitions per SM (two resident CTAs per SM, eight waves),
-  // with partitions of 128..4096 tokens in steps of 64.
-  (void)num_seqs;
-  (void)max_context_len;
-  int sms = 148;
-  DeviceState* d = nullptr;
-  if (device_state(&d) == PA_OK) sms = d->sm_count;
-  const int64_t target = static_cast<int64_t>(sms) * 16;
-  int64_t work = total_context_tokens * (num_kv_heads > 0 ? num_kv_heads : 1);
-  int64_t p = (work + target - 1) / target;
-  p = ((p + 63) / 64) * 64;
-  if (p < 128) p = 128;
-  if (p > 4096) p = 4096;
-  return static_cast<int>(p);
-}
+int pa_decode_default_splits(void) { return decode_default_ctas(); }
 
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
               int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-              int block_size, int num_blocks, float scale, int dtype, int partition_tokens,
+              int block_size, int num_blocks, float scale, int dtype, int split_ctas,
               void* workspace, size_t workspace_bytes, void* stream) {
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
     return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
   const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                      num_blocks, max_blocks_per_seq, max_context_len, partition_tokens};
+                      num_blocks, max_blocks_per_seq, max_context_len, split_ctas};
   if (int rc = check_decode_shape(s, scale)) return rc;
   for (const void* p : {static_cast<const void*>(out), q, k_cache, v_cache})
     if (!aligned(p, 16)) return PA_ERR_INVALID_ARG;
@@ -263,14 +261,14 @@ int pa_decode_fp8(void* out, const void* q, const uint8_t* k_cache, const uint8_
                   const float* k_scale, const float* v_scale, const int32_t* block_tables,
                   int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                  int num_blocks, float scale, int partition_tokens, void* workspace,
+                  int num_blocks, float scale, int split_ctas, void* workspace,
                   size_t workspace_bytes, void* stream) {
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables ||
       !context_lens)
     return PA_ERR_INVALID_ARG;
   const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                      num_blocks, max_blocks_per_seq, max_context_len, partition_tokens};
+                      num_blocks, max_blocks_per_seq, max_context_len, split_ctas};
   if (int rc = check_decode_shape(s, scale)) return rc;
   for (const void* p : {static_cast<const void*>(out), q, static_cast<const void*>(k_cache),
                         static_cast<const void*>(v_cache)})

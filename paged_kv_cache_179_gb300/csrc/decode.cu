@@ -1,5 +1,5 @@
-// decode.cu -- K3/K4: split-K paged GQA decode (16-bit and E4M3 pools) and
-// K5: the log-sum-exp merge of partitions.
+// decode.cu -- K3/K4: split-K paged GQA decode (16-bit and E4M3 pools) with
+// K5, the log-sum-exp merge of partitions, fused into the same kernel.
 //
 // What is computed ("rvLLM: High-performance LLM inference in Rust", CUDA
 // Kernels table, "PagedAttention V2": attention with block-table
@@ -12,25 +12,35 @@
 //   kv head hq / group.
 //
 // Design (sm_103a, one GB300):
-//  * One CTA = one (sequence, kv head, context partition).  It serves the
-//    whole query group, so every K/V byte is read from HBM once.
-//  * Four warps split the partition's blocks round-robin.  Each warp owns a
-//    private ring of STAGES shared-memory slots; lane 0 fetches one (block,
-//    kv head) K tile and V tile per slot with two bulk asynchronous copies
-//    (the TMA engine, cp.async.bulk) that complete on the slot's mbarrier.
-//    No cross-warp synchronisation inside the main loop.
-//  * Per 16-token block the warp computes S^T = K Q^T (16 tokens x 8 query
-//    heads) and O^T += V^T P^T (head_dim x 8) with mma.sync m16n8k16,
-//    fp32 accumulation.  The query group (<= 8 heads) is the N=8 side, so no
-//    tensor-core row is wasted on padding beyond G < 8.  The online softmax
-//    runs on the S fragments (max across lanes with shuffles, exp2 on the
-//    SFU); P goes from accumulator to operand layout with movmatrix.
-//    For E4M3 pools the codes are widened to f16 in registers (exact) right
-//    before the MMA; the page scales are folded into the score scale (K) and
-//    into P (V).
-//  * The warps' partial (max, sum, acc) are combined in shared memory; a
-//    sequence with one partition writes its output directly, otherwise the
-//    partial goes to the workspace and merge_kernel combines partitions.
+//  * The batch is one stream of (sequence, kv head, 16-token block) units.
+//    The grid is persistent (two CTAs per SM by default) and CTA c takes an
+//    equal contiguous share of the stream, so every CTA moves the same number
+//    of bytes whatever the spread of context lengths.  Its share of one
+//    (sequence, kv head) is that sequence's context partition for this CTA:
+//    a short sequence lies inside one CTA and is attended whole, a long one
+//    is split across consecutive CTAs (split-K) and merged by log-sum-exp.
+//    Each CTA serves a whole query group per kv head, so every K/V byte is
+//    read from HBM once.
+//  * Four warps split each 128-block chunk of the share round-robin.  Each
+//    warp owns a ring of STAGES shared-memory slots; lane 0 fills a slot with
+//    the K tile and V tile of one (block, kv head) by two bulk asynchronous
+//    copies (the TMA engine, cp.async.bulk) that complete on the slot's
+//    mbarrier.  The ring runs ahead across chunk and partition boundaries.
+//    Block ids (and E4M3 page scales) are prefetched into registers, one per
+//    lane, two chunks ahead; the next partition's query is prefetched too.
+//  * Per block the warp computes S^T = K Q^T (16 tokens x 8 query heads) and
+//    O^T += V^T P^T (head_dim x 8) with mma.sync m16n8k16 in fp32.  The query
+//    group (<= 8 heads) is the N=8 side.  The online softmax runs on the S
+//    fragments (row max with shuffles, exp2 on the SFU); P moves from
+//    accumulator to operand layout with movmatrix.  E4M3 codes are widened
+//    to f16 in registers (exact) just before the MMA; the page scales fold
+//    into the score scale (K) and into P (V).
+//  * Partition epilogue: the four warps' (max, sum, acc) combine in shared
+//    memory.  A whole sequence writes its output directly.  A split one
+//    writes a partial (at most two per CTA: its first and last partition)
+//    and counts it on a per-(sequence, kv head) counter; at its end, the CTA
+//    whose count completed a sequence merges that sequence's partials and
+//    resets the counter to zero.  No thread ever waits for another CTA.
 //
 // Bounds: block ids outside [0, num_blocks) and context lengths above their
 // bounds are never dereferenced; they set a status bit.  Every mbarrier wait
@@ -46,23 +56,38 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kGroupMax = 8;          // query heads per kv head served by one MMA N=8 tile
-constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kGroupMax = 8;     // query heads per kv head served by one MMA N=8 tile
+constexpr int kCtasPerSm = 2;    // resident CTAs per SM the shared-memory budget is sized for
 // E4M3 path: P * v_scale is scaled by 2^8 before rounding to f16 so small
 // weights stay in f16's normal range; the fp32 result is scaled back.  With
 // fp16-sourced pools v_scale <= 65504/448, so P' <= 146.3 * 256 < 65504.
 constexpr float kPBoost = 256.f;
 
-template <int D, bool FP8>
+template <int D, bool FP8, int STAGES>
 struct Tile {
   static constexpr int ROW = FP8 ? D : 2 * D;   // bytes of one token row of one kv head
   static constexpr int BYTES = 16 * ROW;        // one (block, kv head) tile
-  static constexpr int STAGES = FP8 ? 4 : 3;    // ring slots per warp
   static constexpr int SLOT = 2 * BYTES;        // K tile + V tile
   static constexpr int RING = kWarps * STAGES * SLOT;
-  static constexpr int MERGE = kWarps * kGroupMax * (D + 2) * 4;
-  static_assert(MERGE <= RING, "merge area must fit in the ring");
 };
+
+__host__ __device__ constexpr int round16(int x) { return (x + 15) & ~15; }
+
+// Dynamic shared-memory layout; the host sizes the launch with the same function.
+struct Layout {
+  int merge, sbar, pf, len, misc, total;
+};
+__host__ __device__ inline Layout make_layout(int ring, int D, int stages, int B) {
+  Layout l{};
+  int o = ring;
+  l.merge = o; o += round16(kWarps * kGroupMax * (D + 2) * 4);
+  l.sbar = o;  o += round16(kWarps * stages * 8);
+  l.pf = o;    o += round16((B + 1) * 4);
+  l.len = o;   o += round16(B * 4);
+  l.misc = o;  o += 64;
+  l.total = o;
+  return l;
+}
 
 // d index of the O^T fragment rows (m-tile i, lane row r): low (row r) and
 // high (row r + 8) halves.  Chosen so each lane's V reads are one or two
@@ -96,15 +121,15 @@ template <int D, bool FP8, bool BF16>
 __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf)[D / 16][2],
                                              uint32_t kt, uint32_t vt, int n_valid, float sl2,
                                              float v_mul, int r, int c) {
-  using TL = Tile<D, FP8>;
+  constexpr int ROW = FP8 ? D : 2 * D;
   // ---- S^T = K Q^T : 16 tokens x 8 query heads, k = head_dim
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   if constexpr (!FP8) {
     // lane (r, c) reads 16-byte chunk 4i+c of rows r and r+8: d = 32i + 8c + 0..7
 #pragma unroll
     for (int i = 0; i < D / 32; ++i) {
-      const uint4 ka = lds128(kt + r * TL::ROW + (4 * i + c) * 16);
-      const uint4 kb = lds128(kt + (r + 8) * TL::ROW + (4 * i + c) * 16);
+      const uint4 ka = lds128(kt + r * ROW + (4 * i + c) * 16);
+      const uint4 kb = lds128(kt + (r + 8) * ROW + (4 * i + c) * 16);
       mma16816<BF16>(acc, ka.x, kb.x, ka.y, kb.y, qf[2 * i][0], qf[2 * i][1]);
       mma16816<BF16>(acc, ka.z, kb.z, ka.w, kb.w, qf[2 * i + 1][0], qf[2 * i + 1][1]);
     }
@@ -112,8 +137,8 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
     // lane (r, c) reads 16 codes at byte 64i + 16c of rows r and r+8
 #pragma unroll
     for (int i = 0; i < D / 64; ++i) {
-      const uint4 ka = lds128(kt + r * TL::ROW + 64 * i + 16 * c);
-      const uint4 kb = lds128(kt + (r + 8) * TL::ROW + 64 * i + 16 * c);
+      const uint4 ka = lds128(kt + r * ROW + 64 * i + 16 * c);
+      const uint4 kb = lds128(kt + (r + 8) * ROW + 64 * i + 16 * c);
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         const uint32_t wa = word(ka, q4), wb = word(kb, q4);
@@ -160,10 +185,10 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
     uint4 v[4][U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      v[0][u] = lds128(vt + tk0 * TL::ROW + (8 * u + r) * 16);
-      v[1][u] = lds128(vt + tk1 * TL::ROW + (8 * u + r) * 16);
-      v[2][u] = lds128(vt + tk2 * TL::ROW + (8 * u + r) * 16);
-      v[3][u] = lds128(vt + tk3 * TL::ROW + (8 * u + r) * 16);
+      v[0][u] = lds128(vt + tk0 * ROW + (8 * u + r) * 16);
+      v[1][u] = lds128(vt + tk1 * ROW + (8 * u + r) * 16);
+      v[2][u] = lds128(vt + tk2 * ROW + (8 * u + r) * 16);
+      v[3][u] = lds128(vt + tk3 * ROW + (8 * u + r) * 16);
     }
     if (n_valid < 16) {   // rows past the context may hold anything, NaN included
       const uint4 z = make_uint4(0, 0, 0, 0);
@@ -192,15 +217,15 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
     constexpr int VB = D / 8;   // bytes per lane per token row: 16 (D=128) or 8 (D=64)
     VT v[4];
     if constexpr (D == 128) {
-      v[0] = lds128(vt + tk0 * TL::ROW + VB * r);
-      v[1] = lds128(vt + tk1 * TL::ROW + VB * r);
-      v[2] = lds128(vt + tk2 * TL::ROW + VB * r);
-      v[3] = lds128(vt + tk3 * TL::ROW + VB * r);
+      v[0] = lds128(vt + tk0 * ROW + VB * r);
+      v[1] = lds128(vt + tk1 * ROW + VB * r);
+      v[2] = lds128(vt + tk2 * ROW + VB * r);
+      v[3] = lds128(vt + tk3 * ROW + VB * r);
     } else {
-      v[0] = lds64(vt + tk0 * TL::ROW + VB * r);
-      v[1] = lds64(vt + tk1 * TL::ROW + VB * r);
-      v[2] = lds64(vt + tk2 * TL::ROW + VB * r);
-      v[3] = lds64(vt + tk3 * TL::ROW + VB * r);
+      v[0] = lds64(vt + tk0 * ROW + VB * r);
+      v[1] = lds64(vt + tk1 * ROW + VB * r);
+      v[2] = lds64(vt + tk2 * ROW + VB * r);
+      v[3] = lds64(vt + tk3 * ROW + VB * r);
     }
     if (n_valid < 16) {
       VT z{};
@@ -238,293 +263,553 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
 }
 
-template <int D, bool FP8, bool BF16>
+// ------------------------------------------------------------ work split
+// The batch is a stream of 16-token blocks ordered (sequence, kv head,
+// block): segment (b, h) holds the ceil(L_b / 16) blocks of sequence b for
+// kv head h, and starts at pf[b] + h * nblk_b where pf is the exclusive
+// prefix sum of Hkv * nblk_b.  CTA c of G takes blocks [c*W/G, (c+1)*W/G)
+// of the W in the batch: its share of a segment is one context partition
+// ("piece").  A segment inside one CTA's range is attended whole; one that
+// crosses ranges is split into pieces whose partial results are merged.
+// Each CTA walks its range in chunks of at most kChunk blocks (one block
+// id per lane and warp).
+constexpr int kChunk = 32 * kWarps;
+
+struct Chunk {
+  int b, h;     // segment
+  int cb0;      // first block of the chunk within the segment
+  int nb;       // blocks in the chunk (0: past the end of the CTA's range)
+};
+
+__device__ __forceinline__ int seg_blocks(const int* pf, int b, int Hkv) {
+  return (pf[b + 1] - pf[b]) / Hkv;
+}
+__device__ __forceinline__ int64_t cta_lo(int64_t c, int64_t W, int64_t G) { return c * W / G; }
+// The CTA whose range holds block x.
+__device__ __forceinline__ int cta_of(int64_t x, int64_t W, int64_t G) {
+  return static_cast<int>(((x + 1) * G - 1) / W);
+}
+
+__device__ __forceinline__ Chunk first_chunk(int64_t lo, int64_t hi, const int* pf, int B,
+                                             int Hkv) {
+  Chunk x{0, 0, 0, 0};
+  if (lo >= hi) return x;
+  int l = 0, r = B;                        // pf[l] <= lo < pf[r]
+  while (r - l > 1) {
+    const int mid = (l + r) >> 1;
+    if (pf[mid] <= lo) l = mid;
+    else r = mid;
+  }
+  const int nbk = seg_blocks(pf, l, Hkv);
+  x.b = l;
+  x.h = static_cast<int>((lo - pf[l]) / nbk);
+  const int64_t s0 = pf[l] + static_cast<int64_t>(x.h) * nbk;
+  x.cb0 = static_cast<int>(lo - s0);
+  x.nb = static_cast<int>(min(static_cast<int64_t>(kChunk), min(hi, s0 + nbk) - lo));
+  return x;
+}
+
+__device__ __forceinline__ Chunk next_chunk(const Chunk& x, int64_t hi, const int* pf, int B,
+                                            int Hkv) {
+  Chunk y{0, 0, 0, 0};
+  if (x.nb == 0) return y;
+  int nbk = seg_blocks(pf, x.b, Hkv);
+  int64_t s0 = pf[x.b] + static_cast<int64_t>(x.h) * nbk;
+  const int pend = static_cast<int>(min(hi, s0 + nbk) - s0);
+  const int n0 = x.cb0 + x.nb;
+  if (n0 < pend) return Chunk{x.b, x.h, n0, min(kChunk, pend - n0)};
+  int b = x.b, h = x.h + 1;
+  if (h == Hkv) {
+    h = 0;
+    ++b;
+    while (b < B && pf[b + 1] == pf[b]) ++b;
+  }
+  if (b >= B) return y;
+  nbk = seg_blocks(pf, b, Hkv);
+  s0 = pf[b] + static_cast<int64_t>(h) * nbk;
+  if (s0 >= hi) return y;
+  return Chunk{b, h, 0, static_cast<int>(min(static_cast<int64_t>(kChunk), min(hi, s0 + nbk) - s0))};
+}
+
+__device__ __forceinline__ int chunk_warp_blocks(const Chunk& x, int warp) {
+  return x.nb > warp ? (x.nb - warp + kWarps - 1) / kWarps : 0;
+}
+
+// This lane's block id of chunk x (lane t holds block cb0 + warp + 4t).
+__device__ __forceinline__ int load_chunk_id(const DecodeArgs& a, const Chunk& x, int warp,
+                                             int lane) {
+  if (warp + kWarps * lane >= x.nb) return -1;
+  return __ldg(a.block_tables + static_cast<int64_t>(x.b) * a.mbs + x.cb0 + warp + kWarps * lane);
+}
+
+template <int D, bool FP8>
+__device__ __forceinline__ void load_query(uint32_t (&qf)[D / 16][2], const DecodeArgs& a, int b,
+                                           int h, int r, int c) {
+  const uint4* qrow = reinterpret_cast<const uint4*>(
+      static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(b) * a.Hq + h * a.group + r) * D);
+  const bool live = r < a.group;
+  if constexpr (!FP8) {
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) {
+      const uint4 v = live ? __ldg(qrow + 4 * i + c) : make_uint4(0, 0, 0, 0);
+      qf[2 * i][0] = v.x;
+      qf[2 * i][1] = v.y;
+      qf[2 * i + 1][0] = v.z;
+      qf[2 * i + 1][1] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < D / 64; ++i) {
+      const uint4 lo = live ? __ldg(qrow + 8 * i + 2 * c) : make_uint4(0, 0, 0, 0);
+      const uint4 hi = live ? __ldg(qrow + 8 * i + 2 * c + 1) : make_uint4(0, 0, 0, 0);
+      qf[4 * i + 0][0] = lo.x; qf[4 * i + 0][1] = lo.y;
+      qf[4 * i + 1][0] = lo.z; qf[4 * i + 1][1] = lo.w;
+      qf[4 * i + 2][0] = hi.x; qf[4 * i + 2][1] = hi.y;
+      qf[4 * i + 3][0] = hi.z; qf[4 * i + 3][1] = hi.w;
+    }
+  }
+}
+
+// Partial-result row of (CTA c, piece slot k, query head g): slot 0 is the
+// CTA's first piece, slot 1 its last.
+__device__ __forceinline__ int64_t piece_row(int c, int k, int g) {
+  return (static_cast<int64_t>(c) * 2 + k) * kGroupMax + g;
+}
+
+template <int D, bool FP8, bool BF16, int STAGES>
 __global__ void __launch_bounds__(kThreads)
 decode_kernel(const DecodeArgs a) {
-  using TL = Tile<D, FP8>;
+  using TL = Tile<D, FP8, STAGES>;
   using OutT = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TL::RING);
-  int* s_ids = reinterpret_cast<int*>(smem + TL::RING + kWarps * TL::STAGES * 8);
-  const int max_blk = a.part_tokens / 16;
-  float* s_ks = reinterpret_cast<float*>(s_ids + max_blk);
-  float* s_vs = s_ks + max_blk;
-
-  const int p = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, c = lane & 3;
-  const int G = a.group;
-  OutT* out_rows = static_cast<OutT*>(a.out) + (static_cast<int64_t>(b) * a.Hq + h * G) * D;
+  const int B = a.B, Hkv = a.Hkv, Hq = a.Hq, G = a.group;
+  const Layout lay = make_layout(TL::RING, D, STAGES, B);
+  int* pf = reinterpret_cast<int*>(smem + lay.pf);
+  int* len = reinterpret_cast<int*>(smem + lay.len);
+  int* misc = reinterpret_cast<int*>(smem + lay.misc);   // [0..3] warp sums, [4..7] merge job
+  float* mo = reinterpret_cast<float*>(smem + lay.merge);  // [warp][g][D]
+  float* mm = mo + kWarps * kGroupMax * D;                  // [warp][g]
+  float* ml = mm + kWarps * kGroupMax;                      // [warp][g]
 
-  const int L = a.context_lens[b];
-  if (L < 0 || L > a.max_context_len || L > a.mbs * 16) {
-    if (p == 0) {
-      if (tid == 0) atomicOr(a.status, kStatusBadLen);
-      for (int i = tid; i < G * D; i += kThreads) out_rows[i] = from_f32<OutT>(0.f);
-    }
-    return;
-  }
-  if (L == 0) {
-    if (p == 0)
-      for (int i = tid; i < G * D; i += kThreads) out_rows[i] = from_f32<OutT>(0.f);
-    return;
-  }
-  const int nparts = (L + a.part_tokens - 1) / a.part_tokens;
-  if (p >= nparts) return;
-  const int tok0 = p * a.part_tokens;
-  const int ntok = min(a.part_tokens, L - tok0);
-  const int nblk = (ntok + 15) / 16;
-  const int blk0 = tok0 / 16;
-
-  // ---- query fragments (B operand of S^T = K Q^T): row g = r of the group
-  uint32_t qf[D / 16][2];
+  // ---- 1. blocks per sequence and their prefix sum (segments of Hkv * nblk)
   {
-    const uint4* qrow = reinterpret_cast<const uint4*>(
-        static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(b) * a.Hq + h * G + r) * D);
-    const bool live = r < G;
-    if constexpr (!FP8) {
-#pragma unroll
-      for (int i = 0; i < D / 32; ++i) {
-        const uint4 v = live ? __ldg(qrow + 4 * i + c) : make_uint4(0, 0, 0, 0);
-        qf[2 * i][0] = v.x;
-        qf[2 * i][1] = v.y;
-        qf[2 * i + 1][0] = v.z;
-        qf[2 * i + 1][1] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < D / 64; ++i) {
-        const uint4 lo = live ? __ldg(qrow + 8 * i + 2 * c) : make_uint4(0, 0, 0, 0);
-        const uint4 hi = live ? __ldg(qrow + 8 * i + 2 * c + 1) : make_uint4(0, 0, 0, 0);
-        qf[4 * i + 0][0] = lo.x; qf[4 * i + 0][1] = lo.y;
-        qf[4 * i + 1][0] = lo.z; qf[4 * i + 1][1] = lo.w;
-        qf[4 * i + 2][0] = hi.x; qf[4 * i + 2][1] = hi.y;
-        qf[4 * i + 3][0] = hi.z; qf[4 * i + 3][1] = hi.w;
-      }
+    const int per = (B + kThreads - 1) / kThreads;
+    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int L = a.context_lens[b];
+      const bool ok = L >= 0 && L <= a.max_context_len && L <= a.mbs * 16;
+      len[b] = ok ? L : -1;
+      sum += ok ? ((L + 15) >> 4) * Hkv : 0;
     }
+    int inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    if (lane == 31) misc[warp] = inc;
+    __syncthreads();
+    int ex = inc - sum;
+    for (int w = 0; w < warp; ++w) ex += misc[w];
+    for (int b = b0; b < b1; ++b) {
+      pf[b] = ex;
+      ex += len[b] > 0 ? ((len[b] + 15) >> 4) * Hkv : 0;
+    }
+    if (tid == kThreads - 1) pf[B] = ex;
+    __syncthreads();
   }
+  const int64_t W = pf[B];
+  // Never split across more CTAs than there are blocks: every CTA that takes
+  // part then owns at least one block, which the piece bookkeeping relies on.
+  const int64_t NG = min(static_cast<int64_t>(gridDim.x), W);
+  const int cta = blockIdx.x;
 
-  // ---- this partition's block ids (and page scales) into shared memory
-  const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.mbs + blk0;
-  for (int i = tid; i < nblk; i += kThreads) {
-    int id = bt[i];
-    if (id < 0 || id >= a.num_blocks) {
-      atomicOr(a.status, kStatusBadBlock);
-      id = -1;
-    }
-    s_ids[i] = id;
-    if constexpr (FP8) {
-      const int64_t tile = static_cast<int64_t>(id) * a.Hkv + h;
-      s_ks[i] = id >= 0 ? a.k_scale[tile] : 0.f;
-      s_vs[i] = id >= 0 ? a.v_scale[tile] : 0.f;
-    }
+  // ---- 2. sequences with nothing to attend get a zero output
+  for (int b = cta; b < B; b += gridDim.x) {
+    const int L = len[b];
+    if (L > 0) continue;
+    if (L < 0 && tid == 0) atomicOr(a.status, kStatusBadLen);
+    OutT* o = static_cast<OutT*>(a.out) + static_cast<int64_t>(b) * Hq * D;
+    for (int i = tid; i < Hq * D; i += kThreads) o[i] = from_f32<OutT>(0.f);
   }
-  const uint32_t ring = smem_u32(smem) + warp * TL::STAGES * TL::SLOT;
-  const uint32_t wbar = smem_u32(bars) + warp * TL::STAGES * 8;
+  if (cta >= NG) return;
+  const int64_t lo = cta_lo(cta, W, NG), hi = cta_lo(cta + 1, W, NG);
+
+  // ---- 3. per-warp state
+  const uint32_t ring = smem_u32(smem) + warp * STAGES * TL::SLOT;
+  const uint32_t sbar = smem_u32(smem + lay.sbar) + warp * STAGES * 8;
   if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < TL::STAGES; ++s) mbar_init(wbar + 8 * s, 1);
+    for (int s = 0; s < STAGES; ++s) mbar_init(sbar + 8 * s, 1);
     mbar_init_fence();
   }
-  __syncthreads();
+  __syncwarp();
 
-  // ---- per-warp pipeline over blocks warp, warp + 4, ...
-  const int nb_w = warp < nblk ? (nblk - warp + kWarps - 1) / kWarps : 0;
+  // chunks k (being computed), k+1 and k+2, and this lane's block id in each
+  Chunk ch0 = first_chunk(lo, hi, pf, B, Hkv);
+  Chunk ch1 = next_chunk(ch0, hi, pf, B, Hkv);
+  Chunk ch2 = next_chunk(ch1, hi, pf, B, Hkv);
+  int id0 = load_chunk_id(a, ch0, warp, lane);
+  int id1 = load_chunk_id(a, ch1, warp, lane);
+  int id2 = load_chunk_id(a, ch2, warp, lane);
+  float ks0 = 1.f, vs0 = 1.f, ks1 = 1.f, vs1 = 1.f;   // E4M3 page scales of chunks k, k+1
+  if constexpr (FP8) {
+    if (id0 >= 0 && id0 < a.num_blocks) {
+      ks0 = __ldg(a.k_scale + static_cast<int64_t>(id0) * Hkv + ch0.h);
+      vs0 = __ldg(a.v_scale + static_cast<int64_t>(id0) * Hkv + ch0.h);
+    }
+    if (id1 >= 0 && id1 < a.num_blocks) {
+      ks1 = __ldg(a.k_scale + static_cast<int64_t>(id1) * Hkv + ch1.h);
+      vs1 = __ldg(a.v_scale + static_cast<int64_t>(id1) * Hkv + ch1.h);
+    }
+  }
+  // query fragments of the current piece and of the next one
+  uint32_t qf[D / 16][2], qn[D / 16][2];
+  load_query<D, FP8>(qf, a, ch0.b, ch0.h, r, c);
+  Chunk nxt_piece = ch0;
+  {
+    // first chunk of the following segment, if it is in range
+    int b = ch0.b, h = ch0.h + 1;
+    if (h == Hkv) {
+      h = 0;
+      ++b;
+      while (b < B && pf[b + 1] == pf[b]) ++b;
+    }
+    nxt_piece.nb = 0;
+    if (b < B && pf[b] + static_cast<int64_t>(h) * seg_blocks(pf, b, Hkv) < hi) {
+      nxt_piece = Chunk{b, h, 0, 1};
+      load_query<D, FP8>(qn, a, b, h, r, c);
+    }
+  }
+
   const uint8_t* kbase = static_cast<const uint8_t*>(a.k_cache);
   const uint8_t* vbase = static_cast<const uint8_t*>(a.v_cache);
   const uint64_t pol = l2_policy_evict_first();
-  auto issue = [&](int k) {   // lane 0 only
-    const int j = warp + k * kWarps;
-    const int s = k % TL::STAGES;
-    const uint32_t bar = wbar + 8 * s;
-    const int id = s_ids[j];
-    if (id >= 0) {
-      const int64_t off = (static_cast<int64_t>(id) * a.Hkv + h) * TL::BYTES;
-      mbar_arrive_expect_tx(bar, 2 * TL::BYTES);
-      bulk_g2s(ring + s * TL::SLOT, kbase + off, TL::BYTES, bar, pol);
-      bulk_g2s(ring + s * TL::SLOT + TL::BYTES, vbase + off, TL::BYTES, bar, pol);
-    } else {
-      mbar_arrive(bar);
+  bool dead = false;            // a wait timed out: stop touching the pipeline
+  int issued = 0, computed = 0;
+  int ic = 0, it = 0;           // fetch cursor: chunk k+ic (ic in {0,1}), this warp's block it
+
+  auto top_up = [&]() {
+    while (!dead && issued - computed < STAGES) {
+      const Chunk& x = ic == 0 ? ch0 : ch1;
+      if (x.nb == 0) return;
+      if (it >= chunk_warp_blocks(x, warp)) {
+        if (ic == 1) return;    // never more than one chunk ahead
+        ic = 1;
+        it = 0;
+        continue;
+      }
+      const int id = __shfl_sync(0xffffffffu, ic == 0 ? id0 : id1, it);
+      const int s = issued % STAGES;
+      const uint32_t bar = sbar + 8 * s;
+      if (lane == 0) {
+        if (id >= 0 && id < a.num_blocks) {
+          const int64_t tile = static_cast<int64_t>(id) * Hkv + x.h;
+          mbar_arrive_expect_tx(bar, 2 * TL::BYTES);
+          bulk_g2s(ring + s * TL::SLOT, kbase + tile * TL::BYTES, TL::BYTES, bar, pol);
+          bulk_g2s(ring + s * TL::SLOT + TL::BYTES, vbase + tile * TL::BYTES, TL::BYTES, bar,
+                   pol);
+        } else {
+          atomicOr(a.status, kStatusBadBlock);
+          mbar_arrive(bar);
+        }
+      }
+      ++issued;
+      ++it;
     }
   };
-  if (lane == 0)
-    for (int k = 0; k < min(TL::STAGES, nb_w); ++k) issue(k);
+  top_up();
 
   WarpAcc<D> st;
+  auto reset_acc = [&]() {
 #pragma unroll
-  for (int i = 0; i < D / 16; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
-  st.m0 = st.m1 = -INFINITY;
-  st.l0 = st.l1 = 0.f;
-  const float sl2_base = a.scale_log2;
+    for (int i = 0; i < D / 16; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
+    st.m0 = st.m1 = -INFINITY;
+    st.l0 = st.l1 = 0.f;
+  };
+  reset_acc();
 
-  for (int k = 0; k < nb_w; ++k) {
-    const int s = k % TL::STAGES;
-    const uint32_t parity = (k / TL::STAGES) & 1;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(wbar + 8 * s, parity));
-    if (!ok) {
-      // Report, then wait (bounded) for this warp's copies still in flight.
-      if (lane == 0) atomicOr(a.status, kStatusTimeout);
-      for (int kk = k + 1; kk < min(k + TL::STAGES, nb_w); ++kk)
-        (void)mbar_wait(wbar + 8 * (kk % TL::STAGES), (kk / TL::STAGES) & 1);
-      break;
-    }
-    const int j = warp + k * kWarps;
-    if (s_ids[j] >= 0) {
-      const int n_valid = min(16, ntok - j * 16);
-      float sl2 = sl2_base, v_mul = 1.f;
-      if constexpr (FP8) {
-        sl2 *= s_ks[j];
-        v_mul = s_vs[j] * kPBoost;
-      }
-      attend_block<D, FP8, BF16>(st, qf, ring + s * TL::SLOT, ring + s * TL::SLOT + TL::BYTES,
-                                 n_valid, sl2, v_mul, r, c);
-    }
-    __syncwarp();
-    if (lane == 0 && k + TL::STAGES < nb_w) issue(k + TL::STAGES);
-  }
-
-  // ---- combine the four warps, then write the output or the partition's partial
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, o);
-    st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, o);
-  }
-  __syncthreads();   // every warp is done with its ring: reuse it
-  float* mo = reinterpret_cast<float*>(smem);                 // [warp][g][D]
-  float* mm = mo + kWarps * kGroupMax * D;                    // [warp][g]
-  float* ml = mm + kWarps * kGroupMax;                        // [warp][g]
-  {
-    float* wo = mo + warp * kGroupMax * D;
-#pragma unroll
-    for (int i = 0; i < D / 16; ++i) {
-      const int dl = d_lo<D, FP8>(i, r), dh = d_hi<D, FP8>(i, r);
-      wo[(2 * c) * D + dl] = st.o[i][0];
-      wo[(2 * c + 1) * D + dl] = st.o[i][1];
-      wo[(2 * c) * D + dh] = st.o[i][2];
-      wo[(2 * c + 1) * D + dh] = st.o[i][3];
-    }
-    if (r == 0) {
-      mm[warp * kGroupMax + 2 * c] = st.m0;
-      mm[warp * kGroupMax + 2 * c + 1] = st.m1;
-      ml[warp * kGroupMax + 2 * c] = st.l0;
-      ml[warp * kGroupMax + 2 * c + 1] = st.l1;
-    }
-  }
-  __syncthreads();
   const float unboost = FP8 ? 1.f / kPBoost : 1.f;
-  for (int idx = tid; idx < G * D; idx += kThreads) {
-    const int g = idx / D, d = idx - g * D;
-    float M = -INFINITY;
+  int piece_no = 0;                       // pieces finished by this CTA
+  // pending merge checks (thread 0): slot 0 = first piece, 1 = last piece
+  int pend_b[2] = {-1, -1}, pend_h[2] = {0, 0}, pend_old[2] = {0, 0}, pend_np[2] = {0, 0};
+
+  while (ch0.nb > 0) {
+    const int L = len[ch0.b];
+    const int nbw = chunk_warp_blocks(ch0, warp);
+    for (int t = 0; t < nbw && !dead; ++t) {
+      const int s = computed % STAGES;
+      if (!__all_sync(0xffffffffu, mbar_wait(sbar + 8 * s, (computed / STAGES) & 1))) {
+        if (lane == 0) atomicOr(a.status, kStatusTimeout);
+        dead = true;
+        break;
+      }
+      const int id = __shfl_sync(0xffffffffu, id0, t);
+      float sl2 = a.scale_log2, v_mul = 1.f;
+      if constexpr (FP8) {
+        sl2 *= __shfl_sync(0xffffffffu, ks0, t);
+        v_mul = __shfl_sync(0xffffffffu, vs0, t) * kPBoost;
+      }
+      if (id >= 0 && id < a.num_blocks) {
+        const int j = ch0.cb0 + warp + kWarps * t;
+        const int n_valid = min(16, L - j * 16);
+        attend_block<D, FP8, BF16>(st, qf, ring + s * TL::SLOT, ring + s * TL::SLOT + TL::BYTES,
+                                   n_valid, sl2, v_mul, r, c);
+      }
+      __syncwarp();
+      ++computed;
+      top_up();
+    }
+
+    // does this chunk end its piece?
+    const int nbk = seg_blocks(pf, ch0.b, Hkv);
+    const int64_t s0 = pf[ch0.b] + static_cast<int64_t>(ch0.h) * nbk;
+    const bool piece_end = ch0.cb0 + ch0.nb == static_cast<int>(min(hi, s0 + nbk) - s0);
+    if (piece_end) {
+      // ---- piece epilogue: combine the warps, then output or partial
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * kGroupMax + g]);
-    float sum = 0.f, acc = 0.f;
-    if (M != -INFINITY) {
+      for (int o = 4; o < 32; o <<= 1) {
+        st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, o);
+        st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, o);
+      }
+      {
+        float* wo = mo + warp * kGroupMax * D;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float e = fast_exp2(mm[w * kGroupMax + g] - M);
-        sum += e * ml[w * kGroupMax + g];
-        acc += e * mo[(w * kGroupMax + g) * D + d];
+        for (int i = 0; i < D / 16; ++i) {
+          const int dl = d_lo<D, FP8>(i, r), dh = d_hi<D, FP8>(i, r);
+          wo[(2 * c) * D + dl] = st.o[i][0];
+          wo[(2 * c + 1) * D + dl] = st.o[i][1];
+          wo[(2 * c) * D + dh] = st.o[i][2];
+          wo[(2 * c + 1) * D + dh] = st.o[i][3];
+        }
+        if (r == 0) {
+          mm[warp * kGroupMax + 2 * c] = st.m0;
+          mm[warp * kGroupMax + 2 * c + 1] = st.m1;
+          ml[warp * kGroupMax + 2 * c] = st.l0;
+          ml[warp * kGroupMax + 2 * c + 1] = st.l1;
+        }
+      }
+      __syncthreads();
+      const bool whole = s0 >= lo && s0 + nbk <= hi;
+      const int slot = piece_no == 0 ? 0 : 1;
+      const int64_t row0 = static_cast<int64_t>(ch0.b) * Hq + ch0.h * G;
+      OutT* out_rows = static_cast<OutT*>(a.out) + row0 * D;
+      for (int idx = tid; idx < G * D; idx += kThreads) {
+        const int g = idx / D, d = idx - g * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * kGroupMax + g]);
+        float sum = 0.f, acc = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) {
+            const float e = fast_exp2(mm[w * kGroupMax + g] - M);
+            sum += e * ml[w * kGroupMax + g];
+            acc += e * mo[(w * kGroupMax + g) * D + d];
+          }
+        }
+        acc *= unboost;
+        if (whole) {
+          out_rows[idx] = from_f32<OutT>(sum > 0.f ? acc / sum : 0.f);
+        } else {
+          const int64_t row = piece_row(cta, slot, g);
+          a.ws_acc[row * D + d] = acc;
+          if (d == 0) {
+            a.ws_ml[row * 2] = M;
+            a.ws_ml[row * 2 + 1] = sum;
+          }
+        }
+      }
+      if (!whole) {
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+          // count this piece; whether it was the last is checked at the end
+          pend_b[slot] = ch0.b;
+          pend_h[slot] = ch0.h;
+          pend_np[slot] = cta_of(s0 + nbk - 1, W, NG) - cta_of(s0, W, NG) + 1;
+          pend_old[slot] = atomicAdd(a.counters + static_cast<int64_t>(ch0.b) * Hkv + ch0.h, 1);
+        }
+      }
+      __syncthreads();   // the combine scratch is free again
+      ++piece_no;
+      reset_acc();
+    }
+
+    // ---- advance to chunk k+1
+    const bool new_piece = piece_end;
+    ch0 = ch1;
+    ch1 = ch2;
+    ch2 = next_chunk(ch2, hi, pf, B, Hkv);
+    id0 = id1;
+    id1 = id2;
+    id2 = load_chunk_id(a, ch2, warp, lane);
+    if constexpr (FP8) {
+      ks0 = ks1;
+      vs0 = vs1;
+      ks1 = vs1 = 1.f;
+      if (ch1.nb > 0 && id1 >= 0 && id1 < a.num_blocks) {
+        ks1 = __ldg(a.k_scale + static_cast<int64_t>(id1) * Hkv + ch1.h);
+        vs1 = __ldg(a.v_scale + static_cast<int64_t>(id1) * Hkv + ch1.h);
       }
     }
-    acc *= unboost;
-    if (nparts == 1) {
-      out_rows[idx] = from_f32<OutT>(sum > 0.f ? acc / sum : 0.f);
+    if (ic == 1) {
+      ic = 0;
     } else {
-      const int64_t row = ((static_cast<int64_t>(b) * a.Hq + h * G + g) * a.max_parts + p);
-      a.ws_acc[row * D + d] = acc;
-      if (d == 0) {
-        a.ws_ml[row * 2] = M;
-        a.ws_ml[row * 2 + 1] = sum;
+      ic = 0;
+      it = 0;
+    }
+    if (new_piece && ch0.nb > 0) {
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i) {
+        qf[i][0] = qn[i][0];
+        qf[i][1] = qn[i][1];
+      }
+      // prefetch the query of the piece after this one
+      int b = ch0.b, h = ch0.h + 1;
+      if (h == Hkv) {
+        h = 0;
+        ++b;
+        while (b < B && pf[b + 1] == pf[b]) ++b;
+      }
+      if (b < B && pf[b] + static_cast<int64_t>(h) * seg_blocks(pf, b, Hkv) < hi)
+        load_query<D, FP8>(qn, a, b, h, r, c);
+    }
+    top_up();
+  }
+
+  if (dead) {
+    // Wait (bounded) for this warp's copies still in flight.
+    for (; computed < issued; ++computed)
+      (void)mbar_wait(sbar + 8 * (computed % STAGES), (computed / STAGES) & 1);
+  }
+
+  // ---- 4. merges: for each of this CTA's split pieces, the CTA that
+  // finished the segment's last piece combines all of them
+  for (int k = 0; k < 2; ++k) {
+    if (tid == 0) {
+      int job = -1;
+      if (pend_b[k] >= 0 && pend_old[k] == pend_np[k] - 1) {
+        atomicExch(a.counters + static_cast<int64_t>(pend_b[k]) * Hkv + pend_h[k], 0);
+        job = pend_b[k];
+      }
+      misc[4] = job;
+      misc[5] = pend_h[k];
+    }
+    __syncthreads();
+    const int mb = misc[4], mh = misc[5];
+    if (mb >= 0) {
+      __threadfence();
+      const int nbk = seg_blocks(pf, mb, Hkv);
+      const int64_t s0 = pf[mb] + static_cast<int64_t>(mh) * nbk;
+      const int c0 = cta_of(s0, W, NG), c1 = cta_of(s0 + nbk - 1, W, NG);
+      const int first_slot = s0 > cta_lo(c0, W, NG) ? 1 : 0;   // slot of c0's piece
+      const int np = c1 - c0 + 1;
+      float* sM = mm;
+      float* sS = ml;
+      for (int g = warp; g < G; g += kWarps) {
+        float M = -INFINITY;
+        for (int q = lane; q < np; q += 32) {
+          const int64_t row = piece_row(c0 + q, q == 0 ? first_slot : 0, g);
+          M = fmaxf(M, __ldcg(a.ws_ml + row * 2));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float S = 0.f;
+        for (int q = lane; q < np; q += 32) {
+          const int64_t row = piece_row(c0 + q, q == 0 ? first_slot : 0, g);
+          S += fast_exp2(__ldcg(a.ws_ml + row * 2) - M) * __ldcg(a.ws_ml + row * 2 + 1);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+        if (lane == 0) {
+          sM[g] = M;
+          sS[g] = S;
+        }
+      }
+      __syncthreads();
+      OutT* out_rows = static_cast<OutT*>(a.out) + (static_cast<int64_t>(mb) * Hq + mh * G) * D;
+      for (int idx = tid; idx < G * (D / 4); idx += kThreads) {
+        const int g = idx / (D / 4), d4 = idx - g * (D / 4);
+        const float M = sM[g];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < np; ++q) {
+          const int64_t row = piece_row(c0 + q, q == 0 ? first_slot : 0, g);
+          const float e = fast_exp2(__ldcg(a.ws_ml + row * 2) - M);
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + row * D) + d4);
+          acc.x += e * v.x;
+          acc.y += e * v.y;
+          acc.z += e * v.z;
+          acc.w += e * v.w;
+        }
+        const float S = sS[g];
+        const float ok = S > 0.f ? 1.f : 0.f;
+        OutT* o = out_rows + g * D + 4 * d4;
+        o[0] = from_f32<OutT>(ok * (acc.x / S));
+        o[1] = from_f32<OutT>(ok * (acc.y / S));
+        o[2] = from_f32<OutT>(ok * (acc.z / S));
+        o[3] = from_f32<OutT>(ok * (acc.w / S));
       }
     }
+    __syncthreads();
   }
 }
 
-// K5: one warp per (sequence, query head) with more than one partition:
-//   M = max_p m_p,  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.
-template <int D, typename OutT>
-__global__ void __launch_bounds__(256)
-merge_kernel(const DecodeArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (w >= static_cast<int64_t>(a.B) * a.Hq) return;
-  const int b = static_cast<int>(w / a.Hq);
-  const int L = a.context_lens[b];
-  if (L <= 0 || L > a.max_context_len || L > a.mbs * 16) return;   // written by decode_kernel
-  const int nparts = (L + a.part_tokens - 1) / a.part_tokens;
-  if (nparts <= 1) return;
-  const float* ml = a.ws_ml + w * a.max_parts * 2;
-  const float* acc = a.ws_acc + w * a.max_parts * D;
-  float M = -INFINITY;
-  for (int p = lane; p < nparts; p += 32) M = fmaxf(M, ml[2 * p]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  constexpr int PER = D / 32;
-  float o_acc[PER];
-#pragma unroll
-  for (int k = 0; k < PER; ++k) o_acc[k] = 0.f;
-  float sum = 0.f;
-  for (int p0 = 0; p0 < nparts; p0 += 32) {
-    const int p = p0 + lane;
-    const float wp = p < nparts ? fast_exp2(ml[2 * p] - M) : 0.f;
-    sum += p < nparts ? wp * ml[2 * p + 1] : 0.f;
-    const int n = min(32, nparts - p0);
-    for (int pp = 0; pp < n; ++pp) {
-      const float e = __shfl_sync(0xffffffffu, wp, pp);
-      const float* row = acc + static_cast<int64_t>(p0 + pp) * D;
-#pragma unroll
-      for (int k = 0; k < PER; ++k) o_acc[k] += e * row[lane + 32 * k];
-    }
+template <int D, bool FP8, bool BF16, int STAGES>
+cudaError_t launch_one(const DecodeArgs& a, cudaStream_t s) {
+  using TL = Tile<D, FP8, STAGES>;
+  const Layout lay = make_layout(TL::RING, D, STAGES, a.B);
+  auto* kern = decode_kernel<D, FP8, BF16, STAGES>;
+  static thread_local int last_smem[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (last_smem[dev & 63] != lay.total) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
+    if (e != cudaSuccess) return e;
+    last_smem[dev & 63] = lay.total;
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  OutT* out = static_cast<OutT*>(a.out) + w * D;
-#pragma unroll
-  for (int k = 0; k < PER; ++k) out[lane + 32 * k] = from_f32<OutT>(sum > 0.f ? o_acc[k] / sum : 0.f);
+  kern<<<static_cast<unsigned>(a.split_ctas), kThreads, lay.total, s>>>(a);
+  return cudaGetLastError();
 }
 
 template <int D, bool FP8, bool BF16>
-cudaError_t launch_one(const DecodeArgs& a, cudaStream_t s) {
-  using TL = Tile<D, FP8>;
-  using OutT = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-  const int max_blk = a.part_tokens / 16;
-  const size_t smem = TL::RING + kWarps * TL::STAGES * 8 + static_cast<size_t>(max_blk) * 4 * 3;
-  auto* kern = decode_kernel<D, FP8, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  dim3 grid(a.max_parts, a.Hkv, a.B);
-  kern<<<grid, kThreads, smem, s>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || a.max_parts <= 1) return e;
-  const int64_t warps = static_cast<int64_t>(a.B) * a.Hq;
-  const unsigned mgrid = static_cast<unsigned>((warps * 32 + 255) / 256);
-  merge_kernel<D, OutT><<<mgrid, 256, 0, s>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_dtype(const DecodeArgs& a, cudaStream_t s) {
+  // Ring depth per warp: 2 slots of 8 KB (16-bit, D=128) keep two CTAs per
+  // SM within shared memory; E4M3 tiles are half as large, so 4 slots.
+  constexpr int STAGES = FP8 ? 4 : (D == 128 ? 2 : 4);
+  return launch_one<D, FP8, BF16, STAGES>(a, s);
 }
 
 }  // namespace
 
-size_t decode_workspace_bytes(int B, int Hq, int D, int max_context_len, int part_tokens) {
-  if (B <= 0 || Hq <= 0 || D <= 0 || part_tokens <= 0 || max_context_len < 0) return 0;
-  const int64_t max_parts = (static_cast<int64_t>(max_context_len) + part_tokens - 1) / part_tokens;
-  if (max_parts <= 1) return 0;
-  const int64_t rows = static_cast<int64_t>(B) * Hq * max_parts;
+int decode_default_ctas() { return device_sm_count() * kCtasPerSm; }
+
+size_t decode_workspace_bytes(int B, int Hq, int D, int split_ctas) {
+  if (B <= 0 || Hq <= 0 || D <= 0 || split_ctas <= 0) return 0;
+  const int64_t rows = static_cast<int64_t>(split_ctas) * 2 * kGroupMax;
   const size_t acc = ((static_cast<size_t>(rows) * D * 4) + 255) & ~static_cast<size_t>(255);
-  return acc + static_cast<size_t>(rows) * 2 * 4;
+  const size_t ml = ((static_cast<size_t>(rows) * 2 * 4) + 255) & ~static_cast<size_t>(255);
+  const int64_t Bc = B < kMaxBatchPerLaunch ? B : kMaxBatchPerLaunch;
+  return acc + ml + static_cast<size_t>(Bc) * Hq * 4;
 }
 
-void decode_workspace_split(const DecodeArgs& a, void* ws, float** acc, float** ml) {
-  const int64_t rows = static_cast<int64_t>(a.B) * a.Hq * a.max_parts;
+void decode_workspace_split(const DecodeArgs& a, void* ws, float** acc, float** ml, int** cnt) {
+  const int64_t rows = static_cast<int64_t>(a.split_ctas) * 2 * kGroupMax;
   const size_t acc_bytes = ((static_cast<size_t>(rows) * a.D * 4) + 255) & ~static_cast<size_t>(255);
+  const size_t ml_bytes = ((static_cast<size_t>(rows) * 2 * 4) + 255) & ~static_cast<size_t>(255);
   *acc = static_cast<float*>(ws);
   *ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + acc_bytes);
+  *cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + acc_bytes + ml_bytes);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, bool fp8, bool bf16, cudaStream_t s) {
-  if (fp8) return a.D == 128 ? launch_one<128, true, false>(a, s) : launch_one<64, true, false>(a, s);
-  if (bf16) return a.D == 128 ? launch_one<128, false, true>(a, s) : launch_one<64, false, true>(a, s);
-  return a.D == 128 ? launch_one<128, false, false>(a, s) : launch_one<64, false, false>(a, s);
+  if (fp8) return a.D == 128 ? launch_dtype<128, true, false>(a, s) : launch_dtype<64, true, false>(a, s);
+  if (bf16) return a.D == 128 ? launch_dtype<128, false, true>(a, s) : launch_dtype<64, false, true>(a, s);
+  return a.D == 128 ? launch_dtype<128, false, false>(a, s) : launch_dtype<64, false, false>(a, s);
 }
 
 }  // namespace pa

@@ -8,6 +8,10 @@
 
 namespace pa {
 
+// Sequences per decode launch: each CTA keeps per-sequence prefix sums of
+// the batch in shared memory; the host splits larger batches.
+constexpr int kMaxBatchPerLaunch = 2048;
+
 // All pointers are device pointers; sizes were validated by the caller.
 struct DecodeArgs {
   void* out;                    // [B][Hq][D] f16/bf16
@@ -18,20 +22,22 @@ struct DecodeArgs {
   const float* v_scale;
   const int32_t* block_tables;  // [B][mbs]
   const int32_t* context_lens;  // [B]
-  float* ws_acc;                // [B][Hq][max_parts][D] partial sums (unnormalised)
-  float* ws_ml;                 // [B][Hq][max_parts][2] partial (max, sum) in log2 units
+  float* ws_acc;                // [split_ctas][2][8][D] partial sums (unnormalised)
+  float* ws_ml;                 // [split_ctas][2][8][2] partial (max, sum) in log2 units
+  int* counters;                // [B][Hkv] finished partitions (zero between calls)
   unsigned* status;             // device status word
   int mbs;                      // max blocks per sequence (block table row stride)
   int B, Hq, Hkv, group, D;
   int num_blocks;
   int max_context_len;
-  int part_tokens;              // tokens per partition, multiple of 16
-  int max_parts;                // ceil(max_context_len / part_tokens)
+  int split_ctas;               // CTAs the batch's blocks are divided among
   float scale_log2;             // softmax scale * log2(e)
 };
 
-size_t decode_workspace_bytes(int B, int Hq, int D, int max_context_len, int part_tokens);
-void decode_workspace_split(const DecodeArgs& a, void* ws, float** acc, float** ml);
+int decode_default_ctas();
+size_t decode_workspace_bytes(int B, int Hq, int D, int split_ctas);
+void decode_workspace_split(const DecodeArgs& a, void* ws, float** acc, float** ml,
+                            int** counters);
 
 cudaError_t launch_decode(const DecodeArgs& a, bool fp8, bool bf16, cudaStream_t s);
 

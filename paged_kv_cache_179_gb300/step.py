@@ -21,8 +21,7 @@ class DecodeStep:
     """
 
     def __init__(self, *, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
-                 num_q_heads, k_scale=None, v_scale=None, partition_tokens=None,
-                 total_context_tokens=None):
+                 num_q_heads, k_scale=None, v_scale=None, split_ctas=0):
         self.kv = "fp8" if k_cache.dtype == torch.uint8 else "16"
         self.k_cache, self.v_cache = k_cache, v_cache
         self.k_scale, self.v_scale = k_scale, v_scale
@@ -32,14 +31,9 @@ class DecodeStep:
         self.B = int(block_tables.shape[0])
         self.Hq = int(num_q_heads)
         self.NB, self.Hkv, self.bs, self.D = (int(x) for x in k_cache.shape)
-        if partition_tokens is None:
-            total = (int(total_context_tokens) if total_context_tokens is not None
-                     else self.B * self.max_context_len)
-            partition_tokens = _abi.pa_decode_pick_partition(self.B, self.Hkv, total,
-                                                             self.max_context_len)
-        self.partition_tokens = int(partition_tokens)
-        self.workspace = _abi.alloc_workspace(self.B, self.Hq, self.D, self.max_context_len,
-                                              self.partition_tokens, k_cache.device)
+        self.split_ctas = int(split_ctas) or _abi.pa_decode_default_splits()
+        self.workspace = _abi.alloc_workspace(self.B, self.Hq, self.D, self.split_ctas,
+                                              k_cache.device)
 
     def append(self, k_new, v_new, slot_mapping):
         if self.kv == "fp8":
@@ -52,11 +46,11 @@ class DecodeStep:
         if self.kv == "fp8":
             _abi.pa_decode_fp8(out, q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
                                self.block_tables, self.context_lens, self.max_context_len,
-                               self.scale, self.partition_tokens, self.workspace)
+                               self.scale, self.split_ctas, self.workspace)
         else:
             _abi.pa_decode(out, q, self.k_cache, self.v_cache, self.block_tables,
                            self.context_lens, self.max_context_len, self.scale,
-                           self.partition_tokens, self.workspace)
+                           self.split_ctas, self.workspace)
 
     def __call__(self, q, k_new, v_new, slot_mapping, out):
         self.append(k_new, v_new, slot_mapping)

@@ -45,18 +45,17 @@ def test_library_exports_every_declared_symbol(lib):
 
 def _decode(lib, **kw):
     a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, mbs=8, cl=FAKE, max_ctx=128, B=2, Hq=8,
-             Hkv=2, D=64, bs=16, NB=32, scale=0.125, dtype=0, part=64, ws=FAKE, ws_bytes=1 << 20)
+             Hkv=2, D=64, bs=16, NB=32, scale=0.125, dtype=0, splits=8, ws=FAKE, ws_bytes=1 << 20)
     a.update(kw)
     return lib.pa_decode(a["out"], a["q"], a["k"], a["v"], a["bt"], a["mbs"], a["cl"],
                          a["max_ctx"], a["B"], a["Hq"], a["Hkv"], a["D"], a["bs"], a["NB"],
-                         a["scale"], a["dtype"], a["part"], a["ws"], a["ws_bytes"], None)
+                         a["scale"], a["dtype"], a["splits"], a["ws"], a["ws_bytes"], None)
 
 
 def test_decode_argument_errors(lib):
     assert _decode(lib, q=None) == _abi.PA_ERR_INVALID_ARG
     assert _decode(lib, Hq=7) == _abi.PA_ERR_INVALID_ARG            # 7 % 2 != 0
-    assert _decode(lib, part=8) == _abi.PA_ERR_INVALID_ARG
-    assert _decode(lib, part=40) == _abi.PA_ERR_INVALID_ARG
+    assert _decode(lib, splits=-1) == _abi.PA_ERR_INVALID_ARG
     assert _decode(lib, max_ctx=129) == _abi.PA_ERR_INVALID_ARG     # > mbs * 16
     assert _decode(lib, scale=float("nan")) == _abi.PA_ERR_INVALID_ARG
     assert _decode(lib, dtype=3) == _abi.PA_ERR_INVALID_ARG
@@ -71,12 +70,16 @@ def test_decode_argument_errors(lib):
 
 
 def test_workspace_size_formula(lib):
-    # two partitions of 64 for 128 tokens: [B][Hq][2] rows of D floats, then (m, l)
-    n = lib.pa_decode_workspace_size(2, 8, 64, 128, 64)
-    acc = 2 * 8 * 2 * 64 * 4
-    assert n == ((acc + 255) // 256) * 256 + 2 * 8 * 2 * 2 * 4
-    assert lib.pa_decode_workspace_size(2, 8, 64, 64, 64) == 0     # one partition: no merge
-    assert lib.pa_decode_workspace_size(2, 8, 64, 128, 8) == 0     # invalid partition
+    # partial rows: 2 per CTA, 8 query-head slots each, D floats + (max, sum); then counters
+    n = lib.pa_decode_workspace_size(2, 8, 64, 10)
+    rows = 10 * 2 * 8
+    acc, ml, counters = rows * 64 * 4, rows * 2 * 4, 2 * 8 * 4
+    assert n == ((acc + 255) // 256) * 256 + ((ml + 255) // 256) * 256 + counters
+    assert lib.pa_decode_workspace_size(2, 8, 64, 1) == 0       # one CTA never splits
+    assert lib.pa_decode_workspace_size(2, 8, 64, -1) == 0      # invalid
+    # batches above 2048 sequences run in launches of 2048 that share the workspace
+    assert lib.pa_decode_workspace_size(5000, 8, 64, 10) == \
+        lib.pa_decode_workspace_size(2048, 8, 64, 10)
 
 
 def test_append_and_quantize_argument_errors(lib):

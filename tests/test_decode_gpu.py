@@ -2,7 +2,8 @@
 
 Whole batches of the four 16-bit workloads (append + decode, in the launch
 configuration the benchmark times), random small shapes that span several
-partitions and a ragged last block, partition-size invariance, and the edge
+partitions and a ragged last block, invariance to how the batch is split
+across CTAs, and the edge
 cases: context_len 0 and 1, NaN in unfilled rows, bad block ids and lengths.
 """
 import math
@@ -21,11 +22,10 @@ from _helpers import TOL, max_err, oracle_step, to_cuda, to_np16
 pytestmark = pytest.mark.gpu
 
 
-def _step_for(w, partition_tokens=None):
+def _step_for(w, split_ctas=0):
     return DecodeStep(k_cache=w.k_cache, v_cache=w.v_cache, block_tables=w.block_tables,
                       context_lens=w.context_lens, max_context_len=w.max_context_len,
-                      scale=w.scale, num_q_heads=w.Hq, partition_tokens=partition_tokens,
-                      total_context_tokens=w.total_tokens())
+                      scale=w.scale, num_q_heads=w.Hq, split_ctas=split_ctas)
 
 
 @pytest.mark.parametrize("name,seed", [("tiny", 0), ("tiny", 1), ("smollm2_360m", 0),
@@ -40,7 +40,7 @@ def test_full_step_matches_oracle(name, seed):
     step(w.q, w.k_new, w.v_new, w.slot_mapping, out)
     assert _abi.pa_get_status() == (0, 0)
     err = max_err(out, ref)
-    assert err <= TOL[w.dtype], (name, seed, step.partition_tokens, err)
+    assert err <= TOL[w.dtype], (name, seed, step.split_ctas, err)
 
 
 def _random_workload(seed, B, Hq, Hkv, D, dtype, max_len, fill="zero"):
@@ -71,15 +71,15 @@ def _random_workload(seed, B, Hq, Hkv, D, dtype, max_len, fill="zero"):
 
 
 CASES = [
-    # seed, B, Hq, Hkv, D, dtype, max_len, partition
+    # seed, B, Hq, Hkv, D, dtype, max_len, CTAs the batch is split across
     (10, 5, 8, 2, 64, "f16", 300, 16),
-    (11, 3, 7, 1, 128, "f16", 700, 64),
-    (12, 6, 15, 5, 64, "bf16", 500, 32),
-    (13, 4, 28, 4, 128, "f16", 1000, 256),
-    (14, 2, 12, 2, 128, "bf16", 2100, 128),
-    (15, 7, 4, 4, 128, "f16", 90, 16),       # MHA (group 1)
-    (16, 3, 16, 2, 64, "f16", 333, 48),      # group of 8
-    (17, 8, 6, 3, 128, "bf16", 40, 1024),    # one partition per sequence
+    (11, 3, 7, 1, 128, "f16", 700, 5),
+    (12, 6, 15, 5, 64, "bf16", 500, 33),
+    (13, 4, 28, 4, 128, "f16", 1000, 304),
+    (14, 2, 12, 2, 128, "bf16", 2100, 7),
+    (15, 7, 4, 4, 128, "f16", 90, 1000),     # MHA (group 1); more CTAs than blocks
+    (16, 3, 16, 2, 64, "f16", 333, 3),       # group of 8
+    (17, 8, 6, 3, 128, "bf16", 40, 1),       # one CTA: every sequence whole
 ]
 
 
@@ -95,18 +95,19 @@ def test_random_shapes_match_oracle(case):
     assert max_err(out, ref) <= TOL[dtype]
 
 
-def test_partition_size_invariance():
+def test_split_invariance():
     w = W.make_workload("qwen2_5_1_5b", seed=2)
     ref = oracle_step(w)
     to_cuda(w)
     outs = []
     k0, v0 = w.k_cache.clone(), w.v_cache.clone()
-    for part in (16, 64, 128, 512, 4096, 16384):
+    for splits in (1, 2, 7, 64, 304, 999, 7207):
         w.k_cache.copy_(k0)
         w.v_cache.copy_(v0)
         out = torch.empty_like(w.q)
-        _step_for(w, part)(w.q, w.k_new, w.v_new, w.slot_mapping, out)
-        assert max_err(out, ref) <= TOL["f16"], part
+        _step_for(w, splits)(w.q, w.k_new, w.v_new, w.slot_mapping, out)
+        assert _abi.pa_get_status() == (0, 0)
+        assert max_err(out, ref) <= TOL["f16"], splits
         outs.append(out.float())
     for o in outs[1:]:
         assert (o - outs[0]).abs().max().item() <= 2 * TOL["f16"]
@@ -131,7 +132,7 @@ def test_nan_in_unfilled_rows_is_ignored():
                         w.scale)
     to_cuda(w)
     out = torch.empty_like(w.q)
-    _step_for(w, 32)(w.q, w.k_new, w.v_new, w.slot_mapping, out)
+    _step_for(w, 9)(w.q, w.k_new, w.v_new, w.slot_mapping, out)
     assert torch.isfinite(out).all()
     assert max_err(out, ref) <= TOL["f16"]
 
@@ -141,7 +142,7 @@ def test_context_len_one_returns_v0_and_zero_returns_zeros():
     lens = torch.tensor([1, 0, 1, 0], dtype=torch.int32, device="cuda")
     out = torch.full_like(w.q, 7.0)
     _abi.pa_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, lens, w.max_context_len,
-                   w.scale, 64, _abi.alloc_workspace(4, 8, 64, w.max_context_len, 64, "cuda"))
+                   w.scale, 5, _abi.alloc_workspace(4, 8, 64, 5, "cuda"))
     assert _abi.pa_get_status() == (0, 0)
     for b in (0, 2):
         blk = int(w.block_tables[b, 0])
@@ -155,19 +156,19 @@ def test_bad_block_id_and_length_are_reported_not_read():
     bt = w.block_tables.clone()
     bt[3, 2] = w.num_blocks + 1000          # outside the pool
     out = torch.empty_like(w.q)
-    ws = _abi.alloc_workspace(4, 8, 64, w.max_context_len, 64, "cuda")
+    ws = _abi.alloc_workspace(4, 8, 64, 6, "cuda")
     _abi.pa_decode(out, w.q, w.k_cache, w.v_cache, bt, w.context_lens, w.max_context_len,
-                   w.scale, 64, ws)
+                   w.scale, 6, ws)
     rc, bits = _abi.pa_get_status()
     assert rc == _abi.PA_ERR_BOUNDS and bits & _abi.PA_STATUS_BAD_BLOCK
     lens = w.context_lens.clone()
     lens[1] = w.max_context_len + 5          # longer than the stated bound
     _abi.pa_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, lens, w.max_context_len,
-                   w.scale, 64, ws)
+                   w.scale, 6, ws)
     rc, bits = _abi.pa_get_status()
     assert rc == _abi.PA_ERR_BOUNDS and bits == _abi.PA_STATUS_BAD_LEN
     assert not out[1].any()
     # the context stays usable
     _abi.pa_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
-                   w.max_context_len, w.scale, 64, ws)
+                   w.max_context_len, w.scale, 6, ws)
     assert _abi.pa_get_status() == (0, 0)

@@ -88,11 +88,10 @@ def test_append_fp8_bit_exact(D):
         assert np.array_equal(d.cpu().numpy().view(np.uint8), r.view(np.uint8))
 
 
-def _fp8_step(w, kc, vc, ks, vs, part=None):
+def _fp8_step(w, kc, vc, ks, vs, splits=0):
     return DecodeStep(k_cache=kc, v_cache=vc, k_scale=ks, v_scale=vs, block_tables=w.block_tables,
                       context_lens=w.context_lens, max_context_len=w.max_context_len,
-                      scale=w.scale, num_q_heads=w.Hq, partition_tokens=part,
-                      total_context_tokens=w.total_tokens())
+                      scale=w.scale, num_q_heads=w.Hq, split_ctas=splits)
 
 
 def _quantized_on_gpu(w):
@@ -104,10 +103,10 @@ def _quantized_on_gpu(w):
     return kc, vc, ks, vs
 
 
-@pytest.mark.parametrize("seed,B,Hq,Hkv,D,max_len,part", [
-    (0, 4, 28, 4, 128, 700, 64), (1, 3, 8, 2, 64, 300, 16), (2, 5, 12, 2, 128, 2000, 256),
-    (3, 2, 7, 7, 128, 50, 4096)])
-def test_decode_fp8_small_matches_oracle(seed, B, Hq, Hkv, D, max_len, part):
+@pytest.mark.parametrize("seed,B,Hq,Hkv,D,max_len,splits", [
+    (0, 4, 28, 4, 128, 700, 13), (1, 3, 8, 2, 64, 300, 40), (2, 5, 12, 2, 128, 2000, 304),
+    (3, 2, 7, 7, 128, 50, 1)])
+def test_decode_fp8_small_matches_oracle(seed, B, Hq, Hkv, D, max_len, splits):
     g = torch.Generator().manual_seed(seed)
     lens = torch.randint(1, max_len + 1, (B,), generator=g).to(torch.int32)
     nblk = (lens + 15) // 16
@@ -129,8 +128,9 @@ def test_decode_fp8_small_matches_oracle(seed, B, Hq, Hkv, D, max_len, part):
     ks, vs = torch.from_numpy(ks_o).cuda(), torch.from_numpy(vs_o).cuda()
     out = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
     mcl = int(lens.max())
-    ws = _abi.alloc_workspace(B, Hq, D, mcl, part, "cuda")
-    _abi.pa_decode_fp8(out, q.cuda(), kc, vc, ks, vs, tables.cuda(), lens.cuda(), mcl, scale, part, ws)
+    ws = _abi.alloc_workspace(B, Hq, D, splits, "cuda")
+    _abi.pa_decode_fp8(out, q.cuda(), kc, vc, ks, vs, tables.cuda(), lens.cuda(), mcl, scale,
+                       splits, ws)
     assert _abi.pa_get_status() == (0, 0)
     err = np.abs(out.float().cpu().numpy() - ref).max()
     assert err <= TOL["fp8"], err
