@@ -79,6 +79,7 @@ enum {
 #define PA_STATUS_BAD_LEN 2u     /* context_len < 0, > max_context_len or > max_blocks_per_seq*block_size */
 #define PA_STATUS_BAD_SLOT 4u    /* slot >= num_blocks * block_size */
 #define PA_STATUS_TIMEOUT 8u     /* an mbarrier wait reached its iteration limit */
+#define PA_STATUS_NO_WORKSPACE 16u /* a split partition had no workspace (never written) */
 
 /*
  * Append: for each token i with s = slot_mapping[i] >= 0 and each kv head h,
@@ -138,10 +139,10 @@ int pa_decode_default_splits(void);
 
 /*
  * Bytes of device workspace pa_decode / pa_decode_fp8 need: room for the
- * partial results of the context partitions that cross CTA boundaries (at
- * most two per CTA) and one counter per (sequence, kv head).  split_ctas 0
- * means pa_decode_default_splits() of the current device; 1 needs no
- * workspace (0 is returned).
+ * partial results of the context partitions that cross worker boundaries
+ * (a worker is one warp; four per CTA; at most two partials each) and one
+ * counter per (sequence, kv head).  split_ctas 0 means
+ * pa_decode_default_splits() of the current device.  Every call needs one.
  *
  * The caller allocates the workspace and must zero-fill it once before its
  * first use; every call that completes leaves the counters at zero again,
@@ -159,15 +160,15 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int
  * hq / (num_q_heads / num_kv_heads).  out is rounded to dtype (round to
  * nearest even); a sequence with context_len 0 gets a zero output.
  *
- * The batch's (sequence, kv head, block) units are divided evenly among
- * split_ctas CTAs (0: pa_decode_default_splits()).  A CTA's share of one
- * sequence is a context partition, reduced with an online softmax in fp32;
- * a sequence split across CTAs has its partitions merged by log-sum-exp in
- * the same launch.  Results do not depend on split_ctas beyond fp32
+ * The batch's (sequence, kv head, block) units are divided evenly among the
+ * 4 * split_ctas warps of split_ctas CTAs (0: pa_decode_default_splits()).
+ * A warp's share of one sequence is a context partition, reduced with an
+ * online softmax in fp32; a sequence split across warps has its partitions
+ * merged by log-sum-exp in the same launch.  Results do not depend on split_ctas beyond fp32
  * rounding, and a given split_ctas is deterministic.
  *   max_context_len: host-side upper bound of context_lens (no device read);
  *   workspace: at least pa_decode_workspace_size(...) bytes, 256-byte
- *   aligned, zero-filled before first use (may be NULL when that size is 0).
+ *   aligned, zero-filled before first use.
  * Source: rvLLM, CUDA Kernels table, "PagedAttention V2" (block-table
  * indirection, online softmax); LLM Serving Kernels, Projects table, row 04;
  * rvllm (small engine), How it's put together (GQA, read_blocks).

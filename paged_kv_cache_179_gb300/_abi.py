@@ -20,6 +20,7 @@ PA_F16, PA_BF16 = 0, 1
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_BOUNDS, \
     PA_ERR_TIMEOUT = range(7)
 PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_LEN, PA_STATUS_BAD_SLOT, PA_STATUS_TIMEOUT = 1, 2, 4, 8
+PA_STATUS_NO_WORKSPACE = 16
 
 # (name, argtypes, restype) of every exported entry point
 _vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
@@ -194,9 +195,9 @@ def pa_decode_default_splits() -> int:
 
 
 def alloc_workspace(num_seqs, num_q_heads, head_dim, split_ctas, device):
-    """Caller-owned, zero-filled workspace for pa_decode (None when the sizes need none)."""
+    """Caller-owned, zero-filled workspace for pa_decode."""
     n = pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, split_ctas)
-    return torch.zeros(n, dtype=torch.uint8, device=device) if n else None
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
 
 
 def _decode_common(out, q, block_tables, context_lens, dev):

@@ -72,9 +72,9 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
                const float* ks, const float* vs, const int32_t* bt, const int32_t* cl,
                float scale, bool fp8, bool bf16, void* ws, size_t ws_bytes, void* stream) {
   if (s.B == 0) return PA_OK;
-  auto ws_ok = [&]() {
+  auto ws_ok = [&]() {   // every split needs one: its four warps divide the batch
     const size_t need = decode_workspace_bytes(s.B, s.Hq, s.D, s.splits);
-    return s.splits <= 1 || (ws != nullptr && ws_bytes >= need && aligned(ws, 256));
+    return ws != nullptr && ws_bytes >= need && aligned(ws, 256);
   };
   if (s.splits > 0 && !ws_ok()) return PA_ERR_WORKSPACE;   // checked before touching CUDA
   DeviceState* dev = nullptr;
@@ -109,7 +109,7 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
     c.q = static_cast<const uint8_t*>(q) + b0 * out_row;
     c.block_tables = bt + static_cast<int64_t>(b0) * s.mbs;
     c.context_lens = cl + b0;
-    if (s.splits > 1) decode_workspace_split(c, ws, &c.ws_acc, &c.ws_ml, &c.counters);
+    decode_workspace_split(c, ws, &c.ws_acc, &c.ws_ml, &c.counters);
     if (cudaError_t e = launch_decode(c, fp8, bf16, static_cast<cudaStream_t>(stream)))
       return cuda_status(e);
   }
@@ -232,7 +232,6 @@ int pa_e4m3_encode(const float* x, uint8_t* codes, int64_t n, void* stream) {
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int split_ctas) {
   if (split_ctas < 0) return 0;
   if (split_ctas == 0) split_ctas = decode_default_ctas();
-  if (split_ctas <= 1) return 0;
   return decode_workspace_bytes(num_seqs, num_q_heads, head_dim, split_ctas);
 }
 

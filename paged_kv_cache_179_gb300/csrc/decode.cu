@@ -51,6 +51,29 @@
 #include "pa_launch.h"
 #include "pa_ptx.cuh"
 
+// Opt-in trace build (-DPA_TRACE): thread 0 of each CTA records %globaltimer
+// at the phases of the kernel; pa_trace_read copies them out.
+#ifdef PA_TRACE
+__device__ unsigned long long g_pa_trace[8192 * 8];
+#define PA_TRACE_MARK(k)                                                        \
+  do {                                                                          \
+    if (threadIdx.x == 0 && blockIdx.x < 8192) {                                \
+      unsigned long long t_;                                                    \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                    \
+      g_pa_trace[blockIdx.x * 8 + (k)] = t_;                                    \
+    }                                                                           \
+  } while (0)
+extern "C" int pa_trace_read(unsigned long long* host, int n) {
+  return cudaMemcpyFromSymbol(host, g_pa_trace, sizeof(unsigned long long) * 8 *
+                                                    static_cast<size_t>(n < 8192 ? n : 8192)) ==
+                 cudaSuccess ? 0 : 4;
+}
+#else
+#define PA_TRACE_MARK(k) \
+  do {               \
+  } while (0)
+#endif
+
 namespace pa {
 namespace {
 
@@ -75,12 +98,11 @@ __host__ __device__ constexpr int round16(int x) { return (x + 15) & ~15; }
 
 // Dynamic shared-memory layout; the host sizes the launch with the same function.
 struct Layout {
-  int merge, sbar, pf, len, misc, total;
+  int sbar, pf, len, misc, total;
 };
-__host__ __device__ inline Layout make_layout(int ring, int D, int stages, int B) {
+__host__ __device__ inline Layout make_layout(int ring, int stages, int B) {
   Layout l{};
   int o = ring;
-  l.merge = o; o += round16(kWarps * kGroupMax * (D + 2) * 4);
   l.sbar = o;  o += round16(kWarps * stages * 8);
   l.pf = o;    o += round16((B + 1) * 4);
   l.len = o;   o += round16(B * 4);
@@ -123,7 +145,8 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
                                              float v_mul, int r, int c) {
   constexpr int ROW = FP8 ? D : 2 * D;
   // ---- S^T = K Q^T : 16 tokens x 8 query heads, k = head_dim
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  // two accumulators (even / odd k-steps) halve the dependent MMA chain
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
   if constexpr (!FP8) {
     // lane (r, c) reads 16-byte chunk 4i+c of rows r and r+8: d = 32i + 8c + 0..7
 #pragma unroll
@@ -131,7 +154,7 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
       const uint4 ka = lds128(kt + r * ROW + (4 * i + c) * 16);
       const uint4 kb = lds128(kt + (r + 8) * ROW + (4 * i + c) * 16);
       mma16816<BF16>(acc, ka.x, kb.x, ka.y, kb.y, qf[2 * i][0], qf[2 * i][1]);
-      mma16816<BF16>(acc, ka.z, kb.z, ka.w, kb.w, qf[2 * i + 1][0], qf[2 * i + 1][1]);
+      mma16816<BF16>(acc2, ka.z, kb.z, ka.w, kb.w, qf[2 * i + 1][0], qf[2 * i + 1][1]);
     }
   } else {
     // lane (r, c) reads 16 codes at byte 64i + 16c of rows r and r+8
@@ -142,12 +165,14 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         const uint32_t wa = word(ka, q4), wb = word(kb, q4);
-        mma16816<false>(acc, e4m3x2_to_f16x2(wa), e4m3x2_to_f16x2(wb),
+        mma16816<false>(q4 & 1 ? acc2 : acc, e4m3x2_to_f16x2(wa), e4m3x2_to_f16x2(wb),
                         e4m3x2_to_f16x2(wa >> 16), e4m3x2_to_f16x2(wb >> 16),
                         qf[4 * i + q4][0], qf[4 * i + q4][1]);
       }
     }
   }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] += acc2[k];
 
   // ---- online softmax on the fragment: this lane holds tokens r, r+8 of heads 2c, 2c+1
   float s0 = acc[0] * sl2, s1 = acc[1] * sl2, s2 = acc[2] * sl2, s3 = acc[3] * sl2;
@@ -254,40 +279,31 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
   }
 }
 
-template <typename T>
-__device__ __forceinline__ T from_f32(float x);
-template <>
-__device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
-template <>
-__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
-  return __float2bfloat16_rn(x);
-}
-
 // ------------------------------------------------------------ work split
 // The batch is a stream of 16-token blocks ordered (sequence, kv head,
 // block): segment (b, h) holds the ceil(L_b / 16) blocks of sequence b for
 // kv head h, and starts at pf[b] + h * nblk_b where pf is the exclusive
-// prefix sum of Hkv * nblk_b.  CTA c of G takes blocks [c*W/G, (c+1)*W/G)
-// of the W in the batch: its share of a segment is one context partition
-// ("piece").  A segment inside one CTA's range is attended whole; one that
-// crosses ranges is split into pieces whose partial results are merged.
-// Each CTA walks its range in chunks of at most kChunk blocks (one block
-// id per lane and warp).
-constexpr int kChunk = 32 * kWarps;
+// prefix sum of Hkv * nblk_b.  The N workers (warps of the grid) share the
+// W blocks evenly: worker w takes blocks [w*W/N, (w+1)*W/N), and its share
+// of a segment is one context partition ("piece").  A segment inside one
+// worker's range is attended whole; one that crosses ranges is split into
+// pieces whose partial results are merged.  A worker walks its range in
+// chunks of at most kChunk blocks, one block id per lane.
+constexpr int kChunk = 32;
 
 struct Chunk {
   int b, h;     // segment
   int cb0;      // first block of the chunk within the segment
-  int nb;       // blocks in the chunk (0: past the end of the CTA's range)
+  int nb;       // blocks in the chunk (0: past the end of the worker's range)
 };
 
 __device__ __forceinline__ int seg_blocks(const int* pf, int b, int Hkv) {
   return (pf[b + 1] - pf[b]) / Hkv;
 }
-__device__ __forceinline__ int64_t cta_lo(int64_t c, int64_t W, int64_t G) { return c * W / G; }
-// The CTA whose range holds block x.
-__device__ __forceinline__ int cta_of(int64_t x, int64_t W, int64_t G) {
-  return static_cast<int>(((x + 1) * G - 1) / W);
+__device__ __forceinline__ int64_t worker_lo(int64_t w, int64_t W, int64_t N) { return w * W / N; }
+// The worker whose range holds block x.
+__device__ __forceinline__ int worker_of(int64_t x, int64_t W, int64_t N) {
+  return static_cast<int>(((x + 1) * N - 1) / W);
 }
 
 __device__ __forceinline__ Chunk first_chunk(int64_t lo, int64_t hi, const int* pf, int B,
@@ -331,15 +347,10 @@ __device__ __forceinline__ Chunk next_chunk(const Chunk& x, int64_t hi, const in
   return Chunk{b, h, 0, static_cast<int>(min(static_cast<int64_t>(kChunk), min(hi, s0 + nbk) - s0))};
 }
 
-__device__ __forceinline__ int chunk_warp_blocks(const Chunk& x, int warp) {
-  return x.nb > warp ? (x.nb - warp + kWarps - 1) / kWarps : 0;
-}
-
-// This lane's block id of chunk x (lane t holds block cb0 + warp + 4t).
-__device__ __forceinline__ int load_chunk_id(const DecodeArgs& a, const Chunk& x, int warp,
-                                             int lane) {
-  if (warp + kWarps * lane >= x.nb) return -1;
-  return __ldg(a.block_tables + static_cast<int64_t>(x.b) * a.mbs + x.cb0 + warp + kWarps * lane);
+// This lane's block id of chunk x (lane t holds block cb0 + t), -1 past its end.
+__device__ __forceinline__ int load_chunk_id(const DecodeArgs& a, const Chunk& x, int lane) {
+  if (lane >= x.nb) return -1;
+  return __ldg(a.block_tables + static_cast<int64_t>(x.b) * a.mbs + x.cb0 + lane);
 }
 
 template <int D, bool FP8>
@@ -370,29 +381,150 @@ __device__ __forceinline__ void load_query(uint32_t (&qf)[D / 16][2], const Deco
   }
 }
 
-// Partial-result row of (CTA c, piece slot k, query head g): slot 0 is the
-// CTA's first piece, slot 1 its last.
-__device__ __forceinline__ int64_t piece_row(int c, int k, int g) {
-  return (static_cast<int64_t>(c) * 2 + k) * kGroupMax + g;
+// Partial-result row of (worker w, piece slot k, query head g): slot 0 is the
+// worker's first piece, slot 1 its last.
+__device__ __forceinline__ int64_t piece_row(int w, int k, int g) {
+  return (static_cast<int64_t>(w) * 2 + k) * kGroupMax + g;
+}
+
+// Write a whole piece's result from the warp's fragments: out = o / l.
+template <int D, bool FP8, bool BF16>
+__device__ __forceinline__ void store_output(const WarpAcc<D>& st, uint16_t* rows, int G, int r,
+                                             int c, float unboost) {
+  const int g0 = 2 * c, g1 = 2 * c + 1;
+  const float i0 = st.l0 > 0.f ? unboost / st.l0 : 0.f;
+  const float i1 = st.l1 > 0.f ? unboost / st.l1 : 0.f;
+#pragma unroll
+  for (int i = 0; i < D / 16; i += 2) {
+    const int dl = d_lo<D, FP8>(i, r), dh = d_hi<D, FP8>(i, r);   // d and d+1 with i, i+1
+    if (g0 < G) {
+      *reinterpret_cast<uint32_t*>(rows + g0 * D + dl) =
+          pack2<BF16>(st.o[i][0] * i0, st.o[i + 1][0] * i0);
+      *reinterpret_cast<uint32_t*>(rows + g0 * D + dh) =
+          pack2<BF16>(st.o[i][2] * i0, st.o[i + 1][2] * i0);
+    }
+    if (g1 < G) {
+      *reinterpret_cast<uint32_t*>(rows + g1 * D + dl) =
+          pack2<BF16>(st.o[i][1] * i1, st.o[i + 1][1] * i1);
+      *reinterpret_cast<uint32_t*>(rows + g1 * D + dh) =
+          pack2<BF16>(st.o[i][3] * i1, st.o[i + 1][3] * i1);
+    }
+  }
+}
+
+// Write a split piece's partial (unnormalised acc, running max, sum) to the workspace.
+template <int D, bool FP8>
+__device__ __forceinline__ void store_partial(const WarpAcc<D>& st, const DecodeArgs& a, int w,
+                                              int slot, int r, int c, float unboost) {
+  const int g0 = 2 * c, g1 = 2 * c + 1;
+  float* r0 = a.ws_acc + piece_row(w, slot, g0) * D;
+  float* r1 = a.ws_acc + piece_row(w, slot, g1) * D;
+#pragma unroll
+  for (int i = 0; i < D / 16; i += 2) {
+    const int dl = d_lo<D, FP8>(i, r), dh = d_hi<D, FP8>(i, r);
+    if (g0 < a.group) {
+      __stcg(reinterpret_cast<float2*>(r0 + dl),
+             make_float2(st.o[i][0] * unboost, st.o[i + 1][0] * unboost));
+      __stcg(reinterpret_cast<float2*>(r0 + dh),
+             make_float2(st.o[i][2] * unboost, st.o[i + 1][2] * unboost));
+    }
+    if (g1 < a.group) {
+      __stcg(reinterpret_cast<float2*>(r1 + dl),
+             make_float2(st.o[i][1] * unboost, st.o[i + 1][1] * unboost));
+      __stcg(reinterpret_cast<float2*>(r1 + dh),
+             make_float2(st.o[i][3] * unboost, st.o[i + 1][3] * unboost));
+    }
+  }
+  if (r == 0) {
+    if (g0 < a.group) __stcg(reinterpret_cast<float2*>(a.ws_ml + piece_row(w, slot, g0) * 2),
+                             make_float2(st.m0, st.l0));
+    if (g1 < a.group) __stcg(reinterpret_cast<float2*>(a.ws_ml + piece_row(w, slot, g1) * 2),
+                             make_float2(st.m1, st.l1));
+  }
+}
+
+// (max, sum) pair combine of two partial softmax states in log2 units.
+__device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;   // both empty
+  s = s * fast_exp2(m - mn) + s2 * fast_exp2(m2 - mn);
+  m = mn;
+}
+
+// The warp that completed segment (b, h) merges its np pieces, held by
+// workers w0 .. w0+np-1 (slot first_slot for w0, slot 0 for the others):
+//   out = sum_q 2^(m_q - M) acc_q / sum_q 2^(m_q - M) l_q,  M = max_q m_q.
+template <int D, bool BF16>
+__device__ void merge_pieces(const DecodeArgs& a, int b, int h, int w0, int first_slot, int np,
+                             int lane) {
+  const int G = a.group;
+  // per head g: lanes (g, q mod 4) fold the pieces' (max, sum) pairs
+  const int g1 = lane >> 2, q1 = lane & 3;
+  float mg = -INFINITY, sg = 0.f;
+  if (g1 < G) {
+    for (int q = q1; q < np; q += 4) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(
+          a.ws_ml + piece_row(w0 + q, q == 0 ? first_slot : 0, g1) * 2));
+      ms_combine(mg, sg, ml.x, ml.y);
+    }
+  }
+#pragma unroll
+  for (int o = 1; o < 4; o <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, mg, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, sg, o);
+    ms_combine(mg, sg, m2, s2);
+  }
+  float M[kGroupMax], S[kGroupMax];
+#pragma unroll
+  for (int g = 0; g < kGroupMax; ++g) {
+    M[g] = __shfl_sync(0xffffffffu, mg, 4 * g);
+    S[g] = __shfl_sync(0xffffffffu, sg, 4 * g);
+  }
+  uint16_t* rows = static_cast<uint16_t*>(a.out) + (static_cast<int64_t>(b) * a.Hq + h * G) * D;
+  for (int d4 = lane; d4 < D / 4; d4 += 32) {
+    float4 acc[kGroupMax];
+#pragma unroll
+    for (int g = 0; g < kGroupMax; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < np; ++q) {
+      const int slot = q == 0 ? first_slot : 0;
+#pragma unroll
+      for (int g = 0; g < kGroupMax; ++g) {
+        if (g >= G || M[g] == -INFINITY) continue;
+        const int64_t row = piece_row(w0 + q, slot, g);
+        const float e = fast_exp2(__ldcg(a.ws_ml + row * 2) - M[g]);
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + row * D) + d4);
+        acc[g].x += e * v.x;
+        acc[g].y += e * v.y;
+        acc[g].z += e * v.z;
+        acc[g].w += e * v.w;
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < kGroupMax; ++g) {
+      if (g >= G) continue;
+      const float inv = S[g] > 0.f ? 1.f / S[g] : 0.f;
+      uint2 v;
+      v.x = pack2<BF16>(acc[g].x * inv, acc[g].y * inv);
+      v.y = pack2<BF16>(acc[g].z * inv, acc[g].w * inv);
+      *reinterpret_cast<uint2*>(rows + g * D + 4 * d4) = v;
+    }
+  }
 }
 
 template <int D, bool FP8, bool BF16, int STAGES>
 __global__ void __launch_bounds__(kThreads)
 decode_kernel(const DecodeArgs a) {
   using TL = Tile<D, FP8, STAGES>;
-  using OutT = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, c = lane & 3;
   const int B = a.B, Hkv = a.Hkv, Hq = a.Hq, G = a.group;
-  const Layout lay = make_layout(TL::RING, D, STAGES, B);
+  const Layout lay = make_layout(TL::RING, STAGES, B);
   int* pf = reinterpret_cast<int*>(smem + lay.pf);
   int* len = reinterpret_cast<int*>(smem + lay.len);
-  int* misc = reinterpret_cast<int*>(smem + lay.misc);   // [0..3] warp sums, [4..7] merge job
-  float* mo = reinterpret_cast<float*>(smem + lay.merge);  // [warp][g][D]
-  float* mm = mo + kWarps * kGroupMax * D;                  // [warp][g]
-  float* ml = mm + kWarps * kGroupMax;                      // [warp][g]
+  int* misc = reinterpret_cast<int*>(smem + lay.misc);   // [0..3] warp sums of the scan
 
+  PA_TRACE_MARK(0);
   // ---- 1. blocks per sequence and their prefix sum (segments of Hkv * nblk)
   {
     const int per = (B + kThreads - 1) / kThreads;
@@ -421,10 +553,8 @@ decode_kernel(const DecodeArgs a) {
     if (tid == kThreads - 1) pf[B] = ex;
     __syncthreads();
   }
+  PA_TRACE_MARK(1);
   const int64_t W = pf[B];
-  // Never split across more CTAs than there are blocks: every CTA that takes
-  // part then owns at least one block, which the piece bookkeeping relies on.
-  const int64_t NG = min(static_cast<int64_t>(gridDim.x), W);
   const int cta = blockIdx.x;
 
   // ---- 2. sequences with nothing to attend get a zero output
@@ -432,13 +562,19 @@ decode_kernel(const DecodeArgs a) {
     const int L = len[b];
     if (L > 0) continue;
     if (L < 0 && tid == 0) atomicOr(a.status, kStatusBadLen);
-    OutT* o = static_cast<OutT*>(a.out) + static_cast<int64_t>(b) * Hq * D;
-    for (int i = tid; i < Hq * D; i += kThreads) o[i] = from_f32<OutT>(0.f);
+    uint16_t* o = static_cast<uint16_t*>(a.out) + static_cast<int64_t>(b) * Hq * D;
+    for (int i = tid; i < Hq * D; i += kThreads) o[i] = 0;   // +0.0 in f16 and bf16
   }
-  if (cta >= NG) return;
-  const int64_t lo = cta_lo(cta, W, NG), hi = cta_lo(cta + 1, W, NG);
 
-  // ---- 3. per-warp state
+  // ---- 3. this warp's share of the block stream.  No CTA-wide barrier
+  // follows: every warp is an independent worker from here on.  Never more
+  // workers than blocks, so every worker owns at least one block (the piece
+  // bookkeeping relies on it).
+  const int64_t NW = min(static_cast<int64_t>(gridDim.x) * kWarps, W);
+  const int gw = cta * kWarps + warp;
+  if (gw >= NW) return;
+  const int64_t lo = worker_lo(gw, W, NW), hi = worker_lo(gw + 1, W, NW);
+
   const uint32_t ring = smem_u32(smem) + warp * STAGES * TL::SLOT;
   const uint32_t sbar = smem_u32(smem + lay.sbar) + warp * STAGES * 8;
   if (lane == 0) {
@@ -452,9 +588,9 @@ decode_kernel(const DecodeArgs a) {
   Chunk ch0 = first_chunk(lo, hi, pf, B, Hkv);
   Chunk ch1 = next_chunk(ch0, hi, pf, B, Hkv);
   Chunk ch2 = next_chunk(ch1, hi, pf, B, Hkv);
-  int id0 = load_chunk_id(a, ch0, warp, lane);
-  int id1 = load_chunk_id(a, ch1, warp, lane);
-  int id2 = load_chunk_id(a, ch2, warp, lane);
+  int id0 = load_chunk_id(a, ch0, lane);
+  int id1 = load_chunk_id(a, ch1, lane);
+  int id2 = load_chunk_id(a, ch2, lane);
   float ks0 = 1.f, vs0 = 1.f, ks1 = 1.f, vs1 = 1.f;   // E4M3 page scales of chunks k, k+1
   if constexpr (FP8) {
     if (id0 >= 0 && id0 < a.num_blocks) {
@@ -469,34 +605,30 @@ decode_kernel(const DecodeArgs a) {
   // query fragments of the current piece and of the next one
   uint32_t qf[D / 16][2], qn[D / 16][2];
   load_query<D, FP8>(qf, a, ch0.b, ch0.h, r, c);
-  Chunk nxt_piece = ch0;
-  {
-    // first chunk of the following segment, if it is in range
-    int b = ch0.b, h = ch0.h + 1;
+  auto prefetch_next_query = [&](int b, int h) {
+    ++h;
     if (h == Hkv) {
       h = 0;
       ++b;
       while (b < B && pf[b + 1] == pf[b]) ++b;
     }
-    nxt_piece.nb = 0;
-    if (b < B && pf[b] + static_cast<int64_t>(h) * seg_blocks(pf, b, Hkv) < hi) {
-      nxt_piece = Chunk{b, h, 0, 1};
+    if (b < B && pf[b] + static_cast<int64_t>(h) * seg_blocks(pf, b, Hkv) < hi)
       load_query<D, FP8>(qn, a, b, h, r, c);
-    }
-  }
+  };
+  prefetch_next_query(ch0.b, ch0.h);
 
   const uint8_t* kbase = static_cast<const uint8_t*>(a.k_cache);
   const uint8_t* vbase = static_cast<const uint8_t*>(a.v_cache);
   const uint64_t pol = l2_policy_evict_first();
   bool dead = false;            // a wait timed out: stop touching the pipeline
   int issued = 0, computed = 0;
-  int ic = 0, it = 0;           // fetch cursor: chunk k+ic (ic in {0,1}), this warp's block it
+  int ic = 0, it = 0;           // fetch cursor: chunk k+ic (ic in {0,1}), block it
 
   auto top_up = [&]() {
     while (!dead && issued - computed < STAGES) {
       const Chunk& x = ic == 0 ? ch0 : ch1;
       if (x.nb == 0) return;
-      if (it >= chunk_warp_blocks(x, warp)) {
+      if (it >= x.nb) {
         if (ic == 1) return;    // never more than one chunk ahead
         ic = 1;
         it = 0;
@@ -522,6 +654,7 @@ decode_kernel(const DecodeArgs a) {
     }
   };
   top_up();
+  PA_TRACE_MARK(2);
 
   WarpAcc<D> st;
   auto reset_acc = [&]() {
@@ -533,20 +666,22 @@ decode_kernel(const DecodeArgs a) {
   reset_acc();
 
   const float unboost = FP8 ? 1.f / kPBoost : 1.f;
-  int piece_no = 0;                       // pieces finished by this CTA
-  // pending merge checks (thread 0): slot 0 = first piece, 1 = last piece
+  int piece_no = 0;
+  // pending merge checks (lane 0): slot 0 = first piece, 1 = last piece
   int pend_b[2] = {-1, -1}, pend_h[2] = {0, 0}, pend_old[2] = {0, 0}, pend_np[2] = {0, 0};
 
   while (ch0.nb > 0) {
     const int L = len[ch0.b];
-    const int nbw = chunk_warp_blocks(ch0, warp);
-    for (int t = 0; t < nbw && !dead; ++t) {
+    for (int t = 0; t < ch0.nb && !dead; ++t) {
       const int s = computed % STAGES;
       if (!__all_sync(0xffffffffu, mbar_wait(sbar + 8 * s, (computed / STAGES) & 1))) {
         if (lane == 0) atomicOr(a.status, kStatusTimeout);
         dead = true;
         break;
       }
+#ifdef PA_TRACE
+      if (computed == 0) PA_TRACE_MARK(3);
+#endif
       const int id = __shfl_sync(0xffffffffu, id0, t);
       float sl2 = a.scale_log2, v_mul = 1.f;
       if constexpr (FP8) {
@@ -554,8 +689,7 @@ decode_kernel(const DecodeArgs a) {
         v_mul = __shfl_sync(0xffffffffu, vs0, t) * kPBoost;
       }
       if (id >= 0 && id < a.num_blocks) {
-        const int j = ch0.cb0 + warp + kWarps * t;
-        const int n_valid = min(16, L - j * 16);
+        const int n_valid = min(16, L - (ch0.cb0 + t) * 16);
         attend_block<D, FP8, BF16>(st, qf, ring + s * TL::SLOT, ring + s * TL::SLOT + TL::BYTES,
                                    n_valid, sl2, v_mul, r, c);
       }
@@ -564,89 +698,46 @@ decode_kernel(const DecodeArgs a) {
       top_up();
     }
 
-    // does this chunk end its piece?
+    // ---- does this chunk end its piece?  Then the warp's result is final.
     const int nbk = seg_blocks(pf, ch0.b, Hkv);
     const int64_t s0 = pf[ch0.b] + static_cast<int64_t>(ch0.h) * nbk;
     const bool piece_end = ch0.cb0 + ch0.nb == static_cast<int>(min(hi, s0 + nbk) - s0);
     if (piece_end) {
-      // ---- piece epilogue: combine the warps, then output or partial
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
         st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, o);
         st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, o);
       }
-      {
-        float* wo = mo + warp * kGroupMax * D;
-#pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
-          const int dl = d_lo<D, FP8>(i, r), dh = d_hi<D, FP8>(i, r);
-          wo[(2 * c) * D + dl] = st.o[i][0];
-          wo[(2 * c + 1) * D + dl] = st.o[i][1];
-          wo[(2 * c) * D + dh] = st.o[i][2];
-          wo[(2 * c + 1) * D + dh] = st.o[i][3];
-        }
-        if (r == 0) {
-          mm[warp * kGroupMax + 2 * c] = st.m0;
-          mm[warp * kGroupMax + 2 * c + 1] = st.m1;
-          ml[warp * kGroupMax + 2 * c] = st.l0;
-          ml[warp * kGroupMax + 2 * c + 1] = st.l1;
-        }
-      }
-      __syncthreads();
-      const bool whole = s0 >= lo && s0 + nbk <= hi;
-      const int slot = piece_no == 0 ? 0 : 1;
-      const int64_t row0 = static_cast<int64_t>(ch0.b) * Hq + ch0.h * G;
-      OutT* out_rows = static_cast<OutT*>(a.out) + row0 * D;
-      for (int idx = tid; idx < G * D; idx += kThreads) {
-        const int g = idx / D, d = idx - g * D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * kGroupMax + g]);
-        float sum = 0.f, acc = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < kWarps; ++w) {
-            const float e = fast_exp2(mm[w * kGroupMax + g] - M);
-            sum += e * ml[w * kGroupMax + g];
-            acc += e * mo[(w * kGroupMax + g) * D + d];
-          }
-        }
-        acc *= unboost;
-        if (whole) {
-          out_rows[idx] = from_f32<OutT>(sum > 0.f ? acc / sum : 0.f);
-        } else {
-          const int64_t row = piece_row(cta, slot, g);
-          a.ws_acc[row * D + d] = acc;
-          if (d == 0) {
-            a.ws_ml[row * 2] = M;
-            a.ws_ml[row * 2 + 1] = sum;
-          }
-        }
-      }
-      if (!whole) {
+      if (s0 >= lo && s0 + nbk <= hi) {
+        uint16_t* rows = static_cast<uint16_t*>(a.out) +
+                         (static_cast<int64_t>(ch0.b) * Hq + ch0.h * G) * D;
+        store_output<D, FP8, BF16>(st, rows, G, r, c, unboost);
+      } else if (a.ws_acc == nullptr || a.counters == nullptr) {
+        if (lane == 0) atomicOr(a.status, kStatusNoWorkspace);   // never written through null
+      } else {
+        const int slot = piece_no == 0 ? 0 : 1;
+        store_partial<D, FP8>(st, a, gw, slot, r, c, unboost);
         __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-          // count this piece; whether it was the last is checked at the end
+        __syncwarp();
+        if (lane == 0) {
+          // count this piece; whether it completed the segment is checked at the end
           pend_b[slot] = ch0.b;
           pend_h[slot] = ch0.h;
-          pend_np[slot] = cta_of(s0 + nbk - 1, W, NG) - cta_of(s0, W, NG) + 1;
+          pend_np[slot] = worker_of(s0 + nbk - 1, W, NW) - worker_of(s0, W, NW) + 1;
           pend_old[slot] = atomicAdd(a.counters + static_cast<int64_t>(ch0.b) * Hkv + ch0.h, 1);
         }
       }
-      __syncthreads();   // the combine scratch is free again
       ++piece_no;
       reset_acc();
     }
 
     // ---- advance to chunk k+1
-    const bool new_piece = piece_end;
     ch0 = ch1;
     ch1 = ch2;
     ch2 = next_chunk(ch2, hi, pf, B, Hkv);
     id0 = id1;
     id1 = id2;
-    id2 = load_chunk_id(a, ch2, warp, lane);
+    id2 = load_chunk_id(a, ch2, lane);
     if constexpr (FP8) {
       ks0 = ks1;
       vs0 = vs1;
@@ -656,30 +747,19 @@ decode_kernel(const DecodeArgs a) {
         vs1 = __ldg(a.v_scale + static_cast<int64_t>(id1) * Hkv + ch1.h);
       }
     }
-    if (ic == 1) {
-      ic = 0;
-    } else {
-      ic = 0;
-      it = 0;
-    }
-    if (new_piece && ch0.nb > 0) {
+    if (ic == 0) it = 0;        // the cursor had fetched all of chunk k
+    ic = 0;
+    if (piece_end && ch0.nb > 0) {
 #pragma unroll
       for (int i = 0; i < D / 16; ++i) {
         qf[i][0] = qn[i][0];
         qf[i][1] = qn[i][1];
       }
-      // prefetch the query of the piece after this one
-      int b = ch0.b, h = ch0.h + 1;
-      if (h == Hkv) {
-        h = 0;
-        ++b;
-        while (b < B && pf[b + 1] == pf[b]) ++b;
-      }
-      if (b < B && pf[b] + static_cast<int64_t>(h) * seg_blocks(pf, b, Hkv) < hi)
-        load_query<D, FP8>(qn, a, b, h, r, c);
+      prefetch_next_query(ch0.b, ch0.h);
     }
     top_up();
   }
+  PA_TRACE_MARK(4);
 
   if (dead) {
     // Wait (bounded) for this warp's copies still in flight.
@@ -687,81 +767,33 @@ decode_kernel(const DecodeArgs a) {
       (void)mbar_wait(sbar + 8 * (computed % STAGES), (computed / STAGES) & 1);
   }
 
-  // ---- 4. merges: for each of this CTA's split pieces, the CTA that
-  // finished the segment's last piece combines all of them
+  // ---- 4. merges: for each of this warp's split pieces, the warp that
+  // completed the segment's count combines all of its pieces
+#pragma unroll
   for (int k = 0; k < 2; ++k) {
-    if (tid == 0) {
-      int job = -1;
-      if (pend_b[k] >= 0 && pend_old[k] == pend_np[k] - 1) {
-        atomicExch(a.counters + static_cast<int64_t>(pend_b[k]) * Hkv + pend_h[k], 0);
-        job = pend_b[k];
-      }
-      misc[4] = job;
-      misc[5] = pend_h[k];
+    int job = -1;
+    if (lane == 0 && pend_b[k] >= 0 && pend_old[k] == pend_np[k] - 1) {
+      atomicExch(a.counters + static_cast<int64_t>(pend_b[k]) * Hkv + pend_h[k], 0);
+      job = pend_b[k];
     }
-    __syncthreads();
-    const int mb = misc[4], mh = misc[5];
-    if (mb >= 0) {
+    job = __shfl_sync(0xffffffffu, job, 0);
+    const int mh = __shfl_sync(0xffffffffu, pend_h[k], 0);
+    if (job >= 0) {
       __threadfence();
-      const int nbk = seg_blocks(pf, mb, Hkv);
-      const int64_t s0 = pf[mb] + static_cast<int64_t>(mh) * nbk;
-      const int c0 = cta_of(s0, W, NG), c1 = cta_of(s0 + nbk - 1, W, NG);
-      const int first_slot = s0 > cta_lo(c0, W, NG) ? 1 : 0;   // slot of c0's piece
-      const int np = c1 - c0 + 1;
-      float* sM = mm;
-      float* sS = ml;
-      for (int g = warp; g < G; g += kWarps) {
-        float M = -INFINITY;
-        for (int q = lane; q < np; q += 32) {
-          const int64_t row = piece_row(c0 + q, q == 0 ? first_slot : 0, g);
-          M = fmaxf(M, __ldcg(a.ws_ml + row * 2));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float S = 0.f;
-        for (int q = lane; q < np; q += 32) {
-          const int64_t row = piece_row(c0 + q, q == 0 ? first_slot : 0, g);
-          S += fast_exp2(__ldcg(a.ws_ml + row * 2) - M) * __ldcg(a.ws_ml + row * 2 + 1);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-        if (lane == 0) {
-          sM[g] = M;
-          sS[g] = S;
-        }
-      }
-      __syncthreads();
-      OutT* out_rows = static_cast<OutT*>(a.out) + (static_cast<int64_t>(mb) * Hq + mh * G) * D;
-      for (int idx = tid; idx < G * (D / 4); idx += kThreads) {
-        const int g = idx / (D / 4), d4 = idx - g * (D / 4);
-        const float M = sM[g];
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q = 0; q < np; ++q) {
-          const int64_t row = piece_row(c0 + q, q == 0 ? first_slot : 0, g);
-          const float e = fast_exp2(__ldcg(a.ws_ml + row * 2) - M);
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + row * D) + d4);
-          acc.x += e * v.x;
-          acc.y += e * v.y;
-          acc.z += e * v.z;
-          acc.w += e * v.w;
-        }
-        const float S = sS[g];
-        const float ok = S > 0.f ? 1.f : 0.f;
-        OutT* o = out_rows + g * D + 4 * d4;
-        o[0] = from_f32<OutT>(ok * (acc.x / S));
-        o[1] = from_f32<OutT>(ok * (acc.y / S));
-        o[2] = from_f32<OutT>(ok * (acc.z / S));
-        o[3] = from_f32<OutT>(ok * (acc.w / S));
-      }
+      const int nbk = seg_blocks(pf, job, Hkv);
+      const int64_t s0 = pf[job] + static_cast<int64_t>(mh) * nbk;
+      const int w0 = worker_of(s0, W, NW), w1 = worker_of(s0 + nbk - 1, W, NW);
+      const int first_slot = s0 > worker_lo(w0, W, NW) ? 1 : 0;   // slot of w0's piece
+      merge_pieces<D, BF16>(a, job, mh, w0, first_slot, w1 - w0 + 1, lane);
     }
-    __syncthreads();
   }
+  PA_TRACE_MARK(5);
 }
 
 template <int D, bool FP8, bool BF16, int STAGES>
 cudaError_t launch_one(const DecodeArgs& a, cudaStream_t s) {
   using TL = Tile<D, FP8, STAGES>;
-  const Layout lay = make_layout(TL::RING, D, STAGES, a.B);
+  const Layout lay = make_layout(TL::RING, STAGES, a.B);
   auto* kern = decode_kernel<D, FP8, BF16, STAGES>;
   static thread_local int last_smem[64] = {0};
   int dev = 0;
@@ -776,11 +808,18 @@ cudaError_t launch_one(const DecodeArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+#ifndef PA_RING_KB
+#define PA_RING_KB 96
+#endif
+
 template <int D, bool FP8, bool BF16>
 cudaError_t launch_dtype(const DecodeArgs& a, cudaStream_t s) {
-  // Ring depth per warp: 2 slots of 8 KB (16-bit, D=128) keep two CTAs per
-  // SM within shared memory; E4M3 tiles are half as large, so 4 slots.
-  constexpr int STAGES = FP8 ? 4 : (D == 128 ? 2 : 4);
+  // Ring depth per warp: PA_RING_KB of rings per CTA (96 KB: 3 slots of 8 KB
+  // for 16-bit D=128 tiles, 6 of 4 KB, 12 of 2 KB) keeps two CTAs per SM
+  // within shared memory while one slot per warp is being read.
+  constexpr int SLOT = 2 * 16 * (FP8 ? D : 2 * D);
+  constexpr int STAGES = PA_RING_KB * 1024 / (kWarps * SLOT);
+  static_assert(STAGES >= 2, "ring too small");
   return launch_one<D, FP8, BF16, STAGES>(a, s);
 }
 
@@ -790,7 +829,7 @@ int decode_default_ctas() { return device_sm_count() * kCtasPerSm; }
 
 size_t decode_workspace_bytes(int B, int Hq, int D, int split_ctas) {
   if (B <= 0 || Hq <= 0 || D <= 0 || split_ctas <= 0) return 0;
-  const int64_t rows = static_cast<int64_t>(split_ctas) * 2 * kGroupMax;
+  const int64_t rows = static_cast<int64_t>(split_ctas) * kWarps * 2 * kGroupMax;
   const size_t acc = ((static_cast<size_t>(rows) * D * 4) + 255) & ~static_cast<size_t>(255);
   const size_t ml = ((static_cast<size_t>(rows) * 2 * 4) + 255) & ~static_cast<size_t>(255);
   const int64_t Bc = B < kMaxBatchPerLaunch ? B : kMaxBatchPerLaunch;
@@ -798,7 +837,7 @@ size_t decode_workspace_bytes(int B, int Hq, int D, int split_ctas) {
 }
 
 void decode_workspace_split(const DecodeArgs& a, void* ws, float** acc, float** ml, int** cnt) {
-  const int64_t rows = static_cast<int64_t>(a.split_ctas) * 2 * kGroupMax;
+  const int64_t rows = static_cast<int64_t>(a.split_ctas) * kWarps * 2 * kGroupMax;
   const size_t acc_bytes = ((static_cast<size_t>(rows) * a.D * 4) + 255) & ~static_cast<size_t>(255);
   const size_t ml_bytes = ((static_cast<size_t>(rows) * 2 * 4) + 255) & ~static_cast<size_t>(255);
   *acc = static_cast<float*>(ws);

@@ -10,7 +10,7 @@ namespace pa {
 
 // Sequences per decode launch: each CTA keeps per-sequence prefix sums of
 // the batch in shared memory; the host splits larger batches.
-constexpr int kMaxBatchPerLaunch = 2048;
+constexpr int kMaxBatchPerLaunch = 512;
 
 // All pointers are device pointers; sizes were validated by the caller.
 struct DecodeArgs {

@@ -15,6 +15,7 @@ constexpr unsigned kStatusBadBlock = 1u;   // block id outside [0, num_blocks)
 constexpr unsigned kStatusBadLen = 2u;     // context_len negative or above the stated bounds
 constexpr unsigned kStatusBadSlot = 4u;    // slot outside [0, num_blocks * block_size)
 constexpr unsigned kStatusTimeout = 8u;    // an mbarrier wait hit its iteration limit
+constexpr unsigned kStatusNoWorkspace = 16u;  // a split partition found no workspace
 
 // Iteration limit of every mbarrier wait.  A wait that ends normally takes a
 // few microseconds.  Each try_wait suspends the thread for at most

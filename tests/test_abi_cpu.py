@@ -66,16 +66,18 @@ def test_decode_argument_errors(lib):
     assert _decode(lib, ws=None) == _abi.PA_ERR_WORKSPACE
     assert _decode(lib, ws_bytes=16) == _abi.PA_ERR_WORKSPACE
     assert _decode(lib, ws=FAKE + 16) == _abi.PA_ERR_WORKSPACE      # not 256-aligned
+    assert _decode(lib, splits=1, ws=None) == _abi.PA_ERR_WORKSPACE # a single CTA needs one too
     assert _decode(lib, B=0) == _abi.PA_OK                          # nothing to do
 
 
 def test_workspace_size_formula(lib):
-    # partial rows: 2 per CTA, 8 query-head slots each, D floats + (max, sum); then counters
+    # partial rows: 2 per warp (4 warps per CTA), 8 query-head slots each, D floats +
+    # (max, sum); then counters
     n = lib.pa_decode_workspace_size(2, 8, 64, 10)
-    rows = 10 * 2 * 8
+    rows = 10 * 4 * 2 * 8
     acc, ml, counters = rows * 64 * 4, rows * 2 * 4, 2 * 8 * 4
     assert n == ((acc + 255) // 256) * 256 + ((ml + 255) // 256) * 256 + counters
-    assert lib.pa_decode_workspace_size(2, 8, 64, 1) == 0       # one CTA never splits
+    assert lib.pa_decode_workspace_size(2, 8, 64, 1) > 0        # one CTA's 4 warps still split
     assert lib.pa_decode_workspace_size(2, 8, 64, -1) == 0      # invalid
     # batches above 2048 sequences run in launches of 2048 that share the workspace
     assert lib.pa_decode_workspace_size(5000, 8, 64, 10) == \
