@@ -71,7 +71,8 @@ enum {
     PA_ERR_WORKSPACE = 3,    /* workspace missing, too small or misaligned */
     PA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
     PA_ERR_BOUNDS = 5,       /* pa_get_status: a kernel skipped an out-of-range index */
-    PA_ERR_TIMEOUT = 6       /* pa_get_status: an asynchronous-copy wait gave up */
+    PA_ERR_TIMEOUT = 6,      /* pa_get_status: an asynchronous-copy wait gave up */
+    PA_ERR_SCRATCH_LIMIT = 7 /* pa_decode_noalloc: sizes need more than its static scratch */
 };
 
 /* Bits of the device status word (pa_get_status). */
@@ -192,6 +193,30 @@ int pa_decode_fp8(void *out, const void *q, const uint8_t *k_cache, const uint8_
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                   int num_blocks, float scale, int split_ctas, void *workspace,
                   size_t workspace_bytes, void *stream);
+
+/*
+ * pa_decode without a caller-provided workspace, for callers that cannot
+ * allocate device memory: code inside a host framework that owns all device
+ * memory and forbids raw allocations, latency-critical loops where
+ * cudaMalloc would synchronise the device, plain C callers without a device
+ * allocator.  The paper has no counterpart; it exists for those callers.
+ *
+ * Arguments and results are those of pa_decode (16-bit pools); the scratch
+ * lives in a static array of PA_NOALLOC_SCRATCH_BYTES inside the library,
+ * held by every GPU that loads it until the process exits.  Sizes whose
+ * scratch would exceed it return PA_ERR_SCRATCH_LIMIT (the default split at
+ * head_dim 128 needs about 10 MB on a 152-SM GPU).  The call allocates
+ * nothing and frees nothing; it clears the scratch's merge counters on
+ * `stream` before each launch.  The first call on a device looks up the
+ * array's device address (make it before any stream capture).  All calls on
+ * a device share the array: calls that overlap on the GPU race.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, int max_context_len, int num_seqs,
+                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                      int num_blocks, float scale, int dtype, int split_ctas, void *stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status

@@ -18,7 +18,8 @@ from . import build as _build
 
 PA_F16, PA_BF16 = 0, 1
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_BOUNDS, \
-    PA_ERR_TIMEOUT = range(7)
+    PA_ERR_TIMEOUT, PA_ERR_SCRATCH_LIMIT = range(8)
+PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_LEN, PA_STATUS_BAD_SLOT, PA_STATUS_TIMEOUT = 1, 2, 4, 8
 PA_STATUS_NO_WORKSPACE = 16
 
@@ -38,6 +39,8 @@ SIGNATURES = {
                    _f32, _i32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                        _i32, _i32, _f32, _i32, _vp, _sz, _vp], _i32),
+    "pa_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                           _i32, _i32, _f32, _i32, _i32, _vp], _i32),
     "pa_get_status": ([_vp, ctypes.POINTER(ctypes.c_uint)], _i32),
 }
 
@@ -253,6 +256,24 @@ def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, cont
                                 _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
                                 float(scale), int(split_ctas), _ptr(workspace), ws_bytes,
                                 _stream(dev)), "pa_decode_fp8")
+
+
+def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
+                      max_context_len: int, scale: float, split_ctas: int = 0) -> None:
+    """pa_decode with the library's static scratch instead of a workspace (allocates nothing)."""
+    dev = q.device
+    act = (torch.float16, torch.bfloat16)
+    _need(q, "q", act, 3, dev)
+    _need(out, "out", q.dtype, 3, dev)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, q.dtype, 4, dev)
+    B, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
+    NB, Hkv, bs, _ = k_cache.shape
+    _check(load().pa_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                                    int(max_context_len), B, Hq, Hkv, D, bs, NB, float(scale),
+                                    _act_code(q.dtype), int(split_ctas), _stream(dev)),
+           "pa_decode_noalloc")
 
 
 def pa_get_status(device=None) -> tuple[int, int]:

@@ -123,6 +123,13 @@ int device_sm_count() {
   return device_state(&d) == PA_OK ? d->sm_count : 148;
 }
 
+int device_status_word(unsigned** out) {
+  DeviceState* d = nullptr;
+  if (int rc = device_state(&d)) return rc;
+  *out = d->status;
+  return PA_OK;
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -140,6 +147,7 @@ const char* pa_status_string(int code) {
     case PA_ERR_CUDA: return "CUDA error";
     case PA_ERR_BOUNDS: return "a kernel skipped an out-of-range index";
     case PA_ERR_TIMEOUT: return "an asynchronous-copy wait gave up";
+    case PA_ERR_SCRATCH_LIMIT: return "request exceeds the library's static scratch array";
     default: return "unknown status";
   }
 }

@@ -1,0 +1,120 @@
+// noalloc.cu -- pa_decode_noalloc: paged GQA decode for callers that cannot
+// allocate device memory.
+//
+// pa_decode needs a caller-allocated workspace (the partial results of
+// context partitions split across warps and one merge counter per
+// (sequence, kv head)).  Some callers cannot provide one: code running inside
+// a host framework that owns every byte of device memory and forbids raw
+// allocations, latency-critical serving loops where cudaMalloc would
+// synchronise the device, and plain C callers with no device allocator of
+// their own.  This entry point runs the same kernel with its scratch in a
+// fixed array compiled into the library, so it allocates nothing.
+//
+// The array is PA_NOALLOC_SCRATCH_BYTES (16 MiB); every GPU that loads the
+// library holds it until the process exits.  All calls on a device share it
+// and it keeps the last call's contents; the merge counters, which must start
+// at zero, are cleared on the caller's stream before each launch.  Calls that
+// overlap on the GPU (different streams, or different host threads) race on
+// the array and must not be issued.
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "pa.h"
+#include "pa_launch.h"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device with that device current, and cached.
+int scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return PA_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return PA_OK;
+}
+
+bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                 const void* v_cache, const int32_t* block_tables,
+                                 int max_blocks_per_seq, const int32_t* context_lens,
+                                 int max_context_len, int num_seqs, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                 float scale, int dtype, int split_ctas, void* stream) {
+  using namespace pa;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return PA_ERR_INVALID_ARG;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 || split_ctas < 0)
+    return PA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(max_context_len) >
+      static_cast<int64_t>(max_blocks_per_seq) * block_size)
+    return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size != 16) return PA_ERR_UNSUPPORTED;
+  if (num_q_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  for (const void* p : {static_cast<const void*>(out), q, k_cache, v_cache})
+    if (!aligned_to(p, 16)) return PA_ERR_INVALID_ARG;
+  if (!aligned_to(block_tables, 4) || !aligned_to(context_lens, 4)) return PA_ERR_INVALID_ARG;
+
+  // set-up on the first call on this device: the scratch array's address
+  void* ws = nullptr;
+  if (int rc = scratch_address(&ws)) return rc;
+  unsigned* status = nullptr;
+  if (int rc = device_status_word(&status)) return rc;
+  const int splits = split_ctas == 0 ? decode_default_ctas() : split_ctas;
+  const size_t need = decode_workspace_bytes(num_seqs, num_q_heads, head_dim, splits);
+  if (need == 0 || need > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_SCRATCH_LIMIT;
+
+  DecodeArgs a{};
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.status = status;
+  a.mbs = max_blocks_per_seq;
+  a.Hq = num_q_heads;
+  a.Hkv = num_kv_heads;
+  a.group = num_q_heads / num_kv_heads;
+  a.D = head_dim;
+  a.num_blocks = num_blocks;
+  a.max_context_len = max_context_len;
+  a.split_ctas = splits;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t row = static_cast<size_t>(num_q_heads) * head_dim * 2;
+  for (int b0 = 0; b0 < num_seqs; b0 += kMaxBatchPerLaunch) {
+    DecodeArgs c = a;
+    c.B = num_seqs - b0 < kMaxBatchPerLaunch ? num_seqs - b0 : kMaxBatchPerLaunch;
+    c.out = static_cast<uint8_t*>(out) + b0 * row;
+    c.q = static_cast<const uint8_t*>(q) + b0 * row;
+    c.block_tables = block_tables + static_cast<int64_t>(b0) * max_blocks_per_seq;
+    c.context_lens = context_lens + b0;
+    decode_workspace_split(c, ws, &c.ws_acc, &c.ws_ml, &c.counters);
+    // the merge counters must start at zero: clear them on the stream
+    const size_t cnt_bytes = static_cast<size_t>(c.B) * num_kv_heads * sizeof(int);
+    if (cudaMemsetAsync(c.counters, 0, cnt_bytes, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_decode(c, false, dtype == PA_BF16, s) != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}

@@ -56,5 +56,7 @@ cudaError_t launch_quantize_fp8(const void* src, uint8_t* codes, float* scales,
 cudaError_t launch_e4m3_encode(const float* x, uint8_t* codes, int64_t n, cudaStream_t s);
 
 int device_sm_count();
+// Address of the current device's status word (set up on first use).
+int device_status_word(unsigned** out);
 
 }  // namespace pa
