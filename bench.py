@@ -182,6 +182,23 @@ def oracle_baseline(w, budget_s: float = 10.0) -> dict:
                       f"{w.Hq} q heads) x {reps} passes, fp64 two-pass softmax, {dt:.1f} s"}
 
 
+# ---------------------------------------------------------------- replicas
+def replica_seed(seed: int, rank: int) -> int:
+    """Each rank draws its own batch: N GPUs run N independent replicas."""
+    return seed + rank
+
+
+def reduce_over_ranks(step_ms: float, e2e_ms: float, tokens: int, world: int, dev):
+    """Whole-job figures: the slowest rank's times and the tokens of all ranks."""
+    if world <= 1:
+        return step_ms, e2e_ms, float(tokens)
+    t = torch.tensor([step_ms, e2e_ms], dtype=torch.float64, device=dev)
+    n = torch.tensor([float(tokens)], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(n, op=torch.distributed.ReduceOp.SUM)
+    return t[0].item(), t[1].item(), n[0].item()
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, rank, world, dev):
     from paged_kv_cache_179_gb300 import _abi
@@ -189,7 +206,7 @@ def run_ours(args, rank, world, dev):
     from paged_kv_cache_179_gb300.step import DecodeStep
 
     _abi.load()
-    w = W.make_workload(args.config, seed=args.seed + rank, device=dev)
+    w = W.make_workload(args.config, seed=replica_seed(args.seed, rank), device=dev)
     lens = w.context_lens.cpu().numpy()
     tokens = int(lens.sum())
     if w.kv == "fp8":
@@ -283,16 +300,7 @@ def run_ours(args, rank, world, dev):
         raise RuntimeError(f"device status {rc} bits {bits}")
     clk = clocks.stop() if rank == 0 else None
 
-    # whole-job aggregation: max time over ranks, tokens summed over ranks
-    t = torch.tensor([total_ms, e2e_ms, float(tokens)], dtype=torch.float64, device=dev)
-    if world > 1:
-        tmax = t.clone()
-        torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
-        tsum = t.clone()
-        torch.distributed.all_reduce(tsum, op=torch.distributed.ReduceOp.SUM)
-        total_ms_max, e2e_ms_max, tokens_all = tmax[0].item(), tmax[1].item(), tsum[2].item()
-    else:
-        total_ms_max, e2e_ms_max, tokens_all = total_ms, e2e_ms, float(tokens)
+    total_ms_max, e2e_ms_max, tokens_all = reduce_over_ranks(total_ms, e2e_ms, tokens, world, dev)
     if rank != 0:
         return None
 
