@@ -53,25 +53,32 @@
 
 // Opt-in trace build (-DPA_TRACE): thread 0 of each CTA records %globaltimer
 // at the phases of the kernel; pa_trace_read copies them out.
+// Opt-in trace build (-DPA_TRACE): lane 0 of every worker warp records
+// %globaltimer at its phases and its piece counts; pa_trace_read copies them.
+// Slots per worker: 0 kernel entry, 1 first tile ready, 2 last block done,
+// 3 end, 4 pieces, 5 split pieces, 6 blocks.
 #ifdef PA_TRACE
-__device__ unsigned long long g_pa_trace[8192 * 8];
-#define PA_TRACE_MARK(k)                                                        \
-  do {                                                                          \
-    if (threadIdx.x == 0 && blockIdx.x < 8192) {                                \
-      unsigned long long t_;                                                    \
-      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                    \
-      g_pa_trace[blockIdx.x * 8 + (k)] = t_;                                    \
-    }                                                                           \
+__device__ unsigned long long g_pa_trace[16384 * 8];
+#define PA_TRACE_WARP(w, k, v)                                                   \
+  do {                                                                           \
+    if ((threadIdx.x & 31) == 0 && (w) < 16384) g_pa_trace[(w) * 8 + (k)] = (v);   \
   } while (0)
-extern "C" int pa_trace_read(unsigned long long* host, int n) {
-  return cudaMemcpyFromSymbol(host, g_pa_trace, sizeof(unsigned long long) * 8 *
-                                                    static_cast<size_t>(n < 8192 ? n : 8192)) ==
-                 cudaSuccess ? 0 : 4;
+__device__ __forceinline__ unsigned long long pa_now() {
+  unsigned long long t_;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));
+  return t_;
 }
+extern "C" int pa_trace_read(unsigned long long* host, int n_workers) {
+  const size_t n = static_cast<size_t>(n_workers < 16384 ? n_workers : 16384) * 8;
+  return cudaMemcpyFromSymbol(host, g_pa_trace, sizeof(unsigned long long) * n) == cudaSuccess
+             ? 0 : 4;
+}
+#define PA_TRACE_ONLY(x) x
 #else
-#define PA_TRACE_MARK(k) \
-  do {               \
+#define PA_TRACE_WARP(w, k, v) \
+  do {                         \
   } while (0)
+#define PA_TRACE_ONLY(x)
 #endif
 
 namespace pa {
@@ -443,6 +450,16 @@ __device__ __forceinline__ void store_partial(const WarpAcc<D>& st, const Decode
   }
 }
 
+// atomicAdd with acquire-release semantics at GPU scope: it publishes the
+// warp's partial (stored before it, ordered by __syncwarp) and, for the last
+// arriver, makes every other piece's partial visible.
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 // (max, sum) pair combine of two partial softmax states in log2 units.
 __device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s2) {
   const float mn = fmaxf(m, m2);
@@ -454,7 +471,7 @@ __device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s
 // The warp that completed segment (b, h) merges its np pieces, held by
 // workers w0 .. w0+np-1 (slot first_slot for w0, slot 0 for the others):
 //   out = sum_q 2^(m_q - M) acc_q / sum_q 2^(m_q - M) l_q,  M = max_q m_q.
-template <int D, bool BF16>
+template <int D, bool FP8, bool BF16>
 __device__ void merge_pieces(const DecodeArgs& a, int b, int h, int w0, int first_slot, int np,
                              int lane) {
   const int G = a.group;
@@ -485,6 +502,9 @@ __device__ void merge_pieces(const DecodeArgs& a, int b, int h, int w0, int firs
     float4 acc[kGroupMax];
 #pragma unroll
     for (int g = 0; g < kGroupMax; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // The two-piece passes below keep twice the loads in flight; the E4M3
+    // instantiation keeps the one-piece loop, measured faster for it.
+    if constexpr (FP8) {
     for (int q = 0; q < np; ++q) {
       const int slot = q == 0 ? first_slot : 0;
 #pragma unroll
@@ -498,6 +518,38 @@ __device__ void merge_pieces(const DecodeArgs& a, int b, int h, int w0, int firs
         acc[g].z += e * v.z;
         acc[g].w += e * v.w;
       }
+    }
+    } else {
+    // two pieces per pass, all of a pass's loads issued before they are used
+    for (int q = 0; q < np; q += 2) {
+      const bool two = q + 1 < np;
+      float ma[kGroupMax], mb[kGroupMax];
+      float4 va[kGroupMax], vb[kGroupMax];
+#pragma unroll
+      for (int g = 0; g < kGroupMax; ++g) {
+        ma[g] = mb[g] = -INFINITY;
+        va[g] = vb[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (g >= G || M[g] == -INFINITY) continue;
+        const int64_t ra = piece_row(w0 + q, q == 0 ? first_slot : 0, g);
+        ma[g] = __ldcg(a.ws_ml + ra * 2);
+        va[g] = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + ra * D) + d4);
+        if (two) {
+          const int64_t rb = piece_row(w0 + q + 1, 0, g);
+          mb[g] = __ldcg(a.ws_ml + rb * 2);
+          vb[g] = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + rb * D) + d4);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < kGroupMax; ++g) {
+        if (g >= G || M[g] == -INFINITY) continue;
+        const float ea = fast_exp2(ma[g] - M[g]);
+        const float eb = two ? fast_exp2(mb[g] - M[g]) : 0.f;
+        acc[g].x += ea * va[g].x + eb * vb[g].x;
+        acc[g].y += ea * va[g].y + eb * vb[g].y;
+        acc[g].z += ea * va[g].z + eb * vb[g].z;
+        acc[g].w += ea * va[g].w + eb * vb[g].w;
+      }
+    }
     }
 #pragma unroll
     for (int g = 0; g < kGroupMax; ++g) {
@@ -524,7 +576,7 @@ decode_kernel(const DecodeArgs a) {
   int* len = reinterpret_cast<int*>(smem + lay.len);
   int* misc = reinterpret_cast<int*>(smem + lay.misc);   // [0..3] warp sums of the scan
 
-  PA_TRACE_MARK(0);
+  PA_TRACE_ONLY(const unsigned long long t_entry = pa_now());
   // ---- 1. blocks per sequence and their prefix sum (segments of Hkv * nblk)
   {
     const int per = (B + kThreads - 1) / kThreads;
@@ -553,7 +605,6 @@ decode_kernel(const DecodeArgs a) {
     if (tid == kThreads - 1) pf[B] = ex;
     __syncthreads();
   }
-  PA_TRACE_MARK(1);
   const int64_t W = pf[B];
   const int cta = blockIdx.x;
 
@@ -654,7 +705,8 @@ decode_kernel(const DecodeArgs a) {
     }
   };
   top_up();
-  PA_TRACE_MARK(2);
+  PA_TRACE_WARP(gw, 0, t_entry);
+  PA_TRACE_ONLY(int tr_pieces = 0; int tr_split = 0);
 
   WarpAcc<D> st;
   auto reset_acc = [&]() {
@@ -679,9 +731,7 @@ decode_kernel(const DecodeArgs a) {
         dead = true;
         break;
       }
-#ifdef PA_TRACE
-      if (computed == 0) PA_TRACE_MARK(3);
-#endif
+      PA_TRACE_ONLY(if (computed == 0) PA_TRACE_WARP(gw, 1, pa_now()));
       const int id = __shfl_sync(0xffffffffu, id0, t);
       float sl2 = a.scale_log2, v_mul = 1.f;
       if constexpr (FP8) {
@@ -717,17 +767,18 @@ decode_kernel(const DecodeArgs a) {
       } else {
         const int slot = piece_no == 0 ? 0 : 1;
         store_partial<D, FP8>(st, a, gw, slot, r, c, unboost);
-        __threadfence();
         __syncwarp();
         if (lane == 0) {
           // count this piece; whether it completed the segment is checked at the end
           pend_b[slot] = ch0.b;
           pend_h[slot] = ch0.h;
           pend_np[slot] = worker_of(s0 + nbk - 1, W, NW) - worker_of(s0, W, NW) + 1;
-          pend_old[slot] = atomicAdd(a.counters + static_cast<int64_t>(ch0.b) * Hkv + ch0.h, 1);
+          pend_old[slot] =
+              atomic_add_acq_rel(a.counters + static_cast<int64_t>(ch0.b) * Hkv + ch0.h, 1);
         }
       }
       ++piece_no;
+      PA_TRACE_ONLY(++tr_pieces; tr_split += !(s0 >= lo && s0 + nbk <= hi));
       reset_acc();
     }
 
@@ -759,7 +810,7 @@ decode_kernel(const DecodeArgs a) {
     }
     top_up();
   }
-  PA_TRACE_MARK(4);
+  PA_TRACE_WARP(gw, 2, pa_now());
 
   if (dead) {
     // Wait (bounded) for this warp's copies still in flight.
@@ -779,15 +830,19 @@ decode_kernel(const DecodeArgs a) {
     job = __shfl_sync(0xffffffffu, job, 0);
     const int mh = __shfl_sync(0xffffffffu, pend_h[k], 0);
     if (job >= 0) {
-      __threadfence();
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      __syncwarp();
       const int nbk = seg_blocks(pf, job, Hkv);
       const int64_t s0 = pf[job] + static_cast<int64_t>(mh) * nbk;
       const int w0 = worker_of(s0, W, NW), w1 = worker_of(s0 + nbk - 1, W, NW);
       const int first_slot = s0 > worker_lo(w0, W, NW) ? 1 : 0;   // slot of w0's piece
-      merge_pieces<D, BF16>(a, job, mh, w0, first_slot, w1 - w0 + 1, lane);
+      merge_pieces<D, FP8, BF16>(a, job, mh, w0, first_slot, w1 - w0 + 1, lane);
     }
   }
-  PA_TRACE_MARK(5);
+  PA_TRACE_WARP(gw, 3, pa_now());
+  PA_TRACE_WARP(gw, 4, tr_pieces);
+  PA_TRACE_WARP(gw, 5, tr_split);
+  PA_TRACE_WARP(gw, 6, static_cast<unsigned long long>(hi - lo));
 }
 
 template <int D, bool FP8, bool BF16, int STAGES>
