@@ -4,8 +4,9 @@
 Default workload: the Qwen2.5-7B-shaped batch (128 sequences, 28 q / 4 kv
 heads, head_dim 128, fp16, lognormal context lengths with median 1024 clipped
 to [1, 8192]; seeded synthetic data).  A step is the whole hot path for one
-batch: pa_cache_append of the new token, then pa_decode (split-K attention
-and the log-sum-exp merge).  Between timed steps the L2 is not flushed when
+batch: pa_decode_step appends each sequence's new token and attends over
+its context in one launch (split-K attention with the log-sum-exp merge);
+``--unfused`` times pa_cache_append + pa_decode instead.  Between timed steps the L2 is not flushed when
 the step reads at least 3x the L2 size (429 MB of K/V against a 129 MB L2
 for the default batch); smaller batches have L2 evicted by reading a 2x-L2
 buffer outside the timed region.
@@ -67,7 +68,9 @@ def algorithmic_bytes(w, lens: np.ndarray) -> dict:
     qo = 2 * w.B * w.Hq * w.D * 2
     meta = int(nblk.sum()) * 4 + w.B * 4
     scales = int(nblk.sum()) * w.Hkv * 2 * 4 if w.kv == "fp8" else 0
-    return {"kv": kv, "q_out": qo, "meta": meta, "scales": scales,
+    # the fused step also reads this step's K/V rows and writes them to the pools
+    append = w.B * w.Hkv * w.D * 2 * (2 + e_kv) + w.B * 8
+    return {"kv": kv, "q_out": qo, "meta": meta, "scales": scales, "append": append,
             "total": kv + qo + meta + scales}
 
 
@@ -238,7 +241,11 @@ def run_ours(args, rank, world, dev):
         elif l2_mode == "write":
             flush_buf.add_(1)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 2   # append_kernel + decode_kernel
+    fused = not args.unfused
+    launches_per_step = 1 if fused else 2   # decode_kernel (fused) | append + decode
+
+    def run_step():
+        step(w.q, w.k_new, w.v_new, w.slot_mapping, out, fused=fused)
 
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     if rank == 0:
@@ -246,7 +253,7 @@ def run_ours(args, rank, world, dev):
     clocks.mark("warmup_start")
     for _ in range(args.warmup):
         flush()
-        step(w.q, w.k_new, w.v_new, w.slot_mapping, out)
+        run_step()
     rc, bits = _abi.pa_get_status(dev)
     if rc != 0:
         raise RuntimeError(f"device status {rc} bits {bits}")
@@ -265,18 +272,37 @@ def run_ours(args, rank, world, dev):
     for i in range(K):
         flush()
         ev[i][0].record(stream)
-        step.append(w.k_new, w.v_new, w.slot_mapping)
-        ev[i][1].record(stream)
-        step.decode(w.q, out)
+        if fused:
+            run_step()
+            ev[i][1].record(stream)
+        else:
+            step.append(w.k_new, w.v_new, w.slot_mapping)
+            ev[i][1].record(stream)
+            step.decode(w.q, out)
         ev[i][2].record(stream)
     torch.cuda.synchronize(dev)
     clocks.mark("timed_end")
     if world > 1:
         torch.distributed.barrier()
     step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    app_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    # the dominant kernel: the fused step kernel, or pa_decode's kernel
+    dec_ms = step_ms if fused else [e[1].elapsed_time(e[2]) for e in ev]
     total_ms = sum(step_ms)
+
+    # for reference: the same step as two launches (append, then decode)
+    sep = []
+    for i in range(min(K, 20)):
+        a0, a1, a2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        flush()
+        a0.record(stream)
+        step.append(w.k_new, w.v_new, w.slot_mapping)
+        a1.record(stream)
+        step.decode(w.q, out)
+        a2.record(stream)
+        sep.append((a0, a1, a2))
+    torch.cuda.synchronize(dev)
+    app_ms = [a0.elapsed_time(a1) for a0, a1, _ in sep]
+    dec2_ms = [a1.elapsed_time(a2) for _, a1, a2 in sep]
 
     # end to end through the public API with pinned host buffers
     host_in = {k: getattr(w, k).cpu().pin_memory()
@@ -285,13 +311,13 @@ def run_ours(args, rank, world, dev):
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     for _ in range(max(1, args.warmup)):
-        step.run_from_host(host_in, dev_in, host_out, out)
+        step.run_from_host(host_in, dev_in, host_out, out, fused=fused)
     torch.cuda.synchronize(dev)
     h2d = d2h = 0
     for i in range(K):
         flush()
         e2e_ev[i][0].record(stream)
-        h2d, d2h = step.run_from_host(host_in, dev_in, host_out, out)
+        h2d, d2h = step.run_from_host(host_in, dev_in, host_out, out, fused=fused)
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
@@ -307,7 +333,8 @@ def run_ours(args, rank, world, dev):
     ab = algorithmic_bytes(w, lens)
     dec_mean_s = statistics.mean(dec_ms) / 1e3
     peak, peak_kind = measured_peaks()
-    achieved = ab["total"] / dec_mean_s / 1e9
+    kernel_bytes = ab["total"] + (ab["append"] if fused else 0)
+    achieved = kernel_bytes / dec_mean_s / 1e9
     value = tokens_all * K / (total_ms_max / 1e3)
     traffic = load_traffic(args.config, step.split_ctas)
     line = {
@@ -316,22 +343,25 @@ def run_ours(args, rank, world, dev):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3->f32" if w.kv == "fp8" else w.dtype, "data": "synthetic",
         "config": {
-            "workload": describe(w, tokens), "step": "pa_cache_append + pa_decode",
+            "workload": describe(w, tokens),
+            "step": ("pa_decode_step (append + decode, one launch)" if fused
+                     else "pa_cache_append + pa_decode"),
             "split_ctas": step.split_ctas, "l2": describe_l2(l2_mode, kv_bytes, l2),
             "seed": args.seed, "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "hbm_gbs": round(achieved, 1), "hbm_frac_of_peak": round(achieved / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "pa_decode (decode_kernel, split-K merge fused)",
-                     "bytes_per_launch": ab["total"], "peak_source": peak_kind},
+                     "kernel": ("decode_kernel with fused append and split-K merge" if fused
+                                else "decode_kernel with fused split-K merge"),
+                     "bytes_per_launch": kernel_bytes, "peak_source": peak_kind},
         "decode_us": {"mean": round(statistics.mean(dec_ms) * 1e3, 2),
                       "median": round(statistics.median(dec_ms) * 1e3, 2),
                       "p20": round(float(np.percentile(dec_ms, 20)) * 1e3, 2),
                       "p80": round(float(np.percentile(dec_ms, 80)) * 1e3, 2),
                       "min": round(min(dec_ms) * 1e3, 2)},
-        "append_us": {"mean": round(statistics.mean(app_ms) * 1e3, 2),
-                      "median": round(statistics.median(app_ms) * 1e3, 2)},
+        "as_two_launches_us": {"append": round(statistics.mean(app_ms) * 1e3, 2),
+                               "decode": round(statistics.mean(dec2_ms) * 1e3, 2)},
         "e2e": {"value": round(tokens_all * K / (e2e_ms_max / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * K,
@@ -452,6 +482,8 @@ def main(argv=None):
     ap.add_argument("--l2", choices=["auto", "none", "read", "write"], default="auto",
                     help="L2 handling between timed steps (auto: none when the K/V read "
                          "is >= 3x L2, else evict by reading a 2x-L2 buffer)")
+    ap.add_argument("--unfused", action="store_true",
+                    help="time the step as pa_cache_append + pa_decode (two launches)")
     ap.add_argument("--prime-ms", type=float, default=0.0,
                     help="GPU sleep queued ahead of the timed steps so the host runs ahead")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -60,8 +60,9 @@
 extern "C" {
 #endif
 
-/* Element type of 16-bit activations and pools. */
-enum { PA_F16 = 0, PA_BF16 = 1 };
+/* Element type of activations and pools (PA_E4M3: pools only, for
+ * pa_decode_default_splits). */
+enum { PA_F16 = 0, PA_BF16 = 1, PA_E4M3 = 2 };
 
 /* Return codes. */
 enum {
@@ -133,17 +134,20 @@ int pa_quantize_fp8(const void *k_src, const void *v_src, uint8_t *k_cache, uint
 int pa_e4m3_encode(const float *x, uint8_t *codes, int64_t n, void *stream);
 
 /*
- * Number of CTAs pa_decode divides a batch among when split_ctas is 0: two
- * per SM of the current device, the count that is resident at once.
+ * Number of CTAs a decode divides a batch among when split_ctas is 0, on the
+ * current device, for pools of type pool_type (PA_F16 or PA_BF16: two per
+ * SM; PA_E4M3: three per SM; each the count that is resident at once).
+ * Returns 0 for another pool_type.
  */
-int pa_decode_default_splits(void);
+int pa_decode_default_splits(int pool_type);
 
 /*
  * Bytes of device workspace pa_decode / pa_decode_fp8 need: room for the
  * partial results of the context partitions that cross worker boundaries
  * (a worker is one warp; four per CTA; at most two partials each) and one
- * counter per (sequence, kv head).  split_ctas 0 means
- * pa_decode_default_splits() of the current device.  Every call needs one.
+ * counter per (sequence, kv head).  split_ctas 0 means the largest
+ * pa_decode_default_splits() over pool types on the current device, so the
+ * result serves a default call of any type.  Every call needs one.
  *
  * The caller allocates the workspace and must zero-fill it once before its
  * first use; every call that completes leaves the counters at zero again,
@@ -162,7 +166,7 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int
  * nearest even); a sequence with context_len 0 gets a zero output.
  *
  * The batch's (sequence, kv head, block) units are divided evenly among the
- * 4 * split_ctas warps of split_ctas CTAs (0: pa_decode_default_splits()).
+ * 4 * split_ctas warps of split_ctas CTAs (0: pa_decode_default_splits(dtype)).
  * A warp's share of one sequence is a context partition, reduced with an
  * online softmax in fp32; a sequence split across warps has its partitions
  * merged by log-sum-exp in the same launch.  Results do not depend on split_ctas beyond fp32
@@ -193,6 +197,46 @@ int pa_decode_fp8(void *out, const void *q, const uint8_t *k_cache, const uint8_
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                   int num_blocks, float scale, int split_ctas, void *workspace,
                   size_t workspace_bytes, void *stream);
+
+/*
+ * One whole decode step in one launch: append this step's K/V token of every
+ * sequence, then attend over the sequence's context including it, as
+ * pa_cache_append followed by pa_decode would, with the same results (the
+ * pools bit-identical, out within fp32 rounding).
+ *   k_new, v_new: [num_seqs][num_kv_heads][head_dim], the dtype of q;
+ *   slot_mapping: [num_seqs], the slot of position context_lens[b] - 1 of
+ *   sequence b (a decode step's slot), or negative for a padding sequence
+ *   that appends nothing.  Any other slot is not written and sets
+ *   PA_STATUS_BAD_SLOT.  A sequence with context_len 0 appends nothing.
+ * The warp that attends a sequence's last block writes the new row to the
+ * pool and into its copy of that block, so no launch-wide ordering is
+ * needed.  Other arguments as pa_decode.
+ * Source: rvLLM, CUDA Kernels table, "Reshape and Cache" and "PagedAttention
+ * V2"; rvLLM, Completed Optimizations (fused kernels, fewer launches); rvllm
+ * (small engine), How it's put together (write_positions then read_blocks in
+ * one forward).
+ */
+int pa_decode_step(void *out, const void *q, const void *k_new, const void *v_new,
+                   void *k_cache, void *v_cache, const int64_t *slot_mapping,
+                   const int32_t *block_tables, int max_blocks_per_seq,
+                   const int32_t *context_lens, int max_context_len, int num_seqs,
+                   int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                   int num_blocks, float scale, int dtype, int split_ctas, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/*
+ * pa_decode_step over E4M3 pools: fp16 q, k_new, v_new and out; the new row
+ * is encoded as pa_cache_append_fp8 does (a page's first row sets its K and
+ * V scales, later rows reuse them) and attended as pa_decode_fp8 does.
+ * Source: as pa_decode_step, and rvLLM, CUDA Kernels table, "FP8 KV Cache".
+ */
+int pa_decode_step_fp8(void *out, const void *q, const void *k_new, const void *v_new,
+                       uint8_t *k_cache, uint8_t *v_cache, float *k_scale, float *v_scale,
+                       const int64_t *slot_mapping, const int32_t *block_tables,
+                       int max_blocks_per_seq, const int32_t *context_lens, int max_context_len,
+                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, int num_blocks, float scale, int split_ctas,
+                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * pa_decode without a caller-provided workspace, for callers that cannot

@@ -16,7 +16,7 @@ import torch
 
 from . import build as _build
 
-PA_F16, PA_BF16 = 0, 1
+PA_F16, PA_BF16, PA_E4M3 = 0, 1, 2
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_BOUNDS, \
     PA_ERR_TIMEOUT, PA_ERR_SCRATCH_LIMIT = range(8)
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -34,11 +34,15 @@ SIGNATURES = {
     "pa_quantize_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
     "pa_e4m3_encode": ([_vp, _vp, _i64, _vp], _i32),
     "pa_decode_workspace_size": ([_i32, _i32, _i32, _i32], _sz),
-    "pa_decode_default_splits": ([], _i32),
+    "pa_decode_default_splits": ([_i32], _i32),
     "pa_decode": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                    _f32, _i32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                        _i32, _i32, _f32, _i32, _vp, _sz, _vp], _i32),
+    "pa_decode_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                        _i32, _i32, _i32, _f32, _i32, _i32, _vp, _sz, _vp], _i32),
+    "pa_decode_step_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
+                            _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                            _i32, _i32, _f32, _i32, _i32, _vp], _i32),
     "pa_get_status": ([_vp, ctypes.POINTER(ctypes.c_uint)], _i32),
@@ -193,8 +197,11 @@ def pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, split_ctas=0) -> i
     return int(load().pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, split_ctas))
 
 
-def pa_decode_default_splits() -> int:
-    return int(load().pa_decode_default_splits())
+def pa_decode_default_splits(pool_dtype=torch.float16) -> int:
+    """CTAs a default (split_ctas=0) decode uses over pools of this dtype
+    (torch.uint8 for E4M3 pools)."""
+    code = PA_E4M3 if pool_dtype == torch.uint8 else _act_code(pool_dtype)
+    return int(load().pa_decode_default_splits(code))
 
 
 def alloc_workspace(num_seqs, num_q_heads, head_dim, split_ctas, device):
@@ -256,6 +263,65 @@ def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, cont
                                 _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
                                 float(scale), int(split_ctas), _ptr(workspace), ws_bytes,
                                 _stream(dev)), "pa_decode_fp8")
+
+
+def _ws_bytes(workspace, dev):
+    if workspace is None:
+        return 0
+    _need(workspace, "workspace", None, None, dev)
+    return workspace.numel() * workspace.element_size()
+
+
+def pa_decode_step(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_tables,
+                   context_lens, max_context_len: int, scale: float, split_ctas: int = 0,
+                   workspace=None) -> None:
+    """Append k_new/v_new at slot_mapping, then decode, in one launch (16-bit pools)."""
+    dev = q.device
+    act = (torch.float16, torch.bfloat16)
+    _need(q, "q", act, 3, dev)
+    _need(out, "out", q.dtype, 3, dev)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, n, q.dtype, 3, dev)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, q.dtype, 4, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    B, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
+    NB, Hkv, bs, _ = k_cache.shape
+    if k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape or slot_mapping.shape[0] != B:
+        raise ValueError("shape mismatch")
+    _check(load().pa_decode_step(_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                 _ptr(v_cache), _ptr(slot_mapping), _ptr(block_tables),
+                                 block_tables.shape[1], _ptr(context_lens), int(max_context_len),
+                                 B, Hq, Hkv, D, bs, NB, float(scale), _act_code(q.dtype),
+                                 int(split_ctas), _ptr(workspace), _ws_bytes(workspace, dev),
+                                 _stream(dev)), "pa_decode_step")
+
+
+def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping,
+                       block_tables, context_lens, max_context_len: int, scale: float,
+                       split_ctas: int = 0, workspace=None) -> None:
+    """Append (E4M3-encode) k_new/v_new, then decode over the E4M3 pools, in one launch."""
+    dev = q.device
+    for t, n in ((q, "q"), (out, "out")):
+        _need(t, n, torch.float16, 3, dev)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, n, torch.float16, 3, dev)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.uint8, 4, dev)
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need(t, n, torch.float32, 2, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    B, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
+    NB, Hkv, bs, _ = k_cache.shape
+    if k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape or slot_mapping.shape[0] != B:
+        raise ValueError("shape mismatch")
+    _check(load().pa_decode_step_fp8(_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                     _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                     _ptr(slot_mapping), _ptr(block_tables), block_tables.shape[1],
+                                     _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs,
+                                     NB, float(scale), int(split_ctas), _ptr(workspace),
+                                     _ws_bytes(workspace, dev), _stream(dev)),
+           "pa_decode_step_fp8")
 
 
 def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,

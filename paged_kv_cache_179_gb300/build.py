@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpa.so")
 SOURCES = ["abi.cu", "append.cu", "quantize.cu", "decode.cu", "noalloc.cu"]
-HEADERS = ["pa_launch.h", "pa_ptx.cuh"]
+HEADERS = ["pa_launch.h", "pa_ptx.cuh", "pa_e4m3.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

@@ -68,9 +68,21 @@ int check_decode_shape(const DecodeShape& s, float scale) {
   return PA_OK;
 }
 
+// The fused step's extra inputs (all null for a plain decode).
+struct AppendArgs {
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  const int64_t* slots = nullptr;
+  void* k_pool = nullptr;
+  void* v_pool = nullptr;
+  float* k_scale = nullptr;
+  float* v_scale = nullptr;
+};
+
 int run_decode(DecodeShape s, void* out, const void* q, const void* k, const void* v,
                const float* ks, const float* vs, const int32_t* bt, const int32_t* cl,
-               float scale, bool fp8, bool bf16, void* ws, size_t ws_bytes, void* stream) {
+               float scale, bool fp8, bool bf16, void* ws, size_t ws_bytes, void* stream,
+               const AppendArgs& ap = AppendArgs()) {
   if (s.B == 0) return PA_OK;
   auto ws_ok = [&]() {   // every split needs one: its four warps divide the batch
     const size_t need = decode_workspace_bytes(s.B, s.Hq, s.D, s.splits);
@@ -80,7 +92,7 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
   DeviceState* dev = nullptr;
   if (int rc = device_state(&dev)) return rc;
   if (s.splits == 0) {
-    s.splits = decode_default_ctas();
+    s.splits = decode_default_ctas(fp8);
     if (!ws_ok()) return PA_ERR_WORKSPACE;
   }
   DecodeArgs a{};
@@ -98,6 +110,10 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
   a.max_context_len = s.max_ctx;
   a.split_ctas = s.splits;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.k_pool_w = ap.k_pool;
+  a.v_pool_w = ap.v_pool;
+  a.k_scale_w = ap.k_scale;
+  a.v_scale_w = ap.v_scale;
   // Batches above kMaxBatchPerLaunch run as consecutive launches on the
   // stream; each reuses the workspace (its counters are back to zero when
   // a launch ends).
@@ -109,6 +125,12 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
     c.q = static_cast<const uint8_t*>(q) + b0 * out_row;
     c.block_tables = bt + static_cast<int64_t>(b0) * s.mbs;
     c.context_lens = cl + b0;
+    if (ap.k_new != nullptr) {
+      const size_t new_row = static_cast<size_t>(s.Hkv) * s.D * 2;   // new rows are 16-bit
+      c.k_new = static_cast<const uint8_t*>(ap.k_new) + b0 * new_row;
+      c.v_new = static_cast<const uint8_t*>(ap.v_new) + b0 * new_row;
+      c.slots = ap.slots + b0;
+    }
     decode_workspace_split(c, ws, &c.ws_acc, &c.ws_ml, &c.counters);
     if (cudaError_t e = launch_decode(c, fp8, bf16, static_cast<cudaStream_t>(stream)))
       return cuda_status(e);
@@ -239,11 +261,14 @@ int pa_e4m3_encode(const float* x, uint8_t* codes, int64_t n, void* stream) {
 
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int split_ctas) {
   if (split_ctas < 0) return 0;
-  if (split_ctas == 0) split_ctas = decode_default_ctas();
+  if (split_ctas == 0) split_ctas = decode_max_default_ctas();
   return decode_workspace_bytes(num_seqs, num_q_heads, head_dim, split_ctas);
 }
 
-int pa_decode_default_splits(void) { return decode_default_ctas(); }
+int pa_decode_default_splits(int pool_type) {
+  if (pool_type != PA_F16 && pool_type != PA_BF16 && pool_type != PA_E4M3) return 0;
+  return decode_default_ctas(pool_type == PA_E4M3);
+}
 
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
@@ -285,6 +310,68 @@ int pa_decode_fp8(void* out, const void* q, const uint8_t* k_cache, const uint8_
     return PA_ERR_INVALID_ARG;
   return run_decode(s, out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
                     scale, true, false, workspace, workspace_bytes, stream);
+}
+
+int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_new,
+                   void* k_cache, void* v_cache, const int64_t* slot_mapping,
+                   const int32_t* block_tables, int max_blocks_per_seq,
+                   const int32_t* context_lens, int max_context_len, int num_seqs,
+                   int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                   int num_blocks, float scale, int dtype, int split_ctas, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_new || !v_new || !k_cache || !v_cache || !slot_mapping ||
+      !block_tables || !context_lens)
+    return PA_ERR_INVALID_ARG;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+  const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                      num_blocks, max_blocks_per_seq, max_context_len, split_ctas};
+  if (int rc = check_decode_shape(s, scale)) return rc;
+  for (const void* p : {static_cast<const void*>(out), q, k_new, v_new,
+                        static_cast<const void*>(k_cache), static_cast<const void*>(v_cache)})
+    if (!aligned(p, 16)) return PA_ERR_INVALID_ARG;
+  if (!aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(slot_mapping, 8))
+    return PA_ERR_INVALID_ARG;
+  AppendArgs ap;
+  ap.k_new = k_new;
+  ap.v_new = v_new;
+  ap.slots = slot_mapping;
+  ap.k_pool = k_cache;
+  ap.v_pool = v_cache;
+  return run_decode(s, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens,
+                    scale, false, dtype == PA_BF16, workspace, workspace_bytes, stream, ap);
+}
+
+int pa_decode_step_fp8(void* out, const void* q, const void* k_new, const void* v_new,
+                       uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
+                       const int64_t* slot_mapping, const int32_t* block_tables,
+                       int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
+                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, int num_blocks, float scale, int split_ctas,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_new || !v_new || !k_cache || !v_cache || !k_scale || !v_scale ||
+      !slot_mapping || !block_tables || !context_lens)
+    return PA_ERR_INVALID_ARG;
+  const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                      num_blocks, max_blocks_per_seq, max_context_len, split_ctas};
+  if (int rc = check_decode_shape(s, scale)) return rc;
+  for (const void* p : {static_cast<const void*>(out), q, k_new, v_new,
+                        static_cast<const void*>(k_cache), static_cast<const void*>(v_cache)})
+    if (!aligned(p, 16)) return PA_ERR_INVALID_ARG;
+  if (!aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(k_scale, 4) ||
+      !aligned(v_scale, 4) || !aligned(slot_mapping, 8))
+    return PA_ERR_INVALID_ARG;
+  AppendArgs ap;
+  ap.k_new = k_new;
+  ap.v_new = v_new;
+  ap.slots = slot_mapping;
+  ap.k_pool = k_cache;
+  ap.v_pool = v_cache;
+  ap.k_scale = k_scale;
+  ap.v_scale = v_scale;
+  return run_decode(s, out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                    scale, true, false, workspace, workspace_bytes, stream, ap);
 }
 
 int pa_get_status(void* stream, unsigned* bits) {

@@ -10,6 +10,7 @@
 // Both kernels move a few hundred KB per decode step; they are launch- and
 // latency-bound, so they are written for few instructions per byte and fully
 // coalesced 16-byte accesses, nothing more.
+#include "pa_e4m3.cuh"
 #include "pa_launch.h"
 #include "pa_ptx.cuh"
 
@@ -50,7 +51,6 @@ append_fp8_kernel(const __half* __restrict__ k_new, const __half* __restrict__ v
                   float* __restrict__ k_scale, float* __restrict__ v_scale,
                   const int64_t* __restrict__ slots, int T, int Hkv, int block_size,
                   int64_t num_slots, unsigned* status) {
-  constexpr int PER_LANE = D / 32;         // 2 or 4 values per lane
   const int lane = threadIdx.x & 31;
   const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (w >= static_cast<int64_t>(T) * Hkv * 2) return;
@@ -64,39 +64,18 @@ append_fp8_kernel(const __half* __restrict__ k_new, const __half* __restrict__ v
     return;
   }
   const int64_t blk = s / block_size, row = s - blk * block_size;
-  const __half* src = (kv ? v_new : k_new) + (i * Hkv + h) * D + lane * PER_LANE;
-  float x[PER_LANE];
-  if constexpr (PER_LANE == 4) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(src);
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
-  } else {
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(src));
-    x[0] = a.x; x[1] = a.y;
-  }
+  const RowF16<D> x = load_row_f16<D>((kv ? v_new : k_new) + (i * Hkv + h) * D, lane);
   float* scales = kv ? v_scale : k_scale;
   const int64_t tile = blk * Hkv + h;
   float scale;
   if (row == 0) {
-    float amax = 0.f;
-#pragma unroll
-    for (int j = 0; j < PER_LANE; ++j) amax = fmaxf(amax, fabsf(x[j]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    scale = e4m3_row_scale<D>(x);
     if (lane == 0) scales[tile] = scale;
   } else {
     scale = scales[tile];
   }
-  uint8_t* dst = (kv ? v_cache : k_cache) + (tile * block_size + row) * D + lane * PER_LANE;
-  const uint32_t c01 = f32x2_to_e4m3x2(__fdiv_rn(x[0], scale), __fdiv_rn(x[1], scale));
-  if constexpr (PER_LANE == 4) {
-    const uint32_t c23 = f32x2_to_e4m3x2(__fdiv_rn(x[2], scale), __fdiv_rn(x[3], scale));
-    *reinterpret_cast<uint32_t*>(dst) = c01 | (c23 << 16);
-  } else {
-    *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(c01);
-  }
+  store_row_codes<D>((kv ? v_cache : k_cache) + (tile * block_size + row) * D, lane,
+                     e4m3_row_codes<D>(x, scale));
 }
 
 }  // namespace

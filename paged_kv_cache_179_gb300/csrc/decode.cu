@@ -48,6 +48,7 @@
 #include <cfloat>
 #include <type_traits>
 
+#include "pa_e4m3.cuh"
 #include "pa_launch.h"
 #include "pa_ptx.cuh"
 
@@ -87,7 +88,6 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kGroupMax = 8;     // query heads per kv head served by one MMA N=8 tile
-constexpr int kCtasPerSm = 2;    // resident CTAs per SM the shared-memory budget is sized for
 // E4M3 path: P * v_scale is scaled by 2^8 before rounding to f16 so small
 // weights stay in f16's normal range; the fp32 result is scaled back.  With
 // fp16-sourced pools v_scale <= 65504/448, so P' <= 146.3 * 256 < 65504.
@@ -563,8 +563,55 @@ __device__ void merge_pieces(const DecodeArgs& a, int b, int h, int w0, int firs
   }
 }
 
-template <int D, bool FP8, bool BF16, int STAGES>
-__global__ void __launch_bounds__(kThreads)
+// Fused append: the new (this step's) row of one (sequence, kv head), the
+// lane's D/16 bytes of it, and its slot.
+struct NewRow {
+  uint2 k, v;      // 16-bit values (D=64 uses .x only)
+  int64_t slot;    // slot_mapping[b]; -2 when the chunk holds no sequence end
+};
+
+template <int D>
+__device__ __forceinline__ RowF16<D> row_from_bits(uint2 raw) {
+  RowF16<D> r;
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+  r.x[0] = a.x;
+  r.x[1] = a.y;
+  if constexpr (RowF16<D>::PER_LANE == 4) {
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    r.x[2] = b.x;
+    r.x[3] = b.y;
+  }
+  return r;
+}
+
+// The new row of chunk x's sequence and kv head when x holds the sequence's
+// last block (the one the new token goes to), for this lane.
+template <int D, bool APPEND>
+__device__ __forceinline__ NewRow load_new_row(const DecodeArgs& a, const Chunk& x, const int* pf,
+                                              int lane) {
+  NewRow n;
+  n.k = n.v = make_uint2(0, 0);
+  n.slot = -2;
+  if constexpr (APPEND) {
+    if (x.nb > 0 && x.cb0 + x.nb == seg_blocks(pf, x.b, a.Hkv)) {
+      n.slot = __ldg(a.slots + x.b);
+      const int64_t off = (static_cast<int64_t>(x.b) * a.Hkv + x.h) * D * 2 + lane * (D / 16);
+      const uint8_t* kr = static_cast<const uint8_t*>(a.k_new) + off;
+      const uint8_t* vr = static_cast<const uint8_t*>(a.v_new) + off;
+      if constexpr (D == 128) {
+        n.k = __ldg(reinterpret_cast<const uint2*>(kr));
+        n.v = __ldg(reinterpret_cast<const uint2*>(vr));
+      } else {
+        n.k.x = __ldg(reinterpret_cast<const uint32_t*>(kr));
+        n.v.x = __ldg(reinterpret_cast<const uint32_t*>(vr));
+      }
+    }
+  }
+  return n;
+}
+
+template <int D, bool FP8, bool BF16, int STAGES, bool APPEND, int CTAS>
+__global__ void __launch_bounds__(kThreads, CTAS)
 decode_kernel(const DecodeArgs a) {
   using TL = Tile<D, FP8, STAGES>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -655,6 +702,7 @@ decode_kernel(const DecodeArgs a) {
   }
   // query fragments of the current piece and of the next one
   uint32_t qf[D / 16][2], qn[D / 16][2];
+  uint8_t* const ring_ptr = smem + warp * STAGES * TL::SLOT;   // generic address of the ring
   load_query<D, FP8>(qf, a, ch0.b, ch0.h, r, c);
   auto prefetch_next_query = [&](int b, int h) {
     ++h;
@@ -724,6 +772,12 @@ decode_kernel(const DecodeArgs a) {
 
   while (ch0.nb > 0) {
     const int L = len[ch0.b];
+    // fused append: the new row, when this chunk ends its sequence.  Loaded
+    // here rather than a chunk ahead: held across the loop it would cost the
+    // E4M3 variant its third CTA per SM (or spills).
+    const NewRow nt0 = load_new_row<D, APPEND>(a, ch0, pf, lane);
+    // fused append: index in this chunk of the sequence's last block, if any
+    const int t_last = (APPEND && nt0.slot >= 0) ? seg_blocks(pf, ch0.b, Hkv) - 1 - ch0.cb0 : -1;
     for (int t = 0; t < ch0.nb && !dead; ++t) {
       const int s = computed % STAGES;
       if (!__all_sync(0xffffffffu, mbar_wait(sbar + 8 * s, (computed / STAGES) & 1))) {
@@ -737,6 +791,58 @@ decode_kernel(const DecodeArgs a) {
       if constexpr (FP8) {
         sl2 *= __shfl_sync(0xffffffffu, ks0, t);
         v_mul = __shfl_sync(0xffffffffu, vs0, t) * kPBoost;
+      }
+      if constexpr (APPEND) {
+        // This step's token of the sequence lands in its last block at row
+        // (L-1) % 16: write it to the pool and into the tile just fetched
+        // (which may predate the write), then attend.
+        if (t == t_last && id >= 0 && id < a.num_blocks) {
+          const int row = (L - 1) & 15;
+          if (nt0.slot != static_cast<int64_t>(id) * 16 + row) {
+            if (lane == 0) atomicOr(a.status, kStatusBadSlot);   // not a decode-step slot
+          } else {
+            constexpr int ROWB = TL::BYTES / 16;
+            const int64_t prow = (static_cast<int64_t>(id) * Hkv + ch0.h) * 16 + row;
+            uint8_t* kt = ring_ptr + s * TL::SLOT + row * ROWB;
+            uint8_t* vt = kt + TL::BYTES;
+            uint8_t* kp = static_cast<uint8_t*>(a.k_pool_w) + prow * ROWB;
+            uint8_t* vp = static_cast<uint8_t*>(a.v_pool_w) + prow * ROWB;
+            if constexpr (!FP8) {
+              if constexpr (D == 128) {
+                *reinterpret_cast<uint2*>(kt + 8 * lane) = nt0.k;
+                *reinterpret_cast<uint2*>(vt + 8 * lane) = nt0.v;
+                *reinterpret_cast<uint2*>(kp + 8 * lane) = nt0.k;
+                *reinterpret_cast<uint2*>(vp + 8 * lane) = nt0.v;
+              } else {
+                *reinterpret_cast<uint32_t*>(kt + 4 * lane) = nt0.k.x;
+                *reinterpret_cast<uint32_t*>(vt + 4 * lane) = nt0.v.x;
+                *reinterpret_cast<uint32_t*>(kp + 4 * lane) = nt0.k.x;
+                *reinterpret_cast<uint32_t*>(vp + 4 * lane) = nt0.v.x;
+              }
+            } else {
+              // E4M3: the page's first row sets its scales, later rows reuse them
+              const RowF16<D> xk = row_from_bits<D>(nt0.k), xv = row_from_bits<D>(nt0.v);
+              float ksc = __shfl_sync(0xffffffffu, ks0, t);
+              float vsc = __shfl_sync(0xffffffffu, vs0, t);
+              if (row == 0) {
+                ksc = e4m3_row_scale<D>(xk);
+                vsc = e4m3_row_scale<D>(xv);
+                if (lane == 0) {
+                  a.k_scale_w[prow / 16] = ksc;
+                  a.v_scale_w[prow / 16] = vsc;
+                }
+              }
+              const uint32_t kc = e4m3_row_codes<D>(xk, ksc), vc = e4m3_row_codes<D>(xv, vsc);
+              store_row_codes<D>(kt, lane, kc);
+              store_row_codes<D>(vt, lane, vc);
+              store_row_codes<D>(kp, lane, kc);
+              store_row_codes<D>(vp, lane, vc);
+              sl2 = a.scale_log2 * ksc;
+              v_mul = vsc * kPBoost;
+            }
+            __syncwarp();
+          }
+        }
       }
       if (id >= 0 && id < a.num_blocks) {
         const int n_valid = min(16, L - (ch0.cb0 + t) * 16);
@@ -845,11 +951,11 @@ decode_kernel(const DecodeArgs a) {
   PA_TRACE_WARP(gw, 6, static_cast<unsigned long long>(hi - lo));
 }
 
-template <int D, bool FP8, bool BF16, int STAGES>
+template <int D, bool FP8, bool BF16, int STAGES, bool APPEND, int CTAS>
 cudaError_t launch_one(const DecodeArgs& a, cudaStream_t s) {
   using TL = Tile<D, FP8, STAGES>;
   const Layout lay = make_layout(TL::RING, STAGES, a.B);
-  auto* kern = decode_kernel<D, FP8, BF16, STAGES>;
+  auto* kern = decode_kernel<D, FP8, BF16, STAGES, APPEND, CTAS>;
   static thread_local int last_smem[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -863,24 +969,45 @@ cudaError_t launch_one(const DecodeArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-#ifndef PA_RING_KB
-#define PA_RING_KB 96
+// Shared memory and registers per CTA are traded against resident CTAs per
+// SM.  16-bit pools: 96 KB of rings per CTA (3 slots of 8 KB per warp at
+// D=128), two CTAs per SM.  E4M3 pools move half the bytes per token, so the
+// same in-flight bytes take twice the tokens' worth of dequantisation and
+// MMA work; there a third CTA per SM (64 KB of rings each, registers capped
+// so that 3 x 128 threads fit) hides more of that latency than deeper rings
+// would.
+#ifndef PA_RING_KB_F16
+#define PA_RING_KB_F16 96
 #endif
+#ifndef PA_CTAS_F16
+#define PA_CTAS_F16 2
+#endif
+#ifndef PA_RING_KB_FP8
+#define PA_RING_KB_FP8 64
+#endif
+#ifndef PA_CTAS_FP8
+#define PA_CTAS_FP8 3
+#endif
+constexpr int ring_kb(bool fp8) { return fp8 ? PA_RING_KB_FP8 : PA_RING_KB_F16; }
+constexpr int ctas_per_sm(bool fp8) { return fp8 ? PA_CTAS_FP8 : PA_CTAS_F16; }
 
 template <int D, bool FP8, bool BF16>
 cudaError_t launch_dtype(const DecodeArgs& a, cudaStream_t s) {
-  // Ring depth per warp: PA_RING_KB of rings per CTA (96 KB: 3 slots of 8 KB
-  // for 16-bit D=128 tiles, 6 of 4 KB, 12 of 2 KB) keeps two CTAs per SM
-  // within shared memory while one slot per warp is being read.
-  constexpr int SLOT = 2 * 16 * (FP8 ? D : 2 * D);
-  constexpr int STAGES = PA_RING_KB * 1024 / (kWarps * SLOT);
-  static_assert(STAGES >= 2, "ring too small");
-  return launch_one<D, FP8, BF16, STAGES>(a, s);
+  constexpr int SLOT = 2 * 16 * (FP8 ? D : 2 * D);    // one K and one V tile
+  constexpr int STAGES_R = ring_kb(FP8) * 1024 / (kWarps * SLOT);
+  constexpr int STAGES = STAGES_R < 2 ? 2 : STAGES_R;
+  constexpr int CTAS = ctas_per_sm(FP8);
+  if (a.k_new != nullptr) return launch_one<D, FP8, BF16, STAGES, true, CTAS>(a, s);
+  return launch_one<D, FP8, BF16, STAGES, false, CTAS>(a, s);
 }
 
 }  // namespace
 
-int decode_default_ctas() { return device_sm_count() * kCtasPerSm; }
+int decode_default_ctas(bool fp8) { return device_sm_count() * ctas_per_sm(fp8); }
+
+int decode_max_default_ctas() {
+  return device_sm_count() * (PA_CTAS_F16 > PA_CTAS_FP8 ? PA_CTAS_F16 : PA_CTAS_FP8);
+}
 
 size_t decode_workspace_bytes(int B, int Hq, int D, int split_ctas) {
   if (B <= 0 || Hq <= 0 || D <= 0 || split_ctas <= 0) return 0;

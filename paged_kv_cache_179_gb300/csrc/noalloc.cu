@@ -84,7 +84,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   if (int rc = scratch_address(&ws)) return rc;
   unsigned* status = nullptr;
   if (int rc = device_status_word(&status)) return rc;
-  const int splits = split_ctas == 0 ? decode_default_ctas() : split_ctas;
+  const int splits = split_ctas == 0 ? decode_default_ctas(false) : split_ctas;
   const size_t need = decode_workspace_bytes(num_seqs, num_q_heads, head_dim, splits);
   if (need == 0 || need > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_SCRATCH_LIMIT;
 

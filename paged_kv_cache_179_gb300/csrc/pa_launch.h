@@ -26,6 +26,15 @@ struct DecodeArgs {
   float* ws_ml;                 // [split_ctas][2][8][2] partial (max, sum) in log2 units
   int* counters;                // [B][Hkv] finished partitions (zero between calls)
   unsigned* status;             // device status word
+  // fused append (pa_decode_step*): this step's new rows and where they go;
+  // null for a plain decode
+  const void* k_new;            // [B][Hkv][D] f16/bf16 (fp16 for E4M3 pools)
+  const void* v_new;
+  const int64_t* slots;         // [B], slot of position context_lens[b] - 1
+  void* k_pool_w;               // the pools and scales the new rows are written to
+  void* v_pool_w;
+  float* k_scale_w;
+  float* v_scale_w;
   int mbs;                      // max blocks per sequence (block table row stride)
   int B, Hq, Hkv, group, D;
   int num_blocks;
@@ -34,7 +43,8 @@ struct DecodeArgs {
   float scale_log2;             // softmax scale * log2(e)
 };
 
-int decode_default_ctas();
+int decode_default_ctas(bool fp8);   // CTAs a default launch uses for this pool type
+int decode_max_default_ctas();       // the largest of those over pool types
 size_t decode_workspace_bytes(int B, int Hq, int D, int split_ctas);
 void decode_workspace_split(const DecodeArgs& a, void* ws, float** acc, float** ml,
                             int** counters);

@@ -31,7 +31,7 @@ class DecodeStep:
         self.B = int(block_tables.shape[0])
         self.Hq = int(num_q_heads)
         self.NB, self.Hkv, self.bs, self.D = (int(x) for x in k_cache.shape)
-        self.split_ctas = int(split_ctas) or _abi.pa_decode_default_splits()
+        self.split_ctas = int(split_ctas) or _abi.pa_decode_default_splits(k_cache.dtype)
         self.workspace = _abi.alloc_workspace(self.B, self.Hq, self.D, self.split_ctas,
                                               k_cache.device)
 
@@ -52,12 +52,28 @@ class DecodeStep:
                            self.context_lens, self.max_context_len, self.scale,
                            self.split_ctas, self.workspace)
 
-    def __call__(self, q, k_new, v_new, slot_mapping, out):
+    def fused(self, q, k_new, v_new, slot_mapping, out):
+        """Append and decode in one launch (slot_mapping must hold each
+        sequence's position context_len - 1, as a decode step does)."""
+        if self.kv == "fp8":
+            _abi.pa_decode_step_fp8(out, q, k_new, v_new, self.k_cache, self.v_cache,
+                                    self.k_scale, self.v_scale, slot_mapping, self.block_tables,
+                                    self.context_lens, self.max_context_len, self.scale,
+                                    self.split_ctas, self.workspace)
+        else:
+            _abi.pa_decode_step(out, q, k_new, v_new, self.k_cache, self.v_cache, slot_mapping,
+                                self.block_tables, self.context_lens, self.max_context_len,
+                                self.scale, self.split_ctas, self.workspace)
+        return out
+
+    def __call__(self, q, k_new, v_new, slot_mapping, out, fused=True):
+        if fused:
+            return self.fused(q, k_new, v_new, slot_mapping, out)
         self.append(k_new, v_new, slot_mapping)
         self.decode(q, out)
         return out
 
-    def run_from_host(self, host_in: dict, dev_in: dict, host_out, dev_out):
+    def run_from_host(self, host_in: dict, dev_in: dict, host_out, dev_out, fused=True):
         """Copy the step's inputs from pinned host tensors, run it, copy the output back.
 
         host_in/dev_in map q, k_new, v_new, slot_mapping, block_tables and
@@ -69,6 +85,7 @@ class DecodeStep:
         for k, h in host_in.items():
             dev_in[k].copy_(h, non_blocking=True)
             h2d += h.numel() * h.element_size()
-        self(dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["slot_mapping"], dev_out)
+        self(dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["slot_mapping"], dev_out,
+             fused=fused)
         host_out.copy_(dev_out, non_blocking=True)
         return h2d, host_out.numel() * host_out.element_size()

@@ -1,0 +1,121 @@
+"""pa_decode_step / pa_decode_step_fp8: append and decode in one launch,
+against the oracle's append followed by its decode.  Pools must come out
+bit-identical to the oracle's append; outputs within the decode tolerances."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_179_gb300 import _abi
+from paged_kv_cache_179_gb300 import workloads as W
+from paged_kv_cache_179_gb300.step import DecodeStep
+
+from _helpers import TOL, max_err, oracle_step, to_cuda, to_np16
+
+pytestmark = pytest.mark.gpu
+
+
+def _step(w, splits=0, **pools):
+    pools = pools or dict(k_cache=w.k_cache, v_cache=w.v_cache)
+    return DecodeStep(**pools, block_tables=w.block_tables, context_lens=w.context_lens,
+                      max_context_len=w.max_context_len, scale=w.scale, num_q_heads=w.Hq,
+                      split_ctas=splits)
+
+
+@pytest.mark.parametrize("name,seed,splits", [("tiny", 0, 0), ("tiny", 1, 7),
+                                              ("smollm2_360m", 0, 0), ("qwen2_5_1_5b", 1, 0),
+                                              ("qwen2_5_7b", 0, 0), ("qwen2_5_7b", 2, 1000)])
+def test_fused_step_matches_oracle(name, seed, splits):
+    w = W.make_workload(name, seed=seed, fill="random")
+    kp, vp = to_np16(w.k_cache).copy(), to_np16(w.v_cache).copy()
+    oracle.cache_append(to_np16(w.k_new), to_np16(w.v_new), kp, vp, w.slot_mapping.numpy(), 16)
+    ref = oracle.decode(to_np16(w.q), kp, vp, w.block_tables.numpy(), w.context_lens.numpy(),
+                        w.scale, bf16=(w.dtype == "bf16"))
+    to_cuda(w)
+    out = torch.empty_like(w.q)
+    _step(w, splits).fused(w.q, w.k_new, w.v_new, w.slot_mapping, out)
+    assert _abi.pa_get_status() == (0, 0)
+    assert np.array_equal(to_np16(w.k_cache).view(np.uint16), kp.view(np.uint16))
+    assert np.array_equal(to_np16(w.v_cache).view(np.uint16), vp.view(np.uint16))
+    assert max_err(out, ref) <= TOL[w.dtype]
+
+
+def test_fused_equals_append_then_decode():
+    w = to_cuda(W.make_workload("qwen2_5_1_5b", seed=3))
+    k0, v0 = w.k_cache.clone(), w.v_cache.clone()
+    a = torch.empty_like(w.q)
+    _step(w)(w.q, w.k_new, w.v_new, w.slot_mapping, a, fused=False)
+    w.k_cache.copy_(k0)
+    w.v_cache.copy_(v0)
+    b = torch.empty_like(w.q)
+    _step(w)(w.q, w.k_new, w.v_new, w.slot_mapping, b, fused=True)
+    assert (a.float() - b.float()).abs().max().item() <= TOL["f16"]
+
+
+def test_padding_and_mismatched_slots():
+    w = to_cuda(W.make_workload("tiny", seed=4))
+    slots = w.slot_mapping.clone()
+    slots[1] = -1                        # padding: nothing appended for sequence 1
+    slots[2] = slots[2] + 1              # not position L-1: reported, not written
+    k0 = w.k_cache.clone()
+    out = torch.empty_like(w.q)
+    _step(w).fused(w.q, w.k_new, w.v_new, slots, out)
+    rc, bits = _abi.pa_get_status()
+    assert rc == _abi.PA_ERR_BOUNDS and bits == _abi.PA_STATUS_BAD_SLOT
+    changed = (w.k_cache != k0).flatten(1).any(dim=1).nonzero().flatten().tolist()
+    s0, s3 = int(w.slot_mapping[0]), int(w.slot_mapping[3])
+    assert set(changed) <= {s0 // 16, s3 // 16}
+    assert torch.equal(w.k_cache[s0 // 16, :, s0 % 16], w.k_new[0])
+    assert torch.equal(w.k_cache[s3 // 16, :, s3 % 16], w.k_new[3])
+
+
+def _fp8_case(seed, B, Hq, Hkv, D, lens):
+    g = torch.Generator().manual_seed(seed)
+    lens = torch.tensor(lens, dtype=torch.int32)
+    nblk = (lens + 15) // 16
+    NB = int(nblk.sum()) + 3
+    perm = torch.randperm(NB, generator=g).to(torch.int32)
+    tables = torch.full((B, int(nblk.max())), -1, dtype=torch.int32)
+    c = 0
+    for b in range(B):
+        tables[b, :nblk[b]] = perm[c:c + nblk[b]]
+        c += int(nblk[b])
+    last = lens.to(torch.int64) - 1
+    slots = tables[torch.arange(B), last // 16].to(torch.int64) * 16 + last % 16
+    q = torch.randn(B, Hq, D, generator=g).to(torch.float16)
+    kp = torch.randn(NB, Hkv, 16, D, generator=g).to(torch.float16)
+    vp = torch.randn(NB, Hkv, 16, D, generator=g).to(torch.float16)
+    # rows at and after each sequence's new position hold no token yet
+    for b in range(B):
+        for j in range(int(nblk[b])):
+            r0 = max(0, int(lens[b]) - 1 - 16 * j)
+            if r0 < 16:
+                kp[tables[b, j], :, r0:] = 0
+                vp[tables[b, j], :, r0:] = 0
+    kn = (torch.randn(B, Hkv, D, generator=g) * 2).to(torch.float16)
+    vn = (torch.randn(B, Hkv, D, generator=g) * 2).to(torch.float16)
+    return q, kp, vp, kn, vn, tables, lens, slots
+
+
+@pytest.mark.parametrize("seed,B,Hq,Hkv,D,lens,splits", [
+    (0, 5, 28, 4, 128, [17, 33, 300, 1, 129], 0),     # new rows at the start of pages
+    (1, 4, 8, 2, 64, [20, 50, 77, 200], 9),           # new rows inside pages
+    (2, 6, 12, 2, 128, [1, 16, 17, 32, 48, 1000], 2)])
+def test_fused_step_fp8_matches_oracle(seed, B, Hq, Hkv, D, lens, splits):
+    q, kp, vp, kn, vn, tables, L, slots = _fp8_case(seed, B, Hq, Hkv, D, lens)
+    kc, ks = oracle.quantize_fp8(to_np16(kp))
+    vc, vs = oracle.quantize_fp8(to_np16(vp))
+    dev = [torch.from_numpy(x.copy()).cuda() for x in (kc, vc, ks, vs)]
+    oracle.cache_append_fp8(to_np16(kn), to_np16(vn), kc, vc, ks, vs, slots.numpy(), 16)
+    scale = float(np.float32(1 / math.sqrt(D)))
+    ref = oracle.decode_fp8(to_np16(q), kc, vc, ks, vs, tables.numpy(), L.numpy(), scale)
+    out = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+    ws = _abi.alloc_workspace(B, Hq, D, splits, "cuda")
+    _abi.pa_decode_step_fp8(out, q.cuda(), kn.cuda(), vn.cuda(), *dev, slots.cuda(),
+                            tables.cuda(), L.cuda(), int(L.max()), scale, splits, ws)
+    assert _abi.pa_get_status() == (0, 0)
+    for got, want in zip(dev, (kc, vc, ks, vs)):
+        assert np.array_equal(got.cpu().numpy().view(np.uint8), want.view(np.uint8))
+    assert np.abs(out.float().cpu().numpy() - ref).max() <= TOL["fp8"]
