@@ -372,6 +372,65 @@ def run_ours(args, rank, world, dev):
     return line
 
 
+def run_copy_blocks(args, dev):
+    """``--op copy_blocks``: pa_copy_blocks forking n_pairs random blocks of a
+    pool shaped like the config's (distinct destinations, none a source)."""
+    from paged_kv_cache_179_gb300 import _abi
+    from paged_kv_cache_179_gb300 import workloads as W
+
+    cfg = W.CONFIGS[args.config]
+    Hkv, D = cfg["Hkv"], cfg["D"]
+    fp8 = cfg["kv"] == "fp8"
+    dtype = torch.uint8 if fp8 else W.TORCH_DTYPE[cfg["kv"]]
+    n = args.copy_pairs
+    NB = 3 * n
+    g = torch.Generator().manual_seed(args.seed)
+    k = torch.empty(NB, Hkv, 16, D, dtype=dtype, device=dev)
+    v = torch.empty_like(k)
+    k.view(torch.uint8).random_(0, 256)
+    v.view(torch.uint8).random_(0, 256)
+    ks = torch.rand(NB, Hkv, device=dev) if fp8 else None
+    vs = torch.rand(NB, Hkv, device=dev) if fp8 else None
+    perm = torch.randperm(NB, generator=g)
+    pairs = torch.stack([perm[n:2 * n], perm[:n]], dim=1).to(torch.int64).to(dev)
+    block_bytes = Hkv * 16 * D * k.element_size()
+    moved = 2 * n * (2 * block_bytes + (2 * Hkv * 4 if fp8 else 0))   # read + write, K + V
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        _abi.pa_copy_blocks(k, v, pairs, ks, vs)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for a, b in ev:
+        a.record(stream)
+        _abi.pa_copy_blocks(k, v, pairs, ks, vs)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    rc, bits = _abi.pa_get_status(dev)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} bits {bits}")
+    ms = [a.elapsed_time(b) for a, b in ev]
+    achieved = moved / (statistics.mean(ms) / 1e3) / 1e9
+    peak, peak_kind = measured_peaks()
+    return {
+        "metric": "pa_copy_blocks: bytes moved (read + write) per second", "impl": "ours",
+        "value": round(achieved, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(statistics.mean(ms), 5),
+        "higher_is_better": True, "dtype": "e4m3" if fp8 else cfg["kv"], "data": "synthetic",
+        "config": {"workload": f"{n} block pairs of a {NB}-block pool, {Hkv} kv heads, "
+                               f"head_dim {D}, {block_bytes} B per block per pool",
+                   "l2": "none: the copy moves more than 3x L2 per call" if moved >= 3 * (129 << 20)
+                         else "not flushed"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "copy_blocks_kernel", "bytes_per_launch": moved,
+                     "peak_source": peak_kind},
+        "copy_us": {"mean": round(statistics.mean(ms) * 1e3, 2),
+                    "median": round(statistics.median(ms) * 1e3, 2),
+                    "min": round(min(ms) * 1e3, 2)},
+        "gpu_launches": args.steps,
+    }
+
+
 def describe_l2(mode, kv_bytes, l2):
     if mode == "none":
         return (f"not flushed: inputs larger than L2 ({kv_bytes / 1e6:.0f} MB of K/V per step vs "
@@ -486,6 +545,9 @@ def main(argv=None):
                     help="time the step as pa_cache_append + pa_decode (two launches)")
     ap.add_argument("--prime-ms", type=float, default=0.0,
                     help="GPU sleep queued ahead of the timed steps so the host runs ahead")
+    ap.add_argument("--op", choices=["step", "copy_blocks"], default="step",
+                    help="what to time: the decode step (default) or pa_copy_blocks alone")
+    ap.add_argument("--copy-pairs", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-step-s", type=float, default=2.0)
@@ -507,7 +569,8 @@ def main(argv=None):
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=dev)
     try:
-        line = run_ours(args, rank, world, dev)
+        line = run_copy_blocks(args, dev) if args.op == "copy_blocks" else \
+            run_ours(args, rank, world, dev)
         if rank == 0:
             print(json.dumps(line), flush=True)
     finally:

@@ -61,7 +61,7 @@ extern "C" {
 #endif
 
 /* Element type of activations and pools (PA_E4M3: pools only, for
- * pa_decode_default_splits). */
+ * pa_decode_default_splits and pa_copy_blocks). */
 enum { PA_F16 = 0, PA_BF16 = 1, PA_E4M3 = 2 };
 
 /* Return codes. */
@@ -125,6 +125,28 @@ int pa_cache_append_fp8(const void *k_new, const void *v_new, uint8_t *k_cache, 
 int pa_quantize_fp8(const void *k_src, const void *v_src, uint8_t *k_cache, uint8_t *v_cache,
                     float *k_scale, float *v_scale, int num_blocks, int num_kv_heads,
                     int head_dim, int block_size, void *stream);
+
+/*
+ * Block copy inside the pools: for each pair i, with src = block_mapping[2i]
+ * and dst = block_mapping[2i+1], copy physical block src of k_cache to
+ * physical block dst (all num_kv_heads x block_size rows of head_dim
+ * elements), the same for v_cache and, for PA_E4M3 pools, the block's
+ * num_kv_heads K and V scales.  A byte copy: bit-exact, and no other byte
+ * changes.  The copy that forks a block for its new owner (beam search,
+ * parallel sampling, copy-on-write of a shared prefix).
+ *   pool_type: PA_F16 / PA_BF16 (2-byte elements; scales must be NULL) or
+ *   PA_E4M3 (1-byte codes; k_scale and v_scale [num_blocks][num_kv_heads]
+ *   required).  block_mapping: int64 [num_pairs][2] on the device.
+ * A pair with src == dst is a no-op; a pair with src or dst outside
+ * [0, num_blocks) is skipped and sets PA_STATUS_BAD_BLOCK.  Destinations
+ * must be distinct and must not be the source of another pair in the same
+ * call (those copies race).
+ * Source: rvLLM, CUDA Kernels table, "Block Copy"; Architecture,
+ * rvllm-block-manager (copy-on-write, prefix sharing).
+ */
+int pa_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
+                   const int64_t *block_mapping, int num_pairs, int num_kv_heads, int head_dim,
+                   int block_size, int num_blocks, int pool_type, void *stream);
 
 /*
  * The E4M3 encoder on its own: codes[i] = E4M3_RNE_saturating(x[i]) for n

@@ -64,6 +64,7 @@ def lib():
                                         f32, vp, i32, vp]
             L.oracle_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
                                             i32, f32, vp, i32, vp]
+            L.oracle_copy_blocks.argtypes = [vp, vp, vp, vp, vp, i32, ctypes.c_size_t, i32, i64]
             L.oracle_num_threads.restype = i32
             _lib = L
     return _lib
@@ -109,6 +110,21 @@ def cache_append(k_new, v_new, k_cache, v_cache, slot_mapping, block_size: int) 
     slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     lib().oracle_cache_append(_p(k_new), _p(v_new), _p(k_cache), _p(v_cache), _p(slots), T, Hkv, D,
                               block_size, k_new.dtype.itemsize)
+
+
+def copy_blocks(k_cache, v_cache, pairs, k_scale=None, v_scale=None) -> None:
+    """In place: for each (src, dst) row of pairs, in order, copy physical block
+    src of both pools (and of the scales, when given) to block dst."""
+    NB, Hkv = k_cache.shape[:2]
+    for a in (k_cache, v_cache):
+        assert a.flags.c_contiguous and a.shape == k_cache.shape and a.dtype == k_cache.dtype
+    if k_scale is not None:
+        assert k_scale.dtype == np.float32 and k_scale.shape == (NB, Hkv)
+        assert v_scale.dtype == np.float32 and v_scale.shape == (NB, Hkv)
+    pairs = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+    block_bytes = k_cache[0].nbytes if NB else 0
+    lib().oracle_copy_blocks(_p(k_cache), _p(v_cache), _p(k_scale), _p(v_scale), _p(pairs),
+                             pairs.shape[0], block_bytes, Hkv, NB)
 
 
 def cache_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping,

@@ -164,6 +164,33 @@ void oracle_cache_append(const void *k_new, const void *v_new, void *k_cache, vo
     }
 }
 
+/* ------------------------------------------------------------ block copy */
+
+/* rvLLM: High-performance LLM inference in Rust, CUDA Kernels table, "Block
+ * Copy" (KV cache block copy for beam search); Architecture, the block
+ * manager's copy-on-write.  Pairs (src, dst) are applied in order: the whole
+ * physical block src of each pool (block_bytes) is copied to block dst, and
+ * with scales given, the block's num_kv_heads scales of each pool too.
+ * Pairs naming a block outside [0, num_blocks) are skipped. */
+void oracle_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
+                        const int64_t *pairs, int num_pairs, size_t block_bytes,
+                        int num_kv_heads, int64_t num_blocks)
+{
+    for (int i = 0; i < num_pairs; i++) {
+        int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks || src == dst)
+            continue;
+        memcpy((char *)k_cache + (size_t)dst * block_bytes,
+               (const char *)k_cache + (size_t)src * block_bytes, block_bytes);
+        memcpy((char *)v_cache + (size_t)dst * block_bytes,
+               (const char *)v_cache + (size_t)src * block_bytes, block_bytes);
+        for (int h = 0; h < num_kv_heads && k_scale && v_scale; h++) {
+            k_scale[dst * num_kv_heads + h] = k_scale[src * num_kv_heads + h];
+            v_scale[dst * num_kv_heads + h] = v_scale[src * num_kv_heads + h];
+        }
+    }
+}
+
 /* --------------------------------------------------------- FP8 quantise */
 
 static float e4m3_page_scale(float amax)

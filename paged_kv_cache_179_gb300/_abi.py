@@ -33,6 +33,7 @@ SIGNATURES = {
                             _i32),
     "pa_quantize_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
     "pa_e4m3_encode": ([_vp, _vp, _i64, _vp], _i32),
+    "pa_copy_blocks": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp], _i32),
     "pa_decode_workspace_size": ([_i32, _i32, _i32, _i32], _sz),
     "pa_decode_default_splits": ([_i32], _i32),
     "pa_decode": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
@@ -182,6 +183,32 @@ def pa_quantize_fp8(k_src, v_src, k_cache, v_cache, k_scale, v_scale) -> None:
                                   _ptr(k_scale if k_src is not None else None),
                                   _ptr(v_scale if v_src is not None else None), NB, Hkv, D, bs,
                                   _stream(dev)), "pa_quantize_fp8")
+
+
+def pa_copy_blocks(k_cache, v_cache, block_mapping, k_scale=None, v_scale=None) -> None:
+    """Copy whole physical blocks of both pools: block_mapping is int64
+    [n][2] of (src, dst); E4M3 (uint8) pools also copy their [NB][Hkv] scales."""
+    dev = k_cache.device
+    fp8 = k_cache.dtype == torch.uint8
+    _need(k_cache, "k_cache", (torch.float16, torch.bfloat16, torch.uint8), 4, dev)
+    _need(v_cache, "v_cache", k_cache.dtype, 4, dev)
+    _need(block_mapping, "block_mapping", torch.int64, 2, dev)
+    NB, Hkv, bs, D = k_cache.shape
+    if v_cache.shape != k_cache.shape or block_mapping.shape[1] != 2:
+        raise ValueError("shape mismatch")
+    if fp8:
+        for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+            _need(t, n, torch.float32, 2, dev)
+            if t.shape != (NB, Hkv):
+                raise ValueError("shape mismatch")
+        code = PA_E4M3
+    else:
+        if k_scale is not None or v_scale is not None:
+            raise ValueError("scales are for E4M3 pools only")
+        code = _act_code(k_cache.dtype)
+    _check(load().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                 _ptr(block_mapping), block_mapping.shape[0], Hkv, D, bs, NB,
+                                 code, _stream(dev)), "pa_copy_blocks")
 
 
 def pa_e4m3_encode(x, codes) -> None:

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpa.so")
-SOURCES = ["abi.cu", "append.cu", "quantize.cu", "decode.cu", "noalloc.cu"]
+SOURCES = ["abi.cu", "append.cu", "quantize.cu", "decode.cu", "noalloc.cu", "copy.cu"]
 HEADERS = ["pa_launch.h", "pa_ptx.cuh", "pa_e4m3.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

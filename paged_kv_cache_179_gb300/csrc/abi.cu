@@ -250,6 +250,30 @@ int pa_quantize_fp8(const void* k_src, const void* v_src, uint8_t* k_cache, uint
   return PA_OK;
 }
 
+int pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                   const int64_t* block_mapping, int num_pairs, int num_kv_heads, int head_dim,
+                   int block_size, int num_blocks, int pool_type, void* stream) {
+  if (num_pairs < 0 || num_kv_heads <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+  if (pool_type != PA_F16 && pool_type != PA_BF16 && pool_type != PA_E4M3)
+    return PA_ERR_INVALID_ARG;
+  const bool fp8 = pool_type == PA_E4M3;
+  if (fp8 != (k_scale != nullptr) || fp8 != (v_scale != nullptr)) return PA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size != 16) return PA_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !block_mapping) return PA_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_mapping, 8))
+    return PA_ERR_INVALID_ARG;
+  if ((k_scale && !aligned(k_scale, 4)) || (v_scale && !aligned(v_scale, 4)))
+    return PA_ERR_INVALID_ARG;
+  DeviceState* dev = nullptr;
+  if (int rc = device_state(&dev)) return rc;
+  return cuda_status(launch_copy_blocks(k_cache, v_cache, k_scale, v_scale, block_mapping,
+                                        num_pairs, num_kv_heads, head_dim * (fp8 ? 1 : 2),
+                                        block_size, num_blocks, dev->status,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 int pa_e4m3_encode(const float* x, uint8_t* codes, int64_t n, void* stream) {
   if (!x || !codes || n < 0) return PA_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(codes, 16)) return PA_ERR_INVALID_ARG;

@@ -52,12 +52,10 @@
 #include "pa_launch.h"
 #include "pa_ptx.cuh"
 
-// Opt-in trace build (-DPA_TRACE): thread 0 of each CTA records %globaltimer
-// at the phases of the kernel; pa_trace_read copies them out.
 // Opt-in trace build (-DPA_TRACE): lane 0 of every worker warp records
 // %globaltimer at its phases and its piece counts; pa_trace_read copies them.
 // Slots per worker: 0 kernel entry, 1 first tile ready, 2 last block done,
-// 3 end, 4 pieces, 5 split pieces, 6 blocks.
+// 3 end, 4 pieces, 5 split pieces, 6 blocks, 7 SM id.
 #ifdef PA_TRACE
 __device__ unsigned long long g_pa_trace[16384 * 8];
 #define PA_TRACE_WARP(w, k, v)                                                   \
@@ -68,6 +66,11 @@ __device__ __forceinline__ unsigned long long pa_now() {
   unsigned long long t_;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));
   return t_;
+}
+__device__ __forceinline__ unsigned long long pa_smid() {
+  unsigned v_;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(v_));
+  return v_;
 }
 extern "C" int pa_trace_read(unsigned long long* host, int n_workers) {
   const size_t n = static_cast<size_t>(n_workers < 16384 ? n_workers : 16384) * 8;
@@ -949,6 +952,7 @@ decode_kernel(const DecodeArgs a) {
   PA_TRACE_WARP(gw, 4, tr_pieces);
   PA_TRACE_WARP(gw, 5, tr_split);
   PA_TRACE_WARP(gw, 6, static_cast<unsigned long long>(hi - lo));
+  PA_TRACE_WARP(gw, 7, pa_smid());
 }
 
 template <int D, bool FP8, bool BF16, int STAGES, bool APPEND, int CTAS>

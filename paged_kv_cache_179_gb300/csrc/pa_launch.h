@@ -64,6 +64,10 @@ cudaError_t launch_quantize_fp8(const void* src, uint8_t* codes, float* scales,
                                 int64_t num_tiles, int tile_elems, cudaStream_t s);
 
 cudaError_t launch_e4m3_encode(const float* x, uint8_t* codes, int64_t n, cudaStream_t s);
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                               const int64_t* pairs, int num_pairs, int Hkv, int row_bytes,
+                               int block_size, int64_t num_blocks, unsigned* status,
+                               cudaStream_t s);
 
 int device_sm_count();
 // Address of the current device's status word (set up on first use).

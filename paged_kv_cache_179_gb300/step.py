@@ -73,6 +73,28 @@ class DecodeStep:
         self.decode(q, out)
         return out
 
+    def capture(self, q, k_new, v_new, slot_mapping, out, fused=True, stream=None):
+        """Record the step into a CUDA graph and return it (``torch.cuda.CUDAGraph``).
+
+        The graph holds the launch(es) with these tensors' addresses: for
+        each later step write that step's q, k_new, v_new and slot_mapping
+        (and the grown context_lens / block_tables this object was built
+        with) into the same tensors, then ``replay()``; ``out`` receives the
+        result.  The kernel reads lengths and tables on the device, so one
+        graph serves every step while lengths stay within max_context_len.
+
+        Before capturing, the step runs once eagerly on the current stream
+        (the library's per-device set-up happens outside the capture).  That
+        run is the step itself: it appends the given rows and writes out,
+        and a replay with unchanged inputs writes the same bytes again.
+        """
+        self(q, k_new, v_new, slot_mapping, out, fused=fused)
+        torch.cuda.current_stream().synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            self(q, k_new, v_new, slot_mapping, out, fused=fused)
+        return graph
+
     def run_from_host(self, host_in: dict, dev_in: dict, host_out, dev_out, fused=True):
         """Copy the step's inputs from pinned host tensors, run it, copy the output back.
 

@@ -31,7 +31,7 @@ def header_functions():
 
 def test_header_and_binding_agree():
     names = header_functions()
-    assert len(names) == 14
+    assert len(names) == 15
     assert sorted(_abi.SIGNATURES) == names
 
 

@@ -334,6 +334,52 @@ def test_shared_prefix_equals_copied_blocks():
     assert np.array_equal(shared, copied)
 
 
+def test_copy_blocks_invariants():
+    rng = np.random.default_rng(8)
+    NB, Hkv, D = 10, 2, 64
+    k = rng.standard_normal((NB, Hkv, 16, D)).astype(np.float16)
+    v = rng.standard_normal((NB, Hkv, 16, D)).astype(np.float16)
+    ks = rng.random((NB, Hkv)).astype(np.float32)
+    vs = rng.random((NB, Hkv)).astype(np.float32)
+    k0, v0, ks0, vs0 = k.copy(), v.copy(), ks.copy(), vs.copy()
+    pairs = np.array([[1, 7], [4, 4], [2, 9], [12, 3], [0, -1]], dtype=np.int64)
+    oracle.copy_blocks(k, v, pairs, ks, vs)
+    for src, dst in ((1, 7), (2, 9)):                # applied pairs
+        assert np.array_equal(k[dst].view(np.uint16), k0[src].view(np.uint16))
+        assert np.array_equal(v[dst].view(np.uint16), v0[src].view(np.uint16))
+        assert np.array_equal(ks[dst], ks0[src]) and np.array_equal(vs[dst], vs0[src])
+    rest = [b for b in range(NB) if b not in (7, 9)]  # self-copy and out-of-range pairs: no-ops
+    for a, a0 in ((k, k0), (v, v0)):
+        assert np.array_equal(a[rest].view(np.uint16), a0[rest].view(np.uint16))
+    assert np.array_equal(ks[rest], ks0[rest]) and np.array_equal(vs[rest], vs0[rest])
+    # pairs apply in order: a chain carries the first source along
+    c = np.arange(4 * 16 * 8, dtype=np.uint8).reshape(4, 1, 16, 8)
+    c0 = c.copy()
+    d = c.copy()
+    oracle.copy_blocks(c, d, np.array([[0, 1], [1, 2]]))
+    assert np.array_equal(c[2], c0[0]) and np.array_equal(d[2], c0[0])
+
+
+def test_copy_on_write_fork_keeps_attention():
+    """Forking a sequence's shared prefix into fresh blocks (the block
+    manager's copy-on-write) leaves its attention output unchanged."""
+    w = W.make_workload("smollm2_360m", seed=4)
+    tables = w.block_tables.numpy()
+    lens = w.context_lens.numpy()
+    rows = [0, 1]
+    sub_t, sub_l, (kp, vp) = W.extract_rows(tables, lens, rows, [w.k_cache, w.v_cache])
+    q = W.to_numpy16(w.q)[rows]
+    before = oracle.decode(q, kp, vp, sub_t, sub_l, w.scale, bf16=True)
+    n_sh = len(w.shared_blocks)
+    fresh = np.arange(kp.shape[0], kp.shape[0] + n_sh, dtype=np.int64)
+    kp2 = np.concatenate([kp, np.zeros_like(kp[:n_sh])])
+    vp2 = np.concatenate([vp, np.zeros_like(vp[:n_sh])])
+    oracle.copy_blocks(kp2, vp2, np.stack([sub_t[1, :n_sh].astype(np.int64), fresh], axis=1))
+    t2 = sub_t.copy()
+    t2[1, :n_sh] = fresh
+    assert np.array_equal(oracle.decode(q, kp2, vp2, t2, sub_l, w.scale, bf16=True), before)
+
+
 def test_decode_fp8_matches_dense_on_dequantised_pool():
     rng = np.random.default_rng(9)
     B, Hq, Hkv, D = 3, 28, 4, 128
