@@ -5,7 +5,8 @@ Default workload: the Qwen2.5-7B-shaped batch (128 sequences, 28 q / 4 kv
 heads, head_dim 128, fp16, lognormal context lengths with median 1024 clipped
 to [1, 8192]; seeded synthetic data).  A step is the whole hot path for one
 batch: pa_decode_step appends each sequence's new token and attends over
-its context in one launch (split-K attention with the log-sum-exp merge);
+its context in one attention launch, followed by the launch that merges the
+split contexts by log-sum-exp;
 ``--unfused`` times pa_cache_append + pa_decode instead.  Between timed steps the L2 is not flushed when
 the step reads at least 3x the L2 size (429 MB of K/V against a 129 MB L2
 for the default batch); smaller batches have L2 evicted by reading a 2x-L2
@@ -242,7 +243,8 @@ def run_ours(args, rank, world, dev):
             flush_buf.add_(1)
     stream = torch.cuda.current_stream(dev)
     fused = not args.unfused
-    launches_per_step = 1 if fused else 2   # decode_kernel (fused) | append + decode
+    # decode_kernel + merge_kernel (fused) | append_kernel + decode_kernel + merge_kernel
+    launches_per_step = 2 if fused else 3
 
     def run_step():
         step(w.q, w.k_new, w.v_new, w.slot_mapping, out, fused=fused)
@@ -352,8 +354,9 @@ def run_ours(args, rank, world, dev):
         "hbm_gbs": round(achieved, 1), "hbm_frac_of_peak": round(achieved / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": ("decode_kernel with fused append and split-K merge" if fused
-                                else "decode_kernel with fused split-K merge"),
+                     "kernel": ("decode_kernel with fused append, then merge_kernel (timed "
+                                "together: one decode)" if fused
+                                else "decode_kernel, then merge_kernel (timed together: one decode)"),
                      "bytes_per_launch": kernel_bytes, "peak_source": peak_kind},
         "decode_us": {"mean": round(statistics.mean(dec_ms) * 1e3, 2),
                       "median": round(statistics.median(dec_ms) * 1e3, 2),

@@ -166,15 +166,14 @@ int pa_decode_default_splits(int pool_type);
 /*
  * Bytes of device workspace pa_decode / pa_decode_fp8 need: room for the
  * partial results of the context partitions that cross worker boundaries
- * (a worker is one warp; four per CTA; at most two partials each) and one
- * counter per (sequence, kv head).  split_ctas 0 means the largest
- * pa_decode_default_splits() over pool types on the current device, so the
- * result serves a default call of any type.  Every call needs one.
+ * (a worker is one warp; four per CTA; at most two partials each) and the
+ * batch's block-stream prefix sums, which the merge launch reads.
+ * split_ctas 0 means the largest pa_decode_default_splits() over pool types
+ * on the current device, so the result serves a default call of any type.
+ * Every call needs one.
  *
- * The caller allocates the workspace and must zero-fill it once before its
- * first use; every call that completes leaves the counters at zero again,
- * so the same workspace serves call after call.  After a call whose status
- * reports PA_ERR_TIMEOUT, zero it again.  Calls that share a workspace must
+ * The caller allocates the workspace; it needs no initialisation, and the
+ * same workspace serves call after call.  Calls that share a workspace must
  * not overlap on the device.
  */
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int split_ctas);
@@ -190,12 +189,14 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int
  * The batch's (sequence, kv head, block) units are divided evenly among the
  * 4 * split_ctas warps of split_ctas CTAs (0: pa_decode_default_splits(dtype)).
  * A warp's share of one sequence is a context partition, reduced with an
- * online softmax in fp32; a sequence split across warps has its partitions
- * merged by log-sum-exp in the same launch.  Results do not depend on split_ctas beyond fp32
- * rounding, and a given split_ctas is deterministic.
+ * online softmax in fp32.  A sequence split across warps has its partitions
+ * merged by log-sum-exp in a second launch on the same stream, a
+ * programmatic dependent launch that waits for the first to complete.
+ * Results do not depend on split_ctas beyond fp32 rounding, and a given
+ * split_ctas is deterministic.
  *   max_context_len: host-side upper bound of context_lens (no device read);
  *   workspace: at least pa_decode_workspace_size(...) bytes, 256-byte
- *   aligned, zero-filled before first use.
+ *   aligned.
  * Source: rvLLM, CUDA Kernels table, "PagedAttention V2" (block-table
  * indirection, online softmax); LLM Serving Kernels, Projects table, row 04;
  * rvllm (small engine), How it's put together (GQA, read_blocks).
@@ -221,8 +222,9 @@ int pa_decode_fp8(void *out, const void *q, const uint8_t *k_cache, const uint8_
                   size_t workspace_bytes, void *stream);
 
 /*
- * One whole decode step in one launch: append this step's K/V token of every
- * sequence, then attend over the sequence's context including it, as
+ * One whole decode step in one attention launch (plus pa_decode's merge
+ * launch): append this step's K/V token of every sequence, then attend over
+ * the sequence's context including it, as
  * pa_cache_append followed by pa_decode would, with the same results (the
  * pools bit-identical, out within fp32 rounding).
  *   k_new, v_new: [num_seqs][num_kv_heads][head_dim], the dtype of q;
@@ -272,8 +274,7 @@ int pa_decode_step_fp8(void *out, const void *q, const void *k_new, const void *
  * held by every GPU that loads it until the process exits.  Sizes whose
  * scratch would exceed it return PA_ERR_SCRATCH_LIMIT (the default split at
  * head_dim 128 needs about 10 MB on a 152-SM GPU).  The call allocates
- * nothing and frees nothing; it clears the scratch's merge counters on
- * `stream` before each launch.  The first call on a device looks up the
+ * nothing and frees nothing.  The first call on a device looks up the
  * array's device address (make it before any stream capture).  All calls on
  * a device share the array: calls that overlap on the GPU race.
  */

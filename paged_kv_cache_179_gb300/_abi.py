@@ -232,7 +232,7 @@ def pa_decode_default_splits(pool_dtype=torch.float16) -> int:
 
 
 def alloc_workspace(num_seqs, num_q_heads, head_dim, split_ctas, device):
-    """Caller-owned, zero-filled workspace for pa_decode."""
+    """Caller-owned workspace for pa_decode (needs no initialisation)."""
     n = pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, split_ctas)
     return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
 

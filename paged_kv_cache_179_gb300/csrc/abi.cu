@@ -114,9 +114,8 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
   a.v_pool_w = ap.v_pool;
   a.k_scale_w = ap.k_scale;
   a.v_scale_w = ap.v_scale;
-  // Batches above kMaxBatchPerLaunch run as consecutive launches on the
-  // stream; each reuses the workspace (its counters are back to zero when
-  // a launch ends).
+  // Batches above kMaxBatchPerLaunch run as consecutive launch pairs
+  // (attention, merge) on the stream, each reusing the workspace.
   const size_t out_row = static_cast<size_t>(s.Hq) * s.D * 2;   // q and out are 16-bit
   for (int b0 = 0; b0 < s.B; b0 += kMaxBatchPerLaunch) {
     DecodeArgs c = a;
@@ -131,7 +130,7 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
       c.v_new = static_cast<const uint8_t*>(ap.v_new) + b0 * new_row;
       c.slots = ap.slots + b0;
     }
-    decode_workspace_split(c, ws, &c.ws_acc, &c.ws_ml, &c.counters);
+    decode_workspace_split(c, ws);
     if (cudaError_t e = launch_decode(c, fp8, bf16, static_cast<cudaStream_t>(stream)))
       return cuda_status(e);
   }

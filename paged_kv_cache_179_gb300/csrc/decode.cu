@@ -453,117 +453,12 @@ __device__ __forceinline__ void store_partial(const WarpAcc<D>& st, const Decode
   }
 }
 
-// atomicAdd with acquire-release semantics at GPU scope: it publishes the
-// warp's partial (stored before it, ordered by __syncwarp) and, for the last
-// arriver, makes every other piece's partial visible.
-__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
-  int old;
-  asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
-               : "memory");
-  return old;
-}
-
 // (max, sum) pair combine of two partial softmax states in log2 units.
 __device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s2) {
   const float mn = fmaxf(m, m2);
   if (mn == -INFINITY) return;   // both empty
   s = s * fast_exp2(m - mn) + s2 * fast_exp2(m2 - mn);
   m = mn;
-}
-
-// The warp that completed segment (b, h) merges its np pieces, held by
-// workers w0 .. w0+np-1 (slot first_slot for w0, slot 0 for the others):
-//   out = sum_q 2^(m_q - M) acc_q / sum_q 2^(m_q - M) l_q,  M = max_q m_q.
-template <int D, bool FP8, bool BF16>
-__device__ void merge_pieces(const DecodeArgs& a, int b, int h, int w0, int first_slot, int np,
-                             int lane) {
-  const int G = a.group;
-  // per head g: lanes (g, q mod 4) fold the pieces' (max, sum) pairs
-  const int g1 = lane >> 2, q1 = lane & 3;
-  float mg = -INFINITY, sg = 0.f;
-  if (g1 < G) {
-    for (int q = q1; q < np; q += 4) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(
-          a.ws_ml + piece_row(w0 + q, q == 0 ? first_slot : 0, g1) * 2));
-      ms_combine(mg, sg, ml.x, ml.y);
-    }
-  }
-#pragma unroll
-  for (int o = 1; o < 4; o <<= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, mg, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, sg, o);
-    ms_combine(mg, sg, m2, s2);
-  }
-  float M[kGroupMax], S[kGroupMax];
-#pragma unroll
-  for (int g = 0; g < kGroupMax; ++g) {
-    M[g] = __shfl_sync(0xffffffffu, mg, 4 * g);
-    S[g] = __shfl_sync(0xffffffffu, sg, 4 * g);
-  }
-  uint16_t* rows = static_cast<uint16_t*>(a.out) + (static_cast<int64_t>(b) * a.Hq + h * G) * D;
-  for (int d4 = lane; d4 < D / 4; d4 += 32) {
-    float4 acc[kGroupMax];
-#pragma unroll
-    for (int g = 0; g < kGroupMax; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-    // The two-piece passes below keep twice the loads in flight; the E4M3
-    // instantiation keeps the one-piece loop, measured faster for it.
-    if constexpr (FP8) {
-    for (int q = 0; q < np; ++q) {
-      const int slot = q == 0 ? first_slot : 0;
-#pragma unroll
-      for (int g = 0; g < kGroupMax; ++g) {
-        if (g >= G || M[g] == -INFINITY) continue;
-        const int64_t row = piece_row(w0 + q, slot, g);
-        const float e = fast_exp2(__ldcg(a.ws_ml + row * 2) - M[g]);
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + row * D) + d4);
-        acc[g].x += e * v.x;
-        acc[g].y += e * v.y;
-        acc[g].z += e * v.z;
-        acc[g].w += e * v.w;
-      }
-    }
-    } else {
-    // two pieces per pass, all of a pass's loads issued before they are used
-    for (int q = 0; q < np; q += 2) {
-      const bool two = q + 1 < np;
-      float ma[kGroupMax], mb[kGroupMax];
-      float4 va[kGroupMax], vb[kGroupMax];
-#pragma unroll
-      for (int g = 0; g < kGroupMax; ++g) {
-        ma[g] = mb[g] = -INFINITY;
-        va[g] = vb[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (g >= G || M[g] == -INFINITY) continue;
-        const int64_t ra = piece_row(w0 + q, q == 0 ? first_slot : 0, g);
-        ma[g] = __ldcg(a.ws_ml + ra * 2);
-        va[g] = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + ra * D) + d4);
-        if (two) {
-          const int64_t rb = piece_row(w0 + q + 1, 0, g);
-          mb[g] = __ldcg(a.ws_ml + rb * 2);
-          vb[g] = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + rb * D) + d4);
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < kGroupMax; ++g) {
-        if (g >= G || M[g] == -INFINITY) continue;
-        const float ea = fast_exp2(ma[g] - M[g]);
-        const float eb = two ? fast_exp2(mb[g] - M[g]) : 0.f;
-        acc[g].x += ea * va[g].x + eb * vb[g].x;
-        acc[g].y += ea * va[g].y + eb * vb[g].y;
-        acc[g].z += ea * va[g].z + eb * vb[g].z;
-        acc[g].w += ea * va[g].w + eb * vb[g].w;
-      }
-    }
-    }
-#pragma unroll
-    for (int g = 0; g < kGroupMax; ++g) {
-      if (g >= G) continue;
-      const float inv = S[g] > 0.f ? 1.f / S[g] : 0.f;
-      uint2 v;
-      v.x = pack2<BF16>(acc[g].x * inv, acc[g].y * inv);
-      v.y = pack2<BF16>(acc[g].z * inv, acc[g].w * inv);
-      *reinterpret_cast<uint2*>(rows + g * D + 4 * d4) = v;
-    }
-  }
 }
 
 // Fused append: the new (this step's) row of one (sequence, kv head), the
@@ -666,6 +561,12 @@ decode_kernel(const DecodeArgs a) {
     uint16_t* o = static_cast<uint16_t*>(a.out) + static_cast<int64_t>(b) * Hq * D;
     for (int i = tid; i < Hq * D; i += kThreads) o[i] = 0;   // +0.0 in f16 and bf16
   }
+
+  // The merge launch reads the prefix sums (every CTA computed the same),
+  // and may be scheduled now: it waits for this grid to complete.
+  if (cta == 0 && a.seg_prefix != nullptr)
+    for (int b = tid; b <= B; b += kThreads) a.seg_prefix[b] = pf[b];
+  griddep_launch_dependents();
 
   // ---- 3. this warp's share of the block stream.  No CTA-wide barrier
   // follows: every warp is an independent worker from here on.  Never more
@@ -770,8 +671,6 @@ decode_kernel(const DecodeArgs a) {
 
   const float unboost = FP8 ? 1.f / kPBoost : 1.f;
   int piece_no = 0;
-  // pending merge checks (lane 0): slot 0 = first piece, 1 = last piece
-  int pend_b[2] = {-1, -1}, pend_h[2] = {0, 0}, pend_old[2] = {0, 0}, pend_np[2] = {0, 0};
 
   while (ch0.nb > 0) {
     const int L = len[ch0.b];
@@ -871,20 +770,11 @@ decode_kernel(const DecodeArgs a) {
         uint16_t* rows = static_cast<uint16_t*>(a.out) +
                          (static_cast<int64_t>(ch0.b) * Hq + ch0.h * G) * D;
         store_output<D, FP8, BF16>(st, rows, G, r, c, unboost);
-      } else if (a.ws_acc == nullptr || a.counters == nullptr) {
+      } else if (a.ws_acc == nullptr) {
         if (lane == 0) atomicOr(a.status, kStatusNoWorkspace);   // never written through null
       } else {
-        const int slot = piece_no == 0 ? 0 : 1;
-        store_partial<D, FP8>(st, a, gw, slot, r, c, unboost);
-        __syncwarp();
-        if (lane == 0) {
-          // count this piece; whether it completed the segment is checked at the end
-          pend_b[slot] = ch0.b;
-          pend_h[slot] = ch0.h;
-          pend_np[slot] = worker_of(s0 + nbk - 1, W, NW) - worker_of(s0, W, NW) + 1;
-          pend_old[slot] =
-              atomic_add_acq_rel(a.counters + static_cast<int64_t>(ch0.b) * Hkv + ch0.h, 1);
-        }
+        // a split segment: the merge launch combines its pieces
+        store_partial<D, FP8>(st, a, gw, piece_no == 0 ? 0 : 1, r, c, unboost);
       }
       ++piece_no;
       PA_TRACE_ONLY(++tr_pieces; tr_split += !(s0 >= lo && s0 + nbk <= hi));
@@ -927,32 +817,105 @@ decode_kernel(const DecodeArgs a) {
       (void)mbar_wait(sbar + 8 * (computed % STAGES), (computed / STAGES) & 1);
   }
 
-  // ---- 4. merges: for each of this warp's split pieces, the warp that
-  // completed the segment's count combines all of its pieces
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    int job = -1;
-    if (lane == 0 && pend_b[k] >= 0 && pend_old[k] == pend_np[k] - 1) {
-      atomicExch(a.counters + static_cast<int64_t>(pend_b[k]) * Hkv + pend_h[k], 0);
-      job = pend_b[k];
-    }
-    job = __shfl_sync(0xffffffffu, job, 0);
-    const int mh = __shfl_sync(0xffffffffu, pend_h[k], 0);
-    if (job >= 0) {
-      asm volatile("fence.acq_rel.gpu;" ::: "memory");
-      __syncwarp();
-      const int nbk = seg_blocks(pf, job, Hkv);
-      const int64_t s0 = pf[job] + static_cast<int64_t>(mh) * nbk;
-      const int w0 = worker_of(s0, W, NW), w1 = worker_of(s0 + nbk - 1, W, NW);
-      const int first_slot = s0 > worker_lo(w0, W, NW) ? 1 : 0;   // slot of w0's piece
-      merge_pieces<D, FP8, BF16>(a, job, mh, w0, first_slot, w1 - w0 + 1, lane);
-    }
-  }
   PA_TRACE_WARP(gw, 3, pa_now());
   PA_TRACE_WARP(gw, 4, tr_pieces);
   PA_TRACE_WARP(gw, 5, tr_split);
   PA_TRACE_WARP(gw, 6, static_cast<unsigned long long>(hi - lo));
   PA_TRACE_WARP(gw, 7, pa_smid());
+}
+
+// ------------------------------------------------------------ merge launch
+// The log-sum-exp merge of each split segment's pieces:
+//   out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p
+// (log2 units).  One CTA per (sequence, kv head); thread (g, d4) owns output
+// columns 4*d4 .. 4*d4+3 of query head g and folds the pieces in worker
+// order, kMergeBatch at a time (their loads in flight together), rescaling
+// its running state to each batch's maximum: a fixed order, so results are
+// deterministic.  Segments attended whole by one worker are skipped.  The
+// launch starts with griddepcontrol.wait: the attention grid has completed
+// and its writes are visible.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeBatch = 8;
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kMergeThreads)
+merge_kernel(const DecodeArgs a) {
+  griddep_wait();
+  const int Hkv = a.Hkv, G = a.group;
+  const int b = blockIdx.x / Hkv, h = blockIdx.x - b * Hkv;
+  const int* pf = a.seg_prefix;
+  const int64_t W = pf[a.B];
+  const int nbk = (pf[b + 1] - pf[b]) / Hkv;
+  if (nbk == 0) return;
+  const int64_t NW = min(static_cast<int64_t>(a.split_ctas) * kWarps, W);
+  const int64_t s0 = pf[b] + static_cast<int64_t>(h) * nbk;
+  const int w0 = worker_of(s0, W, NW), w1 = worker_of(s0 + nbk - 1, W, NW);
+  if (w0 == w1) return;                         // attended whole
+  const int first_slot = s0 > worker_lo(w0, W, NW) ? 1 : 0;   // the segment is w0's last piece
+  constexpr int COLS = D / 4;
+  const int tid = threadIdx.x, g = tid / COLS, d4 = tid - g * COLS;
+  if (g >= G) return;
+  float M = -INFINITY, S = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int np = w1 - w0 + 1;
+  for (int p0 = 0; p0 < np; p0 += kMergeBatch) {
+    float2 ml[kMergeBatch];
+    float4 v[kMergeBatch];
+#pragma unroll
+    for (int k = 0; k < kMergeBatch; ++k) {
+      ml[k] = make_float2(-INFINITY, 0.f);
+      v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int p = p0 + k;
+      if (p < np) {
+        const int64_t row = piece_row(w0 + p, p == 0 ? first_slot : 0, g);
+        ml[k] = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + row * 2));
+        v[k] = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + row * D) + d4);
+      }
+    }
+    float mb = M;
+#pragma unroll
+    for (int k = 0; k < kMergeBatch; ++k) mb = fmaxf(mb, ml[k].x);
+    if (mb == -INFINITY) continue;              // nothing attended yet
+    const float keep = fast_exp2(M - mb);
+    acc.x *= keep;
+    acc.y *= keep;
+    acc.z *= keep;
+    acc.w *= keep;
+    S *= keep;
+#pragma unroll
+    for (int k = 0; k < kMergeBatch; ++k) {
+      const float e = fast_exp2(ml[k].x - mb);  // 0 for a missing piece
+      S += e * ml[k].y;
+      acc.x += e * v[k].x;
+      acc.y += e * v[k].y;
+      acc.z += e * v[k].z;
+      acc.w += e * v[k].w;
+    }
+    M = mb;
+  }
+  const float inv = S > 0.f ? 1.f / S : 0.f;
+  uint2 o;
+  o.x = pack2<BF16>(acc.x * inv, acc.y * inv);
+  o.y = pack2<BF16>(acc.z * inv, acc.w * inv);
+  uint16_t* row = static_cast<uint16_t*>(a.out) + (static_cast<int64_t>(b) * a.Hq + h * G + g) * D;
+  *reinterpret_cast<uint2*>(row + 4 * d4) = o;
+}
+
+// The merge launch, allowed to be scheduled while the attention grid runs
+// (programmatic stream serialization); its griddepcontrol.wait orders it.
+template <int D, bool BF16>
+cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B) * static_cast<unsigned>(a.Hkv));
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_kernel<D, BF16>, a);
 }
 
 template <int D, bool FP8, bool BF16, int STAGES, bool APPEND, int CTAS>
@@ -970,7 +933,9 @@ cudaError_t launch_one(const DecodeArgs& a, cudaStream_t s) {
     last_smem[dev & 63] = lay.total;
   }
   kern<<<static_cast<unsigned>(a.split_ctas), kThreads, lay.total, s>>>(a);
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.ws_acc == nullptr || a.seg_prefix == nullptr) return cudaSuccess;
+  return launch_merge<D, BF16 && !FP8>(a, s);
 }
 
 // Shared memory and registers per CTA are traded against resident CTAs per
@@ -1013,22 +978,36 @@ int decode_max_default_ctas() {
   return device_sm_count() * (PA_CTAS_F16 > PA_CTAS_FP8 ? PA_CTAS_F16 : PA_CTAS_FP8);
 }
 
+namespace {
+// Workspace: partial rows (acc, then (max, sum)) of two pieces per worker,
+// then the block-stream prefix sums; each part 256-byte aligned.
+struct WsLayout {
+  size_t acc, ml, pf, total;
+};
+WsLayout ws_layout(int B, int D, int split_ctas) {
+  const int64_t rows = static_cast<int64_t>(split_ctas) * kWarps * 2 * kGroupMax;
+  const int64_t Bc = B < kMaxBatchPerLaunch ? B : kMaxBatchPerLaunch;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  WsLayout l{};
+  l.acc = 0;
+  l.ml = up(static_cast<size_t>(rows) * D * 4);
+  l.pf = l.ml + up(static_cast<size_t>(rows) * 2 * 4);
+  l.total = l.pf + up(static_cast<size_t>(Bc + 1) * 4);
+  return l;
+}
+}  // namespace
+
 size_t decode_workspace_bytes(int B, int Hq, int D, int split_ctas) {
   if (B <= 0 || Hq <= 0 || D <= 0 || split_ctas <= 0) return 0;
-  const int64_t rows = static_cast<int64_t>(split_ctas) * kWarps * 2 * kGroupMax;
-  const size_t acc = ((static_cast<size_t>(rows) * D * 4) + 255) & ~static_cast<size_t>(255);
-  const size_t ml = ((static_cast<size_t>(rows) * 2 * 4) + 255) & ~static_cast<size_t>(255);
-  const int64_t Bc = B < kMaxBatchPerLaunch ? B : kMaxBatchPerLaunch;
-  return acc + ml + static_cast<size_t>(Bc) * Hq * 4;
+  return ws_layout(B, D, split_ctas).total;
 }
 
-void decode_workspace_split(const DecodeArgs& a, void* ws, float** acc, float** ml, int** cnt) {
-  const int64_t rows = static_cast<int64_t>(a.split_ctas) * kWarps * 2 * kGroupMax;
-  const size_t acc_bytes = ((static_cast<size_t>(rows) * a.D * 4) + 255) & ~static_cast<size_t>(255);
-  const size_t ml_bytes = ((static_cast<size_t>(rows) * 2 * 4) + 255) & ~static_cast<size_t>(255);
-  *acc = static_cast<float*>(ws);
-  *ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + acc_bytes);
-  *cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + acc_bytes + ml_bytes);
+void decode_workspace_split(DecodeArgs& a, void* ws) {
+  const WsLayout l = ws_layout(a.B, a.D, a.split_ctas);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  a.ws_acc = reinterpret_cast<float*>(base + l.acc);
+  a.ws_ml = reinterpret_cast<float*>(base + l.ml);
+  a.seg_prefix = reinterpret_cast<int*>(base + l.pf);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, bool fp8, bool bf16, cudaStream_t s) {

@@ -2,8 +2,8 @@
 // allocate device memory.
 //
 // pa_decode needs a caller-allocated workspace (the partial results of
-// context partitions split across warps and one merge counter per
-// (sequence, kv head)).  Some callers cannot provide one: code running inside
+// context partitions split across warps, and the block-stream prefix sums
+// the merge launch reads).  Some callers cannot provide one: code running inside
 // a host framework that owns every byte of device memory and forbids raw
 // allocations, latency-critical serving loops where cudaMalloc would
 // synchronise the device, and plain C callers with no device allocator of
@@ -12,10 +12,9 @@
 //
 // The array is PA_NOALLOC_SCRATCH_BYTES (16 MiB); every GPU that loads the
 // library holds it until the process exits.  All calls on a device share it
-// and it keeps the last call's contents; the merge counters, which must start
-// at zero, are cleared on the caller's stream before each launch.  Calls that
-// overlap on the GPU (different streams, or different host threads) race on
-// the array and must not be issued.
+// and it keeps the last call's contents (nothing in it needs clearing
+// between calls).  Calls that overlap on the GPU (different streams, or
+// different host threads) race on the array and must not be issued.
 #include <climits>
 #include <cmath>
 #include <mutex>
@@ -110,10 +109,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
     c.q = static_cast<const uint8_t*>(q) + b0 * row;
     c.block_tables = block_tables + static_cast<int64_t>(b0) * max_blocks_per_seq;
     c.context_lens = context_lens + b0;
-    decode_workspace_split(c, ws, &c.ws_acc, &c.ws_ml, &c.counters);
-    // the merge counters must start at zero: clear them on the stream
-    const size_t cnt_bytes = static_cast<size_t>(c.B) * num_kv_heads * sizeof(int);
-    if (cudaMemsetAsync(c.counters, 0, cnt_bytes, s) != cudaSuccess) return PA_ERR_CUDA;
+    decode_workspace_split(c, ws);
     if (launch_decode(c, false, dtype == PA_BF16, s) != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;

@@ -24,7 +24,7 @@ struct DecodeArgs {
   const int32_t* context_lens;  // [B]
   float* ws_acc;                // [split_ctas][2][8][D] partial sums (unnormalised)
   float* ws_ml;                 // [split_ctas][2][8][2] partial (max, sum) in log2 units
-  int* counters;                // [B][Hkv] finished partitions (zero between calls)
+  int* seg_prefix;              // [B + 1] block-stream prefix sums, for the merge launch
   unsigned* status;             // device status word
   // fused append (pa_decode_step*): this step's new rows and where they go;
   // null for a plain decode
@@ -46,8 +46,8 @@ struct DecodeArgs {
 int decode_default_ctas(bool fp8);   // CTAs a default launch uses for this pool type
 int decode_max_default_ctas();       // the largest of those over pool types
 size_t decode_workspace_bytes(int B, int Hq, int D, int split_ctas);
-void decode_workspace_split(const DecodeArgs& a, void* ws, float** acc, float** ml,
-                            int** counters);
+// Points a's workspace fields into ws, for a's sizes (a.split_ctas, a.B, a.D).
+void decode_workspace_split(DecodeArgs& a, void* ws);
 
 cudaError_t launch_decode(const DecodeArgs& a, bool fp8, bool bf16, cudaStream_t s);
 

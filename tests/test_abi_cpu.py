@@ -72,14 +72,16 @@ def test_decode_argument_errors(lib):
 
 def test_workspace_size_formula(lib):
     # partial rows: 2 per warp (4 warps per CTA), 8 query-head slots each, D floats +
-    # (max, sum); then counters
+    # (max, sum); then the block-stream prefix sums (num_seqs + 1 ints); each part
+    # rounded up to 256 bytes
     n = lib.pa_decode_workspace_size(2, 8, 64, 10)
+    up = lambda x: (x + 255) // 256 * 256
     rows = 10 * 4 * 2 * 8
-    acc, ml, counters = rows * 64 * 4, rows * 2 * 4, 2 * 8 * 4
-    assert n == ((acc + 255) // 256) * 256 + ((ml + 255) // 256) * 256 + counters
+    acc, ml, prefix = rows * 64 * 4, rows * 2 * 4, (2 + 1) * 4
+    assert n == up(acc) + up(ml) + up(prefix)
     assert lib.pa_decode_workspace_size(2, 8, 64, 1) > 0        # one CTA's 4 warps still split
     assert lib.pa_decode_workspace_size(2, 8, 64, -1) == 0      # invalid
-    # batches above 2048 sequences run in launches of 2048 that share the workspace
+    # batches above 512 sequences run in launches of 512 that share the workspace
     assert lib.pa_decode_workspace_size(5000, 8, 64, 10) == \
         lib.pa_decode_workspace_size(2048, 8, 64, 10)
 
