@@ -452,7 +452,8 @@ def describe(w, tokens):
 def kernel_sha() -> str:
     import hashlib
     h = hashlib.sha256()
-    for p in ("paged_kv_cache_179_gb300/csrc/decode.cu", "paged_kv_cache_179_gb300/csrc/pa_ptx.cuh"):
+    for p in ("paged_kv_cache_179_gb300/csrc/decode.cu", "paged_kv_cache_179_gb300/csrc/pa_ptx.cuh",
+              "paged_kv_cache_179_gb300/csrc/pa_launch.h", "paged_kv_cache_179_gb300/csrc/pa_e4m3.cuh"):
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

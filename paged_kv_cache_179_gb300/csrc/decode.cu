@@ -835,7 +835,10 @@ decode_kernel(const DecodeArgs a) {
 // launch starts with griddepcontrol.wait: the attention grid has completed
 // and its writes are visible.
 constexpr int kMergeThreads = 256;
-constexpr int kMergeBatch = 8;
+#ifndef PA_MERGE_BATCH
+#define PA_MERGE_BATCH 8
+#endif
+constexpr int kMergeBatch = PA_MERGE_BATCH;
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kMergeThreads)
