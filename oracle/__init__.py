@@ -59,11 +59,12 @@ def lib():
             L.oracle_e4m3_value_array.argtypes = [vp, vp, i64]
             L.oracle_cache_append.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32]
             L.oracle_quantize_fp8.argtypes = [vp, i64, i32, i32, i32, vp, vp]
-            L.oracle_cache_append_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32]
+            L.oracle_cache_append_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                  i32]
             L.oracle_decode.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32,
                                         f32, vp, i32, vp]
-            L.oracle_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
-                                            i32, f32, vp, i32, vp]
+            L.oracle_decode_fp8.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
+                                            i32, i32, f32, vp, i32, vp]
             L.oracle_copy_blocks.argtypes = [vp, vp, vp, vp, vp, i32, ctypes.c_size_t, i32, i64]
             L.oracle_num_threads.restype = i32
             _lib = L
@@ -128,15 +129,18 @@ def copy_blocks(k_cache, v_cache, pairs, k_scale=None, v_scale=None) -> None:
 
 
 def cache_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping,
-                     block_size: int) -> None:
-    """In place: E4M3-encode each fp16 token row into its page (first token sets the scale)."""
+                     block_size: int, *, bf16: bool = False) -> None:
+    """In place: E4M3-encode each token row (fp16, or bf16 bits as uint16 when
+    ``bf16``) into its page: the page's first token sets the scale, a later
+    token that would saturate re-scales the page first."""
     T, Hkv, D = k_new.shape
     for a in (k_cache, v_cache, k_scale, v_scale):
         assert a.flags.c_contiguous
     assert k_cache.dtype == np.uint8 and k_scale.dtype == np.float32
     slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     lib().oracle_cache_append_fp8(_p(_u16(k_new)), _p(_u16(v_new)), _p(k_cache), _p(v_cache),
-                                  _p(k_scale), _p(v_scale), _p(slots), T, Hkv, D, block_size)
+                                  _p(k_scale), _p(v_scale), _p(slots), T, Hkv, D, block_size,
+                                  int(bf16))
 
 
 def quantize_fp8(src) -> tuple[np.ndarray, np.ndarray]:
@@ -180,8 +184,9 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, *, bf1
 
 
 def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale: float, *,
-               rows=None, return_wsum: bool = False):
-    """GQA decode over an E4M3 pool with per-(block, kv head) fp32 scales, in double."""
+               bf16: bool = False, rows=None, return_wsum: bool = False):
+    """GQA decode over an E4M3 pool with per-(block, kv head) fp32 scales, in
+    double; q is fp16, or bf16 bits as uint16 when ``bf16``."""
     B, Hq, D = q.shape
     NB, Hkv, bs, D2 = k_codes.shape
     assert D == D2 and Hq % Hkv == 0 and D <= 256
@@ -195,7 +200,7 @@ def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens
     out = np.zeros((B, Hq, D), dtype=np.float64)
     ws = np.zeros((B, Hq), dtype=np.float64) if return_wsum else None
     r, nr = _rows_arg(rows)
-    lib().oracle_decode_fp8(_p(out), _p(_u16(q)), _p(kc), _p(vc), _p(ks), _p(vs), _p(bt),
+    lib().oracle_decode_fp8(_p(out), _p(_u16(q)), int(bf16), _p(kc), _p(vc), _p(ks), _p(vs), _p(bt),
                             bt.shape[1], _p(cl), B, Hq, Hkv, D, bs, float(np.float32(scale)),
                             _p(r), nr, _p(ws))
     return (out, ws) if return_wsum else out

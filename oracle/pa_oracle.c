@@ -227,16 +227,34 @@ void oracle_quantize_fp8(const uint16_t *src, int64_t num_blocks, int num_kv_hea
 }
 
 /*
- * FP8 append: like the plain append, but the token's fp16 row is encoded.  A
- * page that receives its first token (slot % block_size == 0) takes the scale
- * amax(row)/448 of that token's row (per kv head); any later token of the page
- * reuses the stored scale and saturates if it exceeds it.  Tokens are taken
- * in order.
+ * FP8 append: like the plain append, but the token's row (fp16, or bf16 when
+ * is_bf16) is encoded, per kv head and separately for K and V.
+ *   - A page that receives its first token (slot % block_size == 0) takes the
+ *     scale amax(row) / 448 of that row.
+ *   - A later token of the page is encoded with the stored scale s when
+ *     fl32(amax(row) / s) <= 448, that is when no element saturates.
+ *   - Otherwise the page is re-scaled first: s' = amax(row) / 448, each code c
+ *     of the page's rows before the new one becomes
+ *     E4M3(fl32(fl32(e4m3(c) * s) / s')), and s' is stored.
+ * Codes are E4M3_RNE_sat(fl32(x / scale)).  Tokens are taken in order.  (LLM
+ * Serving Kernels, Projects table, row 05: E4M3 storage with page scales;
+ * rvLLM, CUDA Kernels table, "FP8 KV Cache": quantisation on the cache write.)
  */
+static float row_amax(const uint16_t *x, int n, int is_bf16)
+{
+    float amax = 0.0f;
+    for (int d = 0; d < n; d++) {
+        float a = fabsf((float)act_to_double(x[d], is_bf16));
+        if (a > amax)
+            amax = a;
+    }
+    return amax;
+}
+
 void oracle_cache_append_fp8(const uint16_t *k_new, const uint16_t *v_new, uint8_t *k_cache,
                              uint8_t *v_cache, float *k_scale, float *v_scale,
                              const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
-                             int head_dim, int block_size)
+                             int head_dim, int block_size, int is_bf16)
 {
     for (int i = 0; i < num_tokens; i++) {
         int64_t s = slot_mapping[i];
@@ -247,20 +265,23 @@ void oracle_cache_append_fp8(const uint16_t *k_new, const uint16_t *v_new, uint8
             int64_t tile = blk * num_kv_heads + h;
             for (int kv = 0; kv < 2; kv++) {
                 const uint16_t *x = (kv ? v_new : k_new) + ((size_t)i * num_kv_heads + h) * head_dim;
-                uint8_t *dst = (kv ? v_cache : k_cache) + (tile * block_size + off) * head_dim;
+                uint8_t *page = (kv ? v_cache : k_cache) + tile * block_size * head_dim;
                 float *sc = kv ? v_scale : k_scale;
+                float amax = row_amax(x, head_dim, is_bf16);
                 if (off == 0) {
-                    float amax = 0.0f;
-                    for (int d = 0; d < head_dim; d++) {
-                        float a = fabsf((float)half_bits_to_double(x[d]));
-                        if (a > amax)
-                            amax = a;
-                    }
                     sc[tile] = e4m3_page_scale(amax);
+                } else if (amax / sc[tile] > 448.0f) {
+                    float s_old = sc[tile], s_new = e4m3_page_scale(amax);
+                    for (int64_t j = 0; j < off * head_dim; j++) {
+                        float v = (float)oracle_e4m3_value(page[j]) * s_old;
+                        page[j] = oracle_e4m3_encode(v / s_new);
+                    }
+                    sc[tile] = s_new;
                 }
                 float scale = sc[tile];
                 for (int d = 0; d < head_dim; d++)
-                    dst[d] = oracle_e4m3_encode((float)half_bits_to_double(x[d]) / scale);
+                    page[off * head_dim + d] =
+                        oracle_e4m3_encode((float)act_to_double(x[d], is_bf16) / scale);
             }
         }
     }
@@ -367,15 +388,17 @@ void oracle_decode(double *out, const uint16_t *q, const uint16_t *k_cache, cons
                 num_q_heads, num_kv_heads, head_dim, block_size, scale, rows, n_rows, wsum_dev);
 }
 
-/* FP8 pool: K = e4m3(code) * k_scale[block][kv head] exactly (in double); Q is fp16. */
-void oracle_decode_fp8(double *out, const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
-                       const float *k_scale, const float *v_scale, const int32_t *block_tables,
-                       int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
-                       int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+/* FP8 pool: K = e4m3(code) * k_scale[block][kv head] exactly (in double); Q is
+ * fp16, or bf16 when q_is_bf16. */
+void oracle_decode_fp8(double *out, const uint16_t *q, int q_is_bf16, const uint8_t *k_cache,
+                       const uint8_t *v_cache, const float *k_scale, const float *v_scale,
+                       const int32_t *block_tables, int max_blocks_per_seq,
+                       const int32_t *context_lens, int num_seqs, int num_q_heads,
+                       int num_kv_heads, int head_dim, int block_size, float scale,
                        const int32_t *rows, int n_rows, double *wsum_dev)
 {
     pool_view p = {k_cache, v_cache, k_scale, v_scale, 0, 1};
-    decode_impl(out, q, 0, &p, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+    decode_impl(out, q, q_is_bf16, &p, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                 num_q_heads, num_kv_heads, head_dim, block_size, scale, rows, n_rows, wsum_dev);
 }
 

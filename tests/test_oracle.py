@@ -185,7 +185,12 @@ def test_append_writes_rows_and_leaves_other_bytes():
     assert np.array_equal(v.view(np.uint16)[untouched], v0.view(np.uint16)[untouched])
 
 
-def test_append_fp8_first_token_sets_scale_then_reused():
+def _torch_value(codes: np.ndarray) -> np.ndarray:
+    """E4M3 codes -> their fp32 values, by torch's float8_e4m3fn."""
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).float().numpy()
+
+
+def test_append_fp8_first_token_sets_scale_reuses_it_then_rescales():
     rng = np.random.default_rng(4)
     Hkv, D, NB = 2, 64, 4
     kc = np.zeros((NB, Hkv, 16, D), np.uint8)
@@ -195,16 +200,50 @@ def test_append_fp8_first_token_sets_scale_then_reused():
     t0 = rng.standard_normal((1, Hkv, D)).astype(np.float16)
     oracle.cache_append_fp8(t0, t0, kc, vc, ks, vs, np.array([2 * 16]), 16)
     amax = np.abs(t0[0].astype(np.float32)).max(axis=1)
-    assert np.array_equal(ks[2], amax / np.float32(448))
+    s0 = amax / np.float32(448)
+    assert np.array_equal(ks[2], s0)
     assert np.all(ks[[0, 1, 3]] == -1.0)
     assert np.array_equal(kc[2, :, 0], _torch_rne((t0[0].astype(np.float32) / ks[2][:, None])))
-    # second token of the page: same scale, saturating
-    t1 = (t0 * 3).astype(np.float16)
+    # second token within the page's range: the scale is reused
+    t1 = (t0 * 0.5).astype(np.float16)
     oracle.cache_append_fp8(t1, t1, kc, vc, ks, vs, np.array([2 * 16 + 1]), 16)
-    assert np.array_equal(ks[2], amax / np.float32(448))
-    q = t1[0].astype(np.float32) / ks[2][:, None]
-    assert np.array_equal(kc[2, :, 1], _torch_rne(np.clip(q, -448, 448)))
-    assert np.all(kc[2, :, 1] & 0x7F <= 0x7E)
+    assert np.array_equal(ks[2], s0)
+    assert np.array_equal(kc[2, :, 1], _torch_rne(t1[0].astype(np.float32) / s0[:, None]))
+    # third token 3x larger: the page is re-scaled to it and its rows re-encoded
+    before = kc[2].copy()
+    t2 = (t0 * 3).astype(np.float16)
+    oracle.cache_append_fp8(t2, t2, kc, vc, ks, vs, np.array([2 * 16 + 2]), 16)
+    s1 = np.abs(t2[0].astype(np.float32)).max(axis=1) / np.float32(448)
+    assert np.array_equal(ks[2], s1) and np.array_equal(vs[2], s1)
+    for h in range(Hkv):
+        old = (_torch_value(before[h, :2]) * s0[h]).astype(np.float32)
+        assert np.array_equal(kc[2, h, :2], _torch_rne((old / s1[h]).astype(np.float32)))
+        x = t2[0, h].astype(np.float32)
+        assert np.array_equal(kc[2, h, 2], _torch_rne(x / s1[h]))
+        assert np.abs(_torch_value(kc[2, h, 2])).max() == 448.0     # the row's amax, unsaturated
+    assert np.array_equal(kc[2, :, 3:], before[:, 3:])             # rows past the new one
+    # after two roundings every stored value stays within twice E4M3's bound of its token
+    for row, t in ((0, t0), (1, t1), (2, t2)):
+        x = t[0].astype(np.float64)
+        got = _torch_value(kc[2, :, row]).astype(np.float64) * s1[:, None]
+        bound = 2 * (2.0 ** -4 * np.abs(x) + 2.0 ** -10 * s1[:, None])
+        assert np.all(np.abs(got - x) <= bound + 1e-12)
+
+
+def test_append_fp8_bf16_rows():
+    rng = np.random.default_rng(6)
+    Hkv, D, NB = 2, 128, 2
+    x = rng.standard_normal((2, Hkv, D)).astype(np.float32) * 5
+    bits = (torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy()).view(np.uint16)
+    xb = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    kc = np.zeros((NB, Hkv, 16, D), np.uint8)
+    vc = np.zeros_like(kc)
+    ks = np.zeros((NB, Hkv), np.float32)
+    vs = ks.copy()
+    oracle.cache_append_fp8(bits, bits, kc, vc, ks, vs, np.array([16, 17]), 16, bf16=True)
+    s = np.maximum(np.abs(xb[0]).max(axis=1), np.abs(xb[1]).max(axis=1)) / np.float32(448)
+    assert np.array_equal(ks[1], s)
+    assert np.array_equal(kc[1, :, 1], _torch_rne(xb[1] / s[:, None]))
 
 
 # -------------------------------------------------------------------- decode
@@ -397,6 +436,22 @@ def test_decode_fp8_matches_dense_on_dequantised_pool():
     ref = oracle.decode(q, kp, vp, tables, lens, scale)
     err = np.abs(got - ref)
     assert 1e-5 < err.mean() < 2e-2
+
+
+def test_decode_fp8_bf16_query_matches_dense():
+    rng = np.random.default_rng(10)
+    B, Hq, Hkv, D = 2, 12, 2, 128
+    q, kp, vp, tables, lens = _random_case(rng, B, Hq, Hkv, D, 90)
+    kc, ks = oracle.quantize_fp8(kp)
+    vc, vs = oracle.quantize_fp8(vp)
+    qb = torch.from_numpy(q.astype(np.float32) * 3).to(torch.bfloat16)
+    qbits = qb.view(torch.int16).numpy().view(np.uint16)
+    scale = float(np.float32(1 / math.sqrt(D)))
+    got = oracle.decode_fp8(qbits, kc, vc, ks, vs, tables, lens, scale, bf16=True)
+    kd = oracle.e4m3_value(kc) * ks[:, :, None, None].astype(np.float64)
+    vd = oracle.e4m3_value(vc) * vs[:, :, None, None].astype(np.float64)
+    want = _dense(qb.float().numpy().astype(np.float64), kd, vd, tables, lens, scale)
+    assert np.abs(got - want).max() < 1e-12
 
 
 def test_rows_subset_matches_full():
