@@ -4,13 +4,15 @@
 Default workload: the Qwen2.5-7B-shaped batch (128 sequences, 28 q / 4 kv
 heads, head_dim 128, fp16, lognormal context lengths with median 1024 clipped
 to [1, 8192]; seeded synthetic data).  A step is the whole hot path for one
-batch: pa_decode_step appends each sequence's new token and attends over
-its context in one attention launch, followed by the launch that merges the
-split contexts by log-sum-exp;
-``--unfused`` times pa_cache_append + pa_decode instead.  Between timed steps the L2 is not flushed when
-the step reads at least 3x the L2 size (429 MB of K/V against a 129 MB L2
-for the default batch); smaller batches have L2 evicted by reading a 2x-L2
-buffer outside the timed region.
+batch: each sequence's new token is appended and each sequence attends over
+its context, split contexts merged by log-sum-exp in a second launch.  For
+16-bit pools the append runs inside the attention launch (pa_decode_step);
+for E4M3 pools, where that is slower, as its own launch first
+(pa_cache_append_fp8 + pa_decode_fp8); ``--step`` forces either form.
+Between timed steps the L2 is not flushed when the step reads at least 3x
+the L2 size (429 MB of K/V against a 129 MB L2 for the default batch);
+smaller batches have L2 evicted by reading a 2x-L2 buffer outside the timed
+region.
 
 Prints one JSON line.  ``value`` is attended KV tokens/s of the whole job
 (sum of context lengths over all ranks / max-over-ranks step time); the line
@@ -242,7 +244,7 @@ def run_ours(args, rank, world, dev):
         elif l2_mode == "write":
             flush_buf.add_(1)
     stream = torch.cuda.current_stream(dev)
-    fused = not args.unfused
+    fused = step.prefers_fused if args.step == "auto" else args.step == "fused"
     # decode_kernel + merge_kernel (fused) | append_kernel + decode_kernel + merge_kernel
     launches_per_step = 2 if fused else 3
 
@@ -346,8 +348,8 @@ def run_ours(args, rank, world, dev):
         "dtype": "e4m3->f32" if w.kv == "fp8" else w.dtype, "data": "synthetic",
         "config": {
             "workload": describe(w, tokens),
-            "step": ("pa_decode_step (append + decode, one launch)" if fused
-                     else "pa_cache_append + pa_decode"),
+            "step": ("pa_decode_step: append inside the attention launch, then the merge launch"
+                     if fused else "append launch, then attention and merge launches"),
             "split_ctas": step.split_ctas, "l2": describe_l2(l2_mode, kv_bytes, l2),
             "seed": args.seed, "parallelism": "replicas" if world > 1 else "single GPU",
         },
@@ -545,8 +547,10 @@ def main(argv=None):
     ap.add_argument("--l2", choices=["auto", "none", "read", "write"], default="auto",
                     help="L2 handling between timed steps (auto: none when the K/V read "
                          "is >= 3x L2, else evict by reading a 2x-L2 buffer)")
-    ap.add_argument("--unfused", action="store_true",
-                    help="time the step as pa_cache_append + pa_decode (two launches)")
+    ap.add_argument("--step", choices=["auto", "fused", "two-launch"], default="auto",
+                    help="fused: pa_decode_step (append inside the attention launch); two-launch: "
+                         "pa_cache_append + pa_decode; auto: the faster for the pool type "
+                         "(fused for 16-bit pools, two-launch for E4M3)")
     ap.add_argument("--prime-ms", type=float, default=0.0,
                     help="GPU sleep queued ahead of the timed steps so the host runs ahead")
     ap.add_argument("--op", choices=["step", "copy_blocks"], default="step",

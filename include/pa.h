@@ -97,21 +97,26 @@ int pa_cache_append(const void *k_new, const void *v_new, void *k_cache, void *v
                     int block_size, int num_blocks, int dtype, void *stream);
 
 /*
- * FP8 append: like pa_cache_append, but each fp16 row is written as E4M3
- * codes.  A page that receives its first token (slot % block_size == 0)
- * gets, per kv head, scale = amax(|row|) / 448 in fp32 (1.0 when amax is 0),
- * stored to k_scale / v_scale [num_blocks][num_kv_heads]; a later token of
- * the page reuses the stored scale and saturates at +-448.  Codes are
- * E4M3(x / scale) with the quotient rounded in fp32 and the code rounded to
- * nearest even.  Within one call, a page's first token and later tokens of
- * the same page race: give them in separate calls.
+ * FP8 append: like pa_cache_append, but each row (dtype PA_F16 or PA_BF16)
+ * is written as E4M3 codes, with one fp32 scale per (page, kv head) in
+ * k_scale / v_scale [num_blocks][num_kv_heads], for K and V separately:
+ *   - a page that receives its first token (slot % block_size == 0) gets
+ *     scale = amax(|row|) / 448 (1.0 when amax is 0);
+ *   - a later token is encoded with the stored scale s when
+ *     fl32(amax(|row|) / s) <= 448, so that no element saturates;
+ *   - otherwise the page is re-scaled first: s' = amax(|row|) / 448 is
+ *     stored and every code c of the page's rows before the new one becomes
+ *     E4M3(fl32(fl32(e4m3(c) * s) / s')).
+ * Codes are E4M3(x / scale) with the quotient rounded in fp32 and the code
+ * rounded to nearest even.  Within one call, tokens of the same page race:
+ * give them in separate calls (one token per sequence per decode step).
  * Source: rvLLM, CUDA Kernels table, "FP8 KV Cache"; LLM Serving Kernels,
- * Projects table, row 05.
+ * Projects table, row 05 (E4M3 storage, page scales).
  */
 int pa_cache_append_fp8(const void *k_new, const void *v_new, uint8_t *k_cache, uint8_t *v_cache,
                         float *k_scale, float *v_scale, const int64_t *slot_mapping,
                         int num_tokens, int num_kv_heads, int head_dim, int block_size,
-                        int num_blocks, void *stream);
+                        int num_blocks, int dtype, void *stream);
 
 /*
  * Bulk page quantisation of two fp16 pools (K and V) into E4M3 pools: for
@@ -208,9 +213,12 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * Paged GQA decode over an E4M3 pool: as pa_decode with fp16 q and out, K_t
- * = e4m3(k_code) * k_scale[block][kv head] and V_t likewise, dequantised in
- * registers inside the attention loop.
+ * Paged GQA decode over an E4M3 pool: as pa_decode (q and out of dtype
+ * PA_F16 or PA_BF16), K_t = e4m3(k_code) * k_scale[block][kv head] and V_t
+ * likewise, dequantised in registers inside the attention loop.  A bf16 q
+ * enters the fp16 tensor-core products scaled by a power of two per
+ * (sequence, kv head), so that its largest element lies in [2^14, 2^15);
+ * the scale is taken out of the scores.
  * Source: rvLLM, CUDA Kernels table, "FP8 KV Cache" and "PagedAttention V2";
  * LLM Serving Kernels, Projects table, row 05 ("fused dequantization").
  */
@@ -218,7 +226,7 @@ int pa_decode_fp8(void *out, const void *q, const uint8_t *k_cache, const uint8_
                   const float *k_scale, const float *v_scale, const int32_t *block_tables,
                   int max_blocks_per_seq, const int32_t *context_lens, int max_context_len,
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                  int num_blocks, float scale, int split_ctas, void *workspace,
+                  int num_blocks, float scale, int dtype, int split_ctas, void *workspace,
                   size_t workspace_bytes, void *stream);
 
 /*
@@ -249,9 +257,10 @@ int pa_decode_step(void *out, const void *q, const void *k_new, const void *v_ne
                    size_t workspace_bytes, void *stream);
 
 /*
- * pa_decode_step over E4M3 pools: fp16 q, k_new, v_new and out; the new row
- * is encoded as pa_cache_append_fp8 does (a page's first row sets its K and
- * V scales, later rows reuse them) and attended as pa_decode_fp8 does.
+ * pa_decode_step over E4M3 pools: q, k_new, v_new and out of dtype PA_F16 or
+ * PA_BF16; the new row is encoded as pa_cache_append_fp8 does (a page's first
+ * row sets its K and V scales, a later row that would saturate re-scales the
+ * page) and attended as pa_decode_fp8 does.
  * Source: as pa_decode_step, and rvLLM, CUDA Kernels table, "FP8 KV Cache".
  */
 int pa_decode_step_fp8(void *out, const void *q, const void *k_new, const void *v_new,
@@ -259,7 +268,7 @@ int pa_decode_step_fp8(void *out, const void *q, const void *k_new, const void *
                        const int64_t *slot_mapping, const int32_t *block_tables,
                        int max_blocks_per_seq, const int32_t *context_lens, int max_context_len,
                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                       int block_size, int num_blocks, float scale, int split_ctas,
+                       int block_size, int num_blocks, float scale, int dtype, int split_ctas,
                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*

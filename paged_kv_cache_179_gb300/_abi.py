@@ -29,8 +29,8 @@ SIGNATURES = {
     "pa_version": ([], _i32),
     "pa_status_string": ([_i32], ctypes.c_char_p),
     "pa_cache_append": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp], _i32),
-    "pa_cache_append_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp],
-                            _i32),
+    "pa_cache_append_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                             _vp], _i32),
     "pa_quantize_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp], _i32),
     "pa_e4m3_encode": ([_vp, _vp, _i64, _vp], _i32),
     "pa_copy_blocks": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp], _i32),
@@ -39,11 +39,11 @@ SIGNATURES = {
     "pa_decode": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                    _f32, _i32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
-                       _i32, _i32, _f32, _i32, _vp, _sz, _vp], _i32),
+                       _i32, _i32, _f32, _i32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                         _i32, _i32, _i32, _f32, _i32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_step_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
-                            _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _sz, _vp], _i32),
+                            _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                            _i32, _i32, _f32, _i32, _i32, _vp], _i32),
     "pa_get_status": ([_vp, ctypes.POINTER(ctypes.c_uint)], _i32),
@@ -147,10 +147,12 @@ def pa_cache_append(k_new, v_new, k_cache, v_cache, slot_mapping) -> None:
 
 
 def pa_cache_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping) -> None:
-    """E4M3-encode fp16 k_new/v_new into uint8 pools; a page's first token sets its scales."""
+    """E4M3-encode fp16/bf16 k_new/v_new into uint8 pools: a page's first token
+    sets its scales, a later token that would saturate re-scales the page."""
     dev = k_cache.device
     for t, n in ((k_new, "k_new"), (v_new, "v_new")):
-        _need(t, n, torch.float16, 3, dev)
+        _need(t, n, (torch.float16, torch.bfloat16), 3, dev)
+    _need(v_new, "v_new", k_new.dtype)
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, n, torch.uint8, 4, dev)
     for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
@@ -162,7 +164,8 @@ def pa_cache_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_m
         raise ValueError("shape mismatch")
     _check(load().pa_cache_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
                                       _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), T, Hkv,
-                                      D, bs, NB, _stream(dev)), "pa_cache_append_fp8")
+                                      D, bs, NB, _act_code(k_new.dtype), _stream(dev)),
+           "pa_cache_append_fp8")
 
 
 def pa_quantize_fp8(k_src, v_src, k_cache, v_cache, k_scale, v_scale) -> None:
@@ -271,10 +274,11 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_
 def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
                   max_context_len: int, scale: float, split_ctas: int = 0,
                   workspace=None) -> None:
-    """As pa_decode over E4M3 pools with per-(block, kv head) fp32 scales; q/out fp16."""
+    """As pa_decode over E4M3 pools with per-(block, kv head) fp32 scales; q/out
+    fp16 or bf16."""
     dev = q.device
-    _need(q, "q", torch.float16, 3, dev)
-    _need(out, "out", torch.float16, 3, dev)
+    _need(q, "q", (torch.float16, torch.bfloat16), 3, dev)
+    _need(out, "out", q.dtype, 3, dev)
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, n, torch.uint8, 4, dev)
     for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
@@ -288,8 +292,8 @@ def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, cont
     _check(load().pa_decode_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                 _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
                                 _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
-                                float(scale), int(split_ctas), _ptr(workspace), ws_bytes,
-                                _stream(dev)), "pa_decode_fp8")
+                                float(scale), _act_code(q.dtype), int(split_ctas),
+                                _ptr(workspace), ws_bytes, _stream(dev)), "pa_decode_fp8")
 
 
 def _ws_bytes(workspace, dev):
@@ -327,12 +331,12 @@ def pa_decode_step(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_t
 def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping,
                        block_tables, context_lens, max_context_len: int, scale: float,
                        split_ctas: int = 0, workspace=None) -> None:
-    """Append (E4M3-encode) k_new/v_new, then decode over the E4M3 pools, in one launch."""
+    """Append (E4M3-encode) k_new/v_new, then decode over the E4M3 pools, in one
+    attention launch; q, k_new, v_new and out share one dtype (fp16 or bf16)."""
     dev = q.device
-    for t, n in ((q, "q"), (out, "out")):
-        _need(t, n, torch.float16, 3, dev)
-    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
-        _need(t, n, torch.float16, 3, dev)
+    _need(q, "q", (torch.float16, torch.bfloat16), 3, dev)
+    for t, n in ((out, "out"), (k_new, "k_new"), (v_new, "v_new")):
+        _need(t, n, q.dtype, 3, dev)
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, n, torch.uint8, 4, dev)
     for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
@@ -346,8 +350,8 @@ def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
                                      _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                      _ptr(slot_mapping), _ptr(block_tables), block_tables.shape[1],
                                      _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs,
-                                     NB, float(scale), int(split_ctas), _ptr(workspace),
-                                     _ws_bytes(workspace, dev), _stream(dev)),
+                                     NB, float(scale), _act_code(q.dtype), int(split_ctas),
+                                     _ptr(workspace), _ws_bytes(workspace, dev), _stream(dev)),
            "pa_decode_step_fp8")
 
 

@@ -199,8 +199,9 @@ int pa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v
 int pa_cache_append_fp8(const void* k_new, const void* v_new, uint8_t* k_cache, uint8_t* v_cache,
                         float* k_scale, float* v_scale, const int64_t* slot_mapping,
                         int num_tokens, int num_kv_heads, int head_dim, int block_size,
-                        int num_blocks, void* stream) {
+                        int num_blocks, int dtype, void* stream) {
   if (num_tokens == 0) return PA_OK;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
   if (!k_new || !v_new || !k_cache || !v_cache || !k_scale || !v_scale || !slot_mapping)
     return PA_ERR_INVALID_ARG;
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
@@ -216,7 +217,7 @@ int pa_cache_append_fp8(const void* k_new, const void* v_new, uint8_t* k_cache, 
   if (int rc = device_state(&dev)) return rc;
   return cuda_status(launch_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale,
                                        slot_mapping, num_tokens, num_kv_heads, head_dim,
-                                       block_size, num_blocks, dev->status,
+                                       block_size, num_blocks, dtype == PA_BF16, dev->status,
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -316,12 +317,13 @@ int pa_decode_fp8(void* out, const void* q, const uint8_t* k_cache, const uint8_
                   const float* k_scale, const float* v_scale, const int32_t* block_tables,
                   int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                  int num_blocks, float scale, int split_ctas, void* workspace,
+                  int num_blocks, float scale, int dtype, int split_ctas, void* workspace,
                   size_t workspace_bytes, void* stream) {
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables ||
       !context_lens)
     return PA_ERR_INVALID_ARG;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
   const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                       num_blocks, max_blocks_per_seq, max_context_len, split_ctas};
   if (int rc = check_decode_shape(s, scale)) return rc;
@@ -332,7 +334,7 @@ int pa_decode_fp8(void* out, const void* q, const uint8_t* k_cache, const uint8_
       !aligned(v_scale, 4))
     return PA_ERR_INVALID_ARG;
   return run_decode(s, out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
-                    scale, true, false, workspace, workspace_bytes, stream);
+                    scale, true, dtype == PA_BF16, workspace, workspace_bytes, stream);
 }
 
 int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_new,
@@ -370,12 +372,13 @@ int pa_decode_step_fp8(void* out, const void* q, const void* k_new, const void* 
                        const int64_t* slot_mapping, const int32_t* block_tables,
                        int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                       int block_size, int num_blocks, float scale, int split_ctas,
+                       int block_size, int num_blocks, float scale, int dtype, int split_ctas,
                        void* workspace, size_t workspace_bytes, void* stream) {
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_new || !v_new || !k_cache || !v_cache || !k_scale || !v_scale ||
       !slot_mapping || !block_tables || !context_lens)
     return PA_ERR_INVALID_ARG;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
   const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                       num_blocks, max_blocks_per_seq, max_context_len, split_ctas};
   if (int rc = check_decode_shape(s, scale)) return rc;
@@ -394,7 +397,7 @@ int pa_decode_step_fp8(void* out, const void* q, const void* k_new, const void* 
   ap.k_scale = k_scale;
   ap.v_scale = v_scale;
   return run_decode(s, out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
-                    scale, true, false, workspace, workspace_bytes, stream, ap);
+                    scale, true, dtype == PA_BF16, workspace, workspace_bytes, stream, ap);
 }
 
 int pa_get_status(void* stream, unsigned* bits) {

@@ -43,10 +43,11 @@ append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
   v_cache[dst] = v_new[src];
 }
 
-// One warp per (token, kv head, K|V) row of head_dim fp16 values.
-template <int D>
+// One warp per (token, kv head, K|V) row of head_dim 16-bit values; a row
+// that would saturate under its page's scale re-scales the page first.
+template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
-append_fp8_kernel(const __half* __restrict__ k_new, const __half* __restrict__ v_new,
+append_fp8_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
                   uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
                   float* __restrict__ k_scale, float* __restrict__ v_scale,
                   const int64_t* __restrict__ slots, int T, int Hkv, int block_size,
@@ -64,18 +65,25 @@ append_fp8_kernel(const __half* __restrict__ k_new, const __half* __restrict__ v
     return;
   }
   const int64_t blk = s / block_size, row = s - blk * block_size;
-  const RowF16<D> x = load_row_f16<D>((kv ? v_new : k_new) + (i * Hkv + h) * D, lane);
+  const RowF16<D> x = load_row<D, BF16>((kv ? v_new : k_new) + (i * Hkv + h) * D, lane);
   float* scales = kv ? v_scale : k_scale;
   const int64_t tile = blk * Hkv + h;
+  uint8_t* page = (kv ? v_cache : k_cache) + tile * block_size * D;
+  const float amax = e4m3_row_amax<D>(x);
   float scale;
   if (row == 0) {
-    scale = e4m3_row_scale<D>(x);
+    scale = e4m3_page_scale(amax);
     if (lane == 0) scales[tile] = scale;
   } else {
     scale = scales[tile];
+    if (e4m3_saturates(amax, scale)) {   // re-scale the page's earlier rows first
+      const float s_new = e4m3_page_scale(amax);
+      e4m3_rescale_rows<D, true>(page, page, nullptr, static_cast<int>(row), scale, s_new, lane);
+      scale = s_new;
+      if (lane == 0) scales[tile] = scale;
+    }
   }
-  store_row_codes<D>((kv ? v_cache : k_cache) + (tile * block_size + row) * D, lane,
-                     e4m3_row_codes<D>(x, scale));
+  store_row_codes<D>(page + row * D, lane, e4m3_row_codes<D>(x, scale));
 }
 
 }  // namespace
@@ -97,19 +105,24 @@ cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, v
 cudaError_t launch_append_fp8(const void* k_new, const void* v_new, uint8_t* k_cache,
                               uint8_t* v_cache, float* k_scale, float* v_scale,
                               const int64_t* slots, int T, int Hkv, int D, int block_size,
-                              int64_t num_blocks, unsigned* status, cudaStream_t s) {
+                              int64_t num_blocks, bool bf16, unsigned* status, cudaStream_t s) {
   const int64_t warps = static_cast<int64_t>(T) * Hkv * 2;
   const int threads = 256;
-  const int64_t grid = (warps * 32 + threads - 1) / threads;
-  const auto* kn = static_cast<const __half*>(k_new);
-  const auto* vn = static_cast<const __half*>(v_new);
+  const unsigned grid = static_cast<unsigned>((warps * 32 + threads - 1) / threads);
+  const auto* kn = static_cast<const uint16_t*>(k_new);
+  const auto* vn = static_cast<const uint16_t*>(v_new);
   const int64_t ns = num_blocks * block_size;
-  if (D == 128)
-    append_fp8_kernel<128><<<static_cast<unsigned>(grid), threads, 0, s>>>(
-        kn, vn, k_cache, v_cache, k_scale, v_scale, slots, T, Hkv, block_size, ns, status);
-  else
-    append_fp8_kernel<64><<<static_cast<unsigned>(grid), threads, 0, s>>>(
-        kn, vn, k_cache, v_cache, k_scale, v_scale, slots, T, Hkv, block_size, ns, status);
+#define PA_APPEND_FP8(DD, BB)                                                              \
+  append_fp8_kernel<DD, BB><<<grid, threads, 0, s>>>(kn, vn, k_cache, v_cache, k_scale, v_scale, \
+                                                     slots, T, Hkv, block_size, ns, status)
+  if (D == 128) {
+    if (bf16) PA_APPEND_FP8(128, true);
+    else PA_APPEND_FP8(128, false);
+  } else {
+    if (bf16) PA_APPEND_FP8(64, true);
+    else PA_APPEND_FP8(64, false);
+  }
+#undef PA_APPEND_FP8
   return cudaGetLastError();
 }
 

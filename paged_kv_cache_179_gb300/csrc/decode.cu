@@ -363,9 +363,14 @@ __device__ __forceinline__ int load_chunk_id(const DecodeArgs& a, const Chunk& x
   return __ldg(a.block_tables + static_cast<int64_t>(x.b) * a.mbs + x.cb0 + lane);
 }
 
-template <int D, bool FP8>
-__device__ __forceinline__ void load_query(uint32_t (&qf)[D / 16][2], const DecodeArgs& a, int b,
-                                           int h, int r, int c) {
+// The query fragments of (sequence b, kv head h): the group's G rows, the
+// MMA B operand.  Returns the factor the scores carry back: 1, except for a
+// bf16 q over an E4M3 pool, which enters the fp16 products scaled by 2^k so
+// that its largest element lies in [2^14, 2^15) (exact unless an element
+// falls below fp16's subnormal range); the factor is then 2^-k.
+template <int D, bool FP8, bool BF16>
+__device__ __forceinline__ float load_query(uint32_t (&qf)[D / 16][2], const DecodeArgs& a, int b,
+                                            int h, int r, int c) {
   const uint4* qrow = reinterpret_cast<const uint4*>(
       static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(b) * a.Hq + h * a.group + r) * D);
   const bool live = r < a.group;
@@ -378,6 +383,7 @@ __device__ __forceinline__ void load_query(uint32_t (&qf)[D / 16][2], const Deco
       qf[2 * i + 1][0] = v.z;
       qf[2 * i + 1][1] = v.w;
     }
+    return 1.f;
   } else {
 #pragma unroll
     for (int i = 0; i < D / 64; ++i) {
@@ -387,6 +393,33 @@ __device__ __forceinline__ void load_query(uint32_t (&qf)[D / 16][2], const Deco
       qf[4 * i + 1][0] = lo.z; qf[4 * i + 1][1] = lo.w;
       qf[4 * i + 2][0] = hi.x; qf[4 * i + 2][1] = hi.y;
       qf[4 * i + 3][0] = hi.z; qf[4 * i + 3][1] = hi.w;
+    }
+    if constexpr (!BF16) {
+      return 1.f;
+    } else {
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float2 v = bits2_to_float2<true>(qf[i][j]);
+          amax = fmaxf(amax, fmaxf(fabsf(v.x), fabsf(v.y)));
+        }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      // amax = m * 2^e with m in [1, 2): k = 14 - e, kept within fp32's normal exponents
+      const int e = amax > 0.f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xff) - 127 : 14;
+      const int k = max(-126, min(126, 14 - e));
+      const float up = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float2 v = bits2_to_float2<true>(qf[i][j]);
+          const __half2 h2 = __floats2half2_rn(v.x * up, v.y * up);
+          qf[i][j] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+      return __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
     }
   }
 }
@@ -468,18 +501,51 @@ struct NewRow {
   int64_t slot;    // slot_mapping[b]; -2 when the chunk holds no sequence end
 };
 
-template <int D>
-__device__ __forceinline__ RowF16<D> row_from_bits(uint2 raw) {
-  RowF16<D> r;
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-  r.x[0] = a.x;
-  r.x[1] = a.y;
-  if constexpr (RowF16<D>::PER_LANE == 4) {
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-    r.x[2] = b.x;
-    r.x[3] = b.y;
+// Fused E4M3 append of sequence b's new row for kv head h into page `row`
+// of physical block `blk`: the tile just fetched (ktile / vtile, 16 rows of D
+// codes in shared memory) and the pool both get it.  Per pool, the page's
+// first row sets its scale; a later row that would saturate re-scales the
+// page's earlier rows in both copies.  Returns the K and V scales the page
+// then has (ksc / vsc unchanged when nothing is appended: a padding slot, or
+// a slot that is not position context_len - 1, which sets the status bit).
+// Out of line and loading its own inputs: it runs once per sequence and kv
+// head, and inlined, its registers would crowd the attention loop.
+template <int D, bool BF16>
+__device__ __noinline__ float2 append_e4m3_row(const uint16_t* k_new, const uint16_t* v_new,
+                                               const int64_t* slots, uint8_t* ktile,
+                                               uint8_t* vtile, uint8_t* k_pool, uint8_t* v_pool,
+                                               float* k_scale, float* v_scale, unsigned* status,
+                                               int b, int h, int Hkv, int blk, int row, float ksc,
+                                               float vsc, int lane) {
+  const int64_t slot = __ldg(slots + b);
+  if (slot < 0) return make_float2(ksc, vsc);                      // padding: nothing appended
+  if (slot != static_cast<int64_t>(blk) * 16 + row) {
+    if (lane == 0) atomicOr(status, kStatusBadSlot);             // not a decode-step slot
+    return make_float2(ksc, vsc);
   }
-  return r;
+  const int64_t tile = static_cast<int64_t>(blk) * Hkv + h;
+  const int64_t src = (static_cast<int64_t>(b) * Hkv + h) * D;
+  float out[2];
+#pragma unroll
+  for (int kv = 0; kv < 2; ++kv) {
+    uint8_t* t = kv ? vtile : ktile;
+    uint8_t* page = (kv ? v_pool : k_pool) + tile * 16 * D;
+    const RowF16<D> x = load_row<D, BF16>((kv ? v_new : k_new) + src, lane);
+    const float amax = e4m3_row_amax<D>(x);
+    float sc = kv ? vsc : ksc;
+    if (row == 0 || e4m3_saturates(amax, sc)) {
+      const float sn = e4m3_page_scale(amax);
+      e4m3_rescale_rows<D, false>(t, t, page, row, sc, sn, lane);
+      sc = sn;
+      if (lane == 0) (kv ? v_scale : k_scale)[tile] = sc;
+    }
+    const uint32_t codes = e4m3_row_codes<D>(x, sc);
+    store_row_codes<D>(t + row * D, lane, codes);
+    store_row_codes<D>(page + row * D, lane, codes);
+    out[kv] = sc;
+  }
+  __syncwarp();
+  return make_float2(out[0], out[1]);
 }
 
 // The new row of chunk x's sequence and kv head when x holds the sequence's
@@ -607,7 +673,7 @@ decode_kernel(const DecodeArgs a) {
   // query fragments of the current piece and of the next one
   uint32_t qf[D / 16][2], qn[D / 16][2];
   uint8_t* const ring_ptr = smem + warp * STAGES * TL::SLOT;   // generic address of the ring
-  load_query<D, FP8>(qf, a, ch0.b, ch0.h, r, c);
+  float q_mul = load_query<D, FP8, BF16>(qf, a, ch0.b, ch0.h, r, c), qn_mul = 1.f;
   auto prefetch_next_query = [&](int b, int h) {
     ++h;
     if (h == Hkv) {
@@ -616,7 +682,7 @@ decode_kernel(const DecodeArgs a) {
       while (b < B && pf[b + 1] == pf[b]) ++b;
     }
     if (b < B && pf[b] + static_cast<int64_t>(h) * seg_blocks(pf, b, Hkv) < hi)
-      load_query<D, FP8>(qn, a, b, h, r, c);
+      qn_mul = load_query<D, FP8, BF16>(qn, a, b, h, r, c);
   };
   prefetch_next_query(ch0.b, ch0.h);
 
@@ -677,9 +743,11 @@ decode_kernel(const DecodeArgs a) {
     // fused append: the new row, when this chunk ends its sequence.  Loaded
     // here rather than a chunk ahead: held across the loop it would cost the
     // E4M3 variant its third CTA per SM (or spills).
-    const NewRow nt0 = load_new_row<D, APPEND>(a, ch0, pf, lane);
+    const NewRow nt0 = load_new_row<D, APPEND && !FP8>(a, ch0, pf, lane);
     // fused append: index in this chunk of the sequence's last block, if any
-    const int t_last = (APPEND && nt0.slot >= 0) ? seg_blocks(pf, ch0.b, Hkv) - 1 - ch0.cb0 : -1;
+    // (E4M3: the out-of-line append reads the slot and the row itself)
+    const bool ends_seg = ch0.cb0 + ch0.nb == seg_blocks(pf, ch0.b, Hkv);
+    const int t_last = (APPEND && ((FP8 && ends_seg) || nt0.slot >= 0)) ? ch0.nb - 1 : -1;
     for (int t = 0; t < ch0.nb && !dead; ++t) {
       const int s = computed % STAGES;
       if (!__all_sync(0xffffffffu, mbar_wait(sbar + 8 * s, (computed / STAGES) & 1))) {
@@ -689,7 +757,7 @@ decode_kernel(const DecodeArgs a) {
       }
       PA_TRACE_ONLY(if (computed == 0) PA_TRACE_WARP(gw, 1, pa_now()));
       const int id = __shfl_sync(0xffffffffu, id0, t);
-      float sl2 = a.scale_log2, v_mul = 1.f;
+      float sl2 = a.scale_log2 * q_mul, v_mul = 1.f;
       if constexpr (FP8) {
         sl2 *= __shfl_sync(0xffffffffu, ks0, t);
         v_mul = __shfl_sync(0xffffffffu, vs0, t) * kPBoost;
@@ -700,47 +768,35 @@ decode_kernel(const DecodeArgs a) {
         // (which may predate the write), then attend.
         if (t == t_last && id >= 0 && id < a.num_blocks) {
           const int row = (L - 1) & 15;
-          if (nt0.slot != static_cast<int64_t>(id) * 16 + row) {
+          constexpr int ROWB = TL::BYTES / 16;
+          uint8_t* ktile = ring_ptr + s * TL::SLOT;
+          if constexpr (FP8) {
+            const float2 sc = append_e4m3_row<D, BF16>(
+                static_cast<const uint16_t*>(a.k_new), static_cast<const uint16_t*>(a.v_new),
+                a.slots, ktile, ktile + TL::BYTES, static_cast<uint8_t*>(a.k_pool_w),
+                static_cast<uint8_t*>(a.v_pool_w), a.k_scale_w, a.v_scale_w, a.status, ch0.b,
+                ch0.h, Hkv, id, row, __shfl_sync(0xffffffffu, ks0, t),
+                __shfl_sync(0xffffffffu, vs0, t), lane);
+            sl2 = a.scale_log2 * q_mul * sc.x;
+            v_mul = sc.y * kPBoost;
+          } else if (nt0.slot != static_cast<int64_t>(id) * 16 + row) {
             if (lane == 0) atomicOr(a.status, kStatusBadSlot);   // not a decode-step slot
           } else {
-            constexpr int ROWB = TL::BYTES / 16;
             const int64_t prow = (static_cast<int64_t>(id) * Hkv + ch0.h) * 16 + row;
-            uint8_t* kt = ring_ptr + s * TL::SLOT + row * ROWB;
+            uint8_t* kt = ktile + row * ROWB;
             uint8_t* vt = kt + TL::BYTES;
             uint8_t* kp = static_cast<uint8_t*>(a.k_pool_w) + prow * ROWB;
             uint8_t* vp = static_cast<uint8_t*>(a.v_pool_w) + prow * ROWB;
-            if constexpr (!FP8) {
-              if constexpr (D == 128) {
-                *reinterpret_cast<uint2*>(kt + 8 * lane) = nt0.k;
-                *reinterpret_cast<uint2*>(vt + 8 * lane) = nt0.v;
-                *reinterpret_cast<uint2*>(kp + 8 * lane) = nt0.k;
-                *reinterpret_cast<uint2*>(vp + 8 * lane) = nt0.v;
-              } else {
-                *reinterpret_cast<uint32_t*>(kt + 4 * lane) = nt0.k.x;
-                *reinterpret_cast<uint32_t*>(vt + 4 * lane) = nt0.v.x;
-                *reinterpret_cast<uint32_t*>(kp + 4 * lane) = nt0.k.x;
-                *reinterpret_cast<uint32_t*>(vp + 4 * lane) = nt0.v.x;
-              }
+            if constexpr (D == 128) {
+              *reinterpret_cast<uint2*>(kt + 8 * lane) = nt0.k;
+              *reinterpret_cast<uint2*>(vt + 8 * lane) = nt0.v;
+              *reinterpret_cast<uint2*>(kp + 8 * lane) = nt0.k;
+              *reinterpret_cast<uint2*>(vp + 8 * lane) = nt0.v;
             } else {
-              // E4M3: the page's first row sets its scales, later rows reuse them
-              const RowF16<D> xk = row_from_bits<D>(nt0.k), xv = row_from_bits<D>(nt0.v);
-              float ksc = __shfl_sync(0xffffffffu, ks0, t);
-              float vsc = __shfl_sync(0xffffffffu, vs0, t);
-              if (row == 0) {
-                ksc = e4m3_row_scale<D>(xk);
-                vsc = e4m3_row_scale<D>(xv);
-                if (lane == 0) {
-                  a.k_scale_w[prow / 16] = ksc;
-                  a.v_scale_w[prow / 16] = vsc;
-                }
-              }
-              const uint32_t kc = e4m3_row_codes<D>(xk, ksc), vc = e4m3_row_codes<D>(xv, vsc);
-              store_row_codes<D>(kt, lane, kc);
-              store_row_codes<D>(vt, lane, vc);
-              store_row_codes<D>(kp, lane, kc);
-              store_row_codes<D>(vp, lane, vc);
-              sl2 = a.scale_log2 * ksc;
-              v_mul = vsc * kPBoost;
+              *reinterpret_cast<uint32_t*>(kt + 4 * lane) = nt0.k.x;
+              *reinterpret_cast<uint32_t*>(vt + 4 * lane) = nt0.v.x;
+              *reinterpret_cast<uint32_t*>(kp + 4 * lane) = nt0.k.x;
+              *reinterpret_cast<uint32_t*>(vp + 4 * lane) = nt0.v.x;
             }
             __syncwarp();
           }
@@ -805,6 +861,7 @@ decode_kernel(const DecodeArgs a) {
         qf[i][0] = qn[i][0];
         qf[i][1] = qn[i][1];
       }
+      q_mul = qn_mul;
       prefetch_next_query(ch0.b, ch0.h);
     }
     top_up();
@@ -938,7 +995,7 @@ cudaError_t launch_one(const DecodeArgs& a, cudaStream_t s) {
   kern<<<static_cast<unsigned>(a.split_ctas), kThreads, lay.total, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.ws_acc == nullptr || a.seg_prefix == nullptr) return cudaSuccess;
-  return launch_merge<D, BF16 && !FP8>(a, s);
+  return launch_merge<D, BF16>(a, s);
 }
 
 // Shared memory and registers per CTA are traded against resident CTAs per
@@ -1014,6 +1071,8 @@ void decode_workspace_split(DecodeArgs& a, void* ws) {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, bool fp8, bool bf16, cudaStream_t s) {
+  if (fp8 && bf16)
+    return a.D == 128 ? launch_dtype<128, true, true>(a, s) : launch_dtype<64, true, true>(a, s);
   if (fp8) return a.D == 128 ? launch_dtype<128, true, false>(a, s) : launch_dtype<64, true, false>(a, s);
   if (bf16) return a.D == 128 ? launch_dtype<128, false, true>(a, s) : launch_dtype<64, false, true>(a, s);
   return a.D == 128 ? launch_dtype<128, false, false>(a, s) : launch_dtype<64, false, false>(a, s);

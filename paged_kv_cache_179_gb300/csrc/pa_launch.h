@@ -58,7 +58,7 @@ cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, v
 cudaError_t launch_append_fp8(const void* k_new, const void* v_new, uint8_t* k_cache,
                               uint8_t* v_cache, float* k_scale, float* v_scale,
                               const int64_t* slots, int T, int Hkv, int D, int block_size,
-                              int64_t num_blocks, unsigned* status, cudaStream_t s);
+                              int64_t num_blocks, bool bf16, unsigned* status, cudaStream_t s);
 
 cudaError_t launch_quantize_fp8(const void* src, uint8_t* codes, float* scales,
                                 int64_t num_tiles, int tile_elems, cudaStream_t s);

@@ -94,7 +94,8 @@ def test_append_and_quantize_argument_errors(lib):
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 2, 64, 16, 8, 0, None) == _abi.PA_OK
     assert f(None, None, None, None, None, 0, 2, 64, 16, 8, 0, None) == _abi.PA_OK   # empty batch
     g = lib.pa_cache_append_fp8
-    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 96, 16, 8, None) == _abi.PA_ERR_UNSUPPORTED
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 96, 16, 8, 0, None) == _abi.PA_ERR_UNSUPPORTED
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 64, 16, 8, 7, None) == _abi.PA_ERR_INVALID_ARG
     q = lib.pa_quantize_fp8
     assert q(None, None, FAKE, FAKE, FAKE, FAKE, 8, 2, 64, 16, None) == _abi.PA_ERR_INVALID_ARG
     assert q(FAKE, None, FAKE, None, FAKE, None, 8, 2, 64, 32, None) == _abi.PA_ERR_UNSUPPORTED

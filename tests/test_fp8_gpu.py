@@ -64,8 +64,9 @@ def test_quantize_bit_exact(D):
     assert np.array_equal(vc.cpu().numpy(), vc_o)
 
 
-@pytest.mark.parametrize("D", [64, 128])
-def test_append_fp8_bit_exact(D):
+@pytest.mark.parametrize("D,dtype", [(64, torch.float16), (128, torch.float16),
+                                     (128, torch.bfloat16)])
+def test_append_fp8_bit_exact(D, dtype):
     g = torch.Generator().manual_seed(2)
     NB, Hkv = 9, 2
     kc = torch.randint(0, 256, (NB, Hkv, 16, D), generator=g, dtype=torch.uint8)
@@ -79,13 +80,44 @@ def test_append_fp8_bit_exact(D):
     dev = [a.cuda() for a in (kc, vc, ks, vs)]
     for i, slots in enumerate(calls):
         T = slots.numel()
-        kn = (torch.randn(T, Hkv, D, generator=g) * (1 + 3 * i)).to(torch.float16)
-        vn = (torch.randn(T, Hkv, D, generator=g) * (1 + 3 * i)).to(torch.float16)
-        oracle.cache_append_fp8(to_np16(kn), to_np16(vn), *ref, slots.numpy(), 16)
+        kn = (torch.randn(T, Hkv, D, generator=g) * (1 + 3 * i)).to(dtype)
+        vn = (torch.randn(T, Hkv, D, generator=g) * (1 + 3 * i)).to(dtype)
+        oracle.cache_append_fp8(to_np16(kn), to_np16(vn), *ref, slots.numpy(), 16,
+                                bf16=dtype == torch.bfloat16)
         _abi.pa_cache_append_fp8(kn.cuda(), vn.cuda(), *dev, slots.cuda())
     assert _abi.pa_get_status() == (0, 0)
     for r, d in zip(ref, dev):
         assert np.array_equal(d.cpu().numpy().view(np.uint8), r.view(np.uint8))
+
+
+@pytest.mark.parametrize("D,dtype", [(128, torch.float16), (64, torch.bfloat16)])
+def test_append_fp8_rescales_a_page_token_by_token(D, dtype):
+    """A page filled one token per call, magnitudes rising and falling, so that
+    some tokens fit the page's scale and others re-scale its earlier rows."""
+    g = torch.Generator().manual_seed(5)
+    NB, Hkv = 3, 2
+    kc = torch.zeros(NB, Hkv, 16, D, dtype=torch.uint8)
+    vc = kc.clone()
+    ks = torch.ones(NB, Hkv)
+    vs = ks.clone()
+    ref = [a.numpy().copy() for a in (kc, vc, ks, vs)]
+    dev = [a.cuda() for a in (kc, vc, ks, vs)]
+    mags = [1, 0.5, 3, 2, 40, 1, 0.01, 500, 7, 1e3, 1e3, 0, 2e3, 1, 5e4, 1]
+    rescaled = 0
+    for row, m in enumerate(mags):
+        m = m if dtype == torch.bfloat16 else min(m, 2e3)   # fp16 rows stay finite
+        kn = (torch.randn(1, Hkv, D, generator=g) * m).to(dtype)
+        vn = (torch.randn(1, Hkv, D, generator=g) * m * 0.5).to(dtype)
+        before = ref[2].copy()
+        slots = torch.tensor([1 * 16 + row])
+        oracle.cache_append_fp8(to_np16(kn), to_np16(vn), *ref, slots.numpy(), 16,
+                                bf16=dtype == torch.bfloat16)
+        _abi.pa_cache_append_fp8(kn.cuda(), vn.cuda(), *dev, slots.cuda())
+        rescaled += int(row > 0 and not np.array_equal(before[1], ref[2][1]))
+        for r_, d_ in zip(ref, dev):
+            assert np.array_equal(d_.cpu().numpy().view(np.uint8), r_.view(np.uint8)), row
+    assert _abi.pa_get_status() == (0, 0)
+    assert rescaled >= 4
 
 
 def _fp8_step(w, kc, vc, ks, vs, splits=0):
@@ -103,10 +135,11 @@ def _quantized_on_gpu(w):
     return kc, vc, ks, vs
 
 
-@pytest.mark.parametrize("seed,B,Hq,Hkv,D,max_len,splits", [
-    (0, 4, 28, 4, 128, 700, 13), (1, 3, 8, 2, 64, 300, 40), (2, 5, 12, 2, 128, 2000, 304),
-    (3, 2, 7, 7, 128, 50, 1)])
-def test_decode_fp8_small_matches_oracle(seed, B, Hq, Hkv, D, max_len, splits):
+@pytest.mark.parametrize("seed,B,Hq,Hkv,D,max_len,splits,dtype", [
+    (0, 4, 28, 4, 128, 700, 13, torch.float16), (1, 3, 8, 2, 64, 300, 40, torch.float16),
+    (2, 5, 12, 2, 128, 2000, 304, torch.float16), (3, 2, 7, 7, 128, 50, 1, torch.float16),
+    (4, 4, 28, 4, 128, 900, 0, torch.bfloat16), (5, 3, 8, 2, 64, 300, 7, torch.bfloat16)])
+def test_decode_fp8_small_matches_oracle(seed, B, Hq, Hkv, D, max_len, splits, dtype):
     g = torch.Generator().manual_seed(seed)
     lens = torch.randint(1, max_len + 1, (B,), generator=g).to(torch.int32)
     nblk = (lens + 15) // 16
@@ -117,16 +150,18 @@ def test_decode_fp8_small_matches_oracle(seed, B, Hq, Hkv, D, max_len, splits):
     for b in range(B):
         tables[b, :nblk[b]] = perm[c:c + nblk[b]]
         c += int(nblk[b])
-    q = torch.randn(B, Hq, D, generator=g).to(torch.float16)
+    # a bf16 q spans a wider range than fp16 holds: scale it up to exercise that
+    q = (torch.randn(B, Hq, D, generator=g) * (1e6 if dtype == torch.bfloat16 else 1)).to(dtype)
     kp = torch.randn(NB, Hkv, 16, D, generator=g).to(torch.float16)
     vp = torch.randn(NB, Hkv, 16, D, generator=g).to(torch.float16)
-    scale = float(np.float32(1 / math.sqrt(D)))
+    scale = float(np.float32(1 / math.sqrt(D) / (1e6 if dtype == torch.bfloat16 else 1)))
     kc_o, ks_o = oracle.quantize_fp8(to_np16(kp))
     vc_o, vs_o = oracle.quantize_fp8(to_np16(vp))
-    ref = oracle.decode_fp8(to_np16(q), kc_o, vc_o, ks_o, vs_o, tables.numpy(), lens.numpy(), scale)
+    ref = oracle.decode_fp8(to_np16(q), kc_o, vc_o, ks_o, vs_o, tables.numpy(), lens.numpy(), scale,
+                            bf16=dtype == torch.bfloat16)
     kc, vc = torch.from_numpy(kc_o).cuda(), torch.from_numpy(vc_o).cuda()
     ks, vs = torch.from_numpy(ks_o).cuda(), torch.from_numpy(vs_o).cuda()
-    out = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+    out = torch.empty(B, Hq, D, dtype=dtype, device="cuda")
     mcl = int(lens.max())
     ws = _abi.alloc_workspace(B, Hq, D, splits, "cuda")
     _abi.pa_decode_fp8(out, q.cuda(), kc, vc, ks, vs, tables.cuda(), lens.cuda(), mcl, scale,

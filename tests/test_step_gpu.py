@@ -71,7 +71,7 @@ def test_padding_and_mismatched_slots():
     assert torch.equal(w.k_cache[s3 // 16, :, s3 % 16], w.k_new[3])
 
 
-def _fp8_case(seed, B, Hq, Hkv, D, lens):
+def _fp8_case(seed, B, Hq, Hkv, D, lens, dtype=torch.float16):
     g = torch.Generator().manual_seed(seed)
     lens = torch.tensor(lens, dtype=torch.int32)
     nblk = (lens + 15) // 16
@@ -84,7 +84,7 @@ def _fp8_case(seed, B, Hq, Hkv, D, lens):
         c += int(nblk[b])
     last = lens.to(torch.int64) - 1
     slots = tables[torch.arange(B), last // 16].to(torch.int64) * 16 + last % 16
-    q = torch.randn(B, Hq, D, generator=g).to(torch.float16)
+    q = torch.randn(B, Hq, D, generator=g).to(dtype)
     kp = torch.randn(NB, Hkv, 16, D, generator=g).to(torch.float16)
     vp = torch.randn(NB, Hkv, 16, D, generator=g).to(torch.float16)
     # rows at and after each sequence's new position hold no token yet
@@ -94,24 +94,29 @@ def _fp8_case(seed, B, Hq, Hkv, D, lens):
             if r0 < 16:
                 kp[tables[b, j], :, r0:] = 0
                 vp[tables[b, j], :, r0:] = 0
-    kn = (torch.randn(B, Hkv, D, generator=g) * 2).to(torch.float16)
-    vn = (torch.randn(B, Hkv, D, generator=g) * 2).to(torch.float16)
+    # new rows larger than the pool's: most later rows re-scale their page
+    kn = (torch.randn(B, Hkv, D, generator=g) * 2).to(dtype)
+    vn = (torch.randn(B, Hkv, D, generator=g) * 2).to(dtype)
     return q, kp, vp, kn, vn, tables, lens, slots
 
 
-@pytest.mark.parametrize("seed,B,Hq,Hkv,D,lens,splits", [
-    (0, 5, 28, 4, 128, [17, 33, 300, 1, 129], 0),     # new rows at the start of pages
-    (1, 4, 8, 2, 64, [20, 50, 77, 200], 9),           # new rows inside pages
-    (2, 6, 12, 2, 128, [1, 16, 17, 32, 48, 1000], 2)])
-def test_fused_step_fp8_matches_oracle(seed, B, Hq, Hkv, D, lens, splits):
-    q, kp, vp, kn, vn, tables, L, slots = _fp8_case(seed, B, Hq, Hkv, D, lens)
+@pytest.mark.parametrize("seed,B,Hq,Hkv,D,lens,splits,dtype", [
+    (0, 5, 28, 4, 128, [17, 33, 300, 1, 129], 0, torch.float16),  # new rows opening pages
+    (1, 4, 8, 2, 64, [20, 50, 77, 200], 9, torch.float16),        # new rows inside pages
+    (2, 6, 12, 2, 128, [1, 16, 17, 32, 48, 1000], 2, torch.float16),
+    (3, 5, 28, 4, 128, [18, 35, 300, 2, 130], 0, torch.bfloat16),
+    (4, 4, 8, 2, 64, [21, 50, 76, 200], 5, torch.bfloat16)])
+def test_fused_step_fp8_matches_oracle(seed, B, Hq, Hkv, D, lens, splits, dtype):
+    q, kp, vp, kn, vn, tables, L, slots = _fp8_case(seed, B, Hq, Hkv, D, lens, dtype)
     kc, ks = oracle.quantize_fp8(to_np16(kp))
     vc, vs = oracle.quantize_fp8(to_np16(vp))
     dev = [torch.from_numpy(x.copy()).cuda() for x in (kc, vc, ks, vs)]
-    oracle.cache_append_fp8(to_np16(kn), to_np16(vn), kc, vc, ks, vs, slots.numpy(), 16)
+    bf16 = dtype == torch.bfloat16
+    oracle.cache_append_fp8(to_np16(kn), to_np16(vn), kc, vc, ks, vs, slots.numpy(), 16, bf16=bf16)
     scale = float(np.float32(1 / math.sqrt(D)))
-    ref = oracle.decode_fp8(to_np16(q), kc, vc, ks, vs, tables.numpy(), L.numpy(), scale)
-    out = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+    ref = oracle.decode_fp8(to_np16(q), kc, vc, ks, vs, tables.numpy(), L.numpy(), scale,
+                            bf16=bf16)
+    out = torch.empty(B, Hq, D, dtype=dtype, device="cuda")
     ws = _abi.alloc_workspace(B, Hq, D, splits, "cuda")
     _abi.pa_decode_step_fp8(out, q.cuda(), kn.cuda(), vn.cuda(), *dev, slots.cuda(),
                             tables.cuda(), L.cuda(), int(L.max()), scale, splits, ws)
