@@ -62,9 +62,9 @@ def lib():
             L.oracle_cache_append_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                   i32]
             L.oracle_decode.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32,
-                                        f32, vp, i32, vp]
+                                        f32, i32, i32, vp, i32, vp]
             L.oracle_decode_fp8.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
-                                            i32, i32, f32, vp, i32, vp]
+                                            i32, i32, f32, i32, i32, vp, i32, vp]
             L.oracle_copy_blocks.argtypes = [vp, vp, vp, vp, vp, i32, ctypes.c_size_t, i32, i64]
             L.oracle_num_threads.restype = i32
             _lib = L
@@ -160,36 +160,48 @@ def _rows_arg(rows):
     return r, int(r.size)
 
 
+def _q_shape(q):
+    """[B][Hq][D] (one query per sequence) or [B][n_q][Hq][D]."""
+    if q.ndim == 3:
+        B, Hq, D = q.shape
+        return B, 1, Hq, D
+    return q.shape
+
+
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, *, bf16: bool = False,
-           rows=None, return_wsum: bool = False):
+           window: int = 0, rows=None, return_wsum: bool = False):
     """GQA decode over a 16-bit paged pool, in double.
 
-    q: [B][Hq][D] (float16, or bf16 bits as uint16 when ``bf16``); caches
-    [NB][Hkv][bs][D] of the same type; block_tables int32 [B][MBS];
-    context_lens int32 [B].  Returns float64 [B][Hq][D] (rows not selected by
-    ``rows`` are zero) and, with ``return_wsum``, |sum_t w_t/Z - 1| per (b, hq).
+    q: [B][Hq][D], or [B][n_q][Hq][D] for n_q query tokens per sequence at
+    positions L-n_q .. L-1, each attending causally (float16, or bf16 bits as
+    uint16 when ``bf16``); ``window`` > 0 limits each query to its last
+    ``window`` positions.  Caches [NB][Hkv][bs][D] of the same type;
+    block_tables int32 [B][MBS]; context_lens int32 [B].  Returns float64 of
+    q's shape (rows not selected by ``rows`` are zero) and, with
+    ``return_wsum``, |sum_t w_t/Z - 1| per output row.
     """
-    B, Hq, D = q.shape
+    B, nq, Hq, D = _q_shape(q)
     NB, Hkv, bs, D2 = k_cache.shape
-    assert D == D2 and Hq % Hkv == 0 and D <= 256
+    assert D == D2 and Hq % Hkv == 0 and D <= 256 and window >= 0
     bt = np.ascontiguousarray(block_tables, dtype=np.int32)
     cl = np.ascontiguousarray(context_lens, dtype=np.int32)
-    out = np.zeros((B, Hq, D), dtype=np.float64)
-    ws = np.zeros((B, Hq), dtype=np.float64) if return_wsum else None
+    out = np.zeros(q.shape, dtype=np.float64)
+    ws = np.zeros(q.shape[:-1], dtype=np.float64) if return_wsum else None
     r, nr = _rows_arg(rows)
     lib().oracle_decode(_p(out), _p(_u16(q)), _p(_u16(k_cache)), _p(_u16(v_cache)), int(bf16),
                         _p(bt), bt.shape[1], _p(cl), B, Hq, Hkv, D, bs, float(np.float32(scale)),
-                        _p(r), nr, _p(ws))
+                        int(window), nq, _p(r), nr, _p(ws))
     return (out, ws) if return_wsum else out
 
 
 def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale: float, *,
-               bf16: bool = False, rows=None, return_wsum: bool = False):
+               bf16: bool = False, window: int = 0, rows=None, return_wsum: bool = False):
     """GQA decode over an E4M3 pool with per-(block, kv head) fp32 scales, in
-    double; q is fp16, or bf16 bits as uint16 when ``bf16``."""
-    B, Hq, D = q.shape
+    double; q is fp16, or bf16 bits as uint16 when ``bf16``; q's shape,
+    ``window`` and the result as for ``decode``."""
+    B, nq, Hq, D = _q_shape(q)
     NB, Hkv, bs, D2 = k_codes.shape
-    assert D == D2 and Hq % Hkv == 0 and D <= 256
+    assert D == D2 and Hq % Hkv == 0 and D <= 256 and window >= 0
     assert k_codes.dtype == np.uint8 and v_codes.dtype == np.uint8
     ks = np.ascontiguousarray(k_scale, dtype=np.float32)
     vs = np.ascontiguousarray(v_scale, dtype=np.float32)
@@ -197,10 +209,10 @@ def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens
     vc = np.ascontiguousarray(v_codes)
     bt = np.ascontiguousarray(block_tables, dtype=np.int32)
     cl = np.ascontiguousarray(context_lens, dtype=np.int32)
-    out = np.zeros((B, Hq, D), dtype=np.float64)
-    ws = np.zeros((B, Hq), dtype=np.float64) if return_wsum else None
+    out = np.zeros(q.shape, dtype=np.float64)
+    ws = np.zeros(q.shape[:-1], dtype=np.float64) if return_wsum else None
     r, nr = _rows_arg(rows)
     lib().oracle_decode_fp8(_p(out), _p(_u16(q)), int(bf16), _p(kc), _p(vc), _p(ks), _p(vs), _p(bt),
                             bt.shape[1], _p(cl), B, Hq, Hkv, D, bs, float(np.float32(scale)),
-                            _p(r), nr, _p(ws))
+                            int(window), nq, _p(r), nr, _p(ws))
     return (out, ws) if return_wsum else out

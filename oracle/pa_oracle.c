@@ -308,71 +308,87 @@ static double pool_elem(const pool_view *p, int which, size_t tile, size_t idx)
 }
 
 /*
- * out[b][hq][:] = sum_t softmax_t(scale * q[b][hq] . K_t) V_t over the first
- * context_lens[b] tokens of sequence b, token t living in physical block
- * block_tables[b][t / bs] at row t % bs, kv head hq / (Hq / Hkv).
- * rows (optional, n_rows entries) restricts the work to those sequences;
- * wsum_dev (optional, [B][Hq]) receives |sum_t w_t / Z - 1| for each output.
+ * Query i of sequence b (0 <= i < n_q; n_q = 1 for a plain decode step) sits
+ * at position pos = L - n_q + i, where L = context_lens[b] counts every token
+ * in the cache, the queries' own included.  It attends positions
+ * lo..pos (causal), lo = max(0, pos - window + 1) for a sliding window of
+ * `window` tokens, 0 when window is 0:
+ *   out[b][i][hq][:] = sum_t softmax_t(scale * q[b][i][hq] . K_t) V_t,
+ * token t living in physical block block_tables[b][t / bs] at row t % bs,
+ * kv head hq / (Hq / Hkv).  A query with nothing to attend (pos < 0) gets a
+ * zero output.  q and out are [B][n_q][Hq][D].  rows (optional, n_rows
+ * entries) restricts the work to those sequences; wsum_dev (optional,
+ * [B][n_q][Hq]) receives |sum_t w_t / Z - 1| for each output.
+ * (rvLLM, CUDA Kernels table, "PagedAttention V2"; feature list, "Sliding
+ * window attention"; LLM Serving Kernels, Projects table, row 04.)
  */
 static void decode_impl(double *out, const uint16_t *q, int q_is_bf16, const pool_view *pool,
                         const int32_t *block_tables, int max_blocks_per_seq,
                         const int32_t *context_lens, int num_seqs, int num_q_heads,
-                        int num_kv_heads, int head_dim, int block_size, float scale,
-                        const int32_t *rows, int n_rows, double *wsum_dev)
+                        int num_kv_heads, int head_dim, int block_size, float scale, int window,
+                        int n_q, const int32_t *rows, int n_rows, double *wsum_dev)
 {
     int group = num_q_heads / num_kv_heads;
     int nsel = rows ? n_rows : num_seqs;
-    int64_t work = (int64_t)nsel * num_q_heads;
+    int64_t per_seq = (int64_t)n_q * num_q_heads;
+    int64_t work = (int64_t)nsel * per_seq;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t w = 0; w < work; w++) {
-        int b = rows ? rows[w / num_q_heads] : (int)(w / num_q_heads);
+        int b = rows ? rows[w / per_seq] : (int)(w / per_seq);
+        int i = (int)((w % per_seq) / num_q_heads);
         int hq = (int)(w % num_q_heads);
         int h = hq / group;
         int L = context_lens[b];
-        double *o = out + ((size_t)b * num_q_heads + hq) * head_dim;
+        size_t row = ((size_t)b * n_q + i) * num_q_heads + hq;
+        double *o = out + row * head_dim;
         for (int d = 0; d < head_dim; d++)
             o[d] = 0.0;
         if (wsum_dev)
-            wsum_dev[(size_t)b * num_q_heads + hq] = 0.0;
-        if (L <= 0)
+            wsum_dev[row] = 0.0;
+        int pos = L - n_q + i;
+        if (L <= 0 || pos < 0)
             continue;
+        int lo = window > 0 && pos - window + 1 > 0 ? pos - window + 1 : 0;
+        int n = pos + 1 - lo;
 
         double qd[256];
-        const uint16_t *qr = q + ((size_t)b * num_q_heads + hq) * head_dim;
+        const uint16_t *qr = q + row * head_dim;
         for (int d = 0; d < head_dim; d++)
             qd[d] = act_to_double(qr[d], q_is_bf16);
 
-        double *s = (double *)malloc(sizeof(double) * (size_t)L);
-        for (int t = 0; t < L; t++) {
+        double *s = (double *)malloc(sizeof(double) * (size_t)n);
+        for (int j = 0; j < n; j++) {
+            int t = lo + j;
             size_t blk = (size_t)block_tables[(size_t)b * max_blocks_per_seq + t / block_size];
             size_t tile = blk * num_kv_heads + h;
             size_t base = (tile * block_size + t % block_size) * head_dim;
             double dot = 0.0;
             for (int d = 0; d < head_dim; d++)
                 dot += qd[d] * pool_elem(pool, 0, tile, base + d);
-            s[t] = (double)scale * dot;
+            s[j] = (double)scale * dot;
         }
         double m = s[0];
-        for (int t = 1; t < L; t++)
-            if (s[t] > m)
-                m = s[t];
+        for (int j = 1; j < n; j++)
+            if (s[j] > m)
+                m = s[j];
         double Z = 0.0;
-        for (int t = 0; t < L; t++) {
-            s[t] = exp(s[t] - m);
-            Z += s[t];
+        for (int j = 0; j < n; j++) {
+            s[j] = exp(s[j] - m);
+            Z += s[j];
         }
         double wsum = 0.0;
-        for (int t = 0; t < L; t++) {
+        for (int j = 0; j < n; j++) {
+            int t = lo + j;
             size_t blk = (size_t)block_tables[(size_t)b * max_blocks_per_seq + t / block_size];
             size_t tile = blk * num_kv_heads + h;
             size_t base = (tile * block_size + t % block_size) * head_dim;
-            double wt = s[t] / Z;
+            double wt = s[j] / Z;
             wsum += wt;
             for (int d = 0; d < head_dim; d++)
                 o[d] += wt * pool_elem(pool, 1, tile, base + d);
         }
         if (wsum_dev)
-            wsum_dev[(size_t)b * num_q_heads + hq] = fabs(wsum - 1.0);
+            wsum_dev[row] = fabs(wsum - 1.0);
         free(s);
     }
 }
@@ -380,12 +396,13 @@ static void decode_impl(double *out, const uint16_t *q, int q_is_bf16, const poo
 void oracle_decode(double *out, const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                    int is_bf16, const int32_t *block_tables, int max_blocks_per_seq,
                    const int32_t *context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
-                   int head_dim, int block_size, float scale, const int32_t *rows, int n_rows,
-                   double *wsum_dev)
+                   int head_dim, int block_size, float scale, int window, int n_q,
+                   const int32_t *rows, int n_rows, double *wsum_dev)
 {
     pool_view p = {k_cache, v_cache, 0, 0, is_bf16, 0};
     decode_impl(out, q, is_bf16, &p, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-                num_q_heads, num_kv_heads, head_dim, block_size, scale, rows, n_rows, wsum_dev);
+                num_q_heads, num_kv_heads, head_dim, block_size, scale, window, n_q, rows, n_rows,
+                wsum_dev);
 }
 
 /* FP8 pool: K = e4m3(code) * k_scale[block][kv head] exactly (in double); Q is
@@ -394,12 +411,13 @@ void oracle_decode_fp8(double *out, const uint16_t *q, int q_is_bf16, const uint
                        const uint8_t *v_cache, const float *k_scale, const float *v_scale,
                        const int32_t *block_tables, int max_blocks_per_seq,
                        const int32_t *context_lens, int num_seqs, int num_q_heads,
-                       int num_kv_heads, int head_dim, int block_size, float scale,
-                       const int32_t *rows, int n_rows, double *wsum_dev)
+                       int num_kv_heads, int head_dim, int block_size, float scale, int window,
+                       int n_q, const int32_t *rows, int n_rows, double *wsum_dev)
 {
     pool_view p = {k_cache, v_cache, k_scale, v_scale, 0, 1};
     decode_impl(out, q, q_is_bf16, &p, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-                num_q_heads, num_kv_heads, head_dim, block_size, scale, rows, n_rows, wsum_dev);
+                num_q_heads, num_kv_heads, head_dim, block_size, scale, window, n_q, rows, n_rows,
+                wsum_dev);
 }
 
 int oracle_num_threads(void)

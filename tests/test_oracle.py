@@ -454,6 +454,74 @@ def test_decode_fp8_bf16_query_matches_dense():
     assert np.abs(got - want).max() < 1e-12
 
 
+def _last_tokens_relaid(kp, vp, tables, lens, b, W):
+    """Sequence b's last W tokens copied, in order, to fresh blocks starting at
+    position 0 (pure data movement): (k pool, v pool, table row, length)."""
+    L = int(lens[b])
+    lo = max(0, L - W)
+    n = L - lo
+    nb = (n + 15) // 16
+    k2 = np.zeros((nb,) + kp.shape[1:], kp.dtype)
+    v2 = np.zeros_like(k2)
+    for j in range(n):
+        t = lo + j
+        k2[j // 16, :, j % 16] = kp[tables[b, t // 16], :, t % 16]
+        v2[j // 16, :, j % 16] = vp[tables[b, t // 16], :, t % 16]
+    return k2, v2, np.arange(nb, dtype=np.int32)[None, :], np.array([n], np.int32)
+
+
+@pytest.mark.parametrize("W", [1, 5, 16, 33, 100, 1000])
+def test_window_equals_global_decode_of_the_last_tokens(W):
+    rng = np.random.default_rng(20 + W)
+    B, Hq, Hkv, D = 4, 8, 2, 64
+    q, kp, vp, tables, lens = _random_case(rng, B, Hq, Hkv, D, 300)
+    got = oracle.decode(q, kp, vp, tables, lens, 0.125, window=W)
+    for b in range(B):
+        k2, v2, t2, l2 = _last_tokens_relaid(kp, vp, tables, lens, b, W)
+        want = oracle.decode(q[b:b + 1], k2, v2, t2, l2, 0.125)
+        assert np.array_equal(got[b], want[0]), (W, b)
+    if W >= lens.max():
+        assert np.array_equal(got, oracle.decode(q, kp, vp, tables, lens, 0.125))
+
+
+def test_window_of_one_token_returns_its_value():
+    rng = np.random.default_rng(31)
+    q, kp, vp, tables, lens = _random_case(rng, 3, 4, 2, 64, 200)
+    got = oracle.decode(q, kp, vp, tables, lens, 0.125, window=1)
+    for b in range(3):
+        t = int(lens[b]) - 1
+        v = vp[tables[b, t // 16], :, t % 16].astype(np.float64)
+        assert np.array_equal(got[b], np.repeat(v, 2, axis=0))
+
+
+@pytest.mark.parametrize("nq,W,fp8", [(2, 0, False), (4, 0, False), (3, 20, False),
+                                      (4, 0, True), (2, 9, True)])
+def test_query_tokens_equal_single_queries_at_their_positions(nq, W, fp8):
+    """Query i of a sequence with L tokens is the single-query decode of the
+    same cache with length L - nq + i + 1 (its position plus one)."""
+    rng = np.random.default_rng(40 + nq + W)
+    B, Hq, Hkv, D = 3, 8, 2, 128
+    _, kp, vp, tables, lens = _random_case(rng, B, Hq, Hkv, D, 150)
+    lens = np.maximum(lens, nq).astype(np.int32)
+    q = rng.standard_normal((B, nq, Hq, D)).astype(np.float16)
+    if fp8:
+        kc, ks = oracle.quantize_fp8(kp)
+        vc, vs = oracle.quantize_fp8(vp)
+        run = lambda qq, ll: oracle.decode_fp8(qq, kc, vc, ks, vs, tables, ll, 0.125, window=W)
+    else:
+        run = lambda qq, ll: oracle.decode(qq, kp, vp, tables, ll, 0.125, window=W)
+    got = run(q, lens)
+    assert got.shape == q.shape
+    for i in range(nq):
+        want = run(np.ascontiguousarray(q[:, i]), (lens - nq + i + 1).astype(np.int32))
+        assert np.array_equal(got[:, i], want), i
+    # a query whose position precedes the cache gets zeros
+    short = np.array([1, 2, 3], np.int32)
+    z = run(q, short)
+    for b in range(B):
+        assert np.all(z[b, :max(0, nq - int(short[b]))] == 0)
+
+
 def test_rows_subset_matches_full():
     rng = np.random.default_rng(12)
     q, kp, vp, tables, lens = _random_case(rng, 5, 8, 2, 64, 120)
