@@ -59,15 +59,23 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def algorithmic_bytes(w, lens: np.ndarray) -> dict:
+def attended(lens: np.ndarray, window: int = 0) -> np.ndarray:
+    """Tokens each sequence attends: all of them, or its last ``window``."""
+    L = lens.astype(np.int64)
+    return np.minimum(L, window) if window > 0 else L
+
+
+def algorithmic_bytes(w, lens: np.ndarray, window: int = 0) -> dict:
     """Bytes one decode call must move: K+V of every attended token, q, out,
     the block-table entries and context lengths read (plus page scales for an
-    E4M3 pool).  Workspace traffic and the padding rows of each sequence's
-    last block are overhead, not counted."""
+    E4M3 pool).  Workspace traffic, the padding rows of each sequence's last
+    block and the rows before a sliding window in its first block are
+    overhead, not counted."""
     e_kv = 1 if w.kv == "fp8" else 2
     L = lens.astype(np.int64)
-    nblk = (L + w.block_size - 1) // w.block_size
-    kv = int(L.sum()) * w.Hkv * 2 * w.D * e_kv
+    first = np.maximum(L - window, 0) // w.block_size if window > 0 else 0
+    nblk = (L + w.block_size - 1) // w.block_size - first
+    kv = int(attended(lens, window).sum()) * w.Hkv * 2 * w.D * e_kv
     qo = 2 * w.B * w.Hq * w.D * 2
     meta = int(nblk.sum()) * 4 + w.B * 4
     scales = int(nblk.sum()) * w.Hkv * 2 * 4 if w.kv == "fp8" else 0
@@ -148,12 +156,13 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside), "window": window}
 
 
-def oracle_baseline(w, budget_s: float = 10.0) -> dict:
+def oracle_baseline(w, budget_s: float = 10.0, window: int = 0) -> dict:
     """fp64 CPU oracle (as it stands) on a bounded sample of the batch: whole
     passes over a subset of its sequences, repeated to about budget_s."""
     import oracle
     from paged_kv_cache_179_gb300 import workloads as W
     lens = w.context_lens.cpu().numpy()
+    att = attended(lens, window)
     tables = w.block_tables.cpu().numpy()
     q = W.to_numpy16(w.q)
     if w.kv == "fp8":
@@ -164,27 +173,27 @@ def oracle_baseline(w, budget_s: float = 10.0) -> dict:
     # calibrate on 4 sequences, then size the sample to ~budget_s
     probe = order[:4]
     t = time.perf_counter()
-    oracle.decode(q, kp, vp, tables, lens, w.scale, bf16=bf16, rows=probe)
+    oracle.decode(q, kp, vp, tables, lens, w.scale, bf16=bf16, window=window, rows=probe)
     dt = max(time.perf_counter() - t, 1e-3)
-    per_tok = dt / max(1, int(lens[probe].sum()))
+    per_tok = dt / max(1, int(att[probe].sum()))
     n, tok = 0, 0
     for b in order:
-        if (tok + lens[b]) * per_tok > budget_s and n >= 4:
+        if (tok + att[b]) * per_tok > budget_s and n >= 4:
             break
         n += 1
-        tok += int(lens[b])
+        tok += int(att[b])
     rows = order[:n]
     reps, t = 0, time.perf_counter()
     while True:
-        oracle.decode(q, kp, vp, tables, lens, w.scale, bf16=bf16, rows=rows)
+        oracle.decode(q, kp, vp, tables, lens, w.scale, bf16=bf16, window=window, rows=rows)
         reps += 1
         dt = time.perf_counter() - t
         if dt >= budget_s or reps >= 200:
             break
-    tok = int(lens[rows].sum()) * reps
+    tok = int(att[rows].sum()) * reps
     return {"value": round(tok / dt, 1), "unit": UNIT, "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"{n} of {w.B} sequences ({int(lens[rows].sum())} attended tokens, all "
+            "sample": f"{n} of {w.B} sequences ({int(att[rows].sum())} attended tokens, all "
                       f"{w.Hq} q heads) x {reps} passes, fp64 two-pass softmax, {dt:.1f} s"}
 
 
@@ -214,7 +223,7 @@ def run_ours(args, rank, world, dev):
     _abi.load()
     w = W.make_workload(args.config, seed=replica_seed(args.seed, rank), device=dev)
     lens = w.context_lens.cpu().numpy()
-    tokens = int(lens.sum())
+    tokens = int(attended(lens, args.window).sum())
     if w.kv == "fp8":
         kc = torch.empty(w.k_cache.shape, dtype=torch.uint8, device=dev)
         vc = torch.empty_like(kc)
@@ -226,10 +235,10 @@ def run_ours(args, rank, world, dev):
         pools = dict(k_cache=w.k_cache, v_cache=w.v_cache)
     step = DecodeStep(**pools, block_tables=w.block_tables, context_lens=w.context_lens,
                       max_context_len=w.max_context_len, scale=w.scale, num_q_heads=w.Hq,
-                      split_ctas=args.splits)
+                      split_ctas=args.splits, window=args.window)
     out = torch.empty_like(w.q)
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
-    kv_bytes = algorithmic_bytes(w, lens)["kv"]
+    kv_bytes = algorithmic_bytes(w, lens, args.window)["kv"]
     l2_mode = args.l2
     if l2_mode == "auto":
         # Inputs several times larger than L2 stream through it without hits;
@@ -334,7 +343,7 @@ def run_ours(args, rank, world, dev):
     if rank != 0:
         return None
 
-    ab = algorithmic_bytes(w, lens)
+    ab = algorithmic_bytes(w, lens, args.window)
     dec_mean_s = statistics.mean(dec_ms) / 1e3
     peak, peak_kind = measured_peaks()
     kernel_bytes = ab["total"] + (ab["append"] if fused else 0)
@@ -352,6 +361,7 @@ def run_ours(args, rank, world, dev):
                      if fused else "append launch, then attention and merge launches"),
             "split_ctas": step.split_ctas, "l2": describe_l2(l2_mode, kv_bytes, l2),
             "seed": args.seed, "parallelism": "replicas" if world > 1 else "single GPU",
+            **({"window": args.window} if args.window else {}),
         },
         "hbm_gbs": round(achieved, 1), "hbm_frac_of_peak": round(achieved / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -373,7 +383,7 @@ def run_ours(args, rank, world, dev):
         "clocks": clk,
     }
     if not args.no_cpu_baseline and w.kv != "fp8":
-        line["cpu_baseline"] = oracle_baseline(w, args.cpu_budget)
+        line["cpu_baseline"] = oracle_baseline(w, args.cpu_budget, args.window)
     return line
 
 
@@ -482,6 +492,7 @@ def run_reference(args):
     from paged_kv_cache_179_gb300 import workloads as W
     w = W.make_workload(args.config, seed=args.seed, device="cpu")
     lens = w.context_lens.numpy()
+    att = attended(lens, args.window)
     tables = w.block_tables.numpy()
     q, kp, vp = W.to_numpy16(w.q), W.to_numpy16(w.k_cache), W.to_numpy16(w.v_cache)
     bf16 = w.dtype == "bf16"
@@ -495,21 +506,24 @@ def run_reference(args):
     probe = order[:2]
     t = time.perf_counter()
     if w.kv == "fp8":
-        oracle.decode_fp8(q, kc, vc, ks, vs, tables, lens, w.scale, rows=probe)
+        oracle.decode_fp8(q, kc, vc, ks, vs, tables, lens, w.scale, window=args.window,
+                          rows=probe)
     else:
-        oracle.decode(q, kp, vp, tables, lens, w.scale, bf16=bf16, rows=probe)
-    per_tok = max(time.perf_counter() - t, 1e-4) / max(1, int(lens[probe].sum()))
-    n = max(2, min(w.B, int(args.ref_step_s / per_tok / max(1.0, lens.mean()))))
+        oracle.decode(q, kp, vp, tables, lens, w.scale, bf16=bf16, window=args.window, rows=probe)
+    per_tok = max(time.perf_counter() - t, 1e-4) / max(1, int(att[probe].sum()))
+    n = max(2, min(w.B, int(args.ref_step_s / per_tok / max(1.0, att.mean()))))
     rows = order[:n]
-    sample_tokens = int(lens[rows].sum())
+    sample_tokens = int(att[rows].sum())
 
     def one_step():
         if w.kv == "fp8":
             oracle.cache_append_fp8(kn, vn, kc, vc, ks, vs, slots, 16)
-            oracle.decode_fp8(q, kc, vc, ks, vs, tables, lens, w.scale, rows=rows)
+            oracle.decode_fp8(q, kc, vc, ks, vs, tables, lens, w.scale, window=args.window,
+                              rows=rows)
         else:
             oracle.cache_append(kn, vn, kp, vp, slots, 16)
-            oracle.decode(q, kp, vp, tables, lens, w.scale, bf16=bf16, rows=rows)
+            oracle.decode(q, kp, vp, tables, lens, w.scale, bf16=bf16, window=args.window,
+                          rows=rows)
 
     for _ in range(args.warmup):
         one_step()
@@ -525,8 +539,8 @@ def run_reference(args):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": describe(w, int(lens.sum())), "step": "oracle append + decode",
-                   "seed": args.seed},
+        "config": {"workload": describe(w, int(att.sum())), "step": "oracle append + decode",
+                   "seed": args.seed, **({"window": args.window} if args.window else {})},
         "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -556,6 +570,8 @@ def main(argv=None):
     ap.add_argument("--op", choices=["step", "copy_blocks"], default="step",
                     help="what to time: the decode step (default) or pa_copy_blocks alone")
     ap.add_argument("--copy-pairs", type=int, default=8192)
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding window in tokens (0: each sequence attends its whole context)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-step-s", type=float, default=2.0)

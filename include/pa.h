@@ -200,6 +200,8 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int
  * Results do not depend on split_ctas beyond fp32 rounding, and a given
  * split_ctas is deterministic.
  *   max_context_len: host-side upper bound of context_lens (no device read);
+ *   window_size: 0 attends the whole context; W > 0 attends only the last W
+ *   positions (L-W .. L-1; the blocks wholly before them are not read);
  *   workspace: at least pa_decode_workspace_size(...) bytes, 256-byte
  *   aligned.
  * Source: rvLLM, CUDA Kernels table, "PagedAttention V2" (block-table
@@ -209,7 +211,7 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int
 int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
               const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
               int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-              int block_size, int num_blocks, float scale, int dtype, int split_ctas,
+              int block_size, int num_blocks, float scale, int window_size, int dtype, int split_ctas,
               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -226,7 +228,7 @@ int pa_decode_fp8(void *out, const void *q, const uint8_t *k_cache, const uint8_
                   const float *k_scale, const float *v_scale, const int32_t *block_tables,
                   int max_blocks_per_seq, const int32_t *context_lens, int max_context_len,
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                  int num_blocks, float scale, int dtype, int split_ctas, void *workspace,
+                  int num_blocks, float scale, int window_size, int dtype, int split_ctas, void *workspace,
                   size_t workspace_bytes, void *stream);
 
 /*
@@ -253,7 +255,7 @@ int pa_decode_step(void *out, const void *q, const void *k_new, const void *v_ne
                    const int32_t *block_tables, int max_blocks_per_seq,
                    const int32_t *context_lens, int max_context_len, int num_seqs,
                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                   int num_blocks, float scale, int dtype, int split_ctas, void *workspace,
+                   int num_blocks, float scale, int window_size, int dtype, int split_ctas, void *workspace,
                    size_t workspace_bytes, void *stream);
 
 /*
@@ -268,7 +270,7 @@ int pa_decode_step_fp8(void *out, const void *q, const void *k_new, const void *
                        const int64_t *slot_mapping, const int32_t *block_tables,
                        int max_blocks_per_seq, const int32_t *context_lens, int max_context_len,
                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                       int block_size, int num_blocks, float scale, int dtype, int split_ctas,
+                       int block_size, int num_blocks, float scale, int window_size, int dtype, int split_ctas,
                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -292,7 +294,7 @@ int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void 
                       const int32_t *block_tables, int max_blocks_per_seq,
                       const int32_t *context_lens, int max_context_len, int num_seqs,
                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                      int num_blocks, float scale, int dtype, int split_ctas, void *stream);
+                      int num_blocks, float scale, int window_size, int dtype, int split_ctas, void *stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status

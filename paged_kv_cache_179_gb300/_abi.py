@@ -37,15 +37,15 @@ SIGNATURES = {
     "pa_decode_workspace_size": ([_i32, _i32, _i32, _i32], _sz),
     "pa_decode_default_splits": ([_i32], _i32),
     "pa_decode": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
-                   _f32, _i32, _i32, _vp, _sz, _vp], _i32),
+                   _f32, _i32, _i32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
-                       _i32, _i32, _f32, _i32, _i32, _vp, _sz, _vp], _i32),
+                       _i32, _i32, _f32, _i32, _i32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
-                        _i32, _i32, _i32, _f32, _i32, _i32, _vp, _sz, _vp], _i32),
+                        _i32, _i32, _i32, _f32, _i32, _i32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_step_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
-                            _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _sz, _vp], _i32),
+                            _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
-                           _i32, _i32, _f32, _i32, _i32, _vp], _i32),
+                           _i32, _i32, _f32, _i32, _i32, _i32, _vp], _i32),
     "pa_get_status": ([_vp, ctypes.POINTER(ctypes.c_uint)], _i32),
 }
 
@@ -250,7 +250,7 @@ def _decode_common(out, q, block_tables, context_lens, dev):
 
 
 def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
-              scale: float, split_ctas: int = 0, workspace=None) -> None:
+              scale: float, split_ctas: int = 0, workspace=None, *, window: int = 0) -> None:
     """out[b][hq] = softmax(scale q.K) V over each sequence's blocks (16-bit pools)."""
     dev = q.device
     act = (torch.float16, torch.bfloat16)
@@ -266,14 +266,14 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_
         ws_bytes = workspace.numel() * workspace.element_size()
     _check(load().pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                             block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq,
-                            Hkv, D, bs, NB, float(scale), _act_code(q.dtype),
+                            Hkv, D, bs, NB, float(scale), int(window), _act_code(q.dtype),
                             int(split_ctas), _ptr(workspace), ws_bytes, _stream(dev)),
            "pa_decode")
 
 
 def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
-                  max_context_len: int, scale: float, split_ctas: int = 0,
-                  workspace=None) -> None:
+                  max_context_len: int, scale: float, split_ctas: int = 0, workspace=None, *,
+                  window: int = 0) -> None:
     """As pa_decode over E4M3 pools with per-(block, kv head) fp32 scales; q/out
     fp16 or bf16."""
     dev = q.device
@@ -292,7 +292,7 @@ def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, cont
     _check(load().pa_decode_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                 _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
                                 _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
-                                float(scale), _act_code(q.dtype), int(split_ctas),
+                                float(scale), int(window), _act_code(q.dtype), int(split_ctas),
                                 _ptr(workspace), ws_bytes, _stream(dev)), "pa_decode_fp8")
 
 
@@ -305,7 +305,7 @@ def _ws_bytes(workspace, dev):
 
 def pa_decode_step(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_tables,
                    context_lens, max_context_len: int, scale: float, split_ctas: int = 0,
-                   workspace=None) -> None:
+                   workspace=None, *, window: int = 0) -> None:
     """Append k_new/v_new at slot_mapping, then decode, in one launch (16-bit pools)."""
     dev = q.device
     act = (torch.float16, torch.bfloat16)
@@ -323,14 +323,15 @@ def pa_decode_step(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_t
     _check(load().pa_decode_step(_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
                                  _ptr(v_cache), _ptr(slot_mapping), _ptr(block_tables),
                                  block_tables.shape[1], _ptr(context_lens), int(max_context_len),
-                                 B, Hq, Hkv, D, bs, NB, float(scale), _act_code(q.dtype),
-                                 int(split_ctas), _ptr(workspace), _ws_bytes(workspace, dev),
+                                 B, Hq, Hkv, D, bs, NB, float(scale), int(window),
+                                 _act_code(q.dtype), int(split_ctas), _ptr(workspace),
+                                 _ws_bytes(workspace, dev),
                                  _stream(dev)), "pa_decode_step")
 
 
 def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping,
                        block_tables, context_lens, max_context_len: int, scale: float,
-                       split_ctas: int = 0, workspace=None) -> None:
+                       split_ctas: int = 0, workspace=None, *, window: int = 0) -> None:
     """Append (E4M3-encode) k_new/v_new, then decode over the E4M3 pools, in one
     attention launch; q, k_new, v_new and out share one dtype (fp16 or bf16)."""
     dev = q.device
@@ -350,13 +351,15 @@ def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
                                      _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                      _ptr(slot_mapping), _ptr(block_tables), block_tables.shape[1],
                                      _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs,
-                                     NB, float(scale), _act_code(q.dtype), int(split_ctas),
-                                     _ptr(workspace), _ws_bytes(workspace, dev), _stream(dev)),
+                                     NB, float(scale), int(window), _act_code(q.dtype),
+                                     int(split_ctas), _ptr(workspace), _ws_bytes(workspace, dev),
+                                     _stream(dev)),
            "pa_decode_step_fp8")
 
 
 def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
-                      max_context_len: int, scale: float, split_ctas: int = 0) -> None:
+                      max_context_len: int, scale: float, split_ctas: int = 0,
+                      window: int = 0) -> None:
     """pa_decode with the library's static scratch instead of a workspace (allocates nothing)."""
     dev = q.device
     act = (torch.float16, torch.bfloat16)
@@ -369,6 +372,7 @@ def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
     _check(load().pa_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                     _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
                                     int(max_context_len), B, Hq, Hkv, D, bs, NB, float(scale),
+                                    int(window),
                                     _act_code(q.dtype), int(split_ctas), _stream(dev)),
            "pa_decode_noalloc")
 

@@ -52,14 +52,14 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
 
 struct DecodeShape {
-  int B, Hq, Hkv, D, bs, NB, mbs, max_ctx, splits;
+  int B, Hq, Hkv, D, bs, NB, mbs, max_ctx, splits, window;
 };
 
 int check_decode_shape(const DecodeShape& s, float scale) {
   if (s.B < 0 || s.Hq <= 0 || s.Hkv <= 0 || s.Hq % s.Hkv != 0) return PA_ERR_INVALID_ARG;
   if (s.NB <= 0 || s.mbs <= 0 || s.max_ctx < 0) return PA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(s.max_ctx) > static_cast<int64_t>(s.mbs) * s.bs) return PA_ERR_INVALID_ARG;
-  if (s.splits < 0) return PA_ERR_INVALID_ARG;
+  if (s.splits < 0 || s.window < 0) return PA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
   if (s.D != 64 && s.D != 128) return PA_ERR_UNSUPPORTED;
   if (s.bs != 16) return PA_ERR_UNSUPPORTED;
@@ -109,6 +109,7 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
   a.num_blocks = s.NB;
   a.max_context_len = s.max_ctx;
   a.split_ctas = s.splits;
+  a.window = s.window;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.k_pool_w = ap.k_pool;
   a.v_pool_w = ap.v_pool;
@@ -297,14 +298,14 @@ int pa_decode_default_splits(int pool_type) {
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
               int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-              int block_size, int num_blocks, float scale, int dtype, int split_ctas,
+              int block_size, int num_blocks, float scale, int window_size, int dtype, int split_ctas,
               void* workspace, size_t workspace_bytes, void* stream) {
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
     return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
   const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                      num_blocks, max_blocks_per_seq, max_context_len, split_ctas};
+                      num_blocks, max_blocks_per_seq, max_context_len, split_ctas, window_size};
   if (int rc = check_decode_shape(s, scale)) return rc;
   for (const void* p : {static_cast<const void*>(out), q, k_cache, v_cache})
     if (!aligned(p, 16)) return PA_ERR_INVALID_ARG;
@@ -317,7 +318,7 @@ int pa_decode_fp8(void* out, const void* q, const uint8_t* k_cache, const uint8_
                   const float* k_scale, const float* v_scale, const int32_t* block_tables,
                   int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                  int num_blocks, float scale, int dtype, int split_ctas, void* workspace,
+                  int num_blocks, float scale, int window_size, int dtype, int split_ctas, void* workspace,
                   size_t workspace_bytes, void* stream) {
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables ||
@@ -325,7 +326,7 @@ int pa_decode_fp8(void* out, const void* q, const uint8_t* k_cache, const uint8_
     return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
   const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                      num_blocks, max_blocks_per_seq, max_context_len, split_ctas};
+                      num_blocks, max_blocks_per_seq, max_context_len, split_ctas, window_size};
   if (int rc = check_decode_shape(s, scale)) return rc;
   for (const void* p : {static_cast<const void*>(out), q, static_cast<const void*>(k_cache),
                         static_cast<const void*>(v_cache)})
@@ -342,7 +343,7 @@ int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_ne
                    const int32_t* block_tables, int max_blocks_per_seq,
                    const int32_t* context_lens, int max_context_len, int num_seqs,
                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                   int num_blocks, float scale, int dtype, int split_ctas, void* workspace,
+                   int num_blocks, float scale, int window_size, int dtype, int split_ctas, void* workspace,
                    size_t workspace_bytes, void* stream) {
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_new || !v_new || !k_cache || !v_cache || !slot_mapping ||
@@ -350,7 +351,7 @@ int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_ne
     return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
   const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                      num_blocks, max_blocks_per_seq, max_context_len, split_ctas};
+                      num_blocks, max_blocks_per_seq, max_context_len, split_ctas, window_size};
   if (int rc = check_decode_shape(s, scale)) return rc;
   for (const void* p : {static_cast<const void*>(out), q, k_new, v_new,
                         static_cast<const void*>(k_cache), static_cast<const void*>(v_cache)})
@@ -372,7 +373,7 @@ int pa_decode_step_fp8(void* out, const void* q, const void* k_new, const void* 
                        const int64_t* slot_mapping, const int32_t* block_tables,
                        int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                       int block_size, int num_blocks, float scale, int dtype, int split_ctas,
+                       int block_size, int num_blocks, float scale, int window_size, int dtype, int split_ctas,
                        void* workspace, size_t workspace_bytes, void* stream) {
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_new || !v_new || !k_cache || !v_cache || !k_scale || !v_scale ||
@@ -380,7 +381,7 @@ int pa_decode_step_fp8(void* out, const void* q, const void* k_new, const void* 
     return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
   const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                      num_blocks, max_blocks_per_seq, max_context_len, split_ctas};
+                      num_blocks, max_blocks_per_seq, max_context_len, split_ctas, window_size};
   if (int rc = check_decode_shape(s, scale)) return rc;
   for (const void* p : {static_cast<const void*>(out), q, k_new, v_new,
                         static_cast<const void*>(k_cache), static_cast<const void*>(v_cache)})

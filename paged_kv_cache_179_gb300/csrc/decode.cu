@@ -151,7 +151,8 @@ struct WarpAcc {
 // One 16-token block already in shared memory: K tile at kt, V tile at vt.
 template <int D, bool FP8, bool BF16>
 __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf)[D / 16][2],
-                                             uint32_t kt, uint32_t vt, int n_valid, float sl2,
+                                             uint32_t kt, uint32_t vt, int n_skip, int n_valid,
+                                             float sl2,
                                              float v_mul, int r, int c) {
   constexpr int ROW = FP8 ? D : 2 * D;
   // ---- S^T = K Q^T : 16 tokens x 8 query heads, k = head_dim
@@ -186,8 +187,9 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
 
   // ---- online softmax on the fragment: this lane holds tokens r, r+8 of heads 2c, 2c+1
   float s0 = acc[0] * sl2, s1 = acc[1] * sl2, s2 = acc[2] * sl2, s3 = acc[3] * sl2;
-  if (r >= n_valid) s0 = s1 = -INFINITY;
-  if (r + 8 >= n_valid) s2 = s3 = -INFINITY;
+  // rows outside [n_skip, n_valid): before a sliding window, or past the context
+  if (r < n_skip || r >= n_valid) s0 = s1 = -INFINITY;
+  if (r + 8 < n_skip || r + 8 >= n_valid) s2 = s3 = -INFINITY;
   float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
@@ -225,14 +227,14 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
       v[2][u] = lds128(vt + tk2 * ROW + (8 * u + r) * 16);
       v[3][u] = lds128(vt + tk3 * ROW + (8 * u + r) * 16);
     }
-    if (n_valid < 16) {   // rows past the context may hold anything, NaN included
+    if (n_valid < 16 || n_skip > 0) {   // rows past the context may hold anything, NaN included
       const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        if (tk0 >= n_valid) v[0][u] = z;
-        if (tk1 >= n_valid) v[1][u] = z;
-        if (tk2 >= n_valid) v[2][u] = z;
-        if (tk3 >= n_valid) v[3][u] = z;
+        if (tk0 < n_skip || tk0 >= n_valid) v[0][u] = z;
+        if (tk1 < n_skip || tk1 >= n_valid) v[1][u] = z;
+        if (tk2 < n_skip || tk2 >= n_valid) v[2][u] = z;
+        if (tk3 < n_skip || tk3 >= n_valid) v[3][u] = z;
       }
     }
 #pragma unroll
@@ -262,12 +264,12 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
       v[2] = lds64(vt + tk2 * ROW + VB * r);
       v[3] = lds64(vt + tk3 * ROW + VB * r);
     }
-    if (n_valid < 16) {
+    if (n_valid < 16 || n_skip > 0) {
       VT z{};
-      if (tk0 >= n_valid) v[0] = z;
-      if (tk1 >= n_valid) v[1] = z;
-      if (tk2 >= n_valid) v[2] = z;
-      if (tk3 >= n_valid) v[3] = z;
+      if (tk0 < n_skip || tk0 >= n_valid) v[0] = z;
+      if (tk1 < n_skip || tk1 >= n_valid) v[1] = z;
+      if (tk2 < n_skip || tk2 >= n_valid) v[2] = z;
+      if (tk3 < n_skip || tk3 >= n_valid) v[3] = z;
     }
 #pragma unroll
     for (int i = 0; i < D / 16; i += 2) {
@@ -357,10 +359,19 @@ __device__ __forceinline__ Chunk next_chunk(const Chunk& x, int64_t hi, const in
   return Chunk{b, h, 0, static_cast<int>(min(static_cast<int64_t>(kChunk), min(hi, s0 + nbk) - s0))};
 }
 
-// This lane's block id of chunk x (lane t holds block cb0 + t), -1 past its end.
-__device__ __forceinline__ int load_chunk_id(const DecodeArgs& a, const Chunk& x, int lane) {
+// The first block a sequence of L tokens attends: with a sliding window of
+// `window` tokens the blocks before position L - window are skipped.
+// Segments and chunks count blocks from there.
+__device__ __forceinline__ int window_first_block(int L, int window) {
+  return window > 0 && L > window ? (L - window) >> 4 : 0;
+}
+
+// This lane's block id of chunk x (lane t holds block cb0 + t of the
+// segment, block table entry fb + cb0 + t), -1 past its end.
+__device__ __forceinline__ int load_chunk_id(const DecodeArgs& a, const Chunk& x, int fb,
+                                             int lane) {
   if (lane >= x.nb) return -1;
-  return __ldg(a.block_tables + static_cast<int64_t>(x.b) * a.mbs + x.cb0 + lane);
+  return __ldg(a.block_tables + static_cast<int64_t>(x.b) * a.mbs + fb + x.cb0 + lane);
 }
 
 // The query fragments of (sequence b, kv head h): the group's G rows, the
@@ -597,7 +608,7 @@ decode_kernel(const DecodeArgs a) {
       const int L = a.context_lens[b];
       const bool ok = L >= 0 && L <= a.max_context_len && L <= a.mbs * 16;
       len[b] = ok ? L : -1;
-      sum += ok ? ((L + 15) >> 4) * Hkv : 0;
+      sum += ok ? (((L + 15) >> 4) - window_first_block(L, a.window)) * Hkv : 0;
     }
     int inc = sum;
 #pragma unroll
@@ -611,7 +622,7 @@ decode_kernel(const DecodeArgs a) {
     for (int w = 0; w < warp; ++w) ex += misc[w];
     for (int b = b0; b < b1; ++b) {
       pf[b] = ex;
-      ex += len[b] > 0 ? ((len[b] + 15) >> 4) * Hkv : 0;
+      ex += len[b] > 0 ? (((len[b] + 15) >> 4) - window_first_block(len[b], a.window)) * Hkv : 0;
     }
     if (tid == kThreads - 1) pf[B] = ex;
     __syncthreads();
@@ -656,9 +667,12 @@ decode_kernel(const DecodeArgs a) {
   Chunk ch0 = first_chunk(lo, hi, pf, B, Hkv);
   Chunk ch1 = next_chunk(ch0, hi, pf, B, Hkv);
   Chunk ch2 = next_chunk(ch1, hi, pf, B, Hkv);
-  int id0 = load_chunk_id(a, ch0, lane);
-  int id1 = load_chunk_id(a, ch1, lane);
-  int id2 = load_chunk_id(a, ch2, lane);
+  auto chunk_id = [&](const Chunk& x) {
+    return load_chunk_id(a, x, x.nb > 0 ? window_first_block(len[x.b], a.window) : 0, lane);
+  };
+  int id0 = chunk_id(ch0);
+  int id1 = chunk_id(ch1);
+  int id2 = chunk_id(ch2);
   float ks0 = 1.f, vs0 = 1.f, ks1 = 1.f, vs1 = 1.f;   // E4M3 page scales of chunks k, k+1
   if constexpr (FP8) {
     if (id0 >= 0 && id0 < a.num_blocks) {
@@ -740,6 +754,7 @@ decode_kernel(const DecodeArgs a) {
 
   while (ch0.nb > 0) {
     const int L = len[ch0.b];
+    const int fb0 = window_first_block(L, a.window);
     // fused append: the new row, when this chunk ends its sequence.  Loaded
     // here rather than a chunk ahead: held across the loop it would cost the
     // E4M3 variant its third CTA per SM (or spills).
@@ -803,9 +818,11 @@ decode_kernel(const DecodeArgs a) {
         }
       }
       if (id >= 0 && id < a.num_blocks) {
-        const int n_valid = min(16, L - (ch0.cb0 + t) * 16);
+        const int blk0 = (fb0 + ch0.cb0 + t) * 16;   // the block's first position
+        const int n_valid = min(16, L - blk0);
+        const int n_skip = a.window > 0 ? max(0, L - a.window - blk0) : 0;
         attend_block<D, FP8, BF16>(st, qf, ring + s * TL::SLOT, ring + s * TL::SLOT + TL::BYTES,
-                                   n_valid, sl2, v_mul, r, c);
+                                   n_skip, n_valid, sl2, v_mul, r, c);
       }
       __syncwarp();
       ++computed;
@@ -843,7 +860,7 @@ decode_kernel(const DecodeArgs a) {
     ch2 = next_chunk(ch2, hi, pf, B, Hkv);
     id0 = id1;
     id1 = id2;
-    id2 = load_chunk_id(a, ch2, lane);
+    id2 = chunk_id(ch2);
     if constexpr (FP8) {
       ks0 = ks1;
       vs0 = vs1;

@@ -56,7 +56,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
                                  int max_blocks_per_seq, const int32_t* context_lens,
                                  int max_context_len, int num_seqs, int num_q_heads,
                                  int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                                 float scale, int dtype, int split_ctas, void* stream) {
+                                 float scale, int window_size, int dtype, int split_ctas, void* stream) {
   using namespace pa;
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
@@ -64,7 +64,8 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
     return PA_ERR_INVALID_ARG;
-  if (num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 || split_ctas < 0)
+  if (num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 || split_ctas < 0 ||
+      window_size < 0)
     return PA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(max_context_len) >
       static_cast<int64_t>(max_blocks_per_seq) * block_size)
@@ -99,6 +100,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   a.num_blocks = num_blocks;
   a.max_context_len = max_context_len;
   a.split_ctas = splits;
+  a.window = window_size;
   a.scale_log2 = scale * 1.4426950408889634f;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t row = static_cast<size_t>(num_q_heads) * head_dim * 2;

@@ -40,6 +40,7 @@ struct DecodeArgs {
   int num_blocks;
   int max_context_len;
   int split_ctas;               // CTAs the batch's blocks are divided among
+  int window;                   // sliding window in tokens (0: the whole context)
   float scale_log2;             // softmax scale * log2(e)
 };
 

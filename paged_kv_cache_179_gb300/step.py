@@ -21,7 +21,7 @@ class DecodeStep:
     """
 
     def __init__(self, *, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
-                 num_q_heads, k_scale=None, v_scale=None, split_ctas=0):
+                 num_q_heads, k_scale=None, v_scale=None, split_ctas=0, window=0):
         self.kv = "fp8" if k_cache.dtype == torch.uint8 else "16"
         self.k_cache, self.v_cache = k_cache, v_cache
         self.k_scale, self.v_scale = k_scale, v_scale
@@ -32,6 +32,7 @@ class DecodeStep:
         self.Hq = int(num_q_heads)
         self.NB, self.Hkv, self.bs, self.D = (int(x) for x in k_cache.shape)
         self.split_ctas = int(split_ctas) or _abi.pa_decode_default_splits(k_cache.dtype)
+        self.window = int(window)           # sliding window in tokens, 0 for the whole context
         self.workspace = _abi.alloc_workspace(self.B, self.Hq, self.D, self.split_ctas,
                                               k_cache.device)
 
@@ -46,11 +47,11 @@ class DecodeStep:
         if self.kv == "fp8":
             _abi.pa_decode_fp8(out, q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
                                self.block_tables, self.context_lens, self.max_context_len,
-                               self.scale, self.split_ctas, self.workspace)
+                               self.scale, self.split_ctas, self.workspace, window=self.window)
         else:
             _abi.pa_decode(out, q, self.k_cache, self.v_cache, self.block_tables,
                            self.context_lens, self.max_context_len, self.scale,
-                           self.split_ctas, self.workspace)
+                           self.split_ctas, self.workspace, window=self.window)
 
     def fused(self, q, k_new, v_new, slot_mapping, out):
         """Append and decode in one launch (slot_mapping must hold each
@@ -59,11 +60,11 @@ class DecodeStep:
             _abi.pa_decode_step_fp8(out, q, k_new, v_new, self.k_cache, self.v_cache,
                                     self.k_scale, self.v_scale, slot_mapping, self.block_tables,
                                     self.context_lens, self.max_context_len, self.scale,
-                                    self.split_ctas, self.workspace)
+                                    self.split_ctas, self.workspace, window=self.window)
         else:
             _abi.pa_decode_step(out, q, k_new, v_new, self.k_cache, self.v_cache, slot_mapping,
                                 self.block_tables, self.context_lens, self.max_context_len,
-                                self.scale, self.split_ctas, self.workspace)
+                                self.scale, self.split_ctas, self.workspace, window=self.window)
         return out
 
     @property
