@@ -202,6 +202,12 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int
  *   max_context_len: host-side upper bound of context_lens (no device read);
  *   window_size: 0 attends the whole context; W > 0 attends only the last W
  *   positions (L-W .. L-1; the blocks wholly before them are not read);
+ *   queries_per_seq: n_q >= 1 query tokens per sequence (speculative or
+ *   chunked decoding): q and out are [num_seqs][n_q][num_q_heads][head_dim],
+ *   query i sits at position L - n_q + i (its own token and those before it
+ *   are in the cache) and attends causally, positions up to its own (within
+ *   its window); a query before position 0 gets a zero output.
+ *   n_q * (num_q_heads / num_kv_heads) must be at most 8;
  *   workspace: at least pa_decode_workspace_size(...) bytes, 256-byte
  *   aligned.
  * Source: rvLLM, CUDA Kernels table, "PagedAttention V2" (block-table
@@ -211,7 +217,8 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int
 int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
               const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
               int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-              int block_size, int num_blocks, float scale, int window_size, int dtype, int split_ctas,
+              int block_size, int num_blocks, float scale, int window_size, int queries_per_seq,
+              int dtype, int split_ctas,
               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -228,7 +235,8 @@ int pa_decode_fp8(void *out, const void *q, const uint8_t *k_cache, const uint8_
                   const float *k_scale, const float *v_scale, const int32_t *block_tables,
                   int max_blocks_per_seq, const int32_t *context_lens, int max_context_len,
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                  int num_blocks, float scale, int window_size, int dtype, int split_ctas, void *workspace,
+                  int num_blocks, float scale, int window_size, int queries_per_seq,
+                  int dtype, int split_ctas, void *workspace,
                   size_t workspace_bytes, void *stream);
 
 /*
@@ -294,7 +302,8 @@ int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void 
                       const int32_t *block_tables, int max_blocks_per_seq,
                       const int32_t *context_lens, int max_context_len, int num_seqs,
                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                      int num_blocks, float scale, int window_size, int dtype, int split_ctas, void *stream);
+                      int num_blocks, float scale, int window_size, int queries_per_seq,
+                      int dtype, int split_ctas, void *stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status

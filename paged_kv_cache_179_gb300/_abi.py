@@ -37,15 +37,15 @@ SIGNATURES = {
     "pa_decode_workspace_size": ([_i32, _i32, _i32, _i32], _sz),
     "pa_decode_default_splits": ([_i32], _i32),
     "pa_decode": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
-                   _f32, _i32, _i32, _i32, _vp, _sz, _vp], _i32),
+                   _f32, _i32, _i32, _i32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
-                       _i32, _i32, _f32, _i32, _i32, _i32, _vp, _sz, _vp], _i32),
+                       _i32, _i32, _f32, _i32, _i32, _i32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                         _i32, _i32, _i32, _f32, _i32, _i32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_step_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
                             _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _i32, _vp, _sz, _vp], _i32),
     "pa_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
-                           _i32, _i32, _f32, _i32, _i32, _i32, _vp], _i32),
+                           _i32, _i32, _f32, _i32, _i32, _i32, _i32, _vp], _i32),
     "pa_get_status": ([_vp, ctypes.POINTER(ctypes.c_uint)], _i32),
 }
 
@@ -241,12 +241,16 @@ def alloc_workspace(num_seqs, num_q_heads, head_dim, split_ctas, device):
 
 
 def _decode_common(out, q, block_tables, context_lens, dev):
+    """q/out [B][Hq][D], or [B][n_q][Hq][D] for n_q query tokens per sequence."""
     _need(block_tables, "block_tables", torch.int32, 2, dev)
     _need(context_lens, "context_lens", torch.int32, 1, dev)
-    B, Hq, D = q.shape
+    if q.dim() == 3:
+        (B, Hq, D), nq = q.shape, 1
+    else:
+        B, nq, Hq, D = q.shape
     if out.shape != q.shape or block_tables.shape[0] != B or context_lens.shape[0] != B:
         raise ValueError("shape mismatch")
-    return B, Hq, D
+    return B, nq, Hq, D
 
 
 def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
@@ -254,11 +258,11 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_
     """out[b][hq] = softmax(scale q.K) V over each sequence's blocks (16-bit pools)."""
     dev = q.device
     act = (torch.float16, torch.bfloat16)
-    _need(q, "q", act, 3, dev)
-    _need(out, "out", q.dtype, 3, dev)
+    _need(q, "q", act, None, dev)
+    _need(out, "out", q.dtype, None, dev)
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, n, q.dtype, 4, dev)
-    B, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
+    B, nq, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
     NB, Hkv, bs, _ = k_cache.shape
     ws_bytes = 0
     if workspace is not None:
@@ -266,8 +270,9 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_
         ws_bytes = workspace.numel() * workspace.element_size()
     _check(load().pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                             block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq,
-                            Hkv, D, bs, NB, float(scale), int(window), _act_code(q.dtype),
-                            int(split_ctas), _ptr(workspace), ws_bytes, _stream(dev)),
+                            Hkv, D, bs, NB, float(scale), int(window), nq,
+                            _act_code(q.dtype), int(split_ctas), _ptr(workspace), ws_bytes,
+                            _stream(dev)),
            "pa_decode")
 
 
@@ -277,13 +282,13 @@ def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, cont
     """As pa_decode over E4M3 pools with per-(block, kv head) fp32 scales; q/out
     fp16 or bf16."""
     dev = q.device
-    _need(q, "q", (torch.float16, torch.bfloat16), 3, dev)
-    _need(out, "out", q.dtype, 3, dev)
+    _need(q, "q", (torch.float16, torch.bfloat16), None, dev)
+    _need(out, "out", q.dtype, None, dev)
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, n, torch.uint8, 4, dev)
     for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
         _need(t, n, torch.float32, 2, dev)
-    B, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
+    B, nq, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
     NB, Hkv, bs, _ = k_cache.shape
     ws_bytes = 0
     if workspace is not None:
@@ -292,8 +297,9 @@ def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, cont
     _check(load().pa_decode_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                 _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
                                 _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
-                                float(scale), int(window), _act_code(q.dtype), int(split_ctas),
-                                _ptr(workspace), ws_bytes, _stream(dev)), "pa_decode_fp8")
+                                float(scale), int(window), nq, _act_code(q.dtype),
+                                int(split_ctas), _ptr(workspace), ws_bytes, _stream(dev)),
+           "pa_decode_fp8")
 
 
 def _ws_bytes(workspace, dev):
@@ -316,7 +322,9 @@ def pa_decode_step(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_t
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, n, q.dtype, 4, dev)
     _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
-    B, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
+    B, nq, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
+    if nq != 1:
+        raise ValueError("the fused step takes one query token per sequence")
     NB, Hkv, bs, _ = k_cache.shape
     if k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape or slot_mapping.shape[0] != B:
         raise ValueError("shape mismatch")
@@ -343,7 +351,9 @@ def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
     for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
         _need(t, n, torch.float32, 2, dev)
     _need(slot_mapping, "slot_mapping", torch.int64, 1, dev)
-    B, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
+    B, nq, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
+    if nq != 1:
+        raise ValueError("the fused step takes one query token per sequence")
     NB, Hkv, bs, _ = k_cache.shape
     if k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape or slot_mapping.shape[0] != B:
         raise ValueError("shape mismatch")
@@ -363,17 +373,17 @@ def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
     """pa_decode with the library's static scratch instead of a workspace (allocates nothing)."""
     dev = q.device
     act = (torch.float16, torch.bfloat16)
-    _need(q, "q", act, 3, dev)
-    _need(out, "out", q.dtype, 3, dev)
+    _need(q, "q", act, None, dev)
+    _need(out, "out", q.dtype, None, dev)
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
         _need(t, n, q.dtype, 4, dev)
-    B, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
+    B, nq, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
     NB, Hkv, bs, _ = k_cache.shape
     _check(load().pa_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                     _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
                                     int(max_context_len), B, Hq, Hkv, D, bs, NB, float(scale),
-                                    int(window),
-                                    _act_code(q.dtype), int(split_ctas), _stream(dev)),
+                                    int(window), nq, _act_code(q.dtype), int(split_ctas),
+                                    _stream(dev)),
            "pa_decode_noalloc")
 
 

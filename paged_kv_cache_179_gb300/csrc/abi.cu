@@ -53,6 +53,7 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; 
 
 struct DecodeShape {
   int B, Hq, Hkv, D, bs, NB, mbs, max_ctx, splits, window;
+  int nq = 1;   // query tokens per sequence
 };
 
 int check_decode_shape(const DecodeShape& s, float scale) {
@@ -63,7 +64,8 @@ int check_decode_shape(const DecodeShape& s, float scale) {
   if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
   if (s.D != 64 && s.D != 128) return PA_ERR_UNSUPPORTED;
   if (s.bs != 16) return PA_ERR_UNSUPPORTED;
-  if (s.Hq / s.Hkv > 8) return PA_ERR_UNSUPPORTED;
+  if (s.nq < 1) return PA_ERR_INVALID_ARG;
+  if (s.Hq / s.Hkv * s.nq > 8) return PA_ERR_UNSUPPORTED;
   if (s.B > 65535 || s.Hkv > 65535) return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
@@ -110,6 +112,7 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
   a.max_context_len = s.max_ctx;
   a.split_ctas = s.splits;
   a.window = s.window;
+  a.n_q = s.nq;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.k_pool_w = ap.k_pool;
   a.v_pool_w = ap.v_pool;
@@ -117,7 +120,7 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
   a.v_scale_w = ap.v_scale;
   // Batches above kMaxBatchPerLaunch run as consecutive launch pairs
   // (attention, merge) on the stream, each reusing the workspace.
-  const size_t out_row = static_cast<size_t>(s.Hq) * s.D * 2;   // q and out are 16-bit
+  const size_t out_row = static_cast<size_t>(s.nq) * s.Hq * s.D * 2;   // q, out: 16-bit
   for (int b0 = 0; b0 < s.B; b0 += kMaxBatchPerLaunch) {
     DecodeArgs c = a;
     c.B = s.B - b0 < kMaxBatchPerLaunch ? s.B - b0 : kMaxBatchPerLaunch;
@@ -298,14 +301,16 @@ int pa_decode_default_splits(int pool_type) {
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
               int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-              int block_size, int num_blocks, float scale, int window_size, int dtype, int split_ctas,
+              int block_size, int num_blocks, float scale, int window_size, int queries_per_seq,
+              int dtype, int split_ctas,
               void* workspace, size_t workspace_bytes, void* stream) {
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
     return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
-  const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+  DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                       num_blocks, max_blocks_per_seq, max_context_len, split_ctas, window_size};
+  s.nq = queries_per_seq;
   if (int rc = check_decode_shape(s, scale)) return rc;
   for (const void* p : {static_cast<const void*>(out), q, k_cache, v_cache})
     if (!aligned(p, 16)) return PA_ERR_INVALID_ARG;
@@ -318,15 +323,17 @@ int pa_decode_fp8(void* out, const void* q, const uint8_t* k_cache, const uint8_
                   const float* k_scale, const float* v_scale, const int32_t* block_tables,
                   int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                  int num_blocks, float scale, int window_size, int dtype, int split_ctas, void* workspace,
+                  int num_blocks, float scale, int window_size, int queries_per_seq,
+                  int dtype, int split_ctas, void* workspace,
                   size_t workspace_bytes, void* stream) {
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables ||
       !context_lens)
     return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
-  const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+  DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                       num_blocks, max_blocks_per_seq, max_context_len, split_ctas, window_size};
+  s.nq = queries_per_seq;
   if (int rc = check_decode_shape(s, scale)) return rc;
   for (const void* p : {static_cast<const void*>(out), q, static_cast<const void*>(k_cache),
                         static_cast<const void*>(v_cache)})

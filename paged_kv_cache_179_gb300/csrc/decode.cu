@@ -46,6 +46,7 @@
 // bounds are never dereferenced; they set a status bit.  Every mbarrier wait
 // is bounded (kWaitLimit) and reports kStatusTimeout instead of hanging.
 #include <cfloat>
+#include <climits>
 #include <type_traits>
 
 #include "pa_e4m3.cuh"
@@ -149,10 +150,29 @@ struct WarpAcc {
 };
 
 // One 16-token block already in shared memory: K tile at kt, V tile at vt.
-template <int D, bool FP8, bool BF16>
+// The MMA's N = 8 columns are the query rows of one (sequence, kv head):
+// row j is query token i_j = j / G (of n_q; position L - n_q + i_j) and head
+// j % G of the group.  A lane holds columns 2c and 2c+1.  With positions
+// taken relative to the first query's (L - n_q), column j attends relative
+// positions in (i_j - window, i_j] (no lower bound without a window): the
+// causal mask of several query tokens and the sliding window in one test.
+struct ColMask {
+  int ii;        // i_j of the lane's two columns, packed: column 2c + k in byte k
+  int window;    // 0: no lower bound
+  __device__ __forceinline__ bool sees(int e, int k) const {
+    const int i = (ii >> (8 * k)) & 0xff;
+    return e <= i && (window == 0 || e > i - window);
+  }
+};
+
+// GENERAL: a sliding window or several query tokens, masked per column with
+// cm and e (the block's first position relative to the first query's);
+// otherwise one query per sequence over its whole context, where only the
+// rows past n_valid (the context's end) are masked.
+template <int D, bool FP8, bool BF16, bool GENERAL>
 __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf)[D / 16][2],
-                                             uint32_t kt, uint32_t vt, int n_skip, int n_valid,
-                                             float sl2,
+                                             uint32_t kt, uint32_t vt, const ColMask& cm,
+                                             int e, int n_valid, float sl2,
                                              float v_mul, int r, int c) {
   constexpr int ROW = FP8 ? D : 2 * D;
   // ---- S^T = K Q^T : 16 tokens x 8 query heads, k = head_dim
@@ -187,9 +207,18 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
 
   // ---- online softmax on the fragment: this lane holds tokens r, r+8 of heads 2c, 2c+1
   float s0 = acc[0] * sl2, s1 = acc[1] * sl2, s2 = acc[2] * sl2, s3 = acc[3] * sl2;
-  // rows outside [n_skip, n_valid): before a sliding window, or past the context
-  if (r < n_skip || r >= n_valid) s0 = s1 = -INFINITY;
-  if (r + 8 < n_skip || r + 8 >= n_valid) s2 = s3 = -INFINITY;
+  if constexpr (GENERAL) {
+    // token rows r, r+8 sit at e + r, e + r + 8 relative to the first query's
+    // position; column j attends relative positions (i_j - window, i_j]
+    const int e0 = e + r, e1 = e0 + 8;
+    if (!cm.sees(e0, 0)) s0 = -INFINITY;
+    if (!cm.sees(e0, 1)) s1 = -INFINITY;
+    if (!cm.sees(e1, 0)) s2 = -INFINITY;
+    if (!cm.sees(e1, 1)) s3 = -INFINITY;
+  } else {
+    if (r >= n_valid) s0 = s1 = -INFINITY;
+    if (r + 8 >= n_valid) s2 = s3 = -INFINITY;
+  }
   float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
@@ -197,11 +226,16 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
     bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o));
   }
   const float mn0 = fmaxf(st.m0, bm0), mn1 = fmaxf(st.m1, bm1);
-  const float a0 = fast_exp2(st.m0 - mn0), a1 = fast_exp2(st.m1 - mn1);
+  // a column that has seen no token yet (a query before this block, with
+  // several query tokens) keeps max -inf: exponentiate against 0 instead, so
+  // its weights stay 0 rather than NaN
+  const float x0 = GENERAL && mn0 == -INFINITY ? 0.f : mn0;
+  const float x1 = GENERAL && mn1 == -INFINITY ? 0.f : mn1;
+  const float a0 = fast_exp2(st.m0 - x0), a1 = fast_exp2(st.m1 - x1);
   st.m0 = mn0;
   st.m1 = mn1;
-  const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
-  const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
+  const float p0 = fast_exp2(s0 - x0), p1 = fast_exp2(s1 - x1);
+  const float p2 = fast_exp2(s2 - x0), p3 = fast_exp2(s3 - x1);
   st.l0 = st.l0 * a0 + (p0 + p2);
   st.l1 = st.l1 * a1 + (p1 + p3);
 #pragma unroll
@@ -227,14 +261,14 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
       v[2][u] = lds128(vt + tk2 * ROW + (8 * u + r) * 16);
       v[3][u] = lds128(vt + tk3 * ROW + (8 * u + r) * 16);
     }
-    if (n_valid < 16 || n_skip > 0) {   // rows past the context may hold anything, NaN included
+    if (n_valid < 16) {   // rows past the context may hold anything, NaN included
       const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        if (tk0 < n_skip || tk0 >= n_valid) v[0][u] = z;
-        if (tk1 < n_skip || tk1 >= n_valid) v[1][u] = z;
-        if (tk2 < n_skip || tk2 >= n_valid) v[2][u] = z;
-        if (tk3 < n_skip || tk3 >= n_valid) v[3][u] = z;
+        if (tk0 >= n_valid) v[0][u] = z;
+        if (tk1 >= n_valid) v[1][u] = z;
+        if (tk2 >= n_valid) v[2][u] = z;
+        if (tk3 >= n_valid) v[3][u] = z;
       }
     }
 #pragma unroll
@@ -264,12 +298,12 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
       v[2] = lds64(vt + tk2 * ROW + VB * r);
       v[3] = lds64(vt + tk3 * ROW + VB * r);
     }
-    if (n_valid < 16 || n_skip > 0) {
+    if (n_valid < 16) {
       VT z{};
-      if (tk0 < n_skip || tk0 >= n_valid) v[0] = z;
-      if (tk1 < n_skip || tk1 >= n_valid) v[1] = z;
-      if (tk2 < n_skip || tk2 >= n_valid) v[2] = z;
-      if (tk3 < n_skip || tk3 >= n_valid) v[3] = z;
+      if (tk0 >= n_valid) v[0] = z;
+      if (tk1 >= n_valid) v[1] = z;
+      if (tk2 >= n_valid) v[2] = z;
+      if (tk3 >= n_valid) v[3] = z;
     }
 #pragma unroll
     for (int i = 0; i < D / 16; i += 2) {
@@ -360,10 +394,11 @@ __device__ __forceinline__ Chunk next_chunk(const Chunk& x, int64_t hi, const in
 }
 
 // The first block a sequence of L tokens attends: with a sliding window of
-// `window` tokens the blocks before position L - window are skipped.
+// `window` tokens the blocks before the first query's window are skipped.
 // Segments and chunks count blocks from there.
-__device__ __forceinline__ int window_first_block(int L, int window) {
-  return window > 0 && L > window ? (L - window) >> 4 : 0;
+__device__ __forceinline__ int window_first_block(int L, int window, int n_q) {
+  const int first = L - (n_q - 1) - window;   // the first query's window start
+  return window > 0 && first > 0 ? first >> 4 : 0;
 }
 
 // This lane's block id of chunk x (lane t holds block cb0 + t of the
@@ -382,9 +417,12 @@ __device__ __forceinline__ int load_chunk_id(const DecodeArgs& a, const Chunk& x
 template <int D, bool FP8, bool BF16>
 __device__ __forceinline__ float load_query(uint32_t (&qf)[D / 16][2], const DecodeArgs& a, int b,
                                             int h, int r, int c) {
+  // row r: query token r / G, head h*G + r % G; q is [B][n_q][Hq][D]
+  const int G = a.group;
+  const bool live = r < a.n_q * G;
   const uint4* qrow = reinterpret_cast<const uint4*>(
-      static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(b) * a.Hq + h * a.group + r) * D);
-  const bool live = r < a.group;
+      static_cast<const uint16_t*>(a.q) +
+      ((static_cast<int64_t>(b) * a.n_q + r / G) * a.Hq + h * G + r % G) * D);
   if constexpr (!FP8) {
 #pragma unroll
     for (int i = 0; i < D / 32; ++i) {
@@ -442,25 +480,26 @@ __device__ __forceinline__ int64_t piece_row(int w, int k, int g) {
 }
 
 // Write a whole piece's result from the warp's fragments: out = o / l.
+// rows: the output of query row 0 of the (sequence, kv head); off: the
+// offsets of the lane's columns 2c, 2c+1 from it (-1: not a query row).
 template <int D, bool FP8, bool BF16>
-__device__ __forceinline__ void store_output(const WarpAcc<D>& st, uint16_t* rows, int G, int r,
-                                             int c, float unboost) {
-  const int g0 = 2 * c, g1 = 2 * c + 1;
+__device__ __forceinline__ void store_output(const WarpAcc<D>& st, uint16_t* rows,
+                                             const int (&off)[2], int r, int c, float unboost) {
   const float i0 = st.l0 > 0.f ? unboost / st.l0 : 0.f;
   const float i1 = st.l1 > 0.f ? unboost / st.l1 : 0.f;
 #pragma unroll
   for (int i = 0; i < D / 16; i += 2) {
     const int dl = d_lo<D, FP8>(i, r), dh = d_hi<D, FP8>(i, r);   // d and d+1 with i, i+1
-    if (g0 < G) {
-      *reinterpret_cast<uint32_t*>(rows + g0 * D + dl) =
+    if (off[0] >= 0) {
+      *reinterpret_cast<uint32_t*>(rows + off[0] + dl) =
           pack2<BF16>(st.o[i][0] * i0, st.o[i + 1][0] * i0);
-      *reinterpret_cast<uint32_t*>(rows + g0 * D + dh) =
+      *reinterpret_cast<uint32_t*>(rows + off[0] + dh) =
           pack2<BF16>(st.o[i][2] * i0, st.o[i + 1][2] * i0);
     }
-    if (g1 < G) {
-      *reinterpret_cast<uint32_t*>(rows + g1 * D + dl) =
+    if (off[1] >= 0) {
+      *reinterpret_cast<uint32_t*>(rows + off[1] + dl) =
           pack2<BF16>(st.o[i][1] * i1, st.o[i + 1][1] * i1);
-      *reinterpret_cast<uint32_t*>(rows + g1 * D + dh) =
+      *reinterpret_cast<uint32_t*>(rows + off[1] + dh) =
           pack2<BF16>(st.o[i][3] * i1, st.o[i + 1][3] * i1);
     }
   }
@@ -476,13 +515,13 @@ __device__ __forceinline__ void store_partial(const WarpAcc<D>& st, const Decode
 #pragma unroll
   for (int i = 0; i < D / 16; i += 2) {
     const int dl = d_lo<D, FP8>(i, r), dh = d_hi<D, FP8>(i, r);
-    if (g0 < a.group) {
+    if (g0 < a.n_q * a.group) {
       __stcg(reinterpret_cast<float2*>(r0 + dl),
              make_float2(st.o[i][0] * unboost, st.o[i + 1][0] * unboost));
       __stcg(reinterpret_cast<float2*>(r0 + dh),
              make_float2(st.o[i][2] * unboost, st.o[i + 1][2] * unboost));
     }
-    if (g1 < a.group) {
+    if (g1 < a.n_q * a.group) {
       __stcg(reinterpret_cast<float2*>(r1 + dl),
              make_float2(st.o[i][1] * unboost, st.o[i + 1][1] * unboost));
       __stcg(reinterpret_cast<float2*>(r1 + dh),
@@ -490,9 +529,9 @@ __device__ __forceinline__ void store_partial(const WarpAcc<D>& st, const Decode
     }
   }
   if (r == 0) {
-    if (g0 < a.group) __stcg(reinterpret_cast<float2*>(a.ws_ml + piece_row(w, slot, g0) * 2),
+    if (g0 < a.n_q * a.group) __stcg(reinterpret_cast<float2*>(a.ws_ml + piece_row(w, slot, g0) * 2),
                              make_float2(st.m0, st.l0));
-    if (g1 < a.group) __stcg(reinterpret_cast<float2*>(a.ws_ml + piece_row(w, slot, g1) * 2),
+    if (g1 < a.n_q * a.group) __stcg(reinterpret_cast<float2*>(a.ws_ml + piece_row(w, slot, g1) * 2),
                              make_float2(st.m1, st.l1));
   }
 }
@@ -585,7 +624,7 @@ __device__ __forceinline__ NewRow load_new_row(const DecodeArgs& a, const Chunk&
   return n;
 }
 
-template <int D, bool FP8, bool BF16, int STAGES, bool APPEND, int CTAS>
+template <int D, bool FP8, bool BF16, int STAGES, bool APPEND, bool GENERAL, int CTAS>
 __global__ void __launch_bounds__(kThreads, CTAS)
 decode_kernel(const DecodeArgs a) {
   using TL = Tile<D, FP8, STAGES>;
@@ -593,6 +632,14 @@ decode_kernel(const DecodeArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, c = lane & 3;
   const int B = a.B, Hkv = a.Hkv, Hq = a.Hq, G = a.group;
+  // this lane's two columns (query rows 2c, 2c+1): the query token of each
+  // (a dead column, past the n_q * G rows, sees what the last query sees)
+  int cm_ii = 0;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int j = 2 * c + k;
+    cm_ii |= (j < a.n_q * G ? j / G : a.n_q - 1) << (8 * k);
+  }
   const Layout lay = make_layout(TL::RING, STAGES, B);
   int* pf = reinterpret_cast<int*>(smem + lay.pf);
   int* len = reinterpret_cast<int*>(smem + lay.len);
@@ -608,7 +655,7 @@ decode_kernel(const DecodeArgs a) {
       const int L = a.context_lens[b];
       const bool ok = L >= 0 && L <= a.max_context_len && L <= a.mbs * 16;
       len[b] = ok ? L : -1;
-      sum += ok ? (((L + 15) >> 4) - window_first_block(L, a.window)) * Hkv : 0;
+      sum += ok ? (((L + 15) >> 4) - window_first_block(L, a.window, a.n_q)) * Hkv : 0;
     }
     int inc = sum;
 #pragma unroll
@@ -622,7 +669,7 @@ decode_kernel(const DecodeArgs a) {
     for (int w = 0; w < warp; ++w) ex += misc[w];
     for (int b = b0; b < b1; ++b) {
       pf[b] = ex;
-      ex += len[b] > 0 ? (((len[b] + 15) >> 4) - window_first_block(len[b], a.window)) * Hkv : 0;
+      ex += len[b] > 0 ? (((len[b] + 15) >> 4) - window_first_block(len[b], a.window, a.n_q)) * Hkv : 0;
     }
     if (tid == kThreads - 1) pf[B] = ex;
     __syncthreads();
@@ -635,8 +682,8 @@ decode_kernel(const DecodeArgs a) {
     const int L = len[b];
     if (L > 0) continue;
     if (L < 0 && tid == 0) atomicOr(a.status, kStatusBadLen);
-    uint16_t* o = static_cast<uint16_t*>(a.out) + static_cast<int64_t>(b) * Hq * D;
-    for (int i = tid; i < Hq * D; i += kThreads) o[i] = 0;   // +0.0 in f16 and bf16
+    uint16_t* o = static_cast<uint16_t*>(a.out) + static_cast<int64_t>(b) * a.n_q * Hq * D;
+    for (int i = tid; i < a.n_q * Hq * D; i += kThreads) o[i] = 0;   // +0.0 in f16 and bf16
   }
 
   // The merge launch reads the prefix sums (every CTA computed the same),
@@ -668,7 +715,8 @@ decode_kernel(const DecodeArgs a) {
   Chunk ch1 = next_chunk(ch0, hi, pf, B, Hkv);
   Chunk ch2 = next_chunk(ch1, hi, pf, B, Hkv);
   auto chunk_id = [&](const Chunk& x) {
-    return load_chunk_id(a, x, x.nb > 0 ? window_first_block(len[x.b], a.window) : 0, lane);
+    const int fb = GENERAL && x.nb > 0 ? window_first_block(len[x.b], a.window, a.n_q) : 0;
+    return load_chunk_id(a, x, fb, lane);
   };
   int id0 = chunk_id(ch0);
   int id1 = chunk_id(ch1);
@@ -754,7 +802,7 @@ decode_kernel(const DecodeArgs a) {
 
   while (ch0.nb > 0) {
     const int L = len[ch0.b];
-    const int fb0 = window_first_block(L, a.window);
+    const int fb0 = GENERAL ? window_first_block(L, a.window, a.n_q) : 0;
     // fused append: the new row, when this chunk ends its sequence.  Loaded
     // here rather than a chunk ahead: held across the loop it would cost the
     // E4M3 variant its third CTA per SM (or spills).
@@ -820,9 +868,9 @@ decode_kernel(const DecodeArgs a) {
       if (id >= 0 && id < a.num_blocks) {
         const int blk0 = (fb0 + ch0.cb0 + t) * 16;   // the block's first position
         const int n_valid = min(16, L - blk0);
-        const int n_skip = a.window > 0 ? max(0, L - a.window - blk0) : 0;
-        attend_block<D, FP8, BF16>(st, qf, ring + s * TL::SLOT, ring + s * TL::SLOT + TL::BYTES,
-                                   n_skip, n_valid, sl2, v_mul, r, c);
+        attend_block<D, FP8, BF16, GENERAL>(
+            st, qf, ring + s * TL::SLOT, ring + s * TL::SLOT + TL::BYTES,
+            ColMask{cm_ii, a.window}, blk0 - (L - a.n_q), n_valid, sl2, v_mul, r, c);
       }
       __syncwarp();
       ++computed;
@@ -841,8 +889,14 @@ decode_kernel(const DecodeArgs a) {
       }
       if (s0 >= lo && s0 + nbk <= hi) {
         uint16_t* rows = static_cast<uint16_t*>(a.out) +
-                         (static_cast<int64_t>(ch0.b) * Hq + ch0.h * G) * D;
-        store_output<D, FP8, BF16>(st, rows, G, r, c, unboost);
+                         (static_cast<int64_t>(ch0.b) * a.n_q * Hq + ch0.h * G) * D;
+        int col_off[2];   // output offsets of the lane's columns from query row 0
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int j = 2 * c + k;
+          col_off[k] = j < a.n_q * G ? ((j / G) * Hq + j % G) * D : -1;
+        }
+        store_output<D, FP8, BF16>(st, rows, col_off, r, c, unboost);
       } else if (a.ws_acc == nullptr) {
         if (lane == 0) atomicOr(a.status, kStatusNoWorkspace);   // never written through null
       } else {
@@ -930,8 +984,8 @@ merge_kernel(const DecodeArgs a) {
   if (w0 == w1) return;                         // attended whole
   const int first_slot = s0 > worker_lo(w0, W, NW) ? 1 : 0;   // the segment is w0's last piece
   constexpr int COLS = D / 4;
-  const int tid = threadIdx.x, g = tid / COLS, d4 = tid - g * COLS;
-  if (g >= G) return;
+  const int tid = threadIdx.x, g = tid / COLS, d4 = tid - g * COLS;   // g: the query row
+  if (g >= a.n_q * G) return;
   float M = -INFINITY, S = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const int np = w1 - w0 + 1;
@@ -974,7 +1028,8 @@ merge_kernel(const DecodeArgs a) {
   uint2 o;
   o.x = pack2<BF16>(acc.x * inv, acc.y * inv);
   o.y = pack2<BF16>(acc.z * inv, acc.w * inv);
-  uint16_t* row = static_cast<uint16_t*>(a.out) + (static_cast<int64_t>(b) * a.Hq + h * G + g) * D;
+  uint16_t* row = static_cast<uint16_t*>(a.out) +
+                  ((static_cast<int64_t>(b) * a.n_q + g / G) * a.Hq + h * G + g % G) * D;
   *reinterpret_cast<uint2*>(row + 4 * d4) = o;
 }
 
@@ -995,11 +1050,11 @@ cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, merge_kernel<D, BF16>, a);
 }
 
-template <int D, bool FP8, bool BF16, int STAGES, bool APPEND, int CTAS>
+template <int D, bool FP8, bool BF16, int STAGES, bool APPEND, bool GENERAL, int CTAS>
 cudaError_t launch_one(const DecodeArgs& a, cudaStream_t s) {
   using TL = Tile<D, FP8, STAGES>;
   const Layout lay = make_layout(TL::RING, STAGES, a.B);
-  auto* kern = decode_kernel<D, FP8, BF16, STAGES, APPEND, CTAS>;
+  auto* kern = decode_kernel<D, FP8, BF16, STAGES, APPEND, GENERAL, CTAS>;
   static thread_local int last_smem[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1043,8 +1098,12 @@ cudaError_t launch_dtype(const DecodeArgs& a, cudaStream_t s) {
   constexpr int STAGES_R = ring_kb(FP8) * 1024 / (kWarps * SLOT);
   constexpr int STAGES = STAGES_R < 2 ? 2 : STAGES_R;
   constexpr int CTAS = ctas_per_sm(FP8);
-  if (a.k_new != nullptr) return launch_one<D, FP8, BF16, STAGES, true, CTAS>(a, s);
-  return launch_one<D, FP8, BF16, STAGES, false, CTAS>(a, s);
+  const bool general = a.window > 0 || a.n_q > 1;
+  if (a.k_new != nullptr)
+    return general ? launch_one<D, FP8, BF16, STAGES, true, true, CTAS>(a, s)
+                   : launch_one<D, FP8, BF16, STAGES, true, false, CTAS>(a, s);
+  return general ? launch_one<D, FP8, BF16, STAGES, false, true, CTAS>(a, s)
+                 : launch_one<D, FP8, BF16, STAGES, false, false, CTAS>(a, s);
 }
 
 }  // namespace

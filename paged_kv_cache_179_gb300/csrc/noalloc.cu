@@ -56,7 +56,8 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
                                  int max_blocks_per_seq, const int32_t* context_lens,
                                  int max_context_len, int num_seqs, int num_q_heads,
                                  int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                                 float scale, int window_size, int dtype, int split_ctas, void* stream) {
+                                 float scale, int window_size, int queries_per_seq,
+                                 int dtype, int split_ctas, void* stream) {
   using namespace pa;
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
@@ -65,7 +66,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
     return PA_ERR_INVALID_ARG;
   if (num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 || split_ctas < 0 ||
-      window_size < 0)
+      window_size < 0 || queries_per_seq < 1)
     return PA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(max_context_len) >
       static_cast<int64_t>(max_blocks_per_seq) * block_size)
@@ -73,7 +74,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (block_size != 16) return PA_ERR_UNSUPPORTED;
-  if (num_q_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
+  if (num_q_heads / num_kv_heads * queries_per_seq > 8) return PA_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
   for (const void* p : {static_cast<const void*>(out), q, k_cache, v_cache})
     if (!aligned_to(p, 16)) return PA_ERR_INVALID_ARG;
@@ -101,9 +102,10 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   a.max_context_len = max_context_len;
   a.split_ctas = splits;
   a.window = window_size;
+  a.n_q = queries_per_seq;
   a.scale_log2 = scale * 1.4426950408889634f;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t row = static_cast<size_t>(num_q_heads) * head_dim * 2;
+  const size_t row = static_cast<size_t>(queries_per_seq) * num_q_heads * head_dim * 2;
   for (int b0 = 0; b0 < num_seqs; b0 += kMaxBatchPerLaunch) {
     DecodeArgs c = a;
     c.B = num_seqs - b0 < kMaxBatchPerLaunch ? num_seqs - b0 : kMaxBatchPerLaunch;

@@ -41,6 +41,7 @@ struct DecodeArgs {
   int max_context_len;
   int split_ctas;               // CTAs the batch's blocks are divided among
   int window;                   // sliding window in tokens (0: the whole context)
+  int n_q;                      // query tokens per sequence (n_q * group <= 8)
   float scale_log2;             // softmax scale * log2(e)
 };
 

@@ -45,13 +45,13 @@ def test_library_exports_every_declared_symbol(lib):
 
 def _decode(lib, **kw):
     a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, mbs=8, cl=FAKE, max_ctx=128, B=2, Hq=8,
-             Hkv=2, D=64, bs=16, NB=32, scale=0.125, window=0, dtype=0, splits=8, ws=FAKE,
-             ws_bytes=1 << 20)
+             Hkv=2, D=64, bs=16, NB=32, scale=0.125, window=0, nq=1, dtype=0, splits=8,
+             ws=FAKE, ws_bytes=1 << 20)
     a.update(kw)
     return lib.pa_decode(a["out"], a["q"], a["k"], a["v"], a["bt"], a["mbs"], a["cl"],
                          a["max_ctx"], a["B"], a["Hq"], a["Hkv"], a["D"], a["bs"], a["NB"],
-                         a["scale"], a["window"], a["dtype"], a["splits"], a["ws"], a["ws_bytes"],
-                         None)
+                         a["scale"], a["window"], a["nq"], a["dtype"], a["splits"], a["ws"],
+                         a["ws_bytes"], None)
 
 
 def test_decode_argument_errors(lib):
@@ -62,6 +62,8 @@ def test_decode_argument_errors(lib):
     assert _decode(lib, scale=float("nan")) == _abi.PA_ERR_INVALID_ARG
     assert _decode(lib, dtype=3) == _abi.PA_ERR_INVALID_ARG
     assert _decode(lib, window=-1) == _abi.PA_ERR_INVALID_ARG
+    assert _decode(lib, nq=0) == _abi.PA_ERR_INVALID_ARG
+    assert _decode(lib, nq=5) == _abi.PA_ERR_UNSUPPORTED             # 5 tokens x group 4 > 8
     assert _decode(lib, q=MISALIGNED) == _abi.PA_ERR_INVALID_ARG
     assert _decode(lib, D=96) == _abi.PA_ERR_UNSUPPORTED
     assert _decode(lib, bs=32, mbs=4) == _abi.PA_ERR_UNSUPPORTED
