@@ -446,6 +446,72 @@ def run_copy_blocks(args, dev):
     }
 
 
+def run_multiquery(args, dev):
+    """``--op multiquery``: pa_decode with ``--queries`` n query tokens per
+    sequence (the verification pass of speculative decoding: the draft
+    tokens' K/V are already in the cache), on the config's batch with a
+    seeded [B][n][Hq][D] q.  Every KV block is read once for all n queries."""
+    from paged_kv_cache_179_gb300 import _abi
+    from paged_kv_cache_179_gb300 import workloads as W
+    from paged_kv_cache_179_gb300.step import DecodeStep
+
+    w = W.make_workload(args.config, seed=args.seed, device=dev)
+    if w.kv == "fp8":
+        raise SystemExit("--op multiquery runs on 16-bit pools")
+    n = args.queries
+    if n * w.group > 8:
+        raise SystemExit(f"{n} queries x group {w.group} exceed the 8 query rows of a launch")
+    lens = w.context_lens.cpu().numpy()
+    g = torch.Generator(device=dev).manual_seed(args.seed + 17)
+    q = torch.randn(w.B, n, w.Hq, w.D, generator=g, device=dev).to(w.q.dtype)
+    out = torch.empty_like(q)
+    step = DecodeStep(k_cache=w.k_cache, v_cache=w.v_cache, block_tables=w.block_tables,
+                      context_lens=w.context_lens, max_context_len=w.max_context_len,
+                      scale=w.scale, num_q_heads=w.Hq, split_ctas=args.splits, window=args.window)
+    ab = algorithmic_bytes(w, lens, args.window)
+    moved = ab["kv"] + ab["meta"] + n * ab["q_out"]
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
+    flush_buf = torch.ones(max(2 * l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
+    flush = ab["kv"] < 3 * l2
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        step.decode(q, out)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for a, b in ev:
+        if flush:
+            flush_buf.sum(dtype=torch.int64)
+        a.record(stream)
+        step.decode(q, out)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    rc, bits = _abi.pa_get_status(dev)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} bits {bits}")
+    ms = [a.elapsed_time(b) for a, b in ev]
+    t = statistics.mean(ms) / 1e3
+    achieved = moved / t / 1e9
+    peak, peak_kind = measured_peaks()
+    att = int(attended(lens, args.window).sum())
+    return {
+        "metric": "multi-token paged decode: attended (query token, KV token) pairs/s",
+        "impl": "ours", "value": round(att * n / t, 1), "unit": "pairs/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 5),
+        "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": describe(w, att), "queries_per_seq": n,
+                   "step": "pa_decode with n query tokens per sequence (decode and merge launches)",
+                   "split_ctas": step.split_ctas,
+                   "l2": "flushed by reading a 2x-L2 buffer" if flush else "not flushed",
+                   **({"window": args.window} if args.window else {})},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "decode_kernel (general masks), then merge_kernel",
+                     "bytes_per_launch": moved, "peak_source": peak_kind},
+        "decode_us": {"mean": round(t * 1e6, 2), "min": round(min(ms) * 1e3, 2)},
+        "gpu_launches": 2 * args.steps,
+    }
+
+
 def describe_l2(mode, kv_bytes, l2):
     if mode == "none":
         return (f"not flushed: inputs larger than L2 ({kv_bytes / 1e6:.0f} MB of K/V per step vs "
@@ -567,8 +633,10 @@ def main(argv=None):
                          "(fused for 16-bit pools, two-launch for E4M3)")
     ap.add_argument("--prime-ms", type=float, default=0.0,
                     help="GPU sleep queued ahead of the timed steps so the host runs ahead")
-    ap.add_argument("--op", choices=["step", "copy_blocks"], default="step",
-                    help="what to time: the decode step (default) or pa_copy_blocks alone")
+    ap.add_argument("--op", choices=["step", "copy_blocks", "multiquery"], default="step",
+                    help="what to time: the decode step (default), pa_copy_blocks alone, or a "
+                         "decode with --queries query tokens per sequence")
+    ap.add_argument("--queries", type=int, default=2)
     ap.add_argument("--copy-pairs", type=int, default=8192)
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window in tokens (0: each sequence attends its whole context)")
@@ -593,8 +661,12 @@ def main(argv=None):
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=dev)
     try:
-        line = run_copy_blocks(args, dev) if args.op == "copy_blocks" else \
-            run_ours(args, rank, world, dev)
+        if args.op == "copy_blocks":
+            line = run_copy_blocks(args, dev)
+        elif args.op == "multiquery":
+            line = run_multiquery(args, dev)
+        else:
+            line = run_ours(args, rank, world, dev)
         if rank == 0:
             print(json.dumps(line), flush=True)
     finally:
