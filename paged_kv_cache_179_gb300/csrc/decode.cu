@@ -73,6 +73,12 @@ __device__ __forceinline__ unsigned long long pa_smid() {
   asm volatile("mov.u32 %0, %%smid;" : "=r"(v_));
   return v_;
 }
+__device__ unsigned long long g_pa_trace_merge[16384 * 4];   // per merge CTA: entry, wait done, end, pieces
+extern "C" int pa_trace_read_merge(unsigned long long* host, int n_ctas) {
+  const size_t n = static_cast<size_t>(n_ctas < 16384 ? n_ctas : 16384) * 4;
+  return cudaMemcpyFromSymbol(host, g_pa_trace_merge, sizeof(unsigned long long) * n) ==
+                 cudaSuccess ? 0 : 4;
+}
 extern "C" int pa_trace_read(unsigned long long* host, int n_workers) {
   const size_t n = static_cast<size_t>(n_workers < 16384 ? n_workers : 16384) * 8;
   return cudaMemcpyFromSymbol(host, g_pa_trace, sizeof(unsigned long long) * n) == cudaSuccess
@@ -971,7 +977,14 @@ constexpr int kMergeBatch = PA_MERGE_BATCH;
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kMergeThreads)
 merge_kernel(const DecodeArgs a) {
+  PA_TRACE_ONLY(const unsigned long long t_in = pa_now());
   griddep_wait();
+  PA_TRACE_ONLY(if (threadIdx.x == 0 && blockIdx.x < 16384) {
+    g_pa_trace_merge[blockIdx.x * 4 + 0] = t_in;
+    g_pa_trace_merge[blockIdx.x * 4 + 1] = pa_now();
+    g_pa_trace_merge[blockIdx.x * 4 + 2] = 0;
+    g_pa_trace_merge[blockIdx.x * 4 + 3] = 0;
+  });
   const int Hkv = a.Hkv, G = a.group;
   const int b = blockIdx.x / Hkv, h = blockIdx.x - b * Hkv;
   const int* pf = a.seg_prefix;
@@ -1024,6 +1037,10 @@ merge_kernel(const DecodeArgs a) {
     }
     M = mb;
   }
+  PA_TRACE_ONLY(if (threadIdx.x == 0 && blockIdx.x < 16384) {
+    g_pa_trace_merge[blockIdx.x * 4 + 2] = pa_now();
+    g_pa_trace_merge[blockIdx.x * 4 + 3] = np;
+  });
   const float inv = S > 0.f ? 1.f / S : 0.f;
   uint2 o;
   o.x = pack2<BF16>(acc.x * inv, acc.y * inv);
@@ -1039,7 +1056,10 @@ template <int D, bool BF16>
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.B) * static_cast<unsigned>(a.Hkv));
-  cfg.blockDim = dim3(kMergeThreads);
+  // one thread per (query row, 4 output columns), rounded up to whole warps:
+  // no idle warps, so more CTAs fit an SM at once
+  const int threads = (a.n_q * a.group * (D / 4) + 31) & ~31;
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
