@@ -126,3 +126,46 @@ class DecodeStep:
              fused=fused)
         host_out.copy_(dev_out, non_blocking=True)
         return h2d, host_out.numel() * host_out.element_size()
+
+    def run_from_staging(self, staging: "StepStaging", host_out, dev_out, fused=None):
+        """As ``run_from_host`` with the inputs packed in one ``StepStaging``:
+        one host-to-device copy for all of them (this step must have been
+        built with the staging's device block_tables and context_lens).
+        Returns (h2d bytes, d2h bytes)."""
+        h2d = staging.upload()
+        d = staging.dev
+        self(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], dev_out, fused=fused)
+        host_out.copy_(dev_out, non_blocking=True)
+        return h2d, host_out.numel() * host_out.element_size()
+
+
+class StepStaging:
+    """A decode step's per-step inputs packed back to back (each at a 256-byte
+    aligned offset) in one pinned host buffer and one device buffer of the
+    same layout.  ``host[name]`` / ``dev[name]`` are views of the two; fill
+    the host views, then ``upload()`` moves everything in one copy.  A
+    serving loop that uploads its step inputs as one block pays one copy's
+    latency instead of one per tensor."""
+
+    def __init__(self, specs: dict, device):
+        """specs: name -> (shape, torch dtype)."""
+        layout, o = {}, 0
+        for name, (shape, dtype) in specs.items():
+            n = 1
+            for x in shape:
+                n *= int(x)
+            nbytes = n * torch.empty((), dtype=dtype).element_size()
+            layout[name] = (o, tuple(int(x) for x in shape), dtype, nbytes)
+            o = (o + nbytes + 255) // 256 * 256
+        self.nbytes = max(o, 256)
+        self.host_buf = torch.empty(self.nbytes, dtype=torch.uint8).pin_memory()
+        self.dev_buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        self.host, self.dev = {}, {}
+        for name, (off, shape, dtype, nbytes) in layout.items():
+            self.host[name] = self.host_buf[off:off + nbytes].view(dtype).view(shape)
+            self.dev[name] = self.dev_buf[off:off + nbytes].view(dtype).view(shape)
+
+    def upload(self) -> int:
+        """One asynchronous host-to-device copy on the current stream; the bytes copied."""
+        self.dev_buf.copy_(self.host_buf, non_blocking=True)
+        return self.nbytes

@@ -124,3 +124,33 @@ def test_fused_step_fp8_matches_oracle(seed, B, Hq, Hkv, D, lens, splits, dtype)
     for got, want in zip(dev, (kc, vc, ks, vs)):
         assert np.array_equal(got.cpu().numpy().view(np.uint8), want.view(np.uint8))
     assert np.abs(out.float().cpu().numpy() - ref).max() <= TOL["fp8"]
+
+
+def test_run_from_staging_matches_device_call():
+    """The end-to-end form: inputs packed in one pinned buffer, one upload,
+    the output copied back; the same bytes as the step on device inputs."""
+    from paged_kv_cache_179_gb300.step import StepStaging
+    w = W.make_workload("qwen2_5_1_5b", seed=7)
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    staging = StepStaging({k: (getattr(w, k).shape, getattr(w, k).dtype) for k in names}, "cuda")
+    for k in names:
+        staging.host[k].copy_(getattr(w, k))
+    kc, vc = w.k_cache.cuda(), w.v_cache.cuda()
+    k2, v2 = kc.clone(), vc.clone()
+    step = DecodeStep(k_cache=kc, v_cache=vc, block_tables=staging.dev["block_tables"],
+                      context_lens=staging.dev["context_lens"], max_context_len=w.max_context_len,
+                      scale=w.scale, num_q_heads=w.Hq)
+    host_out = torch.empty(w.q.shape, dtype=w.q.dtype).pin_memory()
+    h2d, d2h = step.run_from_staging(staging, host_out, torch.empty_like(w.q, device="cuda"))
+    torch.cuda.synchronize()
+    assert h2d >= sum(getattr(w, k).numel() * getattr(w, k).element_size() for k in names)
+    assert d2h == w.q.numel() * 2
+    to_cuda(w)
+    ref_step = DecodeStep(k_cache=k2, v_cache=v2, block_tables=w.block_tables,
+                          context_lens=w.context_lens, max_context_len=w.max_context_len,
+                          scale=w.scale, num_q_heads=w.Hq)
+    ref = torch.empty_like(w.q)
+    ref_step(w.q, w.k_new, w.v_new, w.slot_mapping, ref)
+    assert _abi.pa_get_status() == (0, 0)
+    assert torch.equal(host_out.view(torch.int16), ref.cpu().view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), k2.view(torch.int16))
