@@ -169,3 +169,81 @@ class StepStaging:
         """One asynchronous host-to-device copy on the current stream; the bytes copied."""
         self.dev_buf.copy_(self.host_buf, non_blocking=True)
         return self.nbytes
+
+
+class StepPipeline:
+    """Decode steps whose host<->device copies overlap the previous step's
+    attention.  ``depth`` stagings (and output buffers) are used in turn:
+    uploads run on one copy stream and read-backs on another (on one stream
+    the next upload would queue behind the read-back that waits for the
+    current step), the steps in order on a compute stream of the pipeline's
+    own, with events keeping a staging from being re-uploaded while a step
+    still reads it and an output buffer from being rewritten before it is
+    read back.
+    Each submit first orders the compute stream after the caller's stream;
+    ``finish`` orders the caller's stream after everything submitted.
+
+    ``make_step(staging)`` builds the DecodeStep for one staging (bound to its
+    device block_tables and context_lens; the pools are shared).  The caller
+    fills ``stagings[k].host`` before ``submit`` uses slot k (``slot()`` says
+    which; ``wait_slot_free()`` waits until its last upload has finished)."""
+
+    def __init__(self, make_step, specs: dict, out_shape, out_dtype, device, depth: int = 2):
+        self.depth = depth
+        self.copy = torch.cuda.Stream(device)       # uploads
+        self.back = torch.cuda.Stream(device)       # read-backs
+        self.compute = torch.cuda.Stream(device)
+        self.stagings = [StepStaging(specs, device) for _ in range(depth)]
+        self.steps = [make_step(s) for s in self.stagings]
+        self.dev_out = [torch.empty(out_shape, dtype=out_dtype, device=device)
+                        for _ in range(depth)]
+        self.host_out = [torch.empty(out_shape, dtype=out_dtype).pin_memory()
+                         for _ in range(depth)]
+        self.uploaded = [None] * depth     # upload of the slot's latest step done
+        self.stepped = [None] * depth      # the slot's latest step done
+        self.read_back = [None] * depth    # the slot's latest output copied to the host
+        self.n = 0
+
+    def slot(self) -> int:
+        return self.n % self.depth
+
+    def wait_slot_free(self):
+        """Block the host until the next slot's host buffer may be refilled."""
+        k = self.slot()
+        if self.uploaded[k] is not None:
+            self.uploaded[k].synchronize()
+
+    def submit(self, fused=None):
+        """Upload the next slot's inputs, run its step, read its output back.
+        Returns (slot, h2d bytes, d2h bytes); ``host_out[slot]`` holds the
+        output once ``read_back[slot]`` has completed."""
+        k = self.slot()
+        cur = self.compute
+        cur.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(self.copy):
+            if self.stepped[k] is not None:
+                self.copy.wait_event(self.stepped[k])     # the slot's last step is done with it
+            h2d = self.stagings[k].upload()
+            self.uploaded[k] = torch.cuda.Event()
+            self.uploaded[k].record(self.copy)
+        cur.wait_event(self.uploaded[k])
+        if self.read_back[k] is not None:
+            cur.wait_event(self.read_back[k])             # the slot's last output was read
+        d = self.stagings[k].dev
+        with torch.cuda.stream(cur):
+            self.steps[k](d["q"], d["k_new"], d["v_new"], d["slot_mapping"], self.dev_out[k],
+                          fused=fused)
+        self.stepped[k] = torch.cuda.Event()
+        self.stepped[k].record(cur)
+        with torch.cuda.stream(self.back):
+            self.back.wait_event(self.stepped[k])
+            self.host_out[k].copy_(self.dev_out[k], non_blocking=True)
+            self.read_back[k] = torch.cuda.Event()
+            self.read_back[k].record(self.back)
+        self.n += 1
+        return k, h2d, self.host_out[k].numel() * self.host_out[k].element_size()
+
+    def finish(self):
+        """Make the caller's stream wait for every step and copy submitted so far."""
+        for st in (self.compute, self.copy, self.back):
+            torch.cuda.current_stream().wait_stream(st)

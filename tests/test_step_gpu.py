@@ -154,3 +154,47 @@ def test_run_from_staging_matches_device_call():
     assert _abi.pa_get_status() == (0, 0)
     assert torch.equal(host_out.view(torch.int16), ref.cpu().view(torch.int16))
     assert torch.equal(kc.view(torch.int16), k2.view(torch.int16))
+
+
+def test_step_pipeline_overlapped_copies_match_direct_calls():
+    """StepPipeline: two slots with different queries, five steps submitted
+    back to back; every read-back equals the step called directly on the
+    same inputs (the appended rows are the same each step)."""
+    from paged_kv_cache_179_gb300.step import StepPipeline
+    w = W.make_workload("qwen2_5_1_5b", seed=8)
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    specs = {k: (getattr(w, k).shape, getattr(w, k).dtype) for k in names}
+    kc, vc = w.k_cache.cuda(), w.v_cache.cuda()
+    k2, v2 = kc.clone(), vc.clone()
+
+    def make_step(st):
+        return DecodeStep(k_cache=kc, v_cache=vc, block_tables=st.dev["block_tables"],
+                          context_lens=st.dev["context_lens"], max_context_len=w.max_context_len,
+                          scale=w.scale, num_q_heads=w.Hq)
+    pipe = StepPipeline(make_step, specs, w.q.shape, w.q.dtype, "cuda")
+    g = torch.Generator().manual_seed(1)
+    qs = [torch.randn(w.q.shape, generator=g).to(w.q.dtype) for _ in range(2)]
+    for k, st in enumerate(pipe.stagings):
+        for n in names:
+            st.host[n].copy_(qs[k] if n == "q" else getattr(w, n))
+    got = []
+    for _ in range(5):
+        k, _, _ = pipe.submit()
+        pipe.read_back[k].synchronize()
+        got.append((k, pipe.host_out[k].clone()))
+    pipe.finish()
+    torch.cuda.synchronize()
+    to_cuda(w)
+    ref_step = DecodeStep(k_cache=k2, v_cache=v2, block_tables=w.block_tables,
+                          context_lens=w.context_lens, max_context_len=w.max_context_len,
+                          scale=w.scale, num_q_heads=w.Hq)
+    refs = []
+    for k in range(2):
+        r = torch.empty_like(w.q)
+        ref_step(qs[k].cuda(), w.k_new, w.v_new, w.slot_mapping, r)
+        refs.append(r.cpu())
+    assert _abi.pa_get_status() == (0, 0)
+    assert [k for k, _ in got] == [0, 1, 0, 1, 0]
+    for k, out in got:
+        assert torch.equal(out.view(torch.int16), refs[k].view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), k2.view(torch.int16))
