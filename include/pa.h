@@ -206,8 +206,11 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int
  *   chunked decoding): q and out are [num_seqs][n_q][num_q_heads][head_dim],
  *   query i sits at position L - n_q + i (its own token and those before it
  *   are in the cache) and attends causally, positions up to its own (within
- *   its window); a query before position 0 gets a zero output.
- *   n_q * (num_q_heads / num_kv_heads) must be at most 8;
+ *   its window); a query before position 0 gets a zero output.  With
+ *   n_q * (num_q_heads / num_kv_heads) <= 8 the K/V is read once for all
+ *   queries; larger n_q (at most 1024) run as consecutive passes of
+ *   8 / group tokens, each reading the K/V again (pa_decode_noalloc rejects
+ *   them with PA_ERR_UNSUPPORTED);
  *   workspace: at least pa_decode_workspace_size(...) bytes, 256-byte
  *   aligned.
  * Source: rvLLM, CUDA Kernels table, "PagedAttention V2" (block-table

@@ -64,8 +64,8 @@ int check_decode_shape(const DecodeShape& s, float scale) {
   if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
   if (s.D != 64 && s.D != 128) return PA_ERR_UNSUPPORTED;
   if (s.bs != 16) return PA_ERR_UNSUPPORTED;
-  if (s.nq < 1) return PA_ERR_INVALID_ARG;
-  if (s.Hq / s.Hkv * s.nq > 8) return PA_ERR_UNSUPPORTED;
+  if (s.nq < 1 || s.nq > 1024) return PA_ERR_INVALID_ARG;
+  if (s.Hq / s.Hkv > 8) return PA_ERR_UNSUPPORTED;
   if (s.B > 65535 || s.Hkv > 65535) return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
@@ -113,6 +113,8 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
   a.split_ctas = s.splits;
   a.window = s.window;
   a.n_q = s.nq;
+  a.q_tokens = s.nq;
+  a.q_first = 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.k_pool_w = ap.k_pool;
   a.v_pool_w = ap.v_pool;
@@ -135,8 +137,17 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
       c.slots = ap.slots + b0;
     }
     decode_workspace_split(c, ws);
-    if (cudaError_t e = launch_decode(c, fp8, bf16, static_cast<cudaStream_t>(stream)))
-      return cuda_status(e);
+    // One launch pair serves up to 8 query rows per (sequence, kv head):
+    // n_q tokens of a group of G heads fit when n_q * G <= 8 and the K/V is
+    // read once for all of them; more tokens run as consecutive passes of
+    // 8 / G tokens each, every pass reading the K/V again.
+    const int per_pass = s.nq * c.group <= 8 ? s.nq : 8 / c.group;
+    for (int t0 = 0; t0 < s.nq; t0 += per_pass) {
+      c.q_first = t0;
+      c.n_q = s.nq - t0 < per_pass ? s.nq - t0 : per_pass;
+      if (cudaError_t e = launch_decode(c, fp8, bf16, static_cast<cudaStream_t>(stream)))
+        return cuda_status(e);
+    }
   }
   return PA_OK;
 }

@@ -423,12 +423,12 @@ __device__ __forceinline__ int load_chunk_id(const DecodeArgs& a, const Chunk& x
 template <int D, bool FP8, bool BF16>
 __device__ __forceinline__ float load_query(uint32_t (&qf)[D / 16][2], const DecodeArgs& a, int b,
                                             int h, int r, int c) {
-  // row r: query token r / G, head h*G + r % G; q is [B][n_q][Hq][D]
+  // row r: query token q_first + r / G, head h*G + r % G; q is [B][q_tokens][Hq][D]
   const int G = a.group;
   const bool live = r < a.n_q * G;
   const uint4* qrow = reinterpret_cast<const uint4*>(
       static_cast<const uint16_t*>(a.q) +
-      ((static_cast<int64_t>(b) * a.n_q + r / G) * a.Hq + h * G + r % G) * D);
+      ((static_cast<int64_t>(b) * a.q_tokens + a.q_first + r / G) * a.Hq + h * G + r % G) * D);
   if constexpr (!FP8) {
 #pragma unroll
     for (int i = 0; i < D / 32; ++i) {
@@ -657,10 +657,14 @@ decode_kernel(const DecodeArgs a) {
     const int per = (B + kThreads - 1) / kThreads;
     const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
     int sum = 0;
+    // a launch serving query tokens q_first .. q_first+n_q-1 of q_tokens sees
+    // the cache up to its last query's position
+    const int len_sub = a.q_tokens - a.q_first - a.n_q;
     for (int b = b0; b < b1; ++b) {
-      const int L = a.context_lens[b];
-      const bool ok = L >= 0 && L <= a.max_context_len && L <= a.mbs * 16;
-      len[b] = ok ? L : -1;
+      const int raw = a.context_lens[b];
+      const bool ok = raw >= 0 && raw <= a.max_context_len && raw <= a.mbs * 16;
+      const int L = ok ? max(0, raw - len_sub) : -1;
+      len[b] = L;
       sum += ok ? (((L + 15) >> 4) - window_first_block(L, a.window, a.n_q)) * Hkv : 0;
     }
     int inc = sum;
@@ -688,7 +692,8 @@ decode_kernel(const DecodeArgs a) {
     const int L = len[b];
     if (L > 0) continue;
     if (L < 0 && tid == 0) atomicOr(a.status, kStatusBadLen);
-    uint16_t* o = static_cast<uint16_t*>(a.out) + static_cast<int64_t>(b) * a.n_q * Hq * D;
+    uint16_t* o = static_cast<uint16_t*>(a.out) +
+                  (static_cast<int64_t>(b) * a.q_tokens + a.q_first) * Hq * D;
     for (int i = tid; i < a.n_q * Hq * D; i += kThreads) o[i] = 0;   // +0.0 in f16 and bf16
   }
 
@@ -895,7 +900,8 @@ decode_kernel(const DecodeArgs a) {
       }
       if (s0 >= lo && s0 + nbk <= hi) {
         uint16_t* rows = static_cast<uint16_t*>(a.out) +
-                         (static_cast<int64_t>(ch0.b) * a.n_q * Hq + ch0.h * G) * D;
+                         ((static_cast<int64_t>(ch0.b) * a.q_tokens + a.q_first) * Hq +
+                          ch0.h * G) * D;
         int col_off[2];   // output offsets of the lane's columns from query row 0
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
@@ -1046,7 +1052,8 @@ merge_kernel(const DecodeArgs a) {
   o.x = pack2<BF16>(acc.x * inv, acc.y * inv);
   o.y = pack2<BF16>(acc.z * inv, acc.w * inv);
   uint16_t* row = static_cast<uint16_t*>(a.out) +
-                  ((static_cast<int64_t>(b) * a.n_q + g / G) * a.Hq + h * G + g % G) * D;
+                  ((static_cast<int64_t>(b) * a.q_tokens + a.q_first + g / G) * a.Hq + h * G +
+                   g % G) * D;
   *reinterpret_cast<uint2*>(row + 4 * d4) = o;
 }
 
@@ -1118,7 +1125,7 @@ cudaError_t launch_dtype(const DecodeArgs& a, cudaStream_t s) {
   constexpr int STAGES_R = ring_kb(FP8) * 1024 / (kWarps * SLOT);
   constexpr int STAGES = STAGES_R < 2 ? 2 : STAGES_R;
   constexpr int CTAS = ctas_per_sm(FP8);
-  const bool general = a.window > 0 || a.n_q > 1;
+  const bool general = a.window > 0 || a.n_q > 1;   // a later pass of 1 token is plain
   if (a.k_new != nullptr)
     return general ? launch_one<D, FP8, BF16, STAGES, true, true, CTAS>(a, s)
                    : launch_one<D, FP8, BF16, STAGES, true, false, CTAS>(a, s);

@@ -103,6 +103,8 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   a.split_ctas = splits;
   a.window = window_size;
   a.n_q = queries_per_seq;
+  a.q_tokens = queries_per_seq;
+  a.q_first = 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t row = static_cast<size_t>(queries_per_seq) * num_q_heads * head_dim * 2;

@@ -41,7 +41,9 @@ struct DecodeArgs {
   int max_context_len;
   int split_ctas;               // CTAs the batch's blocks are divided among
   int window;                   // sliding window in tokens (0: the whole context)
-  int n_q;                      // query tokens per sequence (n_q * group <= 8)
+  int n_q;                      // query tokens this launch serves (n_q * group <= 8)
+  int q_tokens;                 // query tokens per sequence in q and out
+  int q_first;                  // the first of them this launch serves
   float scale_log2;             // softmax scale * log2(e)
 };
 

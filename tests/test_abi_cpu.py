@@ -63,7 +63,7 @@ def test_decode_argument_errors(lib):
     assert _decode(lib, dtype=3) == _abi.PA_ERR_INVALID_ARG
     assert _decode(lib, window=-1) == _abi.PA_ERR_INVALID_ARG
     assert _decode(lib, nq=0) == _abi.PA_ERR_INVALID_ARG
-    assert _decode(lib, nq=5) == _abi.PA_ERR_UNSUPPORTED             # 5 tokens x group 4 > 8
+    assert _decode(lib, nq=1025) == _abi.PA_ERR_INVALID_ARG
     assert _decode(lib, q=MISALIGNED) == _abi.PA_ERR_INVALID_ARG
     assert _decode(lib, D=96) == _abi.PA_ERR_UNSUPPORTED
     assert _decode(lib, bs=32, mbs=4) == _abi.PA_ERR_UNSUPPORTED

@@ -75,11 +75,28 @@ def test_multiquery_fp8_matches_oracle(nq, window, splits):
     assert np.abs(out.float().cpu().numpy() - ref).max() <= TOL["fp8"]
 
 
-def test_multiquery_rejects_more_than_eight_rows():
+@pytest.mark.parametrize("seed,nq,Hq,Hkv,window,splits", [
+    (10, 3, 28, 4, 0, 0),      # group 7: three passes of one token
+    (11, 5, 16, 4, 0, 9),      # group 4: passes of 2, 2 and 1 tokens
+    (12, 4, 28, 4, 50, 0)])    # with a sliding window
+def test_multiquery_beyond_eight_rows_runs_in_passes(seed, nq, Hq, Hkv, window, splits):
+    q, kp, vp, tables, lens = _case(seed, 5, nq, Hq, Hkv, 128, 600, torch.float16, True)
+    scale = float(np.float32(1 / math.sqrt(128)))
+    ref = oracle.decode(to_np16(q), to_np16(kp), to_np16(vp), tables.numpy(), lens.numpy(), scale,
+                        window=window)
+    out = torch.full_like(q, float("nan"), device="cuda")
+    ws = _abi.alloc_workspace(5, Hq, 128, splits, "cuda")
+    _abi.pa_decode(out, q.cuda(), kp.cuda(), vp.cuda(), tables.cuda(), lens.cuda(),
+                   int(lens.max()), scale, splits, ws, window=window)
+    assert _abi.pa_get_status() == (0, 0)
+    assert np.abs(out.float().cpu().numpy() - ref).max() <= TOL["f16"]
+
+
+def test_multiquery_noalloc_rejects_more_than_eight_rows():
     q = torch.zeros(2, 3, 8, 64, dtype=torch.float16, device="cuda")   # 3 tokens x group 4
     k = torch.zeros(4, 2, 16, 64, dtype=torch.float16, device="cuda")
     t = torch.zeros(2, 1, dtype=torch.int32, device="cuda")
     with pytest.raises(_abi.PAError) as e:
-        _abi.pa_decode(torch.empty_like(q), q, k, k, t, torch.ones(2, dtype=torch.int32,
-                       device="cuda"), 16, 0.125, 0, _abi.alloc_workspace(2, 8, 64, 0, "cuda"))
+        _abi.pa_decode_noalloc(torch.empty_like(q), q, k, k, t,
+                               torch.ones(2, dtype=torch.int32, device="cuda"), 16, 0.125, 0)
     assert e.value.code == _abi.PA_ERR_UNSUPPORTED
