@@ -82,6 +82,9 @@ enum {
 #define PA_STATUS_BAD_SLOT 4u    /* slot >= num_blocks * block_size */
 #define PA_STATUS_TIMEOUT 8u     /* an mbarrier wait reached its iteration limit */
 #define PA_STATUS_NO_WORKSPACE 16u /* a split partition had no workspace (never written) */
+#define PA_STATUS_WS_DIRTY 32u   /* a decode read a partial result no decode writes: its workspace
+                                    was not zero-filled (or a call that timed out left it so) and
+                                    results may be wrong; detected on a best-effort basis */
 
 /*
  * Append: for each token i with s = slot_mapping[i] >= 0 and each kv head h,
@@ -171,15 +174,18 @@ int pa_decode_default_splits(int pool_type);
 /*
  * Bytes of device workspace pa_decode / pa_decode_fp8 need: room for the
  * partial results of the context partitions that cross worker boundaries
- * (a worker is one warp; four per CTA; at most two partials each) and the
- * batch's block-stream prefix sums, which the merge launch reads.
- * split_ctas 0 means the largest pa_decode_default_splits() over pool types
- * on the current device, so the result serves a default call of any type.
- * Every call needs one.
+ * (a worker is one warp; four per CTA; at most two partials each), which
+ * the merge launch reads.  split_ctas 0 means the largest
+ * pa_decode_default_splits() over pool types on the current device, so the
+ * result serves a default call of any type.  Every call needs one.
  *
- * The caller allocates the workspace; it needs no initialisation, and the
- * same workspace serves call after call.  Calls that share a workspace must
- * not overlap on the device.
+ * The caller allocates the workspace and zero-fills it once before its
+ * first use (cudaMemsetAsync).  The merge launch tells a written partial
+ * from an empty one by its bits and zeroes each partial it has read, so
+ * every call leaves the workspace zero-filled and the same workspace then
+ * serves call after call, whatever their sizes, without clearing.  After a
+ * call whose status shows PA_STATUS_TIMEOUT or PA_STATUS_WS_DIRTY, zero-fill
+ * it again.  Calls that share a workspace must not overlap on the device.
  */
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int split_ctas);
 
@@ -196,7 +202,9 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int
  * A warp's share of one sequence is a context partition, reduced with an
  * online softmax in fp32.  A sequence split across warps has its partitions
  * merged by log-sum-exp in a second launch on the same stream, a
- * programmatic dependent launch that waits for the first to complete.
+ * programmatic dependent launch that runs beside the first: it merges a
+ * sequence as soon as all its partitions are written, and completes after
+ * the first launch has.
  * Results do not depend on split_ctas beyond fp32 rounding, and a given
  * split_ctas is deterministic.
  *   max_context_len: host-side upper bound of context_lens (no device read);
@@ -298,7 +306,10 @@ int pa_decode_step_fp8(void *out, const void *q, const void *k_new, const void *
  * head_dim 128 needs about 10 MB on a 152-SM GPU).  The call allocates
  * nothing and frees nothing.  The first call on a device looks up the
  * array's device address (make it before any stream capture).  All calls on
- * a device share the array: calls that overlap on the GPU race.
+ * a device share the array: calls that overlap on the GPU race.  The array
+ * starts zero-filled and every call leaves it so; after a pa_get_status
+ * that shows PA_STATUS_TIMEOUT or PA_STATUS_WS_DIRTY, the next call on that
+ * device zeroes it first (a stream-ordered memset).
  */
 #define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
 int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -311,7 +322,8 @@ int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void 
 /*
  * Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns PA_OK when it was clear, PA_ERR_TIMEOUT when a wait gave
- * up, PA_ERR_BOUNDS for index errors, PA_ERR_CUDA when CUDA failed; the raw
+ * up, PA_ERR_WORKSPACE when a decode found its workspace dirty,
+ * PA_ERR_BOUNDS for index errors, PA_ERR_CUDA when CUDA failed; the raw
  * bits go to *bits when bits is not NULL.
  */
 int pa_get_status(void *stream, unsigned *bits);

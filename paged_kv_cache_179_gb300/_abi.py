@@ -22,6 +22,7 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_LEN, PA_STATUS_BAD_SLOT, PA_STATUS_TIMEOUT = 1, 2, 4, 8
 PA_STATUS_NO_WORKSPACE = 16
+PA_STATUS_WS_DIRTY = 32
 
 # (name, argtypes, restype) of every exported entry point
 _vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
@@ -235,7 +236,8 @@ def pa_decode_default_splits(pool_dtype=torch.float16) -> int:
 
 
 def alloc_workspace(num_seqs, num_q_heads, head_dim, split_ctas, device):
-    """Caller-owned workspace for pa_decode (needs no initialisation)."""
+    """Caller-owned workspace for pa_decode, zero-filled as the decode needs
+    it (each call leaves it zero-filled again)."""
     n = pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, split_ctas)
     return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
 

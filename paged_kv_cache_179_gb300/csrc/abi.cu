@@ -429,7 +429,9 @@ int pa_get_status(void* stream, unsigned* bits) {
   if (cudaMemcpy(dev->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
     return PA_ERR_CUDA;
   if (bits) *bits = v;
+  if (v & (PA_STATUS_TIMEOUT | PA_STATUS_WS_DIRTY)) noalloc_scratch_suspect();
   if (v & PA_STATUS_TIMEOUT) return PA_ERR_TIMEOUT;
+  if (v & PA_STATUS_WS_DIRTY) return PA_ERR_WORKSPACE;
   if (v) return PA_ERR_BOUNDS;
   return PA_OK;
 }

@@ -73,7 +73,8 @@ __device__ __forceinline__ unsigned long long pa_smid() {
   asm volatile("mov.u32 %0, %%smid;" : "=r"(v_));
   return v_;
 }
-__device__ unsigned long long g_pa_trace_merge[16384 * 4];   // per merge CTA: entry, wait done, end, pieces
+// per merge CTA: entry, layout known, end, pieces + 1000 x polling rounds
+__device__ unsigned long long g_pa_trace_merge[16384 * 4];
 extern "C" int pa_trace_read_merge(unsigned long long* host, int n_ctas) {
   const size_t n = static_cast<size_t>(n_ctas < 16384 ? n_ctas : 16384) * 4;
   return cudaMemcpyFromSymbol(host, g_pa_trace_merge, sizeof(unsigned long long) * n) ==
@@ -407,6 +408,18 @@ __device__ __forceinline__ int window_first_block(int L, int window, int n_q) {
   return window > 0 && first > 0 ? first >> 4 : 0;
 }
 
+// The context length a launch sees for a context_lens entry (-1: outside the
+// stated bounds).  A launch serving query tokens q_first .. q_first+n_q-1 of
+// q_tokens sees the cache up to its last query's position.
+__device__ __forceinline__ int launch_len(const DecodeArgs& a, int raw) {
+  const bool ok = raw >= 0 && raw <= a.max_context_len && raw <= a.mbs * 16;
+  return ok ? max(0, raw - (a.q_tokens - a.q_first - a.n_q)) : -1;
+}
+// Blocks per kv head a sequence of launch length L puts in the block stream.
+__device__ __forceinline__ int stream_blocks(const DecodeArgs& a, int L) {
+  return L > 0 ? ((L + 15) >> 4) - window_first_block(L, a.window, a.n_q) : 0;
+}
+
 // This lane's block id of chunk x (lane t holds block cb0 + t of the
 // segment, block table entry fb + cb0 + t), -1 past its end.
 __device__ __forceinline__ int load_chunk_id(const DecodeArgs& a, const Chunk& x, int fb,
@@ -511,6 +524,14 @@ __device__ __forceinline__ void store_output(const WarpAcc<D>& st, uint16_t* row
   }
 }
 
+// Partial results sit in the workspace bit-inverted, so that a zero word
+// means "not written yet": no value the kernel computes has all 32 bits set
+// (a NaN the GPU's arithmetic produces is 0x7fffffff).  A zero-filled
+// workspace therefore holds no partial, and the merge launch, having read a
+// partial, zeroes it again.
+__device__ __forceinline__ uint32_t ws_enc(float x) { return ~__float_as_uint(x); }
+__device__ __forceinline__ float ws_dec(uint32_t u) { return __uint_as_float(~u); }
+
 // Write a split piece's partial (unnormalised acc, running max, sum) to the workspace.
 template <int D, bool FP8>
 __device__ __forceinline__ void store_partial(const WarpAcc<D>& st, const DecodeArgs& a, int w,
@@ -522,32 +543,20 @@ __device__ __forceinline__ void store_partial(const WarpAcc<D>& st, const Decode
   for (int i = 0; i < D / 16; i += 2) {
     const int dl = d_lo<D, FP8>(i, r), dh = d_hi<D, FP8>(i, r);
     if (g0 < a.n_q * a.group) {
-      __stcg(reinterpret_cast<float2*>(r0 + dl),
-             make_float2(st.o[i][0] * unboost, st.o[i + 1][0] * unboost));
-      __stcg(reinterpret_cast<float2*>(r0 + dh),
-             make_float2(st.o[i][2] * unboost, st.o[i + 1][2] * unboost));
+      st_relaxed_v2(r0 + dl, ws_enc(st.o[i][0] * unboost), ws_enc(st.o[i + 1][0] * unboost));
+      st_relaxed_v2(r0 + dh, ws_enc(st.o[i][2] * unboost), ws_enc(st.o[i + 1][2] * unboost));
     }
     if (g1 < a.n_q * a.group) {
-      __stcg(reinterpret_cast<float2*>(r1 + dl),
-             make_float2(st.o[i][1] * unboost, st.o[i + 1][1] * unboost));
-      __stcg(reinterpret_cast<float2*>(r1 + dh),
-             make_float2(st.o[i][3] * unboost, st.o[i + 1][3] * unboost));
+      st_relaxed_v2(r1 + dl, ws_enc(st.o[i][1] * unboost), ws_enc(st.o[i + 1][1] * unboost));
+      st_relaxed_v2(r1 + dh, ws_enc(st.o[i][3] * unboost), ws_enc(st.o[i + 1][3] * unboost));
     }
   }
   if (r == 0) {
-    if (g0 < a.n_q * a.group) __stcg(reinterpret_cast<float2*>(a.ws_ml + piece_row(w, slot, g0) * 2),
-                             make_float2(st.m0, st.l0));
-    if (g1 < a.n_q * a.group) __stcg(reinterpret_cast<float2*>(a.ws_ml + piece_row(w, slot, g1) * 2),
-                             make_float2(st.m1, st.l1));
+    if (g0 < a.n_q * a.group)
+      st_relaxed_v2(a.ws_ml + piece_row(w, slot, g0) * 2, ws_enc(st.m0), ws_enc(st.l0));
+    if (g1 < a.n_q * a.group)
+      st_relaxed_v2(a.ws_ml + piece_row(w, slot, g1) * 2, ws_enc(st.m1), ws_enc(st.l1));
   }
-}
-
-// (max, sum) pair combine of two partial softmax states in log2 units.
-__device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s2) {
-  const float mn = fmaxf(m, m2);
-  if (mn == -INFINITY) return;   // both empty
-  s = s * fast_exp2(m - mn) + s2 * fast_exp2(m2 - mn);
-  m = mn;
 }
 
 // Fused append: the new (this step's) row of one (sequence, kv head), the
@@ -657,15 +666,10 @@ decode_kernel(const DecodeArgs a) {
     const int per = (B + kThreads - 1) / kThreads;
     const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
     int sum = 0;
-    // a launch serving query tokens q_first .. q_first+n_q-1 of q_tokens sees
-    // the cache up to its last query's position
-    const int len_sub = a.q_tokens - a.q_first - a.n_q;
     for (int b = b0; b < b1; ++b) {
-      const int raw = a.context_lens[b];
-      const bool ok = raw >= 0 && raw <= a.max_context_len && raw <= a.mbs * 16;
-      const int L = ok ? max(0, raw - len_sub) : -1;
+      const int L = launch_len(a, a.context_lens[b]);
       len[b] = L;
-      sum += ok ? (((L + 15) >> 4) - window_first_block(L, a.window, a.n_q)) * Hkv : 0;
+      sum += stream_blocks(a, L) * Hkv;
     }
     int inc = sum;
 #pragma unroll
@@ -679,7 +683,7 @@ decode_kernel(const DecodeArgs a) {
     for (int w = 0; w < warp; ++w) ex += misc[w];
     for (int b = b0; b < b1; ++b) {
       pf[b] = ex;
-      ex += len[b] > 0 ? (((len[b] + 15) >> 4) - window_first_block(len[b], a.window, a.n_q)) * Hkv : 0;
+      ex += stream_blocks(a, len[b]) * Hkv;
     }
     if (tid == kThreads - 1) pf[B] = ex;
     __syncthreads();
@@ -697,10 +701,7 @@ decode_kernel(const DecodeArgs a) {
     for (int i = tid; i < a.n_q * Hq * D; i += kThreads) o[i] = 0;   // +0.0 in f16 and bf16
   }
 
-  // The merge launch reads the prefix sums (every CTA computed the same),
-  // and may be scheduled now: it waits for this grid to complete.
-  if (cta == 0 && a.seg_prefix != nullptr)
-    for (int b = tid; b <= B; b += kThreads) a.seg_prefix[b] = pf[b];
+  // The merge launch may be scheduled now: it waits for the partials it reads.
   griddep_launch_dependents();
 
   // ---- 3. this warp's share of the block stream.  No CTA-wide barrier
@@ -912,7 +913,8 @@ decode_kernel(const DecodeArgs a) {
       } else if (a.ws_acc == nullptr) {
         if (lane == 0) atomicOr(a.status, kStatusNoWorkspace);   // never written through null
       } else {
-        // a split segment: the merge launch combines its pieces
+        // a split segment: the merge launch, running beside this grid,
+        // combines its pieces as soon as all are written
         store_partial<D, FP8>(st, a, gw, piece_no == 0 ? 0 : 1, r, c, unboost);
       }
       ++piece_no;
@@ -971,9 +973,19 @@ decode_kernel(const DecodeArgs a) {
 // columns 4*d4 .. 4*d4+3 of query head g and folds the pieces in worker
 // order, kMergeBatch at a time (their loads in flight together), rescaling
 // its running state to each batch's maximum: a fixed order, so results are
-// deterministic.  Segments attended whole by one worker are skipped.  The
-// launch starts with griddepcontrol.wait: the attention grid has completed
-// and its writes are visible.
+// deterministic.  Segments attended whole by one worker are skipped.
+//
+// The launch runs beside the attention grid: it is scheduled once every
+// attention CTA has passed its prologue, so it never holds resources an
+// attention CTA waits for.  It finds the block stream's layout from the
+// context lengths, as each attention CTA did, and reads its pieces as they
+// are written (a zero word is a partial not written yet): a segment is
+// merged as soon as its last piece lands, and only the segments of the last
+// warps to finish are merged after the attention ends.  While a batch is
+// incomplete, warp 0 polls the first word of each missing piece, so waiting
+// costs one load per piece per poll.  The CTA zeroes the partials it read.
+// The last CTA ends with griddepcontrol.wait: the launch completes after the
+// attention grid has completed and its writes are visible.
 constexpr int kMergeThreads = 256;
 #ifndef PA_MERGE_BATCH
 #define PA_MERGE_BATCH 8
@@ -981,84 +993,189 @@ constexpr int kMergeThreads = 256;
 constexpr int kMergeBatch = PA_MERGE_BATCH;
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kMergeThreads)
+__global__ void __launch_bounds__(kMergeThreads, 2)
 merge_kernel(const DecodeArgs a) {
   PA_TRACE_ONLY(const unsigned long long t_in = pa_now());
-  griddep_wait();
-  PA_TRACE_ONLY(if (threadIdx.x == 0 && blockIdx.x < 16384) {
+  __shared__ int red[kMergeThreads / 32][2];
+  __shared__ unsigned want;
+  __shared__ int fail;
+  const int Hkv = a.Hkv, G = a.group;
+  const int b = blockIdx.x / Hkv, h = blockIdx.x - b * Hkv;
+  const int tid = threadIdx.x, lane = tid & 31;
+
+  // ---- the block stream: its length W and the start of sequence b's segments
+  int before = 0, total = 0;
+  for (int i = tid; i < a.B; i += blockDim.x) {
+    const int n = stream_blocks(a, launch_len(a, __ldg(a.context_lens + i))) * Hkv;
+    total += n;
+    before += i < b ? n : 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    total += __shfl_xor_sync(0xffffffffu, total, o);
+  }
+  if (lane == 0) {
+    red[tid >> 5][0] = before;
+    red[tid >> 5][1] = total;
+  }
+  if (tid == 0) fail = 0;
+  __syncthreads();
+  before = total = 0;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+    before += red[w][0];
+    total += red[w][1];
+  }
+  const int nbk = stream_blocks(a, launch_len(a, __ldg(a.context_lens + b)));
+  int w0 = 0, np = 0, first_slot = 0;
+  if (nbk > 0) {
+    const int64_t W = total;
+    const int64_t NW = min(static_cast<int64_t>(a.split_ctas) * kWarps, W);
+    const int64_t s0 = before + static_cast<int64_t>(h) * nbk;
+    w0 = worker_of(s0, W, NW);
+    np = worker_of(s0 + nbk - 1, W, NW) - w0 + 1;
+    first_slot = s0 > worker_lo(w0, W, NW) ? 1 : 0;   // the segment is w0's last piece
+  }
+  PA_TRACE_ONLY(if (tid == 0 && blockIdx.x < 16384) {
     g_pa_trace_merge[blockIdx.x * 4 + 0] = t_in;
     g_pa_trace_merge[blockIdx.x * 4 + 1] = pa_now();
     g_pa_trace_merge[blockIdx.x * 4 + 2] = 0;
     g_pa_trace_merge[blockIdx.x * 4 + 3] = 0;
   });
-  const int Hkv = a.Hkv, G = a.group;
-  const int b = blockIdx.x / Hkv, h = blockIdx.x - b * Hkv;
-  const int* pf = a.seg_prefix;
-  const int64_t W = pf[a.B];
-  const int nbk = (pf[b + 1] - pf[b]) / Hkv;
-  if (nbk == 0) return;
-  const int64_t NW = min(static_cast<int64_t>(a.split_ctas) * kWarps, W);
-  const int64_t s0 = pf[b] + static_cast<int64_t>(h) * nbk;
-  const int w0 = worker_of(s0, W, NW), w1 = worker_of(s0 + nbk - 1, W, NW);
-  if (w0 == w1) return;                         // attended whole
-  const int first_slot = s0 > worker_lo(w0, W, NW) ? 1 : 0;   // the segment is w0's last piece
-  constexpr int COLS = D / 4;
-  const int tid = threadIdx.x, g = tid / COLS, d4 = tid - g * COLS;   // g: the query row
-  if (g >= a.n_q * G) return;
-  float M = -INFINITY, S = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int np = w1 - w0 + 1;
-  for (int p0 = 0; p0 < np; p0 += kMergeBatch) {
-    float2 ml[kMergeBatch];
-    float4 v[kMergeBatch];
+
+  if (np > 1) {                                  // a split segment (np is CTA-uniform)
+    constexpr int COLS = D / 4;
+    const int g = tid / COLS, d4 = tid - g * COLS;   // g: the query row
+    const bool row = g < a.n_q * G;
+    // partial row of piece p for query row q
+    auto prow = [&](int p, int q) { return piece_row(w0 + p, p == 0 ? first_slot : 0, q); };
+    float M = -INFINITY, S = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool dirty = false;
+    PA_TRACE_ONLY(int tr_waits = 0);
+    for (int p0 = 0; p0 < np; p0 += kMergeBatch) {
+      const int pn = min(kMergeBatch, np - p0);
+      uint2 ml[kMergeBatch];
+      uint4 v[kMergeBatch];
+      // Issue every load of the batch before looking at any (they are in
+      // flight together); then note the pieces not yet seen whole.  Piece
+      // p0 + k sits 16 rows after piece p0 + k - 1 (slot 0 of the next
+      // worker), except that the segment's first piece may be its worker's
+      // slot 1.
+      const int64_t rb = static_cast<int64_t>(w0 + p0) * 2 * kGroupMax + g;
+      const float* mlb = a.ws_ml + rb * 2;
+      const float* vb = a.ws_acc + rb * D + 4 * d4;
+      const int s0x = p0 == 0 ? first_slot * kGroupMax : 0;
+      auto load = [&](int k) {
+        const int dr = k == 0 ? s0x : 2 * kGroupMax * k;
+        ml[k] = ld_relaxed_v2(mlb + dr * 2);
+        v[k] = ld_relaxed_v4(vb + static_cast<int64_t>(dr) * D);
+      };
+      auto missing_of = [&](unsigned set) {
+        unsigned m = 0;
 #pragma unroll
-    for (int k = 0; k < kMergeBatch; ++k) {
-      ml[k] = make_float2(-INFINITY, 0.f);
-      v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      const int p = p0 + k;
-      if (p < np) {
-        const int64_t row = piece_row(w0 + p, p == 0 ? first_slot : 0, g);
-        ml[k] = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + row * 2));
-        v[k] = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + row * D) + d4);
+        for (int k = 0; k < kMergeBatch; ++k)
+          if ((set >> k & 1u) &&
+              !(ml[k].x && ml[k].y && v[k].x && v[k].y && v[k].z && v[k].w))
+            m |= 1u << k;
+        return m;
+      };
+      const unsigned mine = row ? (1u << pn) - 1u : 0u;
+#pragma unroll
+      for (int k = 0; k < kMergeBatch; ++k)
+        if (mine >> k & 1u) load(k);
+      unsigned missing = missing_of(mine);       // pieces this thread has not seen whole
+      if (__syncthreads_or(missing != 0u)) {
+        // wait for the batch's missing pieces (bounded), then read them again
+        const uint64_t t0 = tid == 0 ? global_ns() : 0;
+        for (;;) {
+          if (tid == 0) want = 0u;
+          __syncthreads();
+          if (missing) atomicOr(&want, missing);
+          __syncthreads();
+          const unsigned need = want;
+          if (need == 0u) break;
+          PA_TRACE_ONLY(++tr_waits);
+          if (tid < 32 && lane < pn && (need >> lane & 1u)) {
+            const uint32_t* first = reinterpret_cast<const uint32_t*>(a.ws_ml + prow(p0 + lane, 0) * 2);
+            const uint64_t tl = global_ns();
+            while (ld_relaxed_b32(first) == 0u) {
+              __nanosleep(64);
+              if (global_ns() - tl > kPollLimitNs) {
+                fail = 1;
+                break;
+              }
+            }
+          }
+          if (tid == 0 && global_ns() - t0 > kPollLimitNs) fail = 1;
+          __syncthreads();
+          if (fail) break;
+#pragma unroll
+          for (int k = 0; k < kMergeBatch; ++k)
+            if (missing >> k & 1u) load(k);
+          missing = missing_of(missing);
+        }
+        if (fail) break;                         // (uniform: read after a barrier)
+      }
+      if (!row) continue;
+      float mk[kMergeBatch];
+      float mb = M;
+#pragma unroll
+      for (int k = 0; k < kMergeBatch; ++k) {
+        mk[k] = k < pn ? ws_dec(ml[k].x) : -INFINITY;
+        // a written piece has attended nothing (max -inf) or has a sum of at
+        // least 1 (its largest score's own weight)
+        if (k < pn && mk[k] != -INFINITY && ws_dec(ml[k].y) < 0.5f) dirty = true;
+        mb = fmaxf(mb, mk[k]);
+      }
+      if (mb == -INFINITY) continue;             // nothing attended yet
+      const float keep = fast_exp2(M - mb);
+      acc.x *= keep;
+      acc.y *= keep;
+      acc.z *= keep;
+      acc.w *= keep;
+      S *= keep;
+#pragma unroll
+      for (int k = 0; k < kMergeBatch; ++k) {
+        if (k >= pn) continue;
+        const float e = fast_exp2(mk[k] - mb);
+        S += e * ws_dec(ml[k].y);
+        acc.x += e * ws_dec(v[k].x);
+        acc.y += e * ws_dec(v[k].y);
+        acc.z += e * ws_dec(v[k].z);
+        acc.w += e * ws_dec(v[k].w);
+      }
+      M = mb;
+    }
+    if (fail) {
+      if (tid == 0) atomicOr(a.status, kStatusTimeout);
+    } else if (row) {
+      if (dirty) atomicOr(a.status, kStatusWsDirty);
+      const float inv = S > 0.f ? 1.f / S : 0.f;
+      uint2 o;
+      o.x = pack2<BF16>(acc.x * inv, acc.y * inv);
+      o.y = pack2<BF16>(acc.z * inv, acc.w * inv);
+      uint16_t* out = static_cast<uint16_t*>(a.out) +
+                      ((static_cast<int64_t>(b) * a.q_tokens + a.q_first + g / G) * a.Hq +
+                       h * G + g % G) * D;
+      *reinterpret_cast<uint2*>(out + 4 * d4) = o;
+      // leave the workspace zero-filled for the next call
+      for (int p = 0; p < np; ++p) {
+        const int64_t r = prow(p, g);
+        __stcg(reinterpret_cast<uint4*>(a.ws_acc + r * D) + d4, make_uint4(0u, 0u, 0u, 0u));
+        if (d4 == 0) __stcg(reinterpret_cast<uint2*>(a.ws_ml + r * 2), make_uint2(0u, 0u));
       }
     }
-    float mb = M;
-#pragma unroll
-    for (int k = 0; k < kMergeBatch; ++k) mb = fmaxf(mb, ml[k].x);
-    if (mb == -INFINITY) continue;              // nothing attended yet
-    const float keep = fast_exp2(M - mb);
-    acc.x *= keep;
-    acc.y *= keep;
-    acc.z *= keep;
-    acc.w *= keep;
-    S *= keep;
-#pragma unroll
-    for (int k = 0; k < kMergeBatch; ++k) {
-      const float e = fast_exp2(ml[k].x - mb);  // 0 for a missing piece
-      S += e * ml[k].y;
-      acc.x += e * v[k].x;
-      acc.y += e * v[k].y;
-      acc.z += e * v[k].z;
-      acc.w += e * v[k].w;
-    }
-    M = mb;
+    PA_TRACE_ONLY(if (tid == 0 && blockIdx.x < 16384) {
+      g_pa_trace_merge[blockIdx.x * 4 + 2] = pa_now();
+      g_pa_trace_merge[blockIdx.x * 4 + 3] = np + 1000ull * tr_waits;
+    });
   }
-  PA_TRACE_ONLY(if (threadIdx.x == 0 && blockIdx.x < 16384) {
-    g_pa_trace_merge[blockIdx.x * 4 + 2] = pa_now();
-    g_pa_trace_merge[blockIdx.x * 4 + 3] = np;
-  });
-  const float inv = S > 0.f ? 1.f / S : 0.f;
-  uint2 o;
-  o.x = pack2<BF16>(acc.x * inv, acc.y * inv);
-  o.y = pack2<BF16>(acc.z * inv, acc.w * inv);
-  uint16_t* row = static_cast<uint16_t*>(a.out) +
-                  ((static_cast<int64_t>(b) * a.q_tokens + a.q_first + g / G) * a.Hq + h * G +
-                   g % G) * D;
-  *reinterpret_cast<uint2*>(row + 4 * d4) = o;
+  if (blockIdx.x == gridDim.x - 1 && tid == 0) griddep_wait();
 }
 
 // The merge launch, allowed to be scheduled while the attention grid runs
-// (programmatic stream serialization); its griddepcontrol.wait orders it.
+// (programmatic stream serialization).
 template <int D, bool BF16>
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
@@ -1093,7 +1210,7 @@ cudaError_t launch_one(const DecodeArgs& a, cudaStream_t s) {
   }
   kern<<<static_cast<unsigned>(a.split_ctas), kThreads, lay.total, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (a.ws_acc == nullptr || a.seg_prefix == nullptr) return cudaSuccess;
+  if (a.ws_acc == nullptr) return cudaSuccess;
   return launch_merge<D, BF16>(a, s);
 }
 
@@ -1143,34 +1260,31 @@ int decode_max_default_ctas() {
 
 namespace {
 // Workspace: partial rows (acc, then (max, sum)) of two pieces per worker,
-// then the block-stream prefix sums; each part 256-byte aligned.
+// each part 256-byte aligned.  Zero-filled between calls.
 struct WsLayout {
-  size_t acc, ml, pf, total;
+  size_t acc, ml, total;
 };
-WsLayout ws_layout(int B, int D, int split_ctas) {
+WsLayout ws_layout(int D, int split_ctas) {
   const int64_t rows = static_cast<int64_t>(split_ctas) * kWarps * 2 * kGroupMax;
-  const int64_t Bc = B < kMaxBatchPerLaunch ? B : kMaxBatchPerLaunch;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   WsLayout l{};
   l.acc = 0;
   l.ml = up(static_cast<size_t>(rows) * D * 4);
-  l.pf = l.ml + up(static_cast<size_t>(rows) * 2 * 4);
-  l.total = l.pf + up(static_cast<size_t>(Bc + 1) * 4);
+  l.total = l.ml + up(static_cast<size_t>(rows) * 2 * 4);
   return l;
 }
 }  // namespace
 
 size_t decode_workspace_bytes(int B, int Hq, int D, int split_ctas) {
   if (B <= 0 || Hq <= 0 || D <= 0 || split_ctas <= 0) return 0;
-  return ws_layout(B, D, split_ctas).total;
+  return ws_layout(D, split_ctas).total;
 }
 
 void decode_workspace_split(DecodeArgs& a, void* ws) {
-  const WsLayout l = ws_layout(a.B, a.D, a.split_ctas);
+  const WsLayout l = ws_layout(a.D, a.split_ctas);
   uint8_t* base = static_cast<uint8_t*>(ws);
   a.ws_acc = reinterpret_cast<float*>(base + l.acc);
   a.ws_ml = reinterpret_cast<float*>(base + l.ml);
-  a.seg_prefix = reinterpret_cast<int*>(base + l.pf);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, bool fp8, bool bf16, cudaStream_t s) {

@@ -2,8 +2,7 @@
 // allocate device memory.
 //
 // pa_decode needs a caller-allocated workspace (the partial results of
-// context partitions split across warps, and the block-stream prefix sums
-// the merge launch reads).  Some callers cannot provide one: code running inside
+// context partitions split across warps, which the merge launch reads).  Some callers cannot provide one: code running inside
 // a host framework that owns every byte of device memory and forbids raw
 // allocations, latency-critical serving loops where cudaMalloc would
 // synchronise the device, and plain C callers with no device allocator of
@@ -11,9 +10,11 @@
 // fixed array compiled into the library, so it allocates nothing.
 //
 // The array is PA_NOALLOC_SCRATCH_BYTES (16 MiB); every GPU that loads the
-// library holds it until the process exits.  All calls on a device share it
-// and it keeps the last call's contents (nothing in it needs clearing
-// between calls).  Calls that overlap on the GPU (different streams, or
+// library holds it until the process exits.  All calls on a device share it.
+// It starts zero-filled, as every static device array does, and each call
+// leaves it zero-filled again, so it never needs clearing; after a status
+// read that shows a wait that gave up or a dirty workspace, the next call
+// zeroes it first.  Calls that overlap on the GPU (different streams, or
 // different host threads) race on the array and must not be issued.
 #include <climits>
 #include <cmath>
@@ -29,6 +30,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRA
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
+bool g_scratch_suspect[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
@@ -50,6 +52,13 @@ int scratch_address(void** out) {
 bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
+
+void pa::noalloc_scratch_suspect() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  g_scratch_suspect[dev] = true;
+}
 
 extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
                                  const void* v_cache, const int32_t* block_tables,
@@ -107,6 +116,18 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   a.q_first = 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  {
+    // a status read saw a wait give up or a dirty workspace: partials may be
+    // left in the scratch, so zero it (stream-ordered) before this call
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_suspect[dev]) {
+      if (cudaMemsetAsync(ws, 0, PA_NOALLOC_SCRATCH_BYTES, s) != cudaSuccess)
+        return PA_ERR_CUDA;
+      g_scratch_suspect[dev] = false;
+    }
+  }
   const size_t row = static_cast<size_t>(queries_per_seq) * num_q_heads * head_dim * 2;
   for (int b0 = 0; b0 < num_seqs; b0 += kMaxBatchPerLaunch) {
     DecodeArgs c = a;

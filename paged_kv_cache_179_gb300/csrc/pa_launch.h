@@ -22,9 +22,9 @@ struct DecodeArgs {
   const float* v_scale;
   const int32_t* block_tables;  // [B][mbs]
   const int32_t* context_lens;  // [B]
-  float* ws_acc;                // [split_ctas][2][8][D] partial sums (unnormalised)
-  float* ws_ml;                 // [split_ctas][2][8][2] partial (max, sum) in log2 units
-  int* seg_prefix;              // [B + 1] block-stream prefix sums, for the merge launch
+  float* ws_acc;                // [split_ctas*4][2][8][D] partial sums (unnormalised), and
+  float* ws_ml;                 // [split_ctas*4][2][8][2] partial (max, sum) in log2 units;
+                                // both bit-inverted, zero when not written
   unsigned* status;             // device status word
   // fused append (pa_decode_step*): this step's new rows and where they go;
   // null for a plain decode
@@ -76,5 +76,9 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, float* k_scale, flo
 int device_sm_count();
 // Address of the current device's status word (set up on first use).
 int device_status_word(unsigned** out);
+// Called when a status read shows a wait that gave up or a dirty workspace
+// on the current device: the no-alloc scratch's flags are cleared before
+// its next use.
+void noalloc_scratch_suspect();
 
 }  // namespace pa

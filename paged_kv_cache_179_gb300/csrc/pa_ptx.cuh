@@ -16,6 +16,7 @@ constexpr unsigned kStatusBadLen = 2u;     // context_len negative or above the 
 constexpr unsigned kStatusBadSlot = 4u;    // slot outside [0, num_blocks * block_size)
 constexpr unsigned kStatusTimeout = 8u;    // an mbarrier wait hit its iteration limit
 constexpr unsigned kStatusNoWorkspace = 16u;  // a split partition found no workspace
+constexpr unsigned kStatusWsDirty = 32u;   // a partial no decode writes: workspace not zero-filled
 
 // Iteration limit of every mbarrier wait.  A wait that ends normally takes a
 // few microseconds.  Each try_wait suspends the thread for at most
@@ -59,6 +60,40 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
+
+// ------------------------------------------ data shared with a concurrent grid
+// One grid's warps store partial results while another grid's CTAs poll
+// them, so both sides use strong (relaxed, gpu-scope) accesses: each 32-bit
+// word is then read either as it was or as written, never torn.
+__device__ __forceinline__ void st_relaxed_v2(void* p, uint32_t x, uint32_t y) {
+  asm volatile("st.relaxed.gpu.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t ld_relaxed_b32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_relaxed_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.relaxed.gpu.global.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint4 ld_relaxed_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Time limit of a wait for another grid's data: a wait that gives up
+// reports kStatusTimeout instead of hanging the kernel.
+constexpr uint64_t kPollLimitNs = 2000000000ull;
 
 // ------------------------------------------------------- bulk async copies
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {

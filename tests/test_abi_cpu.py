@@ -77,18 +77,17 @@ def test_decode_argument_errors(lib):
 
 def test_workspace_size_formula(lib):
     # partial rows: 2 per warp (4 warps per CTA), 8 query-head slots each, D floats +
-    # (max, sum); then the block-stream prefix sums (num_seqs + 1 ints); each part
-    # rounded up to 256 bytes
+    # (max, sum); each part rounded up to 256 bytes
     n = lib.pa_decode_workspace_size(2, 8, 64, 10)
     up = lambda x: (x + 255) // 256 * 256
     rows = 10 * 4 * 2 * 8
-    acc, ml, prefix = rows * 64 * 4, rows * 2 * 4, (2 + 1) * 4
-    assert n == up(acc) + up(ml) + up(prefix)
+    acc, ml = rows * 64 * 4, rows * 2 * 4
+    assert n == up(acc) + up(ml)
     assert lib.pa_decode_workspace_size(2, 8, 64, 1) > 0        # one CTA's 4 warps still split
     assert lib.pa_decode_workspace_size(2, 8, 64, -1) == 0      # invalid
-    # batches above 512 sequences run in launches of 512 that share the workspace
+    # the size does not grow with the batch (launches of 512 sequences share it)
     assert lib.pa_decode_workspace_size(5000, 8, 64, 10) == \
-        lib.pa_decode_workspace_size(2048, 8, 64, 10)
+        lib.pa_decode_workspace_size(2, 8, 64, 10)
 
 
 def test_append_and_quantize_argument_errors(lib):

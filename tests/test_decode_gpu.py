@@ -101,7 +101,7 @@ def test_split_invariance():
     to_cuda(w)
     outs = []
     k0, v0 = w.k_cache.clone(), w.v_cache.clone()
-    for splits in (1, 2, 7, 64, 304, 999, 7207):
+    for splits in (1, 2, 7, 64, 304, 999, 7207):   # the last: more warps than blocks
         w.k_cache.copy_(k0)
         w.v_cache.copy_(v0)
         out = torch.empty_like(w.q)
