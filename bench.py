@@ -233,18 +233,31 @@ def run_ours(args, rank, world, dev):
         pools = dict(k_cache=kc, v_cache=vc, k_scale=ks, v_scale=vs)
     else:
         pools = dict(k_cache=w.k_cache, v_cache=w.v_cache)
-    step = DecodeStep(**pools, block_tables=w.block_tables, context_lens=w.context_lens,
-                      max_context_len=w.max_context_len, scale=w.scale, num_q_heads=w.Hq,
-                      split_ctas=args.splits, window=args.window)
     out = torch.empty_like(w.q)
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
     kv_bytes = algorithmic_bytes(w, lens, args.window)["kv"]
     l2_mode = args.l2
+    copies = 1
     if l2_mode == "auto":
-        # Inputs several times larger than L2 stream through it without hits;
-        # smaller batches get L2 evicted by reading a 2x-L2 buffer (a read
-        # leaves clean lines, so the timed step pays no write-backs).
-        l2_mode = "none" if kv_bytes >= 3 * l2 else "read"
+        # Inputs several times larger than L2 stream through it without hits
+        # and run back to back.  Smaller pools are replicated (one copy per
+        # layer of a model, as a serving step has) and the steps cycle over
+        # the copies, so each step's K/V is cold; when that would take more
+        # than 16 copies, L2 is evicted before each step by reading a 2x-L2
+        # buffer (a read leaves clean lines, so the timed step pays no
+        # write-backs) and steps are timed one by one.
+        copies = -(-3 * l2 // max(kv_bytes, 1))
+        l2_mode = "none" if kv_bytes >= 3 * l2 else ("rotate" if copies <= 16 else "read")
+    if l2_mode == "rotate":
+        copies = max(2, min(16, -(-3 * l2 // max(kv_bytes, 1))))
+    else:
+        copies = 1
+    pool_sets = [pools] + [{k: t.clone() for k, t in pools.items()} for _ in range(copies - 1)]
+    steps = [DecodeStep(**ps, block_tables=w.block_tables, context_lens=w.context_lens,
+                        max_context_len=w.max_context_len, scale=w.scale, num_q_heads=w.Hq,
+                        split_ctas=args.splits, window=args.window) for ps in pool_sets]
+    step = steps[0]
+    back_to_back = l2_mode in ("none", "rotate")
     flush_buf = torch.ones(max(2 * l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
 
     def flush():
@@ -256,53 +269,81 @@ def run_ours(args, rank, world, dev):
     fused = step.prefers_fused if args.step == "auto" else args.step == "fused"
     # decode_kernel + merge_kernel (fused) | append_kernel + decode_kernel + merge_kernel
     launches_per_step = 2 if fused else 3
+    # each copy's step, and its decode alone, bound once (arguments checked and
+    # marshalled outside the timed region)
+    calls = [st.bind(w.q, w.k_new, w.v_new, w.slot_mapping, out, fused=fused, stream=stream)
+             for st in steps]
+    decodes = [_abi.prepare(lambda st=st: st.decode(w.q, out), stream) for st in steps]
 
-    def run_step():
-        step(w.q, w.k_new, w.v_new, w.slot_mapping, out, fused=fused)
+    def run_step(i=0):
+        calls[i % copies]()
 
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     if rank == 0:
         clocks.start()
     clocks.mark("warmup_start")
-    for _ in range(args.warmup):
+    for i in range(max(args.warmup, copies)):
         flush()
-        run_step()
+        run_step(i)
     rc, bits = _abi.pa_get_status(dev)
     if rc != 0:
         raise RuntimeError(f"device status {rc} bits {bits}")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     clocks.mark("timed_start")
-    if args.prime_ms > 0:
-        # Keep the GPU busy while the host enqueues the K steps, so host-side
-        # Python time between launches does not show up as GPU idle time
-        # between the events (the events time GPU execution only).
-        torch.cuda._sleep(int(args.prime_ms * 1e-3 * 1.5e9))
-    for i in range(K):
-        flush()
-        ev[i][0].record(stream)
-        if fused:
-            run_step()
+    if back_to_back:
+        # K steps back to back between two events: an event recorded between
+        # steps costs the GPU about 2 us (measured), which is not the step's
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(K):
+            run_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        total_ms = e0.elapsed_time(e1)
+        step_ms = [total_ms / K] * K
+    else:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for i in range(K):
+            flush()
+            ev[i][0].record(stream)
+            run_step(i)
             ev[i][1].record(stream)
-        else:
-            step.append(w.k_new, w.v_new, w.slot_mapping)
-            ev[i][1].record(stream)
-            step.decode(w.q, out)
-        ev[i][2].record(stream)
-    torch.cuda.synchronize(dev)
+        torch.cuda.synchronize(dev)
+        step_ms = [a.elapsed_time(b) for a, b in ev]
+        total_ms = sum(step_ms)
     clocks.mark("timed_end")
     if world > 1:
         torch.distributed.barrier()
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    # the dominant kernel: the fused step kernel, or pa_decode's kernel
-    dec_ms = step_ms if fused else [e[1].elapsed_time(e[2]) for e in ev]
-    total_ms = sum(step_ms)
 
-    # for reference: the same step as two launches (append, then decode)
+    # the dominant kernel (decode_kernel, then merge_kernel): the fused step
+    # itself, or pa_decode timed alone the same way
+    if fused:
+        dec_ms = step_ms
+    elif back_to_back:
+        torch.cuda.synchronize(dev)
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for i in range(K):
+            decodes[i % copies]()
+        d1.record(stream)
+        torch.cuda.synchronize(dev)
+        dec_ms = [d0.elapsed_time(d1) / K] * K
+    else:
+        dv = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for i in range(K):
+            flush()
+            dv[i][0].record(stream)
+            decodes[i % copies]()
+            dv[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        dec_ms = [a.elapsed_time(b) for a, b in dv]
+
+    # for reference: the same step as two launches (append, then decode), each
+    # timed with its own events (they include the events' own cost)
     sep = []
     for i in range(min(K, 20)):
         a0, a1, a2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
@@ -318,28 +359,32 @@ def run_ours(args, rank, world, dev):
     dec2_ms = [a1.elapsed_time(a2) for _, a1, a2 in sep]
 
     # end to end through the public API: the step's inputs packed in one pinned
-    # host buffer and uploaded by one copy, the output copied back.  Batches
-    # several times larger than L2 run as a pipeline (the next step's upload
-    # and the last step's read-back overlap the current step's attention),
-    # timed over the K steps; smaller ones step by step, L2 evicted outside
-    # each step's events.
+    # host buffer and uploaded by one copy, the output copied back.  Back to
+    # back (large or replicated pools) the steps run as a pipeline (the next
+    # step's upload and the last step's read-back overlap the current step's
+    # attention; one slot per pool copy), timed over the K steps; otherwise
+    # step by step, L2 evicted outside each step's events.
     from paged_kv_cache_179_gb300.step import StepPipeline, StepStaging
     names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
     specs = {k: (getattr(w, k).shape, getattr(w, k).dtype) for k in names}
+    made = []
 
     def make_step(staging):
-        return DecodeStep(**pools, block_tables=staging.dev["block_tables"],
+        ps = pool_sets[len(made) % copies]
+        made.append(staging)
+        return DecodeStep(**ps, block_tables=staging.dev["block_tables"],
                           context_lens=staging.dev["context_lens"],
                           max_context_len=w.max_context_len, scale=w.scale, num_q_heads=w.Hq,
                           split_ctas=args.splits, window=args.window)
     h2d = d2h = 0
-    if l2_mode == "none":
-        e2e_mode = "pipelined: uploads and read-backs on two copy streams, overlapping the steps"
-        pipe = StepPipeline(make_step, specs, out.shape, out.dtype, dev)
+    if back_to_back:
+        e2e_mode = ("pipelined: uploads and read-backs on two copy streams, overlapping the "
+                    f"steps ({max(2, copies)} slots)")
+        pipe = StepPipeline(make_step, specs, out.shape, out.dtype, dev, depth=max(2, copies))
         for st_ in pipe.stagings:
             for k in names:
                 st_.host[k].copy_(getattr(w, k).cpu())
-        for _ in range(max(1, args.warmup)):
+        for _ in range(max(args.warmup, pipe.depth)):
             pipe.submit(fused=fused)
         pipe.finish()
         torch.cuda.synchronize(dev)
@@ -393,7 +438,7 @@ def run_ours(args, rank, world, dev):
             "workload": describe(w, tokens),
             "step": ("pa_decode_step: append inside the attention launch, then the merge launch"
                      if fused else "append launch, then attention and merge launches"),
-            "split_ctas": step.split_ctas, "l2": describe_l2(l2_mode, kv_bytes, l2),
+            "split_ctas": step.split_ctas, "l2": describe_l2(l2_mode, kv_bytes, l2, copies),
             "seed": args.seed, "parallelism": "replicas" if world > 1 else "single GPU",
             **({"window": args.window} if args.window else {}),
         },
@@ -404,11 +449,14 @@ def run_ours(args, rank, world, dev):
                                 "together: one decode)" if fused
                                 else "decode_kernel, then merge_kernel (timed together: one decode)"),
                      "bytes_per_launch": kernel_bytes, "peak_source": peak_kind},
-        "decode_us": {"mean": round(statistics.mean(dec_ms) * 1e3, 2),
-                      "median": round(statistics.median(dec_ms) * 1e3, 2),
-                      "p20": round(float(np.percentile(dec_ms, 20)) * 1e3, 2),
-                      "p80": round(float(np.percentile(dec_ms, 80)) * 1e3, 2),
-                      "min": round(min(dec_ms) * 1e3, 2)},
+        "decode_us": ({"mean": round(statistics.mean(dec_ms) * 1e3, 2),
+                       "timing": "K decodes back to back between two events"} if back_to_back else
+                      {"mean": round(statistics.mean(dec_ms) * 1e3, 2),
+                       "median": round(statistics.median(dec_ms) * 1e3, 2),
+                       "p20": round(float(np.percentile(dec_ms, 20)) * 1e3, 2),
+                       "p80": round(float(np.percentile(dec_ms, 80)) * 1e3, 2),
+                       "min": round(min(dec_ms) * 1e3, 2),
+                       "timing": "each decode between its own events, L2 evicted before it"}),
         "as_two_launches_us": {"append": round(statistics.mean(app_ms) * 1e3, 2),
                                "decode": round(statistics.mean(dec2_ms) * 1e3, 2)},
         "e2e": {"value": round(tokens_all * K / (e2e_ms_max / 1e3), 1), "unit": UNIT,
@@ -546,7 +594,11 @@ def run_multiquery(args, dev):
     }
 
 
-def describe_l2(mode, kv_bytes, l2):
+def describe_l2(mode, kv_bytes, l2, copies=1):
+    if mode == "rotate":
+        return (f"not flushed: the steps cycle over {copies} copies of the pools "
+                f"({copies * kv_bytes / 1e6:.0f} MB of K/V vs {l2 / 1e6:.0f} MB L2), so each "
+                f"step's K/V is cold; steps back to back")
     if mode == "none":
         return (f"not flushed: inputs larger than L2 ({kv_bytes / 1e6:.0f} MB of K/V per step vs "
                 f"{l2 / 1e6:.0f} MB L2), tiles fetched with an L2 evict-first policy")
@@ -658,15 +710,14 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--splits", type=int, default=0,
                     help="CTAs the batch is divided among (0 = two per SM)")
-    ap.add_argument("--l2", choices=["auto", "none", "read", "write"], default="auto",
-                    help="L2 handling between timed steps (auto: none when the K/V read "
-                         "is >= 3x L2, else evict by reading a 2x-L2 buffer)")
+    ap.add_argument("--l2", choices=["auto", "none", "rotate", "read", "write"], default="auto",
+                    help="L2 handling between timed steps (auto: none when the K/V read is "
+                         ">= 3x L2; else rotate over copies of the pools, >= 3x L2 together, "
+                         "when 16 copies suffice; else evict by reading a 2x-L2 buffer)")
     ap.add_argument("--step", choices=["auto", "fused", "two-launch"], default="auto",
                     help="fused: pa_decode_step (append inside the attention launch); two-launch: "
                          "pa_cache_append + pa_decode; auto: the faster for the pool type "
                          "(fused for 16-bit pools, two-launch for E4M3)")
-    ap.add_argument("--prime-ms", type=float, default=0.0,
-                    help="GPU sleep queued ahead of the timed steps so the host runs ahead")
     ap.add_argument("--op", choices=["step", "copy_blocks", "multiquery"], default="step",
                     help="what to time: the decode step (default), pa_copy_blocks alone, or a "
                          "decode with --queries query tokens per sequence")

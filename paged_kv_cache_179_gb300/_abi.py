@@ -92,11 +92,68 @@ def _check(rc: int, where: str):
         raise PAError(rc, where)
 
 
+class _Recording(threading.local):
+    """Per-thread state of ``prepare``: while active, entry points record
+    their C calls (with marshalled arguments) instead of making them."""
+    active = False
+    stream = None
+    calls = None
+
+
+_rec = _Recording()
+
+
+def _call(fn, where: str, *args):
+    if _rec.active:
+        conv = []
+        for t, a in zip(fn.argtypes, args):
+            conv.append(a if a is None or isinstance(a, t) else t(a))
+        _rec.calls.append((fn, tuple(conv), where))
+        return
+    _check(fn(*args), where)
+
+
+class Prepared:
+    """C-ABI calls recorded once, with their arguments already marshalled;
+    calling the object makes them again, in order, on the recorded stream.
+    Checking shapes, dtypes and devices and converting arguments is done
+    once, at ``prepare``; the tensors must stay alive and in place."""
+
+    def __init__(self, calls):
+        self.calls = calls
+
+    def __call__(self):
+        for fn, args, where in self.calls:
+            rc = fn(*args)
+            if rc != PA_OK:
+                raise PAError(rc, where)
+
+
+def prepare(body, stream=None) -> Prepared:
+    """Run ``body()`` (which calls entry points of this module) with every C
+    call recorded instead of made, launching on ``stream`` (a
+    torch.cuda.Stream; default: the current stream when the calls run).
+    Returns the recorded calls as one callable: a serving loop that repeats
+    a step on the same tensors pays the argument checks once."""
+    if _rec.active:
+        raise RuntimeError("prepare() does not nest")
+    _rec.active = True
+    _rec.stream = None if stream is None else ctypes.c_void_p(stream.cuda_stream)
+    _rec.calls = []
+    try:
+        body()
+        return Prepared(_rec.calls)
+    finally:
+        _rec.active, _rec.stream, _rec.calls = False, None, None
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(dev) -> ctypes.c_void_p:
+    if _rec.active and _rec.stream is not None:
+        return _rec.stream
     return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
 
 
@@ -142,9 +199,9 @@ def pa_cache_append(k_new, v_new, k_cache, v_cache, slot_mapping) -> None:
     if (Hkv2, D2) != (Hkv, D) or v_new.shape != k_new.shape or v_cache.shape != k_cache.shape \
             or slot_mapping.shape[0] != T:
         raise ValueError("shape mismatch")
-    _check(load().pa_cache_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-                                  _ptr(slot_mapping), T, Hkv, D, bs, NB, _act_code(k_new.dtype),
-                                  _stream(dev)), "pa_cache_append")
+    _call(load().pa_cache_append, "pa_cache_append",
+          _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), T, Hkv, D,
+          bs, NB, _act_code(k_new.dtype), _stream(dev))
 
 
 def pa_cache_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping) -> None:
@@ -163,10 +220,9 @@ def pa_cache_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_m
     NB, _, bs, _ = k_cache.shape
     if k_scale.shape != (NB, Hkv) or v_scale.shape != (NB, Hkv) or v_cache.shape != k_cache.shape:
         raise ValueError("shape mismatch")
-    _check(load().pa_cache_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-                                      _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), T, Hkv,
-                                      D, bs, NB, _act_code(k_new.dtype), _stream(dev)),
-           "pa_cache_append_fp8")
+    _call(load().pa_cache_append_fp8, "pa_cache_append_fp8",
+          _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+          _ptr(slot_mapping), T, Hkv, D, bs, NB, _act_code(k_new.dtype), _stream(dev))
 
 
 def pa_quantize_fp8(k_src, v_src, k_cache, v_cache, k_scale, v_scale) -> None:
@@ -182,11 +238,11 @@ def pa_quantize_fp8(k_src, v_src, k_cache, v_cache, k_scale, v_scale) -> None:
         _need(sc, n + "_scale", torch.float32, 2, dev)
         if src.shape != ref.shape or codes.shape != ref.shape or sc.shape != (NB, Hkv):
             raise ValueError("shape mismatch")
-    _check(load().pa_quantize_fp8(_ptr(k_src), _ptr(v_src), _ptr(k_cache if k_src is not None else None),
-                                  _ptr(v_cache if v_src is not None else None),
-                                  _ptr(k_scale if k_src is not None else None),
-                                  _ptr(v_scale if v_src is not None else None), NB, Hkv, D, bs,
-                                  _stream(dev)), "pa_quantize_fp8")
+    _call(load().pa_quantize_fp8, "pa_quantize_fp8",
+          _ptr(k_src), _ptr(v_src), _ptr(k_cache if k_src is not None else None),
+          _ptr(v_cache if v_src is not None else None),
+          _ptr(k_scale if k_src is not None else None),
+          _ptr(v_scale if v_src is not None else None), NB, Hkv, D, bs, _stream(dev))
 
 
 def pa_copy_blocks(k_cache, v_cache, block_mapping, k_scale=None, v_scale=None) -> None:
@@ -210,9 +266,9 @@ def pa_copy_blocks(k_cache, v_cache, block_mapping, k_scale=None, v_scale=None) 
         if k_scale is not None or v_scale is not None:
             raise ValueError("scales are for E4M3 pools only")
         code = _act_code(k_cache.dtype)
-    _check(load().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-                                 _ptr(block_mapping), block_mapping.shape[0], Hkv, D, bs, NB,
-                                 code, _stream(dev)), "pa_copy_blocks")
+    _call(load().pa_copy_blocks, "pa_copy_blocks",
+          _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_mapping),
+          block_mapping.shape[0], Hkv, D, bs, NB, code, _stream(dev))
 
 
 def pa_e4m3_encode(x, codes) -> None:
@@ -220,8 +276,8 @@ def pa_e4m3_encode(x, codes) -> None:
     _need(codes, "codes", torch.uint8, None, x.device)
     if codes.numel() != x.numel():
         raise ValueError("size mismatch")
-    _check(load().pa_e4m3_encode(_ptr(x), _ptr(codes), x.numel(), _stream(x.device)),
-           "pa_e4m3_encode")
+    _call(load().pa_e4m3_encode, "pa_e4m3_encode",
+          _ptr(x), _ptr(codes), x.numel(), _stream(x.device))
 
 
 def pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, split_ctas=0) -> int:
@@ -270,12 +326,11 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_
     if workspace is not None:
         _need(workspace, "workspace", None, None, dev)
         ws_bytes = workspace.numel() * workspace.element_size()
-    _check(load().pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                            block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq,
-                            Hkv, D, bs, NB, float(scale), int(window), nq,
-                            _act_code(q.dtype), int(split_ctas), _ptr(workspace), ws_bytes,
-                            _stream(dev)),
-           "pa_decode")
+    _call(load().pa_decode, "pa_decode",
+          _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+          block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
+          float(scale), int(window), nq, _act_code(q.dtype), int(split_ctas), _ptr(workspace),
+          ws_bytes, _stream(dev))
 
 
 def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
@@ -296,12 +351,11 @@ def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, cont
     if workspace is not None:
         _need(workspace, "workspace", None, None, dev)
         ws_bytes = workspace.numel() * workspace.element_size()
-    _check(load().pa_decode_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
-                                _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
-                                _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
-                                float(scale), int(window), nq, _act_code(q.dtype),
-                                int(split_ctas), _ptr(workspace), ws_bytes, _stream(dev)),
-           "pa_decode_fp8")
+    _call(load().pa_decode_fp8, "pa_decode_fp8",
+          _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+          _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), int(max_context_len), B,
+          Hq, Hkv, D, bs, NB, float(scale), int(window), nq, _act_code(q.dtype), int(split_ctas),
+          _ptr(workspace), ws_bytes, _stream(dev))
 
 
 def _ws_bytes(workspace, dev):
@@ -330,13 +384,12 @@ def pa_decode_step(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_t
     NB, Hkv, bs, _ = k_cache.shape
     if k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape or slot_mapping.shape[0] != B:
         raise ValueError("shape mismatch")
-    _check(load().pa_decode_step(_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
-                                 _ptr(v_cache), _ptr(slot_mapping), _ptr(block_tables),
-                                 block_tables.shape[1], _ptr(context_lens), int(max_context_len),
-                                 B, Hq, Hkv, D, bs, NB, float(scale), int(window),
-                                 _act_code(q.dtype), int(split_ctas), _ptr(workspace),
-                                 _ws_bytes(workspace, dev),
-                                 _stream(dev)), "pa_decode_step")
+    _call(load().pa_decode_step, "pa_decode_step",
+          _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+          _ptr(slot_mapping), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+          int(max_context_len), B, Hq, Hkv, D, bs, NB, float(scale), int(window),
+          _act_code(q.dtype), int(split_ctas), _ptr(workspace), _ws_bytes(workspace, dev),
+          _stream(dev))
 
 
 def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping,
@@ -359,14 +412,12 @@ def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
     NB, Hkv, bs, _ = k_cache.shape
     if k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape or slot_mapping.shape[0] != B:
         raise ValueError("shape mismatch")
-    _check(load().pa_decode_step_fp8(_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
-                                     _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-                                     _ptr(slot_mapping), _ptr(block_tables), block_tables.shape[1],
-                                     _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs,
-                                     NB, float(scale), int(window), _act_code(q.dtype),
-                                     int(split_ctas), _ptr(workspace), _ws_bytes(workspace, dev),
-                                     _stream(dev)),
-           "pa_decode_step_fp8")
+    _call(load().pa_decode_step_fp8, "pa_decode_step_fp8",
+          _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+          _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), _ptr(block_tables),
+          block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
+          float(scale), int(window), _act_code(q.dtype), int(split_ctas), _ptr(workspace),
+          _ws_bytes(workspace, dev), _stream(dev))
 
 
 def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
@@ -381,12 +432,10 @@ def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
         _need(t, n, q.dtype, 4, dev)
     B, nq, Hq, D = _decode_common(out, q, block_tables, context_lens, dev)
     NB, Hkv, bs, _ = k_cache.shape
-    _check(load().pa_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
-                                    _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
-                                    int(max_context_len), B, Hq, Hkv, D, bs, NB, float(scale),
-                                    int(window), nq, _act_code(q.dtype), int(split_ctas),
-                                    _stream(dev)),
-           "pa_decode_noalloc")
+    _call(load().pa_decode_noalloc, "pa_decode_noalloc",
+          _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+          block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
+          float(scale), int(window), nq, _act_code(q.dtype), int(split_ctas), _stream(dev))
 
 
 def pa_get_status(device=None) -> tuple[int, int]:

@@ -35,6 +35,7 @@ class DecodeStep:
         self.window = int(window)           # sliding window in tokens, 0 for the whole context
         self.workspace = _abi.alloc_workspace(self.B, self.Hq, self.D, self.split_ctas,
                                               k_cache.device)
+        self._bound = {}     # run_from_staging's bound steps
 
     def append(self, k_new, v_new, slot_mapping):
         if self.kv == "fp8":
@@ -88,6 +89,13 @@ class DecodeStep:
         self.decode(q, out)
         return out
 
+    def bind(self, q, k_new, v_new, slot_mapping, out, fused=None, stream=None):
+        """The step on these tensors as a callable with its C-ABI arguments
+        checked and marshalled once (``_abi.prepare``), launching on
+        ``stream`` (default: the current stream at each call).  Each call
+        runs one step; refill the tensors in place between calls."""
+        return _abi.prepare(lambda: self(q, k_new, v_new, slot_mapping, out, fused=fused), stream)
+
     def capture(self, q, k_new, v_new, slot_mapping, out, fused=None, stream=None):
         """Record the step into a CUDA graph and return it (``torch.cuda.CUDAGraph``).
 
@@ -130,11 +138,18 @@ class DecodeStep:
     def run_from_staging(self, staging: "StepStaging", host_out, dev_out, fused=None):
         """As ``run_from_host`` with the inputs packed in one ``StepStaging``:
         one host-to-device copy for all of them (this step must have been
-        built with the staging's device block_tables and context_lens).
-        Returns (h2d bytes, d2h bytes)."""
+        built with the staging's device block_tables and context_lens).  The
+        step is bound (``bind``) on first use with a staging and output and
+        reused after.  Returns (h2d bytes, d2h bytes)."""
         h2d = staging.upload()
-        d = staging.dev
-        self(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], dev_out, fused=fused)
+        key = (id(staging), id(dev_out), fused, torch.cuda.current_stream().cuda_stream)
+        call = self._bound.get(key)
+        if call is None:             # bound once per (staging, output, form, stream)
+            d = staging.dev
+            call = self.bind(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], dev_out,
+                             fused=fused, stream=torch.cuda.current_stream())
+            self._bound[key] = call
+        call()
         host_out.copy_(dev_out, non_blocking=True)
         return h2d, host_out.numel() * host_out.element_size()
 
@@ -179,7 +194,9 @@ class StepPipeline:
     current step), the steps in order on a compute stream of the pipeline's
     own, with events keeping a staging from being re-uploaded while a step
     still reads it and an output buffer from being rewritten before it is
-    read back.
+    read back.  Each slot's step is bound once (``DecodeStep.bind``), and
+    the events are made once and recorded again at every use, so a submit
+    costs the host a handful of calls.
     Each submit first orders the compute stream after the caller's stream;
     ``finish`` orders the caller's stream after everything submitted.
 
@@ -199,9 +216,10 @@ class StepPipeline:
                         for _ in range(depth)]
         self.host_out = [torch.empty(out_shape, dtype=out_dtype).pin_memory()
                          for _ in range(depth)]
-        self.uploaded = [None] * depth     # upload of the slot's latest step done
-        self.stepped = [None] * depth      # the slot's latest step done
-        self.read_back = [None] * depth    # the slot's latest output copied to the host
+        self.uploaded = [torch.cuda.Event() for _ in range(depth)]    # the slot's upload done
+        self.stepped = [torch.cuda.Event() for _ in range(depth)]     # the slot's step done
+        self.read_back = [torch.cuda.Event() for _ in range(depth)]   # its output on the host
+        self.calls = {}        # (slot, fused) -> the bound step
         self.n = 0
 
     def slot(self) -> int:
@@ -209,37 +227,40 @@ class StepPipeline:
 
     def wait_slot_free(self):
         """Block the host until the next slot's host buffer may be refilled."""
-        k = self.slot()
-        if self.uploaded[k] is not None:
-            self.uploaded[k].synchronize()
+        if self.n >= self.depth:
+            self.uploaded[self.slot()].synchronize()
+
+    def _call(self, k, fused):
+        key = (k, fused)
+        if key not in self.calls:
+            d = self.stagings[k].dev
+            self.calls[key] = self.steps[k].bind(d["q"], d["k_new"], d["v_new"],
+                                                 d["slot_mapping"], self.dev_out[k], fused=fused,
+                                                 stream=self.compute)
+        return self.calls[key]
 
     def submit(self, fused=None):
         """Upload the next slot's inputs, run its step, read its output back.
         Returns (slot, h2d bytes, d2h bytes); ``host_out[slot]`` holds the
         output once ``read_back[slot]`` has completed."""
         k = self.slot()
-        cur = self.compute
-        cur.wait_stream(torch.cuda.current_stream())
+        reused = self.n >= self.depth
+        step = self._call(k, fused)
+        self.compute.wait_stream(torch.cuda.current_stream())
+        if reused:
+            self.copy.wait_event(self.stepped[k])         # the slot's last step is done with it
         with torch.cuda.stream(self.copy):
-            if self.stepped[k] is not None:
-                self.copy.wait_event(self.stepped[k])     # the slot's last step is done with it
             h2d = self.stagings[k].upload()
-            self.uploaded[k] = torch.cuda.Event()
-            self.uploaded[k].record(self.copy)
-        cur.wait_event(self.uploaded[k])
-        if self.read_back[k] is not None:
-            cur.wait_event(self.read_back[k])             # the slot's last output was read
-        d = self.stagings[k].dev
-        with torch.cuda.stream(cur):
-            self.steps[k](d["q"], d["k_new"], d["v_new"], d["slot_mapping"], self.dev_out[k],
-                          fused=fused)
-        self.stepped[k] = torch.cuda.Event()
-        self.stepped[k].record(cur)
+        self.uploaded[k].record(self.copy)
+        self.compute.wait_event(self.uploaded[k])
+        if reused:
+            self.compute.wait_event(self.read_back[k])    # the slot's last output was read
+        step()
+        self.stepped[k].record(self.compute)
+        self.back.wait_event(self.stepped[k])
         with torch.cuda.stream(self.back):
-            self.back.wait_event(self.stepped[k])
             self.host_out[k].copy_(self.dev_out[k], non_blocking=True)
-            self.read_back[k] = torch.cuda.Event()
-            self.read_back[k].record(self.back)
+        self.read_back[k].record(self.back)
         self.n += 1
         return k, h2d, self.host_out[k].numel() * self.host_out[k].element_size()
 

@@ -198,3 +198,29 @@ def test_step_pipeline_overlapped_copies_match_direct_calls():
     for k, out in got:
         assert torch.equal(out.view(torch.int16), refs[k].view(torch.int16))
     assert torch.equal(kc.view(torch.int16), k2.view(torch.int16))
+
+
+def test_bound_step_records_once_and_matches_direct_calls():
+    """DecodeStep.bind: recording launches nothing; each call of the bound
+    step equals a direct step on the same inputs, pools included."""
+    w = to_cuda(W.make_workload("qwen2_5_1_5b", seed=11))
+    k2, v2 = w.k_cache.clone(), w.v_cache.clone()
+    step = DecodeStep(k_cache=w.k_cache, v_cache=w.v_cache, block_tables=w.block_tables,
+                      context_lens=w.context_lens, max_context_len=w.max_context_len,
+                      scale=w.scale, num_q_heads=w.Hq)
+    ref_step = DecodeStep(k_cache=k2, v_cache=v2, block_tables=w.block_tables,
+                          context_lens=w.context_lens, max_context_len=w.max_context_len,
+                          scale=w.scale, num_q_heads=w.Hq)
+    for fused in (True, False):
+        out = torch.full_like(w.q, float("nan"))
+        call = step.bind(w.q, w.k_new, w.v_new, w.slot_mapping, out, fused=fused)
+        torch.cuda.synchronize()
+        assert torch.isnan(out).all()              # nothing ran while recording
+        ref = torch.empty_like(w.q)
+        for _ in range(2):
+            call()
+            ref_step(w.q, w.k_new, w.v_new, w.slot_mapping, ref, fused=fused)
+            assert _abi.pa_get_status() == (0, 0)
+            assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+        assert torch.equal(w.k_cache.view(torch.int16), k2.view(torch.int16))
+        assert torch.equal(w.v_cache.view(torch.int16), v2.view(torch.int16))
