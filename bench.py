@@ -81,8 +81,20 @@ def algorithmic_bytes(w, lens: np.ndarray, window: int = 0) -> dict:
     scales = int(nblk.sum()) * w.Hkv * 2 * 4 if w.kv == "fp8" else 0
     # the fused step also reads this step's K/V rows and writes them to the pools
     append = w.B * w.Hkv * w.D * 2 * (2 + e_kv) + w.B * 8
+    # K/V bytes of distinct physical blocks (a shared prefix counted once): the
+    # rows of each block attended by any sequence
+    tables = w.block_tables.cpu().numpy()
+    rows = {}
+    for b in range(w.B):
+        lo = int(first[b]) if window > 0 else 0
+        for j in range(lo, lo + int(nblk[b])):
+            blk = int(tables[b, j])
+            r0 = max(0, int(L[b]) - window - j * w.block_size) if window > 0 else 0
+            n = min(w.block_size, int(L[b]) - j * w.block_size) - min(r0, w.block_size)
+            rows[blk] = max(rows.get(blk, 0), n)
+    kv_unique = sum(rows.values()) * w.Hkv * 2 * w.D * e_kv
     return {"kv": kv, "q_out": qo, "meta": meta, "scales": scales, "append": append,
-            "total": kv + qo + meta + scales}
+            "total": kv + qo + meta + scales, "kv_unique": kv_unique}
 
 
 class ClockSampler:
@@ -319,6 +331,18 @@ def run_ours(args, rank, world, dev):
     if world > 1:
         torch.distributed.barrier()
 
+    # for the spread of single steps: each step between its own two events
+    # (which add about 2 us each to what they time), after the timed region
+    per_ev = []
+    if back_to_back:
+        pe = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for i in range(K):
+            pe[i][0].record(stream)
+            run_step(i)
+            pe[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        per_ev = [a.elapsed_time(b) for a, b in pe]
+
     # the dominant kernel (decode_kernel, then merge_kernel): the fused step
     # itself, or pa_decode timed alone the same way
     if fused:
@@ -448,7 +472,11 @@ def run_ours(args, rank, world, dev):
                      "kernel": ("decode_kernel with fused append, then merge_kernel (timed "
                                 "together: one decode)" if fused
                                 else "decode_kernel, then merge_kernel (timed together: one decode)"),
-                     "bytes_per_launch": kernel_bytes, "peak_source": peak_kind},
+                     "bytes_per_launch": kernel_bytes, "peak_source": peak_kind,
+                     **({"kv_bytes_unique": ab["kv_unique"],
+                         "note": "a shared prefix is read by each sequence attending it and "
+                                 "counted each time; kv_bytes_unique counts it once"}
+                        if ab["kv_unique"] != ab["kv"] else {})},
         "decode_us": ({"mean": round(statistics.mean(dec_ms) * 1e3, 2),
                        "timing": "K decodes back to back between two events"} if back_to_back else
                       {"mean": round(statistics.mean(dec_ms) * 1e3, 2),
@@ -457,6 +485,13 @@ def run_ours(args, rank, world, dev):
                        "p80": round(float(np.percentile(dec_ms, 80)) * 1e3, 2),
                        "min": round(min(dec_ms) * 1e3, 2),
                        "timing": "each decode between its own events, L2 evicted before it"}),
+        **({"step_us_own_events": {
+            "median": round(statistics.median(per_ev) * 1e3, 2),
+            "p20": round(float(np.percentile(per_ev, 20)) * 1e3, 2),
+            "p80": round(float(np.percentile(per_ev, 80)) * 1e3, 2),
+            "min": round(min(per_ev) * 1e3, 2),
+            "note": "each step between its own two events; the events add about 2 us"}}
+           if per_ev else {}),
         "as_two_launches_us": {"append": round(statistics.mean(app_ms) * 1e3, 2),
                                "decode": round(statistics.mean(dec2_ms) * 1e3, 2)},
         "e2e": {"value": round(tokens_all * K / (e2e_ms_max / 1e3), 1), "unit": UNIT,
