@@ -265,9 +265,14 @@ def run_ours(args, rank, world, dev):
     else:
         copies = 1
     pool_sets = [pools] + [{k: t.clone() for k, t in pools.items()} for _ in range(copies - 1)]
+    # the timed steps: nothing between them writes context_lens or block_tables,
+    # so the attention launch may start its prologue while the previous
+    # step's merge finishes (PA_DECODE_EARLY_PROLOGUE)
+    early = args.early_prologue == "on"
     steps = [DecodeStep(**ps, block_tables=w.block_tables, context_lens=w.context_lens,
                         max_context_len=w.max_context_len, scale=w.scale, num_q_heads=w.Hq,
-                        split_ctas=args.splits, window=args.window) for ps in pool_sets]
+                        split_ctas=args.splits, window=args.window, early_prologue=early)
+             for ps in pool_sets]
     step = steps[0]
     back_to_back = l2_mode in ("none", "rotate")
     flush_buf = torch.ones(max(2 * l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
@@ -463,6 +468,9 @@ def run_ours(args, rank, world, dev):
             "step": ("pa_decode_step: append inside the attention launch, then the merge launch"
                      if fused else "append launch, then attention and merge launches"),
             "split_ctas": step.split_ctas, "l2": describe_l2(l2_mode, kv_bytes, l2, copies),
+            "launch": ("attention launch with an early prologue (PA_DECODE_EARLY_PROLOGUE: "
+                       "it may start while the previous step's merge finishes)" if early else
+                       "plain launches"),
             "seed": args.seed, "parallelism": "replicas" if world > 1 else "single GPU",
             **({"window": args.window} if args.window else {}),
         },
@@ -760,6 +768,9 @@ def main(argv=None):
     ap.add_argument("--copy-pairs", type=int, default=8192)
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window in tokens (0: each sequence attends its whole context)")
+    ap.add_argument("--early-prologue", choices=["on", "off"], default="on",
+                    help="timed steps with PA_DECODE_EARLY_PROLOGUE (the end-to-end run, whose "
+                         "steps follow uploads of their tables, never uses it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-step-s", type=float, default=2.0)

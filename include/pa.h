@@ -86,6 +86,9 @@ enum {
                                     was not zero-filled (or a call that timed out left it so) and
                                     results may be wrong; detected on a best-effort basis */
 
+/* Decode flags (the flags argument of the decode entry points). */
+#define PA_DECODE_EARLY_PROLOGUE 1u   /* the prologue may overlap the previous kernel: see pa_decode */
+
 /*
  * Append: for each token i with s = slot_mapping[i] >= 0 and each kv head h,
  * copy k_new[i][h][:] to k_cache[s / block_size][h][s % block_size][:] and
@@ -220,7 +223,16 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int
  *   8 / group tokens, each reading the K/V again (pa_decode_noalloc rejects
  *   them with PA_ERR_UNSUPPORTED);
  *   workspace: at least pa_decode_workspace_size(...) bytes, 256-byte
- *   aligned.
+ *   aligned;
+ *   flags: 0, or PA_DECODE_EARLY_PROLOGUE: the attention launch becomes a
+ *   programmatic dependent launch.  Its prologue (reading context_lens and
+ *   block_tables, dividing the batch among the warps, reading each warp's
+ *   first block ids) may then run while the kernel before it on the stream
+ *   is still finishing; everything else (q, the pools and scales, the new
+ *   rows, out, the workspace) waits until that kernel has completed.  Set it
+ *   only when the kernel just before the call on the stream does not write
+ *   context_lens or block_tables (for example, when they are uploaded by a
+ *   copy before the forward pass).  Results are the same either way.
  * Source: rvLLM, CUDA Kernels table, "PagedAttention V2" (block-table
  * indirection, online softmax); LLM Serving Kernels, Projects table, row 04;
  * rvllm (small engine), How it's put together (GQA, read_blocks).
@@ -230,7 +242,7 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
               int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
               int block_size, int num_blocks, float scale, int window_size, int queries_per_seq,
               int dtype, int split_ctas,
-              void *workspace, size_t workspace_bytes, void *stream);
+              void *workspace, size_t workspace_bytes, unsigned flags, void *stream);
 
 /*
  * Paged GQA decode over an E4M3 pool: as pa_decode (q and out of dtype
@@ -248,7 +260,7 @@ int pa_decode_fp8(void *out, const void *q, const uint8_t *k_cache, const uint8_
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                   int num_blocks, float scale, int window_size, int queries_per_seq,
                   int dtype, int split_ctas, void *workspace,
-                  size_t workspace_bytes, void *stream);
+                  size_t workspace_bytes, unsigned flags, void *stream);
 
 /*
  * One whole decode step in one attention launch (plus pa_decode's merge
@@ -274,8 +286,8 @@ int pa_decode_step(void *out, const void *q, const void *k_new, const void *v_ne
                    const int32_t *block_tables, int max_blocks_per_seq,
                    const int32_t *context_lens, int max_context_len, int num_seqs,
                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                   int num_blocks, float scale, int window_size, int dtype, int split_ctas, void *workspace,
-                   size_t workspace_bytes, void *stream);
+                   int num_blocks, float scale, int window_size, int dtype, int split_ctas,
+                   void *workspace, size_t workspace_bytes, unsigned flags, void *stream);
 
 /*
  * pa_decode_step over E4M3 pools: q, k_new, v_new and out of dtype PA_F16 or
@@ -289,8 +301,9 @@ int pa_decode_step_fp8(void *out, const void *q, const void *k_new, const void *
                        const int64_t *slot_mapping, const int32_t *block_tables,
                        int max_blocks_per_seq, const int32_t *context_lens, int max_context_len,
                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                       int block_size, int num_blocks, float scale, int window_size, int dtype, int split_ctas,
-                       void *workspace, size_t workspace_bytes, void *stream);
+                       int block_size, int num_blocks, float scale, int window_size, int dtype,
+                       int split_ctas, void *workspace, size_t workspace_bytes, unsigned flags,
+                       void *stream);
 
 /*
  * pa_decode without a caller-provided workspace, for callers that cannot
@@ -317,7 +330,7 @@ int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void 
                       const int32_t *context_lens, int max_context_len, int num_seqs,
                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                       int num_blocks, float scale, int window_size, int queries_per_seq,
-                      int dtype, int split_ctas, void *stream);
+                      int dtype, int split_ctas, unsigned flags, void *stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status

@@ -23,9 +23,11 @@ PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_LEN, PA_STATUS_BAD_SLOT, PA_STATUS_TIMEOUT = 1, 2, 4, 8
 PA_STATUS_NO_WORKSPACE = 16
 PA_STATUS_WS_DIRTY = 32
+PA_DECODE_EARLY_PROLOGUE = 1
 
 # (name, argtypes, restype) of every exported entry point
 _vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_u32 = ctypes.c_uint
 SIGNATURES = {
     "pa_version": ([], _i32),
     "pa_status_string": ([_i32], ctypes.c_char_p),
@@ -38,15 +40,16 @@ SIGNATURES = {
     "pa_decode_workspace_size": ([_i32, _i32, _i32, _i32], _sz),
     "pa_decode_default_splits": ([_i32], _i32),
     "pa_decode": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
-                   _f32, _i32, _i32, _i32, _i32, _vp, _sz, _vp], _i32),
+                   _f32, _i32, _i32, _i32, _i32, _vp, _sz, _u32, _vp], _i32),
     "pa_decode_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
-                       _i32, _i32, _f32, _i32, _i32, _i32, _i32, _vp, _sz, _vp], _i32),
+                       _i32, _i32, _f32, _i32, _i32, _i32, _i32, _vp, _sz, _u32, _vp], _i32),
     "pa_decode_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
-                        _i32, _i32, _i32, _f32, _i32, _i32, _i32, _vp, _sz, _vp], _i32),
+                        _i32, _i32, _i32, _f32, _i32, _i32, _i32, _vp, _sz, _u32, _vp], _i32),
     "pa_decode_step_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
-                            _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _i32, _vp, _sz, _vp], _i32),
+                            _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _i32, _vp, _sz, _u32,
+                            _vp], _i32),
     "pa_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
-                           _i32, _i32, _f32, _i32, _i32, _i32, _i32, _vp], _i32),
+                           _i32, _i32, _f32, _i32, _i32, _i32, _i32, _u32, _vp], _i32),
     "pa_get_status": ([_vp, ctypes.POINTER(ctypes.c_uint)], _i32),
 }
 
@@ -170,6 +173,10 @@ def _need(t, name, dtype=None, ndim=None, device=None):
         raise ValueError(f"{name} must have {ndim} dims, has {t.dim()}")
     if device is not None and t.device != device:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _flags(early_prologue: bool) -> int:
+    return PA_DECODE_EARLY_PROLOGUE if early_prologue else 0
 
 
 def _act_code(dtype) -> int:
@@ -312,8 +319,11 @@ def _decode_common(out, q, block_tables, context_lens, dev):
 
 
 def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
-              scale: float, split_ctas: int = 0, workspace=None, *, window: int = 0) -> None:
-    """out[b][hq] = softmax(scale q.K) V over each sequence's blocks (16-bit pools)."""
+              scale: float, split_ctas: int = 0, workspace=None, *, window: int = 0,
+              early_prologue: bool = False) -> None:
+    """out[b][hq] = softmax(scale q.K) V over each sequence's blocks (16-bit pools).
+    early_prologue: PA_DECODE_EARLY_PROLOGUE (the kernel before this call on
+    the stream must not write context_lens or block_tables)."""
     dev = q.device
     act = (torch.float16, torch.bfloat16)
     _need(q, "q", act, None, dev)
@@ -330,12 +340,12 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_
           _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
           block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
           float(scale), int(window), nq, _act_code(q.dtype), int(split_ctas), _ptr(workspace),
-          ws_bytes, _stream(dev))
+          ws_bytes, _flags(early_prologue), _stream(dev))
 
 
 def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
                   max_context_len: int, scale: float, split_ctas: int = 0, workspace=None, *,
-                  window: int = 0) -> None:
+                  window: int = 0, early_prologue: bool = False) -> None:
     """As pa_decode over E4M3 pools with per-(block, kv head) fp32 scales; q/out
     fp16 or bf16."""
     dev = q.device
@@ -355,7 +365,7 @@ def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, cont
           _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
           _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), int(max_context_len), B,
           Hq, Hkv, D, bs, NB, float(scale), int(window), nq, _act_code(q.dtype), int(split_ctas),
-          _ptr(workspace), ws_bytes, _stream(dev))
+          _ptr(workspace), ws_bytes, _flags(early_prologue), _stream(dev))
 
 
 def _ws_bytes(workspace, dev):
@@ -367,7 +377,7 @@ def _ws_bytes(workspace, dev):
 
 def pa_decode_step(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_tables,
                    context_lens, max_context_len: int, scale: float, split_ctas: int = 0,
-                   workspace=None, *, window: int = 0) -> None:
+                   workspace=None, *, window: int = 0, early_prologue: bool = False) -> None:
     """Append k_new/v_new at slot_mapping, then decode, in one launch (16-bit pools)."""
     dev = q.device
     act = (torch.float16, torch.bfloat16)
@@ -389,12 +399,13 @@ def pa_decode_step(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_t
           _ptr(slot_mapping), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
           int(max_context_len), B, Hq, Hkv, D, bs, NB, float(scale), int(window),
           _act_code(q.dtype), int(split_ctas), _ptr(workspace), _ws_bytes(workspace, dev),
-          _stream(dev))
+          _flags(early_prologue), _stream(dev))
 
 
 def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping,
                        block_tables, context_lens, max_context_len: int, scale: float,
-                       split_ctas: int = 0, workspace=None, *, window: int = 0) -> None:
+                       split_ctas: int = 0, workspace=None, *, window: int = 0,
+                       early_prologue: bool = False) -> None:
     """Append (E4M3-encode) k_new/v_new, then decode over the E4M3 pools, in one
     attention launch; q, k_new, v_new and out share one dtype (fp16 or bf16)."""
     dev = q.device
@@ -417,12 +428,12 @@ def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
           _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), _ptr(block_tables),
           block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
           float(scale), int(window), _act_code(q.dtype), int(split_ctas), _ptr(workspace),
-          _ws_bytes(workspace, dev), _stream(dev))
+          _ws_bytes(workspace, dev), _flags(early_prologue), _stream(dev))
 
 
 def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
                       max_context_len: int, scale: float, split_ctas: int = 0,
-                      window: int = 0) -> None:
+                      window: int = 0, early_prologue: bool = False) -> None:
     """pa_decode with the library's static scratch instead of a workspace (allocates nothing)."""
     dev = q.device
     act = (torch.float16, torch.bfloat16)
@@ -435,7 +446,8 @@ def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
     _call(load().pa_decode_noalloc, "pa_decode_noalloc",
           _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
           block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
-          float(scale), int(window), nq, _act_code(q.dtype), int(split_ctas), _stream(dev))
+          float(scale), int(window), nq, _act_code(q.dtype), int(split_ctas),
+          _flags(early_prologue), _stream(dev))
 
 
 def pa_get_status(device=None) -> tuple[int, int]:

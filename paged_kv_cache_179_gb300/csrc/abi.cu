@@ -54,6 +54,7 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; 
 struct DecodeShape {
   int B, Hq, Hkv, D, bs, NB, mbs, max_ctx, splits, window;
   int nq = 1;   // query tokens per sequence
+  unsigned flags = 0;   // PA_DECODE_* flags
 };
 
 int check_decode_shape(const DecodeShape& s, float scale) {
@@ -66,6 +67,7 @@ int check_decode_shape(const DecodeShape& s, float scale) {
   if (s.bs != 16) return PA_ERR_UNSUPPORTED;
   if (s.nq < 1 || s.nq > 1024) return PA_ERR_INVALID_ARG;
   if (s.Hq / s.Hkv > 8) return PA_ERR_UNSUPPORTED;
+  if (s.flags & ~PA_DECODE_EARLY_PROLOGUE) return PA_ERR_INVALID_ARG;
   if (s.B > 65535 || s.Hkv > 65535) return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
@@ -115,6 +117,7 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
   a.n_q = s.nq;
   a.q_tokens = s.nq;
   a.q_first = 0;
+  a.early = (s.flags & PA_DECODE_EARLY_PROLOGUE) ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.k_pool_w = ap.k_pool;
   a.v_pool_w = ap.v_pool;
@@ -172,7 +175,7 @@ using namespace pa;
 
 extern "C" {
 
-int pa_version(void) { return 100; }
+int pa_version(void) { return 101; }
 
 const char* pa_status_string(int code) {
   switch (code) {
@@ -314,7 +317,7 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
               int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
               int block_size, int num_blocks, float scale, int window_size, int queries_per_seq,
               int dtype, int split_ctas,
-              void* workspace, size_t workspace_bytes, void* stream) {
+              void* workspace, size_t workspace_bytes, unsigned flags, void* stream) {
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
     return PA_ERR_INVALID_ARG;
@@ -322,6 +325,7 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                       num_blocks, max_blocks_per_seq, max_context_len, split_ctas, window_size};
   s.nq = queries_per_seq;
+  s.flags = flags;
   if (int rc = check_decode_shape(s, scale)) return rc;
   for (const void* p : {static_cast<const void*>(out), q, k_cache, v_cache})
     if (!aligned(p, 16)) return PA_ERR_INVALID_ARG;
@@ -336,7 +340,7 @@ int pa_decode_fp8(void* out, const void* q, const uint8_t* k_cache, const uint8_
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                   int num_blocks, float scale, int window_size, int queries_per_seq,
                   int dtype, int split_ctas, void* workspace,
-                  size_t workspace_bytes, void* stream) {
+                  size_t workspace_bytes, unsigned flags, void* stream) {
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables ||
       !context_lens)
@@ -345,6 +349,7 @@ int pa_decode_fp8(void* out, const void* q, const uint8_t* k_cache, const uint8_
   DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                       num_blocks, max_blocks_per_seq, max_context_len, split_ctas, window_size};
   s.nq = queries_per_seq;
+  s.flags = flags;
   if (int rc = check_decode_shape(s, scale)) return rc;
   for (const void* p : {static_cast<const void*>(out), q, static_cast<const void*>(k_cache),
                         static_cast<const void*>(v_cache)})
@@ -361,15 +366,16 @@ int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_ne
                    const int32_t* block_tables, int max_blocks_per_seq,
                    const int32_t* context_lens, int max_context_len, int num_seqs,
                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                   int num_blocks, float scale, int window_size, int dtype, int split_ctas, void* workspace,
-                   size_t workspace_bytes, void* stream) {
+                   int num_blocks, float scale, int window_size, int dtype, int split_ctas,
+                   void* workspace, size_t workspace_bytes, unsigned flags, void* stream) {
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_new || !v_new || !k_cache || !v_cache || !slot_mapping ||
       !block_tables || !context_lens)
     return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
-  const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                      num_blocks, max_blocks_per_seq, max_context_len, split_ctas, window_size};
+  DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                num_blocks, max_blocks_per_seq, max_context_len, split_ctas, window_size};
+  s.flags = flags;
   if (int rc = check_decode_shape(s, scale)) return rc;
   for (const void* p : {static_cast<const void*>(out), q, k_new, v_new,
                         static_cast<const void*>(k_cache), static_cast<const void*>(v_cache)})
@@ -391,15 +397,17 @@ int pa_decode_step_fp8(void* out, const void* q, const void* k_new, const void* 
                        const int64_t* slot_mapping, const int32_t* block_tables,
                        int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                       int block_size, int num_blocks, float scale, int window_size, int dtype, int split_ctas,
-                       void* workspace, size_t workspace_bytes, void* stream) {
+                       int block_size, int num_blocks, float scale, int window_size, int dtype,
+                       int split_ctas, void* workspace, size_t workspace_bytes, unsigned flags,
+                       void* stream) {
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_new || !v_new || !k_cache || !v_cache || !k_scale || !v_scale ||
       !slot_mapping || !block_tables || !context_lens)
     return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
-  const DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                      num_blocks, max_blocks_per_seq, max_context_len, split_ctas, window_size};
+  DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                num_blocks, max_blocks_per_seq, max_context_len, split_ctas, window_size};
+  s.flags = flags;
   if (int rc = check_decode_shape(s, scale)) return rc;
   for (const void* p : {static_cast<const void*>(out), q, k_new, v_new,
                         static_cast<const void*>(k_cache), static_cast<const void*>(v_cache)})

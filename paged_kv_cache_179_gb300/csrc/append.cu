@@ -23,6 +23,9 @@ append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
               uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
               const int64_t* __restrict__ slots, int T, int Hkv, int chunks_per_row,
               int block_size, int64_t num_slots, unsigned* status) {
+  // a decode launched next with an early prologue may start its prologue now
+  // (it waits for this launch to complete before reading the pools)
+  griddep_launch_dependents();
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t per_tok = static_cast<int64_t>(Hkv) * chunks_per_row;
   if (idx >= per_tok * T) return;
@@ -52,6 +55,7 @@ append_fp8_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict
                   float* __restrict__ k_scale, float* __restrict__ v_scale,
                   const int64_t* __restrict__ slots, int T, int Hkv, int block_size,
                   int64_t num_slots, unsigned* status) {
+  griddep_launch_dependents();   // as in append_kernel
   const int lane = threadIdx.x & 31;
   const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (w >= static_cast<int64_t>(T) * Hkv * 2) return;

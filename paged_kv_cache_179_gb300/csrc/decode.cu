@@ -691,18 +691,25 @@ decode_kernel(const DecodeArgs a) {
   const int64_t W = pf[B];
   const int cta = blockIdx.x;
 
-  // ---- 2. sequences with nothing to attend get a zero output
-  for (int b = cta; b < B; b += gridDim.x) {
-    const int L = len[b];
-    if (L > 0) continue;
-    if (L < 0 && tid == 0) atomicOr(a.status, kStatusBadLen);
-    uint16_t* o = static_cast<uint16_t*>(a.out) +
-                  (static_cast<int64_t>(b) * a.q_tokens + a.q_first) * Hq * D;
-    for (int i = tid; i < a.n_q * Hq * D; i += kThreads) o[i] = 0;   // +0.0 in f16 and bf16
-  }
-
   // The merge launch may be scheduled now: it waits for the partials it reads.
   griddep_launch_dependents();
+
+  // ---- 2. the previous kernel on the stream.  With an early prologue this
+  // launch may have started before it finished: the prologue above and the
+  // block-table reads below touch only what that kernel does not write
+  // (context_lens, block_tables); everything else waits for it here.
+  // Then sequences with nothing to attend get a zero output (one warp each).
+  auto after_previous_kernel = [&]() {
+    if (a.early) griddep_wait();
+    for (int b = cta * kWarps + warp; b < B; b += static_cast<int>(gridDim.x) * kWarps) {
+      const int L = len[b];
+      if (L > 0) continue;
+      if (L < 0 && lane == 0) atomicOr(a.status, kStatusBadLen);
+      uint16_t* o = static_cast<uint16_t*>(a.out) +
+                    (static_cast<int64_t>(b) * a.q_tokens + a.q_first) * Hq * D;
+      for (int i = lane; i < a.n_q * Hq * D; i += 32) o[i] = 0;   // +0.0 in f16 and bf16
+    }
+  };
 
   // ---- 3. this warp's share of the block stream.  No CTA-wide barrier
   // follows: every warp is an independent worker from here on.  Never more
@@ -710,7 +717,10 @@ decode_kernel(const DecodeArgs a) {
   // bookkeeping relies on it).
   const int64_t NW = min(static_cast<int64_t>(gridDim.x) * kWarps, W);
   const int gw = cta * kWarps + warp;
-  if (gw >= NW) return;
+  if (gw >= NW) {
+    after_previous_kernel();
+    return;
+  }
   const int64_t lo = worker_lo(gw, W, NW), hi = worker_lo(gw + 1, W, NW);
 
   const uint32_t ring = smem_u32(smem) + warp * STAGES * TL::SLOT;
@@ -733,6 +743,7 @@ decode_kernel(const DecodeArgs a) {
   int id0 = chunk_id(ch0);
   int id1 = chunk_id(ch1);
   int id2 = chunk_id(ch2);
+  after_previous_kernel();
   float ks0 = 1.f, vs0 = 1.f, ks1 = 1.f, vs1 = 1.f;   // E4M3 page scales of chunks k, k+1
   if constexpr (FP8) {
     if (id0 >= 0 && id0 < a.num_blocks) {
@@ -996,6 +1007,9 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(kMergeThreads, 2)
 merge_kernel(const DecodeArgs a) {
   PA_TRACE_ONLY(const unsigned long long t_in = pa_now());
+  // a decode launched after this one with an early prologue may start now:
+  // it waits for this launch to complete before touching what it writes
+  griddep_launch_dependents();
   __shared__ int red[kMergeThreads / 32][2];
   __shared__ unsigned want;
   __shared__ int fail;
@@ -1208,8 +1222,25 @@ cudaError_t launch_one(const DecodeArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     last_smem[dev & 63] = lay.total;
   }
-  kern<<<static_cast<unsigned>(a.split_ctas), kThreads, lay.total, s>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.early) {
+    // a programmatic dependent launch: the prologue may overlap the previous
+    // kernel on the stream, the rest waits for it (griddepcontrol.wait)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.split_ctas));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(lay.total);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a);
+  } else {
+    kern<<<static_cast<unsigned>(a.split_ctas), kThreads, lay.total, s>>>(a);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) return e;
   if (a.ws_acc == nullptr) return cudaSuccess;
   return launch_merge<D, BF16>(a, s);
 }

@@ -66,7 +66,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
                                  int max_context_len, int num_seqs, int num_q_heads,
                                  int num_kv_heads, int head_dim, int block_size, int num_blocks,
                                  float scale, int window_size, int queries_per_seq,
-                                 int dtype, int split_ctas, void* stream) {
+                                 int dtype, int split_ctas, unsigned flags, void* stream) {
   using namespace pa;
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
@@ -75,7 +75,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
     return PA_ERR_INVALID_ARG;
   if (num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 || split_ctas < 0 ||
-      window_size < 0 || queries_per_seq < 1)
+      window_size < 0 || queries_per_seq < 1 || (flags & ~PA_DECODE_EARLY_PROLOGUE) != 0)
     return PA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(max_context_len) >
       static_cast<int64_t>(max_blocks_per_seq) * block_size)
@@ -114,6 +114,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   a.n_q = queries_per_seq;
   a.q_tokens = queries_per_seq;
   a.q_first = 0;
+  a.early = (flags & PA_DECODE_EARLY_PROLOGUE) ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   {

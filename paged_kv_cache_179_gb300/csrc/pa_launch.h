@@ -44,6 +44,7 @@ struct DecodeArgs {
   int n_q;                      // query tokens this launch serves (n_q * group <= 8)
   int q_tokens;                 // query tokens per sequence in q and out
   int q_first;                  // the first of them this launch serves
+  int early;                    // programmatic dependent launch: prologue before griddepcontrol.wait
   float scale_log2;             // softmax scale * log2(e)
 };
 

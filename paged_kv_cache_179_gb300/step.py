@@ -21,7 +21,8 @@ class DecodeStep:
     """
 
     def __init__(self, *, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
-                 num_q_heads, k_scale=None, v_scale=None, split_ctas=0, window=0):
+                 num_q_heads, k_scale=None, v_scale=None, split_ctas=0, window=0,
+                 early_prologue=False):
         self.kv = "fp8" if k_cache.dtype == torch.uint8 else "16"
         self.k_cache, self.v_cache = k_cache, v_cache
         self.k_scale, self.v_scale = k_scale, v_scale
@@ -33,6 +34,9 @@ class DecodeStep:
         self.NB, self.Hkv, self.bs, self.D = (int(x) for x in k_cache.shape)
         self.split_ctas = int(split_ctas) or _abi.pa_decode_default_splits(k_cache.dtype)
         self.window = int(window)           # sliding window in tokens, 0 for the whole context
+        # the attention launch's prologue may overlap the kernel before it on
+        # the stream (which must then not write context_lens or block_tables)
+        self.early_prologue = bool(early_prologue)
         self.workspace = _abi.alloc_workspace(self.B, self.Hq, self.D, self.split_ctas,
                                               k_cache.device)
         self._bound = {}     # run_from_staging's bound steps
@@ -48,11 +52,13 @@ class DecodeStep:
         if self.kv == "fp8":
             _abi.pa_decode_fp8(out, q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
                                self.block_tables, self.context_lens, self.max_context_len,
-                               self.scale, self.split_ctas, self.workspace, window=self.window)
+                               self.scale, self.split_ctas, self.workspace, window=self.window,
+                               early_prologue=self.early_prologue)
         else:
             _abi.pa_decode(out, q, self.k_cache, self.v_cache, self.block_tables,
                            self.context_lens, self.max_context_len, self.scale,
-                           self.split_ctas, self.workspace, window=self.window)
+                           self.split_ctas, self.workspace, window=self.window,
+                           early_prologue=self.early_prologue)
 
     def fused(self, q, k_new, v_new, slot_mapping, out):
         """Append and decode in one launch (slot_mapping must hold each
@@ -61,11 +67,13 @@ class DecodeStep:
             _abi.pa_decode_step_fp8(out, q, k_new, v_new, self.k_cache, self.v_cache,
                                     self.k_scale, self.v_scale, slot_mapping, self.block_tables,
                                     self.context_lens, self.max_context_len, self.scale,
-                                    self.split_ctas, self.workspace, window=self.window)
+                                    self.split_ctas, self.workspace, window=self.window,
+                                    early_prologue=self.early_prologue)
         else:
             _abi.pa_decode_step(out, q, k_new, v_new, self.k_cache, self.v_cache, slot_mapping,
                                 self.block_tables, self.context_lens, self.max_context_len,
-                                self.scale, self.split_ctas, self.workspace, window=self.window)
+                                self.scale, self.split_ctas, self.workspace, window=self.window,
+                                early_prologue=self.early_prologue)
         return out
 
     @property

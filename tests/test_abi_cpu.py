@@ -38,7 +38,7 @@ def test_header_and_binding_agree():
 def test_library_exports_every_declared_symbol(lib):
     for name in header_functions():
         assert hasattr(lib, name), name
-    assert lib.pa_version() == 100
+    assert lib.pa_version() == 101
     assert lib.pa_status_string(0) == b"ok"
     assert b"workspace" in lib.pa_status_string(3)
 
@@ -46,18 +46,19 @@ def test_library_exports_every_declared_symbol(lib):
 def _decode(lib, **kw):
     a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, mbs=8, cl=FAKE, max_ctx=128, B=2, Hq=8,
              Hkv=2, D=64, bs=16, NB=32, scale=0.125, window=0, nq=1, dtype=0, splits=8,
-             ws=FAKE, ws_bytes=1 << 20)
+             ws=FAKE, ws_bytes=1 << 20, flags=0)
     a.update(kw)
     return lib.pa_decode(a["out"], a["q"], a["k"], a["v"], a["bt"], a["mbs"], a["cl"],
                          a["max_ctx"], a["B"], a["Hq"], a["Hkv"], a["D"], a["bs"], a["NB"],
                          a["scale"], a["window"], a["nq"], a["dtype"], a["splits"], a["ws"],
-                         a["ws_bytes"], None)
+                         a["ws_bytes"], a["flags"], None)
 
 
 def test_decode_argument_errors(lib):
     assert _decode(lib, q=None) == _abi.PA_ERR_INVALID_ARG
     assert _decode(lib, Hq=7) == _abi.PA_ERR_INVALID_ARG            # 7 % 2 != 0
     assert _decode(lib, splits=-1) == _abi.PA_ERR_INVALID_ARG
+    assert _decode(lib, flags=2) == _abi.PA_ERR_INVALID_ARG         # unknown flag bit
     assert _decode(lib, max_ctx=129) == _abi.PA_ERR_INVALID_ARG     # > mbs * 16
     assert _decode(lib, scale=float("nan")) == _abi.PA_ERR_INVALID_ARG
     assert _decode(lib, dtype=3) == _abi.PA_ERR_INVALID_ARG
