@@ -584,36 +584,55 @@ def run_multiquery(args, dev):
     if w.kv == "fp8":
         raise SystemExit("--op multiquery runs on 16-bit pools")
     n = args.queries
-    if n * w.group > 8:
-        raise SystemExit(f"{n} queries x group {w.group} exceed the 8 query rows of a launch")
+    per_pass = n if n * w.group <= 8 else 8 // w.group     # query tokens per launch pair
+    passes = -(-n // per_pass)
     lens = w.context_lens.cpu().numpy()
     g = torch.Generator(device=dev).manual_seed(args.seed + 17)
     q = torch.randn(w.B, n, w.Hq, w.D, generator=g, device=dev).to(w.q.dtype)
     out = torch.empty_like(q)
-    step = DecodeStep(k_cache=w.k_cache, v_cache=w.v_cache, block_tables=w.block_tables,
-                      context_lens=w.context_lens, max_context_len=w.max_context_len,
-                      scale=w.scale, num_q_heads=w.Hq, split_ctas=args.splits, window=args.window)
     ab = algorithmic_bytes(w, lens, args.window)
     moved = ab["kv"] + ab["meta"] + n * ab["q_out"]
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
-    flush_buf = torch.ones(max(2 * l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
-    flush = ab["kv"] < 3 * l2
+    # as for the decode step: K/V above 3x L2 runs as is, smaller K/V from
+    # cycled copies of the pools (up to 16), else L2 is evicted before each
+    # step and each step timed between its own events
+    copies = 1 if ab["kv"] >= 3 * l2 else -(-3 * l2 // max(ab["kv"], 1))
+    back_to_back = copies <= 16
+    copies = copies if back_to_back else 1
+    early = args.early_prologue == "on"
+    pool_sets = [(w.k_cache, w.v_cache)] + [(w.k_cache.clone(), w.v_cache.clone())
+                                           for _ in range(copies - 1)]
+    steps = [DecodeStep(k_cache=kc, v_cache=vc, block_tables=w.block_tables,
+                        context_lens=w.context_lens, max_context_len=w.max_context_len,
+                        scale=w.scale, num_q_heads=w.Hq, split_ctas=args.splits,
+                        window=args.window, early_prologue=early) for kc, vc in pool_sets]
+    step = steps[0]
     stream = torch.cuda.current_stream(dev)
-    for _ in range(args.warmup):
-        step.decode(q, out)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    calls = [_abi.prepare(lambda st=st: st.decode(q, out), stream) for st in steps]
+    flush_buf = torch.ones(max(2 * l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
+    for i in range(max(args.warmup, copies)):
+        calls[i % copies]()
     torch.cuda.synchronize(dev)
-    for a, b in ev:
-        if flush:
-            flush_buf.sum(dtype=torch.int64)
+    if back_to_back:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        step.decode(q, out)
+        for i in range(args.steps):
+            calls[i % copies]()
         b.record(stream)
-    torch.cuda.synchronize(dev)
+        torch.cuda.synchronize(dev)
+        ms = [a.elapsed_time(b) / args.steps] * args.steps
+    else:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for a, b in ev:
+            flush_buf.sum(dtype=torch.int64)
+            a.record(stream)
+            calls[0]()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = [a.elapsed_time(b) for a, b in ev]
     rc, bits = _abi.pa_get_status(dev)
     if rc != 0:
         raise RuntimeError(f"device status {rc} bits {bits}")
-    ms = [a.elapsed_time(b) for a, b in ev]
     t = statistics.mean(ms) / 1e3
     achieved = moved / t / 1e9
     peak, peak_kind = measured_peaks()
@@ -624,16 +643,23 @@ def run_multiquery(args, dev):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 5),
         "higher_is_better": True, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": describe(w, att), "queries_per_seq": n,
-                   "step": "pa_decode with n query tokens per sequence (decode and merge launches)",
+                   "step": ("pa_decode with n query tokens per sequence (decode and merge "
+                            f"launches; {passes} pass(es) of {per_pass} token(s), each reading "
+                            "the K/V)"),
                    "split_ctas": step.split_ctas,
-                   "l2": "flushed by reading a 2x-L2 buffer" if flush else "not flushed",
+                   "l2": (describe_l2("rotate" if copies > 1 else "none", ab["kv"], l2, copies)
+                          if back_to_back else describe_l2("read", ab["kv"], l2)),
+                   "launch": ("attention launch with an early prologue" if early
+                              else "plain launches"),
                    **({"window": args.window} if args.window else {})},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
                      "kernel": "decode_kernel (general masks), then merge_kernel",
                      "bytes_per_launch": moved, "peak_source": peak_kind},
-        "decode_us": {"mean": round(t * 1e6, 2), "min": round(min(ms) * 1e3, 2)},
-        "gpu_launches": 2 * args.steps,
+        "decode_us": {"mean": round(t * 1e6, 2),
+                      "timing": ("K decodes back to back between two events" if back_to_back
+                                 else "each decode between its own events, L2 evicted")},
+        "gpu_launches": 2 * passes * args.steps,
     }
 
 

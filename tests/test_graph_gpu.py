@@ -1,7 +1,8 @@
 """DecodeStep.capture: the fused step recorded once into a CUDA graph and
 replayed over successive decode steps must produce, step by step, the same
 bytes (outputs and pools) as the same step called eagerly: one kernel, one
-split, the same inputs."""
+split, the same inputs.  Also with the captured attention launch as an
+early-prologue (programmatic dependent) launch."""
 import pytest
 import torch
 
@@ -23,9 +24,12 @@ def _slots(tables, lens):
     return tables[rows, last // 16].to(torch.int64) * 16 + last % 16
 
 
-@pytest.mark.parametrize("name,fp8", [("qwen2_5_1_5b", False), ("smollm2_360m", False),
-                                      ("qwen2_5_1_5b", True)])
-def test_graph_replay_matches_eager_over_steps(name, fp8):
+@pytest.mark.parametrize("name,fp8,early", [("qwen2_5_1_5b", False, False),
+                                            ("smollm2_360m", False, False),
+                                            ("qwen2_5_1_5b", True, False),
+                                            ("qwen2_5_1_5b", False, True),
+                                            ("qwen2_5_1_5b", True, True)])
+def test_graph_replay_matches_eager_over_steps(name, fp8, early):
     g = torch.Generator().manual_seed(11)
     cfg = W.CONFIGS[name]
     B = cfg["B"]
@@ -48,13 +52,14 @@ def test_graph_replay_matches_eager_over_steps(name, fp8):
     max_ctx = int(lens0.max()) + STEPS
     act = w.q.dtype
 
-    def make_step(pl, lens):
+    def make_step(pl, lens, early_prologue=False):
         return DecodeStep(**dict(zip(names, pl)), block_tables=tables, context_lens=lens,
-                          max_context_len=max_ctx, scale=w.scale, num_q_heads=w.Hq)
+                          max_context_len=max_ctx, scale=w.scale, num_q_heads=w.Hq,
+                          early_prologue=early_prologue)
 
     lens_g = w.context_lens.clone()       # the graph's lengths, grown in place
     lens_e = w.context_lens.clone()
-    step_g = make_step(pools, lens_g)
+    step_g = make_step(pools, lens_g, early)     # the graph's kernels may start early
     step_e = make_step(eager_pools, lens_e)
     q = torch.empty_like(w.q)
     kn = torch.empty_like(w.k_new)
