@@ -207,6 +207,10 @@ class StepPipeline:
     costs the host a handful of calls.
     Each submit first orders the compute stream after the caller's stream;
     ``finish`` orders the caller's stream after everything submitted.
+    Steps built with ``early_prologue`` are fine here: the kernel before a
+    step on the compute stream is the previous step's merge, and the upload
+    of the step's lengths and tables is ordered before it by an event (a
+    full dependency, which the early prologue does not relax).
 
     ``make_step(staging)`` builds the DecodeStep for one staging (bound to its
     device block_tables and context_lens; the pools are shared).  The caller

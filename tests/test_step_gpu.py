@@ -224,3 +224,71 @@ def test_bound_step_records_once_and_matches_direct_calls():
             assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
         assert torch.equal(w.k_cache.view(torch.int16), k2.view(torch.int16))
         assert torch.equal(w.v_cache.view(torch.int16), v2.view(torch.int16))
+
+
+def test_step_pipeline_early_prologue_new_lengths_each_step():
+    """StepPipeline with the early prologue: every step uploads new context
+    lengths and slots (one token more each step), so a prologue that read
+    its slot's lengths before that upload had landed would attend the wrong
+    contexts.  The uploads are ordered before the step by events, which the
+    early prologue does not relax: the outputs and pools must equal plain
+    direct steps on the same inputs, step by step."""
+    from paged_kv_cache_179_gb300.step import StepPipeline
+    STEPS = 6
+    name = "qwen2_5_1_5b"
+    B = W.CONFIGS[name]["B"]
+    g = torch.Generator().manual_seed(3)
+    lens0 = (torch.randint(2, 100, (B,), generator=g) * 16
+             + torch.randint(1, 16 - STEPS + 1, (B,), generator=g))
+    w = W.make_workload(name, seed=9, lens_override=lens0.tolist(), fill="random")
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    specs = {k: (getattr(w, k).shape, getattr(w, k).dtype) for k in names}
+    kc, vc = w.k_cache.cuda(), w.v_cache.cuda()
+    k2, v2 = kc.clone(), vc.clone()
+    max_ctx = int(lens0.max()) + STEPS
+    tables = w.block_tables
+    inputs = []
+    for n in range(STEPS):
+        lens = (lens0 + n).to(torch.int32)
+        last = lens.to(torch.int64) - 1
+        slots = tables[torch.arange(B), last // 16].to(torch.int64) * 16 + last % 16
+        inputs.append(dict(q=torch.randn(w.q.shape, generator=g).to(w.q.dtype),
+                           k_new=torch.randn(w.k_new.shape, generator=g).to(w.q.dtype),
+                           v_new=torch.randn(w.k_new.shape, generator=g).to(w.q.dtype),
+                           slot_mapping=slots, block_tables=tables, context_lens=lens))
+
+    def make_step(st):
+        return DecodeStep(k_cache=kc, v_cache=vc, block_tables=st.dev["block_tables"],
+                          context_lens=st.dev["context_lens"], max_context_len=max_ctx,
+                          scale=w.scale, num_q_heads=w.Hq, early_prologue=True)
+    pipe = StepPipeline(make_step, specs, w.q.shape, w.q.dtype, "cuda")
+    got = [None] * STEPS
+    pending = None
+    for n in range(STEPS):
+        pipe.wait_slot_free()
+        if pending is not None and pending[1] == pipe.slot():
+            pipe.read_back[pending[1]].synchronize()
+            got[pending[0]] = pipe.host_out[pending[1]].clone()
+            pending = None
+        for k in names:
+            pipe.stagings[pipe.slot()].host[k].copy_(inputs[n][k])
+        slot, _, _ = pipe.submit()
+        if pending is not None:
+            pipe.read_back[pending[1]].synchronize()
+            got[pending[0]] = pipe.host_out[pending[1]].clone()
+        pending = (n, slot)
+    pipe.finish()
+    torch.cuda.synchronize()
+    got[pending[0]] = pipe.host_out[pending[1]].clone()
+    assert _abi.pa_get_status() == (0, 0)
+
+    lens_d = torch.empty(B, dtype=torch.int32, device="cuda")
+    ref_step = DecodeStep(k_cache=k2, v_cache=v2, block_tables=tables.cuda(), context_lens=lens_d,
+                          max_context_len=max_ctx, scale=w.scale, num_q_heads=w.Hq)
+    for n in range(STEPS):
+        lens_d.copy_(inputs[n]["context_lens"])
+        r = torch.empty_like(w.q, device="cuda")
+        d = {k: inputs[n][k].cuda() for k in ("q", "k_new", "v_new", "slot_mapping")}
+        ref_step(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], r)
+        assert torch.equal(got[n].view(torch.int16), r.cpu().view(torch.int16)), n
+    assert torch.equal(kc.view(torch.int16), k2.view(torch.int16))
