@@ -2,7 +2,8 @@
 sizes, split counts, windows, query counts and pool types, each call
 leaving it zero-filled for the next (the merge launch zeroes every partial
 it reads); a workspace that was not zero-filled is reported
-(PA_STATUS_WS_DIRTY), and zero-filling it again restores exact results."""
+(PA_STATUS_WS_DIRTY) where it matters, and zero-filling it again restores
+exact results."""
 import math
 
 import numpy as np
@@ -81,12 +82,20 @@ def test_one_workspace_serves_calls_of_every_size():
 
 
 def test_dirty_workspace_is_reported_and_zeroing_restores_it():
+    """A workspace filled with 0xFF bytes holds what reads as written partials
+    (zero maxima and sums).  A partial the merge reads before its piece
+    overwrites it is reported (PA_STATUS_WS_DIRTY); one overwritten first does
+    no harm; which happens depends on timing.  So the call either reports the
+    bit or is exact, and after zero-filling, calls are exact and clean."""
     c = CALLS[0]
     ws = torch.full((_abi.pa_decode_workspace_size(c[1], c[2], c[4], c[8]),), 0xFF,
                     dtype=torch.uint8, device="cuda")
-    _run(ws, *c)
+    out, ref, tol = _run(ws, *c)
     rc, bits = _abi.pa_get_status()
-    assert rc == _abi.PA_ERR_WORKSPACE and bits & _abi.PA_STATUS_WS_DIRTY, (rc, bits)
+    if rc == 0:
+        assert max_err(out, ref) <= tol
+    else:
+        assert rc == _abi.PA_ERR_WORKSPACE and bits == _abi.PA_STATUS_WS_DIRTY, (rc, bits)
     ws.zero_()
     for _ in range(2):
         out, ref, tol = _run(ws, *c)
