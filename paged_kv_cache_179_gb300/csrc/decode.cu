@@ -49,6 +49,8 @@
 #include <climits>
 #include <type_traits>
 
+#include <cudaTypedefs.h>
+
 #include "pa_e4m3.cuh"
 #include "pa_launch.h"
 #include "pa_ptx.cuh"
@@ -110,7 +112,22 @@ struct Tile {
   static constexpr int BYTES = 16 * ROW;        // one (block, kv head) tile
   static constexpr int SLOT = 2 * BYTES;        // K tile + V tile
   static constexpr int RING = kWarps * STAGES * SLOT;
+  // 16-bit tiles are copied by tensor map in boxes of 16 rows x 64 elements
+  // with the 128-byte swizzle (see swz), which wants the ring on a 1024-byte
+  // boundary: the layout reserves PAD bytes to align it.  E4M3 tiles are one
+  // contiguous bulk copy each, stored as they are in the pool.
+  static constexpr bool SWZ = !FP8;
+  static constexpr int PAD = SWZ ? 1024 : 0;
 };
+
+// Byte offset, in a swizzled 16-bit tile, of 16-byte chunk j (elements
+// 8j .. 8j+7) of token row t.  The tile is [D/64][16 rows][128 bytes]: the
+// box of elements 64h .. 64h+63 of all 16 rows, then the next; chunk q of a
+// 128-byte line t sits at q ^ (t % 8) (the TMA engine's 128-byte swizzle of a
+// 1024-byte aligned box).
+__device__ __forceinline__ uint32_t swz(int t, int j) {
+  return static_cast<uint32_t>((j >> 3) * 2048 + t * 128 + (((j & 7) ^ (t & 7)) << 4));
+}
 
 __host__ __device__ constexpr int round16(int x) { return (x + 15) & ~15; }
 
@@ -186,11 +203,15 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
   // two accumulators (even / odd k-steps) halve the dependent MMA chain
   float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
   if constexpr (!FP8) {
-    // lane (r, c) reads 16-byte chunk 4i+c of rows r and r+8: d = 32i + 8c + 0..7
+    // lane (r, c) reads 16-byte chunk j = 8(i/2) + 2c + i%2 of rows r and r+8
+    // (d = 8j .. 8j+7; the query fragments follow the same order).  A quarter
+    // warp (rows r, r+1, c = 0..3) then reads chunks of one parity from row r
+    // and of the other from row r+1, swizzled to 8 distinct bank groups.
 #pragma unroll
     for (int i = 0; i < D / 32; ++i) {
-      const uint4 ka = lds128(kt + r * ROW + (4 * i + c) * 16);
-      const uint4 kb = lds128(kt + (r + 8) * ROW + (4 * i + c) * 16);
+      const int j = 8 * (i >> 1) + 2 * c + (i & 1);
+      const uint4 ka = lds128(kt + swz(r, j));
+      const uint4 kb = lds128(kt + swz(r + 8, j));
       mma16816<BF16>(acc, ka.x, kb.x, ka.y, kb.y, qf[2 * i][0], qf[2 * i][1]);
       mma16816<BF16>(acc2, ka.z, kb.z, ka.w, kb.w, qf[2 * i + 1][0], qf[2 * i + 1][1]);
     }
@@ -259,14 +280,16 @@ __device__ __forceinline__ void attend_block(WarpAcc<D>& st, const uint32_t (&qf
   // ---- O^T += V^T P^T : lane needs tokens 2c, 2c+1, 2c+8, 2c+9
   const int tk0 = 2 * c, tk1 = 2 * c + 1, tk2 = 2 * c + 8, tk3 = 2 * c + 9;
   if constexpr (!FP8) {
+    // rows 2c, 2c+1, 2c+8, 2c+9 at chunk r: a quarter warp (r, r+1; c = 0..3)
+    // reads 8 distinct bank groups through the swizzle
     constexpr int U = D / 64;   // 16-byte chunks per token row for this lane
     uint4 v[4][U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      v[0][u] = lds128(vt + tk0 * ROW + (8 * u + r) * 16);
-      v[1][u] = lds128(vt + tk1 * ROW + (8 * u + r) * 16);
-      v[2][u] = lds128(vt + tk2 * ROW + (8 * u + r) * 16);
-      v[3][u] = lds128(vt + tk3 * ROW + (8 * u + r) * 16);
+    for (int u = 0; u < U; ++u) {   // chunk 8u + r: d = 64u + 8r .. +7
+      v[0][u] = lds128(vt + swz(tk0, 8 * u + r));
+      v[1][u] = lds128(vt + swz(tk1, 8 * u + r));
+      v[2][u] = lds128(vt + swz(tk2, 8 * u + r));
+      v[3][u] = lds128(vt + swz(tk3, 8 * u + r));
     }
     if (n_valid < 16) {   // rows past the context may hold anything, NaN included
       const uint4 z = make_uint4(0, 0, 0, 0);
@@ -443,9 +466,10 @@ __device__ __forceinline__ float load_query(uint32_t (&qf)[D / 16][2], const Dec
       static_cast<const uint16_t*>(a.q) +
       ((static_cast<int64_t>(b) * a.q_tokens + a.q_first + r / G) * a.Hq + h * G + r % G) * D);
   if constexpr (!FP8) {
+    // k-step pair i holds chunk 8(i/2) + 2c + i%2, as the K fragments do
 #pragma unroll
     for (int i = 0; i < D / 32; ++i) {
-      const uint4 v = live ? __ldg(qrow + 4 * i + c) : make_uint4(0, 0, 0, 0);
+      const uint4 v = live ? __ldg(qrow + 8 * (i >> 1) + 2 * c + (i & 1)) : make_uint4(0, 0, 0, 0);
       qf[2 * i][0] = v.x;
       qf[2 * i][1] = v.y;
       qf[2 * i + 1][0] = v.z;
@@ -641,7 +665,7 @@ __device__ __forceinline__ NewRow load_new_row(const DecodeArgs& a, const Chunk&
 
 template <int D, bool FP8, bool BF16, int STAGES, bool APPEND, bool GENERAL, int CTAS>
 __global__ void __launch_bounds__(kThreads, CTAS)
-decode_kernel(const DecodeArgs a) {
+decode_kernel(const __grid_constant__ DecodeArgs a) {
   using TL = Tile<D, FP8, STAGES>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -655,7 +679,7 @@ decode_kernel(const DecodeArgs a) {
     const int j = 2 * c + k;
     cm_ii |= (j < a.n_q * G ? j / G : a.n_q - 1) << (8 * k);
   }
-  const Layout lay = make_layout(TL::RING, STAGES, B);
+  const Layout lay = make_layout(TL::RING + TL::PAD, STAGES, B);
   int* pf = reinterpret_cast<int*>(smem + lay.pf);
   int* len = reinterpret_cast<int*>(smem + lay.len);
   int* misc = reinterpret_cast<int*>(smem + lay.misc);   // [0..3] warp sums of the scan
@@ -723,7 +747,9 @@ decode_kernel(const DecodeArgs a) {
   }
   const int64_t lo = worker_lo(gw, W, NW), hi = worker_lo(gw + 1, W, NW);
 
-  const uint32_t ring = smem_u32(smem) + warp * STAGES * TL::SLOT;
+  uint32_t ring_at = 0;   // the rings start at the first 1024-byte boundary (swizzled tiles)
+  if constexpr (TL::SWZ) ring_at = (1024u - (smem_u32(smem) & 1023u)) & 1023u;
+  const uint32_t ring = smem_u32(smem) + ring_at + warp * STAGES * TL::SLOT;
   const uint32_t sbar = smem_u32(smem + lay.sbar) + warp * STAGES * 8;
   if (lane == 0) {
 #pragma unroll
@@ -757,7 +783,7 @@ decode_kernel(const DecodeArgs a) {
   }
   // query fragments of the current piece and of the next one
   uint32_t qf[D / 16][2], qn[D / 16][2];
-  uint8_t* const ring_ptr = smem + warp * STAGES * TL::SLOT;   // generic address of the ring
+  uint8_t* const ring_ptr = smem + ring_at + warp * STAGES * TL::SLOT;   // generic address
   float q_mul = load_query<D, FP8, BF16>(qf, a, ch0.b, ch0.h, r, c), qn_mul = 1.f;
   auto prefetch_next_query = [&](int b, int h) {
     ++h;
@@ -795,9 +821,20 @@ decode_kernel(const DecodeArgs a) {
         if (id >= 0 && id < a.num_blocks) {
           const int64_t tile = static_cast<int64_t>(id) * Hkv + x.h;
           mbar_arrive_expect_tx(bar, 2 * TL::BYTES);
-          bulk_g2s(ring + s * TL::SLOT, kbase + tile * TL::BYTES, TL::BYTES, bar, pol);
-          bulk_g2s(ring + s * TL::SLOT + TL::BYTES, vbase + tile * TL::BYTES, TL::BYTES, bar,
-                   pol);
+          if constexpr (TL::SWZ) {
+            // boxes of 64 elements x 16 rows: D / 64 per tile
+            const uint32_t kd = ring + s * TL::SLOT, vd = kd + TL::BYTES;
+            const int ti = static_cast<int>(tile);
+#pragma unroll
+            for (int hb = 0; hb < D / 64; ++hb) {
+              tensor3_g2s(kd + hb * 2048, &a.tm_k, 64 * hb, 0, ti, bar, pol);
+              tensor3_g2s(vd + hb * 2048, &a.tm_v, 64 * hb, 0, ti, bar, pol);
+            }
+          } else {
+            bulk_g2s(ring + s * TL::SLOT, kbase + tile * TL::BYTES, TL::BYTES, bar, pol);
+            bulk_g2s(ring + s * TL::SLOT + TL::BYTES, vbase + tile * TL::BYTES, TL::BYTES, bar,
+                     pol);
+          }
         } else {
           atomicOr(a.status, kStatusBadBlock);
           mbar_arrive(bar);
@@ -869,18 +906,21 @@ decode_kernel(const DecodeArgs a) {
             if (lane == 0) atomicOr(a.status, kStatusBadSlot);   // not a decode-step slot
           } else {
             const int64_t prow = (static_cast<int64_t>(id) * Hkv + ch0.h) * 16 + row;
-            uint8_t* kt = ktile + row * ROWB;
-            uint8_t* vt = kt + TL::BYTES;
             uint8_t* kp = static_cast<uint8_t*>(a.k_pool_w) + prow * ROWB;
             uint8_t* vp = static_cast<uint8_t*>(a.v_pool_w) + prow * ROWB;
+            // the lane's D/16 elements of the row, at their swizzled place in the tile
+            const uint32_t so = D == 128 ? swz(row, lane >> 1) + 8 * (lane & 1)
+                                         : swz(row, lane >> 2) + 4 * (lane & 3);
+            uint8_t* kt = ktile + so;
+            uint8_t* vt = kt + TL::BYTES;
             if constexpr (D == 128) {
-              *reinterpret_cast<uint2*>(kt + 8 * lane) = nt0.k;
-              *reinterpret_cast<uint2*>(vt + 8 * lane) = nt0.v;
+              *reinterpret_cast<uint2*>(kt) = nt0.k;
+              *reinterpret_cast<uint2*>(vt) = nt0.v;
               *reinterpret_cast<uint2*>(kp + 8 * lane) = nt0.k;
               *reinterpret_cast<uint2*>(vp + 8 * lane) = nt0.v;
             } else {
-              *reinterpret_cast<uint32_t*>(kt + 4 * lane) = nt0.k.x;
-              *reinterpret_cast<uint32_t*>(vt + 4 * lane) = nt0.v.x;
+              *reinterpret_cast<uint32_t*>(kt) = nt0.k.x;
+              *reinterpret_cast<uint32_t*>(vt) = nt0.v.x;
               *reinterpret_cast<uint32_t*>(kp + 4 * lane) = nt0.k.x;
               *reinterpret_cast<uint32_t*>(vp + 4 * lane) = nt0.v.x;
             }
@@ -1208,10 +1248,68 @@ cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, merge_kernel<D, BF16>, a);
 }
 
+// cuTensorMapEncodeTiled, from the driver (no link against libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// The tensor map of a 16-bit pool [tiles][16 rows][D], seen as a 3-D tensor
+// (D elements, 16 rows, tiles; innermost first) and copied in boxes of 64
+// elements x 16 rows x 1 tile with the 128-byte swizzle.  Encoding is host
+// work only; the last few maps are kept per thread, keyed by pool and shape,
+// since a serving loop passes the same pools call after call.
+cudaError_t tile_tensor_map(CUtensorMap* m, const void* pool, int D, int64_t tiles) {
+  struct Entry {
+    const void* pool;
+    int64_t tiles;
+    int D;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 40;
+  static thread_local Entry cache[kEntries] = {};
+  static thread_local int next = 0;
+  for (const Entry& e : cache)
+    if (e.pool == pool && e.tiles == tiles && e.D == D) {
+      *m = e.map;
+      return cudaSuccess;
+    }
+  const auto enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  if (tiles <= 0 || tiles > INT_MAX) return cudaErrorInvalidValue;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), 16, static_cast<cuuint64_t>(tiles)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(2 * D), static_cast<cuuint64_t>(32 * D)};
+  const cuuint32_t box[3] = {64, 16, 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  const CUresult r =
+      enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(pool), dims, strides, box, elem,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  cache[next] = Entry{pool, tiles, D, *m};
+  next = (next + 1) % kEntries;
+  return cudaSuccess;
+}
+
 template <int D, bool FP8, bool BF16, int STAGES, bool APPEND, bool GENERAL, int CTAS>
-cudaError_t launch_one(const DecodeArgs& a, cudaStream_t s) {
+cudaError_t launch_one(const DecodeArgs& args, cudaStream_t s) {
   using TL = Tile<D, FP8, STAGES>;
-  const Layout lay = make_layout(TL::RING, STAGES, a.B);
+  DecodeArgs a = args;
+  if constexpr (TL::SWZ) {
+    const int64_t tiles = static_cast<int64_t>(a.num_blocks) * a.Hkv;
+    cudaError_t e = tile_tensor_map(&a.tm_k, a.k_cache, D, tiles);
+    if (e == cudaSuccess) e = tile_tensor_map(&a.tm_v, a.v_cache, D, tiles);
+    if (e != cudaSuccess) return e;
+  }
+  const Layout lay = make_layout(TL::RING + TL::PAD, STAGES, a.B);
   auto* kern = decode_kernel<D, FP8, BF16, STAGES, APPEND, GENERAL, CTAS>;
   static thread_local int last_smem[64] = {0};
   int dev = 0;

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace pa {
@@ -14,6 +15,9 @@ constexpr int kMaxBatchPerLaunch = 512;
 
 // All pointers are device pointers; sizes were validated by the caller.
 struct DecodeArgs {
+  // 16-bit pools: tensor maps of k_cache and v_cache that copy one
+  // (block, kv head) tile with the 128-byte swizzle (set by the launcher)
+  CUtensorMap tm_k, tm_v;
   void* out;                    // [B][Hq][D] f16/bf16
   const void* q;                // [B][Hq][D] f16/bf16
   const void* k_cache;          // [NB][Hkv][16][D] f16/bf16 or e4m3

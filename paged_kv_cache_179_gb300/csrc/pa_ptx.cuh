@@ -101,6 +101,19 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
+// One box of a 3-D tensor map at coordinates (x0, x1, x2), innermost first,
+// into this CTA's shared memory, completing on mbarrier bar.  tmap is the
+// generic address of a CUtensorMap in kernel parameter space (a
+// __grid_constant__ argument); x0 times the element size is a multiple of 16.
+__device__ __forceinline__ void tensor3_g2s(uint32_t dst, const void* tmap, int x0, int x1,
+                                            int x2, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(tmap), "r"(x0), "r"(x1), "r"(x2), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // Global -> shared bulk copy of `bytes` (multiple of 16, both addresses
 // 16-byte aligned); completion is counted on the mbarrier as transaction bytes.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
