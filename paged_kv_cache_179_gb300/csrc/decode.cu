@@ -663,6 +663,13 @@ __device__ __forceinline__ NewRow load_new_row(const DecodeArgs& a, const Chunk&
   return n;
 }
 
+// With an early prologue, each warp asks L2 for its first
+// PA_EARLY_PREFETCH x STAGES tiles (at most a chunk) before it waits for the
+// previous kernel; 0 turns this off.
+#ifndef PA_EARLY_PREFETCH
+#define PA_EARLY_PREFETCH 1
+#endif
+
 template <int D, bool FP8, bool BF16, int STAGES, bool APPEND, bool GENERAL, int CTAS>
 __global__ void __launch_bounds__(kThreads, CTAS)
 decode_kernel(const __grid_constant__ DecodeArgs a) {
@@ -769,6 +776,18 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   int id0 = chunk_id(ch0);
   int id1 = chunk_id(ch1);
   int id2 = chunk_id(ch2);
+  if (PA_EARLY_PREFETCH > 0 && a.early) {
+    // While the previous kernel ends, warm L2 with the warp's first tiles
+    // (lane t: block t of its first chunk), so that the first copies after
+    // the wait are served from L2: a prefetch reads nothing into the SM, so
+    // what that kernel writes before it completes is still what they read.
+    if (lane < PA_EARLY_PREFETCH * STAGES && lane < ch0.nb && id0 >= 0 &&
+        id0 < a.num_blocks) {
+      const int64_t tile = static_cast<int64_t>(id0) * Hkv + ch0.h;
+      prefetch_l2(static_cast<const uint8_t*>(a.k_cache) + tile * TL::BYTES, TL::BYTES);
+      prefetch_l2(static_cast<const uint8_t*>(a.v_cache) + tile * TL::BYTES, TL::BYTES);
+    }
+  }
   after_previous_kernel();
   float ks0 = 1.f, vs0 = 1.f, ks1 = 1.f, vs1 = 1.f;   // E4M3 page scales of chunks k, k+1
   if constexpr (FP8) {

@@ -125,6 +125,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Hint: bring `bytes` (multiple of 16, address 16-byte aligned) of global
+// memory into L2.  Nothing is read into the SM, so no later read can see an
+// older copy: L2 is where the GPU keeps global memory coherent.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------------ shared loads
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
