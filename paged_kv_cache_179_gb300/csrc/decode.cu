@@ -1,5 +1,5 @@
-// decode.cu -- K3/K4: split-K paged GQA decode (16-bit and E4M3 pools) with
-// K5, the log-sum-exp merge of partitions, fused into the same kernel.
+// decode.cu -- K3/K4: split-K paged GQA decode (16-bit and E4M3 pools), and
+// K5, the log-sum-exp merge of the split partitions (merge_kernel).
 //
 // What is computed ("rvLLM: High-performance LLM inference in Rust", CUDA
 // Kernels table, "PagedAttention V2": attention with block-table
@@ -13,34 +13,45 @@
 //
 // Design (sm_103a, one GB300):
 //  * The batch is one stream of (sequence, kv head, 16-token block) units.
-//    The grid is persistent (two CTAs per SM by default) and CTA c takes an
-//    equal contiguous share of the stream, so every CTA moves the same number
-//    of bytes whatever the spread of context lengths.  Its share of one
-//    (sequence, kv head) is that sequence's context partition for this CTA:
-//    a short sequence lies inside one CTA and is attended whole, a long one
-//    is split across consecutive CTAs (split-K) and merged by log-sum-exp.
-//    Each CTA serves a whole query group per kv head, so every K/V byte is
-//    read from HBM once.
-//  * Four warps split each 128-block chunk of the share round-robin.  Each
-//    warp owns a ring of STAGES shared-memory slots; lane 0 fills a slot with
-//    the K tile and V tile of one (block, kv head) by two bulk asynchronous
-//    copies (the TMA engine, cp.async.bulk) that complete on the slot's
-//    mbarrier.  The ring runs ahead across chunk and partition boundaries.
-//    Block ids (and E4M3 page scales) are prefetched into registers, one per
-//    lane, two chunks ahead; the next partition's query is prefetched too.
-//  * Per block the warp computes S^T = K Q^T (16 tokens x 8 query heads) and
+//    The grid is persistent (two CTAs of four warps per SM for 16-bit pools,
+//    three for E4M3) and every warp is an independent worker that takes an
+//    equal contiguous share of the stream, so every warp moves the same
+//    number of bytes whatever the spread of context lengths.  A warp's share
+//    of one (sequence, kv head) is that sequence's context partition on this
+//    worker: a short sequence lies inside one share and is attended whole, a
+//    long one is split across consecutive workers (split-K).  Each worker
+//    serves a whole query group per kv head, so every K/V byte is read from
+//    HBM once.  The only CTA-wide step is the prologue: the prefix sums of
+//    the per-sequence block counts, in shared memory.
+//  * Each warp owns a ring of STAGES shared-memory slots; lane 0 fills a
+//    slot with the K tile and V tile of one (block, kv head) by TMA copies
+//    that complete on the slot's mbarrier: 16-bit tiles by tensor map
+//    (boxes of 64 elements x 16 rows, 128-byte swizzle, so the fragment
+//    reads below are free of bank conflicts), E4M3 tiles by one contiguous
+//    bulk copy each.  The ring runs ahead across chunk and partition
+//    boundaries.  Block ids (and E4M3 page scales) are prefetched into
+//    registers, one per lane, two 32-block chunks ahead; the next
+//    partition's query is prefetched too.
+//  * Per block the warp computes S^T = K Q^T (16 tokens x 8 query rows) and
 //    O^T += V^T P^T (head_dim x 8) with mma.sync m16n8k16 in fp32.  The query
-//    group (<= 8 heads) is the N=8 side.  The online softmax runs on the S
+//    group (<= 8 rows) is the N=8 side.  The online softmax runs on the S
 //    fragments (row max with shuffles, exp2 on the SFU); P moves from
 //    accumulator to operand layout with movmatrix.  E4M3 codes are widened
 //    to f16 in registers (exact) just before the MMA; the page scales fold
 //    into the score scale (K) and into P (V).
-//  * Partition epilogue: the four warps' (max, sum, acc) combine in shared
-//    memory.  A whole sequence writes its output directly.  A split one
-//    writes a partial (at most two per CTA: its first and last partition)
-//    and counts it on a per-(sequence, kv head) counter; at its end, the CTA
-//    whose count completed a sequence merges that sequence's partials and
-//    resets the counter to zero.  No thread ever waits for another CTA.
+//  * Partition end: a partition inside the worker's share writes its output
+//    from registers; a split one writes its partial (running max, sum,
+//    unnormalised acc) to the workspace, bit-inverted so that a zero word
+//    means "not written".  The log-sum-exp merge is a second launch that
+//    runs beside this grid (programmatic stream serialization) and merges
+//    each split sequence as soon as its partials land.  No warp ever waits
+//    for another.
+//  * Optional fused append: the step's new K/V row is written to the pool
+//    and into the tile just fetched by the warp that attends the sequence's
+//    last block.  Optional early prologue: the launch may start while the
+//    kernel before it ends; the prologue reads only context_lens and
+//    block_tables and asks L2 for each warp's first tiles, and everything
+//    else waits for griddepcontrol.wait.
 //
 // Bounds: block ids outside [0, num_blocks) and context lengths above their
 // bounds are never dereferenced; they set a status bit.  Every mbarrier wait
