@@ -229,7 +229,10 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int
  *   block_tables, dividing the batch among the warps, reading each warp's
  *   first block ids) may then run while the kernel before it on the stream
  *   is still finishing; everything else (q, the pools and scales, the new
- *   rows, out, the workspace) waits until that kernel has completed.  Set it
+ *   rows, out, the workspace) waits until that kernel has completed, except
+ *   that the prologue asks L2 to prefetch each warp's first K/V tiles (a
+ *   hint that reads nothing into the SMs; L2 is coherent, so writes that
+ *   kernel makes to the pools are still seen).  Set it
  *   only when the kernel just before the call on the stream does not write
  *   context_lens or block_tables (for example, when they are uploaded by a
  *   copy before the forward pass).  Results are the same either way.
