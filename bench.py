@@ -265,16 +265,18 @@ def run_ours(args, rank, world, dev):
     else:
         copies = 1
     pool_sets = [pools] + [{k: t.clone() for k, t in pools.items()} for _ in range(copies - 1)]
+    back_to_back = l2_mode in ("none", "rotate")
     # the timed steps: nothing between them writes context_lens or block_tables,
     # so the attention launch may start its prologue while the previous
-    # step's merge finishes (PA_DECODE_EARLY_PROLOGUE)
-    early = args.early_prologue == "on"
+    # step's merge finishes (PA_DECODE_EARLY_PROLOGUE).  Steps that each
+    # follow an L2-evicting kernel (not one of ours, which would let the
+    # launch start early) gain nothing by it, and launch plainly.
+    early = args.early_prologue == "on" and back_to_back
     steps = [DecodeStep(**ps, block_tables=w.block_tables, context_lens=w.context_lens,
                         max_context_len=w.max_context_len, scale=w.scale, num_q_heads=w.Hq,
                         split_ctas=args.splits, window=args.window, early_prologue=early)
              for ps in pool_sets]
     step = steps[0]
-    back_to_back = l2_mode in ("none", "rotate")
     flush_buf = torch.ones(max(2 * l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
 
     def flush():
@@ -401,14 +403,15 @@ def run_ours(args, rank, world, dev):
     def make_step(staging):
         ps = pool_sets[len(made) % copies]
         made.append(staging)
-        # the pipeline's uploads of lengths and tables are ordered before each
-        # step by events, which an early prologue does not relax; the
-        # step-by-step form follows an L2-evicting kernel, so it gains nothing
+        # the pipeline orders each step after its upload and after the last
+        # read-back of its slot by events; with those between two steps the
+        # attention launch starts once the previous merge has completed, early
+        # prologue or not (a full dependency, which it does not relax)
         return DecodeStep(**ps, block_tables=staging.dev["block_tables"],
                           context_lens=staging.dev["context_lens"],
                           max_context_len=w.max_context_len, scale=w.scale, num_q_heads=w.Hq,
                           split_ctas=args.splits, window=args.window,
-                          early_prologue=early and back_to_back)
+                          early_prologue=early)
     h2d = d2h = 0
     if back_to_back:
         e2e_mode = ("pipelined: uploads and read-backs on two copy streams, overlapping the "
@@ -603,7 +606,7 @@ def run_multiquery(args, dev):
     copies = 1 if ab["kv"] >= 3 * l2 else -(-3 * l2 // max(ab["kv"], 1))
     back_to_back = copies <= 16
     copies = copies if back_to_back else 1
-    early = args.early_prologue == "on"
+    early = args.early_prologue == "on" and back_to_back   # as for the decode step
     pool_sets = [(w.k_cache, w.v_cache)] + [(w.k_cache.clone(), w.v_cache.clone())
                                            for _ in range(copies - 1)]
     steps = [DecodeStep(k_cache=kc, v_cache=vc, block_tables=w.block_tables,
