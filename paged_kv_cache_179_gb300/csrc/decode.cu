@@ -675,10 +675,14 @@ __device__ __forceinline__ NewRow load_new_row(const DecodeArgs& a, const Chunk&
 }
 
 // With an early prologue, each warp asks L2 for its first
-// PA_EARLY_PREFETCH x STAGES tiles (at most a chunk) before it waits for the
-// previous kernel; 0 turns this off.
+// PA_EARLY_PREFETCH x STAGES tiles before it waits for the previous kernel,
+// twice that when its share holds PA_EARLY_PREFETCH_LONG blocks or more;
+// 0 turns this off.
 #ifndef PA_EARLY_PREFETCH
 #define PA_EARLY_PREFETCH 1
+#endif
+#ifndef PA_EARLY_PREFETCH_LONG
+#define PA_EARLY_PREFETCH_LONG 32
 #endif
 
 template <int D, bool FP8, bool BF16, int STAGES, bool APPEND, bool GENERAL, int CTAS>
@@ -792,8 +796,10 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     // (lane t: block t of its first chunk), so that the first copies after
     // the wait are served from L2: a prefetch reads nothing into the SM, so
     // what that kernel writes before it completes is still what they read.
-    if (lane < PA_EARLY_PREFETCH * STAGES && lane < ch0.nb && id0 >= 0 &&
-        id0 < a.num_blocks) {
+    // a long share (PA_EARLY_PREFETCH_LONG blocks or more) prefetches twice
+    // as many: its first tiles are a small part of its work
+    const int n_pf = PA_EARLY_PREFETCH * STAGES * (hi - lo >= PA_EARLY_PREFETCH_LONG ? 2 : 1);
+    if (lane < n_pf && lane < ch0.nb && id0 >= 0 && id0 < a.num_blocks) {
       const int64_t tile = static_cast<int64_t>(id0) * Hkv + ch0.h;
       prefetch_l2(static_cast<const uint8_t*>(a.k_cache) + tile * TL::BYTES, TL::BYTES);
       prefetch_l2(static_cast<const uint8_t*>(a.v_cache) + tile * TL::BYTES, TL::BYTES);
