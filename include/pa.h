@@ -49,6 +49,11 @@
  *     library's device status word, which pa_get_status reads.
  *   - Supported now: head_dim 64 or 128, block_size 16, num_q_heads /
  *     num_kv_heads from 1 to 8.  Other shapes return PA_ERR_UNSUPPORTED.
+ *   - Host state: for 16-bit pools the decode entry points encode TMA
+ *     tensor maps of k_cache and v_cache (host memory, passed by value with
+ *     the launch) and keep the last 40 per host thread, keyed by pool
+ *     address, tile count and head_dim; the library allocates no device
+ *     memory for them.  An encode failure returns PA_ERR_CUDA.
  */
 #ifndef PA_H
 #define PA_H
