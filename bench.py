@@ -26,6 +26,7 @@ this path) on the host cores instead, on a bounded sample of the workload.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import math
 import os
@@ -125,8 +126,10 @@ class ClockSampler:
         self.marks[name] = time.time()
 
     def stop(self) -> dict:
+        """Stop sampling; the summary of the timed region (marks timed_start / timed_end)."""
+        self.rows = []
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return self.summary()
         time.sleep(0.1)
         self.proc.terminate()
         try:
@@ -135,7 +138,6 @@ class ClockSampler:
             self.proc.kill()
         self.file.flush()
         self.file.seek(0)
-        rows = []
         for line in self.file.read().splitlines():
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 10:
@@ -143,15 +145,24 @@ class ClockSampler:
             try:
                 ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
                 ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
-                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+                self.rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
             except (ValueError, IndexError):
                 continue
         os.unlink(self.file.name)
-        t0, t1 = self.marks.get("timed_start", 0), self.marks.get("timed_end", 1e30)
+        return self.summary()
+
+    def summary(self, start="timed_start", end="timed_end", before=None) -> dict:
+        """Median SM clock, max clock and throttle reasons seen between two
+        marks (falling back to the mark ``before`` .. end, then the whole run,
+        when fewer than 3 samples fall inside)."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = getattr(self, "rows", [])
+        t0, t1 = self.marks.get(start, 0), self.marks.get(end, 1e30)
         inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
         window = "timed"
         if len(inside) < 3:
-            t0w = self.marks.get("warmup_start", t0)
+            t0w = self.marks.get(before or "warmup_start", t0)
             inside = [r for r in rows if t0w - 0.05 <= r[0] <= t1 + 0.05]
             window = "warmup+timed"
         if not inside:
@@ -168,45 +179,67 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside), "window": window}
 
 
-def oracle_baseline(w, budget_s: float = 10.0, window: int = 0) -> dict:
-    """fp64 CPU oracle (as it stands) on a bounded sample of the batch: whole
-    passes over a subset of its sequences, repeated to about budget_s."""
+def oracle_baseline(w, pools, budget_s: float = 10.0, window: int = 0,
+                    threads: int = 0) -> dict:
+    """The fp64 CPU oracle (as it stands) on a bounded sample of the batch:
+    whole passes over a subset of its sequences (their blocks copied to the
+    host), repeated to about budget_s.  ``threads`` > 0 runs it on that many
+    OpenMP threads (1: one core), else on all host cores."""
     import oracle
     from paged_kv_cache_179_gb300 import workloads as W
     lens = w.context_lens.cpu().numpy()
     att = attended(lens, window)
     tables = w.block_tables.cpu().numpy()
-    q = W.to_numpy16(w.q)
-    if w.kv == "fp8":
-        raise NotImplementedError
-    kp, vp = W.to_numpy16(w.k_cache), W.to_numpy16(w.v_cache)
+    fp8 = w.kv == "fp8"
     bf16 = w.dtype == "bf16"
-    order = np.random.default_rng(0).permutation(w.B)
-    # calibrate on 4 sequences, then size the sample to ~budget_s
-    probe = order[:4]
-    t = time.perf_counter()
-    oracle.decode(q, kp, vp, tables, lens, w.scale, bf16=bf16, window=window, rows=probe)
-    dt = max(time.perf_counter() - t, 1e-3)
-    per_tok = dt / max(1, int(att[probe].sum()))
-    n, tok = 0, 0
-    for b in order:
-        if (tok + att[b]) * per_tok > budget_s and n >= 4:
-            break
-        n += 1
-        tok += int(att[b])
-    rows = order[:n]
-    reps, t = 0, time.perf_counter()
-    while True:
-        oracle.decode(q, kp, vp, tables, lens, w.scale, bf16=bf16, window=window, rows=rows)
-        reps += 1
-        dt = time.perf_counter() - t
-        if dt >= budget_s or reps >= 200:
-            break
+    all_threads = oracle.num_threads()
+    if threads > 0:
+        oracle.set_num_threads(threads)
+    try:
+        cores = oracle.num_threads()
+        order = np.random.default_rng(0).permutation(w.B)
+
+        def host_sample(rows):
+            names = ("k_cache", "v_cache", "k_scale", "v_scale") if fp8 else ("k_cache", "v_cache")
+            sub_t, sub_l, arrs = W.extract_rows(tables, lens, rows, [pools[n] for n in names])
+            q = W.to_numpy16(w.q[torch.as_tensor(np.asarray(rows), device=w.q.device)])
+            return q, sub_t, sub_l, arrs
+
+        def run(sample):
+            q, sub_t, sub_l, arrs = sample
+            if fp8:
+                oracle.decode_fp8(q, *arrs, sub_t, sub_l, w.scale, bf16=bf16, window=window)
+            else:
+                oracle.decode(q, *arrs, sub_t, sub_l, w.scale, bf16=bf16, window=window)
+
+        # calibrate on 4 sequences, then size the sample to about budget_s
+        probe = host_sample(order[:4])
+        t = time.perf_counter()
+        run(probe)
+        per_tok = max(time.perf_counter() - t, 1e-3) / max(1, int(att[order[:4]].sum()))
+        n, tok = 0, 0
+        for b in order:
+            if (tok + att[b]) * per_tok > budget_s and n >= 4:
+                break
+            n += 1
+            tok += int(att[b])
+        rows = order[:n]
+        sample = host_sample(rows)
+        reps, t = 0, time.perf_counter()
+        while True:
+            run(sample)
+            reps += 1
+            dt = time.perf_counter() - t
+            if dt >= budget_s or reps >= 200:
+                break
+    finally:
+        if threads > 0:
+            oracle.set_num_threads(all_threads)
     tok = int(att[rows].sum()) * reps
-    return {"value": round(tok / dt, 1), "unit": UNIT, "cores": oracle.num_threads(),
-            "kind": "oracle",
+    return {"value": round(tok / dt, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{n} of {w.B} sequences ({int(att[rows].sum())} attended tokens, all "
-                      f"{w.Hq} q heads) x {reps} passes, fp64 two-pass softmax, {dt:.1f} s"}
+                      f"{w.Hq} q heads{', E4M3 pool' if fp8 else ''}) x {reps} passes on "
+                      f"{cores} thread(s), fp64 two-pass softmax, {dt:.1f} s"}
 
 
 # ---------------------------------------------------------------- replicas
@@ -227,181 +260,224 @@ def reduce_over_ranks(step_ms: float, e2e_ms: float, tokens: int, world: int, de
 
 
 # ---------------------------------------------------------------- our arm
-def run_ours(args, rank, world, dev):
-    from paged_kv_cache_179_gb300 import _abi
-    from paged_kv_cache_179_gb300 import workloads as W
-    from paged_kv_cache_179_gb300.step import DecodeStep
+OTHER_CONFIGS = ("tiny", "smollm2_360m", "qwen2_5_1_5b", "qwen2_5_7b_fp8")
 
-    _abi.load()
-    w = W.make_workload(args.config, seed=replica_seed(args.seed, rank), device=dev)
-    lens = w.context_lens.cpu().numpy()
-    tokens = int(attended(lens, args.window).sum())
-    if w.kv == "fp8":
-        kc = torch.empty(w.k_cache.shape, dtype=torch.uint8, device=dev)
-        vc = torch.empty_like(kc)
-        ks = torch.empty(w.num_blocks, w.Hkv, dtype=torch.float32, device=dev)
-        vs = torch.empty_like(ks)
-        _abi.pa_quantize_fp8(w.k_cache, w.v_cache, kc, vc, ks, vs)
-        pools = dict(k_cache=kc, v_cache=vc, k_scale=ks, v_scale=vs)
-    else:
-        pools = dict(k_cache=w.k_cache, v_cache=w.v_cache)
-    out = torch.empty_like(w.q)
-    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
-    kv_bytes = algorithmic_bytes(w, lens, args.window)["kv"]
-    l2_mode = args.l2
-    copies = 1
-    if l2_mode == "auto":
-        # Inputs several times larger than L2 stream through it without hits
-        # and run back to back.  Smaller pools are replicated (one copy per
-        # layer of a model, as a serving step has) and the steps cycle over
-        # the copies, so each step's K/V is cold; when that would take more
-        # than 16 copies, L2 is evicted before each step by reading a 2x-L2
-        # buffer (a read leaves clean lines, so the timed step pays no
-        # write-backs) and steps are timed one by one.
-        copies = -(-3 * l2 // max(kv_bytes, 1))
-        l2_mode = "none" if kv_bytes >= 3 * l2 else ("rotate" if copies <= 16 else "read")
-    if l2_mode == "rotate":
-        copies = max(2, min(16, -(-3 * l2 // max(kv_bytes, 1))))
-    else:
-        copies = 1
-    pool_sets = [pools] + [{k: t.clone() for k, t in pools.items()} for _ in range(copies - 1)]
-    back_to_back = l2_mode in ("none", "rotate")
-    # the timed steps: nothing between them writes context_lens or block_tables,
-    # so the attention launch may start its prologue while the previous
-    # step's merge finishes (PA_DECODE_EARLY_PROLOGUE).  Steps that each
-    # follow an L2-evicting kernel (not one of ours, which would let the
-    # launch start early) gain nothing by it, and launch plainly.
-    early = args.early_prologue == "on" and back_to_back
-    steps = [DecodeStep(**ps, block_tables=w.block_tables, context_lens=w.context_lens,
-                        max_context_len=w.max_context_len, scale=w.scale, num_q_heads=w.Hq,
-                        split_ctas=args.splits, window=args.window, early_prologue=early)
-             for ps in pool_sets]
-    step = steps[0]
-    flush_buf = torch.ones(max(2 * l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
 
-    def flush():
-        if l2_mode == "read":
-            flush_buf.sum(dtype=torch.int64)
-        elif l2_mode == "write":
-            flush_buf.add_(1)
-    stream = torch.cuda.current_stream(dev)
-    fused = step.prefers_fused if args.step == "auto" else args.step == "fused"
-    # decode_kernel + merge_kernel (fused) | append_kernel + decode_kernel + merge_kernel
-    launches_per_step = 2 if fused else 3
-    # each copy's step, and its decode alone, bound once (arguments checked and
-    # marshalled outside the timed region)
-    calls = [st.bind(w.q, w.k_new, w.v_new, w.slot_mapping, out, fused=fused, stream=stream)
-             for st in steps]
-    decodes = [_abi.prepare(lambda st=st: st.decode(w.q, out), stream) for st in steps]
+class ConfigRun:
+    """One workload's batch on the device, its decode steps bound once, and
+    the device-timed steps: everything a bench line measures except the
+    end-to-end leg."""
 
-    def run_step(i=0):
-        calls[i % copies]()
+    def __init__(self, args, name, seed, dev, window=0):
+        from paged_kv_cache_179_gb300 import _abi
+        from paged_kv_cache_179_gb300 import workloads as W
+        from paged_kv_cache_179_gb300.step import DecodeStep
 
-    clocks = ClockSampler(dev.index if dev.index is not None else 0)
-    if rank == 0:
-        clocks.start()
-    clocks.mark("warmup_start")
-    for i in range(max(args.warmup, copies)):
-        flush()
-        run_step(i)
-    rc, bits = _abi.pa_get_status(dev)
-    if rc != 0:
-        raise RuntimeError(f"device status {rc} bits {bits}")
+        self.args, self.name, self.dev, self.window = args, name, dev, window
+        w = self.w = W.make_workload(name, seed=seed, device=dev)
+        self.lens = w.context_lens.cpu().numpy()
+        self.tokens = int(attended(self.lens, window).sum())
+        if w.kv == "fp8":
+            kc = torch.empty(w.k_cache.shape, dtype=torch.uint8, device=dev)
+            vc = torch.empty_like(kc)
+            ks = torch.empty(w.num_blocks, w.Hkv, dtype=torch.float32, device=dev)
+            vs = torch.empty_like(ks)
+            _abi.pa_quantize_fp8(w.k_cache, w.v_cache, kc, vc, ks, vs)
+            pools = dict(k_cache=kc, v_cache=vc, k_scale=ks, v_scale=vs)
+            # the fp16 source pools are not read again (the new rows are in w)
+            w.k_cache = w.v_cache = None
+            torch.cuda.empty_cache()
+        else:
+            pools = dict(k_cache=w.k_cache, v_cache=w.v_cache)
+        self.pools = pools
+        self.out = torch.empty_like(w.q)
+        l2 = self.l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
+        self.ab = algorithmic_bytes(w, self.lens, window)
+        kv_bytes = self.kv_bytes = self.ab["kv"]
+        l2_mode = args.l2
+        if l2_mode == "auto":
+            # Inputs several times larger than L2 stream through it without
+            # hits and run back to back.  Smaller pools are replicated (one
+            # copy per layer of a model, as a serving step has) and the steps
+            # cycle over the copies, so each step's K/V is cold; when that
+            # would take more than 16 copies, L2 is evicted before each step by
+            # reading a 2x-L2 buffer (a read leaves clean lines, so the timed
+            # step pays no write-backs) and steps are timed one by one.
+            copies = -(-3 * l2 // max(kv_bytes, 1))
+            l2_mode = "none" if kv_bytes >= 3 * l2 else ("rotate" if copies <= 16 else "read")
+        copies = max(2, min(16, -(-3 * l2 // max(kv_bytes, 1)))) if l2_mode == "rotate" else 1
+        self.l2_mode, self.copies = l2_mode, copies
+        self.pool_sets = [pools] + [{k: t.clone() for k, t in pools.items()}
+                                    for _ in range(copies - 1)]
+        self.back_to_back = l2_mode in ("none", "rotate")
+        # the timed steps: nothing between them writes context_lens or
+        # block_tables, so the attention launch may start its prologue while
+        # the previous step's merge finishes (PA_DECODE_EARLY_PROLOGUE).  Steps
+        # that each follow an L2-evicting kernel (not one of ours, which would
+        # let the launch start early) gain nothing by it, and launch plainly.
+        self.early = args.early_prologue == "on" and self.back_to_back
+        self.steps = [DecodeStep(**ps, block_tables=w.block_tables, context_lens=w.context_lens,
+                                 max_context_len=w.max_context_len, scale=w.scale,
+                                 num_q_heads=w.Hq, split_ctas=args.splits, window=window,
+                                 early_prologue=self.early)
+                      for ps in self.pool_sets]
+        self.step = self.steps[0]
+        self.flush_buf = torch.ones(max(2 * l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.fused = (self.step.prefers_fused if args.step == "auto"
+                      else args.step == "fused")
+        # decode_kernel + merge_kernel (fused) | append_kernel + decode_kernel + merge_kernel
+        self.launches_per_step = 2 if self.fused else 3
+        # each copy's step, and its decode alone, bound once (arguments checked
+        # and marshalled outside the timed region)
+        self.calls = [st.bind(w.q, w.k_new, w.v_new, w.slot_mapping, self.out, fused=self.fused,
+                              stream=self.stream) for st in self.steps]
+        self.decodes = [_abi.prepare(lambda st=st: st.decode(w.q, self.out), self.stream)
+                        for st in self.steps]
 
-    K = args.steps
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    clocks.mark("timed_start")
-    if back_to_back:
-        # K steps back to back between two events: an event recorded between
-        # steps costs the GPU about 2 us (measured), which is not the step's
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(K):
-            run_step(i)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        total_ms = e0.elapsed_time(e1)
-        step_ms = [total_ms / K] * K
-    else:
+    def flush(self):
+        if self.l2_mode == "read":
+            self.flush_buf.sum(dtype=torch.int64)
+        elif self.l2_mode == "write":
+            self.flush_buf.add_(1)
+
+    def run_step(self, i=0):
+        self.calls[i % self.copies]()
+
+    def _timed(self, fn, K):
+        """K calls of fn(i): back to back between two events (an event
+        recorded between steps costs the GPU about 2 us, measured, which is
+        not the step's), or each after an L2 eviction between its own events."""
+        if self.back_to_back:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            for i in range(K):
+                fn(i)
+            e1.record(self.stream)
+            torch.cuda.synchronize(self.dev)
+            return [e0.elapsed_time(e1) / K] * K
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
         for i in range(K):
-            flush()
-            ev[i][0].record(stream)
-            run_step(i)
-            ev[i][1].record(stream)
-        torch.cuda.synchronize(dev)
-        step_ms = [a.elapsed_time(b) for a, b in ev]
-        total_ms = sum(step_ms)
-    clocks.mark("timed_end")
-    if world > 1:
-        torch.distributed.barrier()
+            self.flush()
+            ev[i][0].record(self.stream)
+            fn(i)
+            ev[i][1].record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return [a.elapsed_time(b) for a, b in ev]
 
-    # for the spread of single steps: each step between its own two events
-    # (which add about 2 us each to what they time), after the timed region
-    per_ev = []
-    if back_to_back:
-        pe = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-        for i in range(K):
-            pe[i][0].record(stream)
-            run_step(i)
-            pe[i][1].record(stream)
-        torch.cuda.synchronize(dev)
-        per_ev = [a.elapsed_time(b) for a, b in pe]
+    def warm(self, warmup):
+        from paged_kv_cache_179_gb300 import _abi
+        for i in range(max(warmup, self.copies)):
+            self.flush()
+            self.run_step(i)
+        rc, bits = _abi.pa_get_status(self.dev)
+        if rc != 0:
+            raise RuntimeError(f"{self.name}: device status {rc} bits {bits}")
 
-    # the dominant kernel (decode_kernel, then merge_kernel): the fused step
-    # itself, or pa_decode timed alone the same way
-    if fused:
-        dec_ms = step_ms
-    elif back_to_back:
-        torch.cuda.synchronize(dev)
-        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        d0.record(stream)
-        for i in range(K):
-            decodes[i % copies]()
-        d1.record(stream)
-        torch.cuda.synchronize(dev)
-        dec_ms = [d0.elapsed_time(d1) / K] * K
-    else:
-        dv = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-        for i in range(K):
-            flush()
-            dv[i][0].record(stream)
-            decodes[i % copies]()
-            dv[i][1].record(stream)
-        torch.cuda.synchronize(dev)
-        dec_ms = [a.elapsed_time(b) for a, b in dv]
+    def time_steps(self, K):
+        self.step_ms = self._timed(self.run_step, K)
+        return self.step_ms
 
-    # for reference: the same step as two launches (append, then decode), each
-    # timed with its own events (they include the events' own cost)
-    sep = []
-    for i in range(min(K, 20)):
-        a0, a1, a2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        flush()
-        a0.record(stream)
-        step.append(w.k_new, w.v_new, w.slot_mapping)
-        a1.record(stream)
-        step.decode(w.q, out)
-        a2.record(stream)
-        sep.append((a0, a1, a2))
+    def time_decode(self, K):
+        """The dominant kernel (decode_kernel, then merge_kernel): the fused
+        step itself, or the decode alone timed the same way."""
+        if self.fused:
+            self.dec_ms = self.step_ms
+        else:
+            torch.cuda.synchronize(self.dev)
+            self.dec_ms = self._timed(lambda i: self.decodes[i % self.copies](), K)
+        return self.dec_ms
+
+    def kernel_bytes(self):
+        return self.ab["total"] + (self.ab["append"] if self.fused else 0)
+
+    def check(self):
+        from paged_kv_cache_179_gb300 import _abi
+        rc, bits = _abi.pa_get_status(self.dev)
+        if rc != 0:
+            raise RuntimeError(f"{self.name}: device status {rc} bits {bits}")
+
+    def describe_step(self):
+        return ("pa_decode_step: append inside the attention launch, then the merge launch"
+                if self.fused else "append launch, then attention and merge launches")
+
+    def describe_launch(self):
+        return ("attention launch with an early prologue (PA_DECODE_EARLY_PROLOGUE: it may "
+                "start while the previous step's merge finishes)" if self.early
+                else "plain launches")
+
+    def decode_us(self):
+        d = self.dec_ms
+        if self.back_to_back:
+            return {"mean": round(statistics.mean(d) * 1e3, 2),
+                    "timing": "K decodes back to back between two events"}
+        return {"mean": round(statistics.mean(d) * 1e3, 2),
+                "median": round(statistics.median(d) * 1e3, 2),
+                "p20": round(float(np.percentile(d, 20)) * 1e3, 2),
+                "p80": round(float(np.percentile(d, 80)) * 1e3, 2),
+                "min": round(min(d) * 1e3, 2),
+                "timing": "each decode between its own events, L2 evicted before it"}
+
+
+def measure_other_config(args, name, dev, clocks, peak):
+    """A config other than the headline's: its steps and decode timed as the
+    headline's are (same K, warm-up, L2 handling and launch form), with the
+    clocks seen during its own timed region."""
+    run = ConfigRun(args, name, args.seed, dev)
+    run.warm(args.warmup)
     torch.cuda.synchronize(dev)
-    app_ms = [a0.elapsed_time(a1) for a0, a1, _ in sep]
-    dec2_ms = [a1.elapsed_time(a2) for _, a1, a2 in sep]
+    clocks.mark(f"{name}:start")
+    run.time_steps(args.steps)
+    clocks.mark(f"{name}:end")
+    run.time_decode(args.steps)
+    run.check()
+    step_s = statistics.mean(run.step_ms) / 1e3
+    dec_s = statistics.mean(run.dec_ms) / 1e3
+    kb = run.kernel_bytes()
+    entry = {
+        "workload": describe(run.w, run.tokens), "step": run.describe_step(),
+        "ms_per_step": round(step_s * 1e3, 5), "tokens_per_s": round(run.tokens / step_s, 1),
+        "dtype": "e4m3->f32" if run.w.kv == "fp8" else run.w.dtype,
+        "split_ctas": run.step.split_ctas,
+        "l2": describe_l2(run.l2_mode, run.kv_bytes, run.l2, run.copies),
+        "launch": run.describe_launch(),
+        "decode_us": run.decode_us(),
+        "bytes_per_decode": kb, "hbm_gbs": round(kb / dec_s / 1e9, 1),
+        "frac_of_peak": round(kb / dec_s / 1e9 / peak, 4),
+        "gpu_launches": run.launches_per_step * args.steps,
+        "clocks_marks": (f"{name}:start", f"{name}:end"),
+    }
+    if name == "tiny":
+        entry["note"] = ("0.03 MB per step: parity case, launch- and latency-bound; its "
+                         "fraction of peak is no bandwidth claim")
+    cpu = None
+    if run.w.kv == "fp8" and not args.no_cpu_baseline:
+        cpu = oracle_baseline(run.w, run.pools, args.cpu_budget / 2)
+    del run
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    if cpu is not None:
+        entry["cpu_baseline"] = cpu
+    return entry
 
-    # end to end through the public API: the step's inputs packed in one pinned
-    # host buffer and uploaded by one copy, the output copied back.  Back to
-    # back (large or replicated pools) the steps run as a pipeline (the next
-    # step's upload and the last step's read-back overlap the current step's
-    # attention; one slot per pool copy), timed over the K steps; otherwise
-    # step by step, L2 evicted outside each step's events.
-    from paged_kv_cache_179_gb300.step import StepPipeline, StepStaging
+
+def measure_e2e(args, run, dev):
+    """End to end through the public API: the step's inputs packed in one
+    pinned host buffer and uploaded by one copy, the output copied back.  Back
+    to back (large or replicated pools) the steps run as a pipeline (the next
+    step's upload and the last step's read-back overlap the current step's
+    attention; one slot per pool copy), timed over the K steps; otherwise step
+    by step, L2 evicted outside each step's events.  Returns (total ms, bytes
+    uploaded per step, bytes read back per step, mode)."""
+    from paged_kv_cache_179_gb300.step import DecodeStep, StepPipeline, StepStaging
+    w, out, stream, K = run.w, run.out, run.stream, args.steps
     names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
     specs = {k: (getattr(w, k).shape, getattr(w, k).dtype) for k in names}
     made = []
+    fused, copies = run.fused, run.copies
 
     def make_step(staging):
-        ps = pool_sets[len(made) % copies]
+        ps = run.pool_sets[len(made) % copies]
         made.append(staging)
         # the pipeline orders each step after its upload and after the last
         # read-back of its slot by events; with those between two steps the
@@ -410,12 +486,12 @@ def run_ours(args, rank, world, dev):
         return DecodeStep(**ps, block_tables=staging.dev["block_tables"],
                           context_lens=staging.dev["context_lens"],
                           max_context_len=w.max_context_len, scale=w.scale, num_q_heads=w.Hq,
-                          split_ctas=args.splits, window=args.window,
-                          early_prologue=early)
+                          split_ctas=args.splits, window=run.window,
+                          early_prologue=run.early)
     h2d = d2h = 0
-    if back_to_back:
-        e2e_mode = ("pipelined: uploads and read-backs on two copy streams, overlapping the "
-                    f"steps ({max(2, copies)} slots)")
+    if run.back_to_back:
+        mode = ("pipelined: uploads and read-backs on two copy streams, overlapping the "
+                f"steps ({max(2, copies)} slots)")
         pipe = StepPipeline(make_step, specs, out.shape, out.dtype, dev, depth=max(2, copies))
         for st_ in pipe.stagings:
             for k in names:
@@ -430,54 +506,106 @@ def run_ours(args, rank, world, dev):
             _, h2d, d2h = pipe.submit(fused=fused)
         pipe.finish()
         e1.record(stream)
-        e2e_ev = [(e0, e1)]
+        ev = [(e0, e1)]
     else:
-        e2e_mode = "step by step: upload, step, read-back, L2 evicted between steps"
+        mode = "step by step: upload, step, read-back, L2 evicted between steps"
         staging = StepStaging(specs, dev)
         for k in names:
             staging.host[k].copy_(getattr(w, k).cpu())
         e2e_step = make_step(staging)
         host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
         for _ in range(max(1, args.warmup)):
             e2e_step.run_from_staging(staging, host_out, out, fused=fused)
         torch.cuda.synchronize(dev)
         for i in range(K):
-            flush()
-            e2e_ev[i][0].record(stream)
+            run.flush()
+            ev[i][0].record(stream)
             h2d, d2h = e2e_step.run_from_staging(staging, host_out, out, fused=fused)
-            e2e_ev[i][1].record(stream)
+            ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
-    rc, bits = _abi.pa_get_status(dev)
-    if rc != 0:
-        raise RuntimeError(f"device status {rc} bits {bits}")
-    clk = clocks.stop() if rank == 0 else None
+    return sum(a.elapsed_time(b) for a, b in ev), h2d, d2h, mode
 
-    total_ms_max, e2e_ms_max, tokens_all = reduce_over_ranks(total_ms, e2e_ms, tokens, world, dev)
+
+def run_ours(args, rank, world, dev):
+    from paged_kv_cache_179_gb300 import _abi
+
+    _abi.load()
+    run = ConfigRun(args, args.config, replica_seed(args.seed, rank), dev, args.window)
+    w, out, stream, K = run.w, run.out, run.stream, args.steps
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    if rank == 0:
+        clocks.start()
+    clocks.mark("warmup_start")
+    run.warm(args.warmup)
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.mark("timed_start")
+    step_ms = run.time_steps(K)
+    total_ms = sum(step_ms)
+    clocks.mark("timed_end")
+    if world > 1:
+        torch.distributed.barrier()
+
+    # for the spread of single steps: each step between its own two events
+    # (which add about 2 us each to what they time), after the timed region
+    per_ev = []
+    if run.back_to_back:
+        pe = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for i in range(K):
+            pe[i][0].record(stream)
+            run.run_step(i)
+            pe[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        per_ev = [a.elapsed_time(b) for a, b in pe]
+
+    dec_ms = run.time_decode(K)
+
+    # for reference: the same step as two launches (append, then decode), each
+    # timed with its own events (they include the events' own cost)
+    sep = []
+    for i in range(min(K, 20)):
+        a0, a1, a2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        run.flush()
+        a0.record(stream)
+        run.step.append(w.k_new, w.v_new, w.slot_mapping)
+        a1.record(stream)
+        run.step.decode(w.q, out)
+        a2.record(stream)
+        sep.append((a0, a1, a2))
+    torch.cuda.synchronize(dev)
+    app_ms = [a0.elapsed_time(a1) for a0, a1, _ in sep]
+    dec2_ms = [a1.elapsed_time(a2) for _, a1, a2 in sep]
+
+    e2e_ms, h2d, d2h, e2e_mode = measure_e2e(args, run, dev)
+    run.check()
+
+    total_ms_max, e2e_ms_max, tokens_all = reduce_over_ranks(total_ms, e2e_ms, run.tokens,
+                                                             world, dev)
     if rank != 0:
+        clocks.stop()
         return None
 
-    ab = algorithmic_bytes(w, lens, args.window)
-    dec_mean_s = statistics.mean(dec_ms) / 1e3
     peak, peak_kind = measured_peaks()
-    kernel_bytes = ab["total"] + (ab["append"] if fused else 0)
+    dec_mean_s = statistics.mean(dec_ms) / 1e3
+    kernel_bytes = run.kernel_bytes()
+    ab = run.ab
     achieved = kernel_bytes / dec_mean_s / 1e9
     value = tokens_all * K / (total_ms_max / 1e3)
-    traffic = load_traffic(args.config, step.split_ctas)
+    traffic = load_traffic(args.config, run.step.split_ctas)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms_max / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3->f32" if w.kv == "fp8" else w.dtype, "data": "synthetic",
         "config": {
-            "workload": describe(w, tokens),
-            "step": ("pa_decode_step: append inside the attention launch, then the merge launch"
-                     if fused else "append launch, then attention and merge launches"),
-            "split_ctas": step.split_ctas, "l2": describe_l2(l2_mode, kv_bytes, l2, copies),
-            "launch": ("attention launch with an early prologue (PA_DECODE_EARLY_PROLOGUE: "
-                       "it may start while the previous step's merge finishes)" if early else
-                       "plain launches"),
+            "workload": describe(w, run.tokens), "step": run.describe_step(),
+            "split_ctas": run.step.split_ctas,
+            "l2": describe_l2(run.l2_mode, run.kv_bytes, run.l2, run.copies),
+            "launch": run.describe_launch(),
             "seed": args.seed, "parallelism": "replicas" if world > 1 else "single GPU",
             **({"window": args.window} if args.window else {}),
         },
@@ -485,21 +613,14 @@ def run_ours(args, rank, world, dev):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": ("decode_kernel with fused append, then merge_kernel (timed "
-                                "together: one decode)" if fused
+                                "together: one decode)" if run.fused
                                 else "decode_kernel, then merge_kernel (timed together: one decode)"),
                      "bytes_per_launch": kernel_bytes, "peak_source": peak_kind,
                      **({"kv_bytes_unique": ab["kv_unique"],
                          "note": "a shared prefix is read by each sequence attending it and "
                                  "counted each time; kv_bytes_unique counts it once"}
                         if ab["kv_unique"] != ab["kv"] else {})},
-        "decode_us": ({"mean": round(statistics.mean(dec_ms) * 1e3, 2),
-                       "timing": "K decodes back to back between two events"} if back_to_back else
-                      {"mean": round(statistics.mean(dec_ms) * 1e3, 2),
-                       "median": round(statistics.median(dec_ms) * 1e3, 2),
-                       "p20": round(float(np.percentile(dec_ms, 20)) * 1e3, 2),
-                       "p80": round(float(np.percentile(dec_ms, 80)) * 1e3, 2),
-                       "min": round(min(dec_ms) * 1e3, 2),
-                       "timing": "each decode between its own events, L2 evicted before it"}),
+        "decode_us": run.decode_us(),
         **({"step_us_own_events": {
             "median": round(statistics.median(per_ev) * 1e3, 2),
             "p20": round(float(np.percentile(per_ev, 20)) * 1e3, 2),
@@ -511,11 +632,32 @@ def run_ours(args, rank, world, dev):
                                "decode": round(statistics.mean(dec2_ms) * 1e3, 2)},
         "e2e": {"value": round(tokens_all * K / (e2e_ms_max / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "mode": e2e_mode},
-        "gpu_launches": launches_per_step * K,
-        "clocks": clk,
+        "gpu_launches": run.launches_per_step * K,
     }
-    if not args.no_cpu_baseline and w.kv != "fp8":
-        line["cpu_baseline"] = oracle_baseline(w, args.cpu_budget, args.window)
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_baseline(w, run.pools, args.cpu_budget, args.window)
+        if args.config == DEFAULT_CONFIG and world == 1:
+            line["cpu_baseline_single_core"] = oracle_baseline(
+                w, run.pools, args.cpu_budget / 2, args.window, threads=1)
+
+    # the other configs, one after another, each batch freed before the next
+    # is drawn (single-GPU default runs only)
+    others = {}
+    if args.configs == "all" and world == 1 and args.config == DEFAULT_CONFIG and not args.window:
+        del run, w, out
+        gc.collect()
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        line["gpu_launches_all_configs"] = line["gpu_launches"]
+        for name in OTHER_CONFIGS:
+            others[name] = measure_other_config(args, name, dev, clocks, peak)
+            line["gpu_launches_all_configs"] += others[name]["gpu_launches"]
+    line["clocks"] = clocks.stop()
+    if others:
+        for name, e in others.items():
+            start, end = e.pop("clocks_marks")
+            e["clocks"] = clocks.summary(start, end, before=start)
+        line["configs"] = others
     return line
 
 
@@ -804,6 +946,10 @@ def main(argv=None):
     ap.add_argument("--early-prologue", choices=["on", "off"], default="on",
                     help="steps with PA_DECODE_EARLY_PROLOGUE (the device-timed steps and the "
                          "pipelined end-to-end run)")
+    ap.add_argument("--configs", choices=["all", "none"], default="all",
+                    help="all: the default single-GPU run also times the other four configs "
+                         "(tiny, SmolLM2-360M, Qwen2.5-1.5B, E4M3 Qwen2.5-7B) one after another "
+                         "and reports them under 'configs'")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-step-s", type=float, default=2.0)

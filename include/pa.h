@@ -77,7 +77,7 @@ enum {
     PA_ERR_WORKSPACE = 3,    /* workspace missing, too small or misaligned */
     PA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
     PA_ERR_BOUNDS = 5,       /* pa_get_status: a kernel skipped an out-of-range index */
-    PA_ERR_TIMEOUT = 6,      /* pa_get_status: an asynchronous-copy wait gave up */
+    PA_ERR_TIMEOUT = 6,      /* pa_get_status: a kernel's bounded wait gave up */
     PA_ERR_SCRATCH_LIMIT = 7 /* pa_decode_noalloc: sizes need more than its static scratch */
 };
 
@@ -85,7 +85,7 @@ enum {
 #define PA_STATUS_BAD_BLOCK 1u   /* block table entry outside [0, num_blocks) */
 #define PA_STATUS_BAD_LEN 2u     /* context_len < 0, > max_context_len or > max_blocks_per_seq*block_size */
 #define PA_STATUS_BAD_SLOT 4u    /* slot >= num_blocks * block_size */
-#define PA_STATUS_TIMEOUT 8u     /* an mbarrier wait reached its iteration limit */
+#define PA_STATUS_TIMEOUT 8u     /* a wait (for a copy, or for partial results) reached its time limit */
 #define PA_STATUS_NO_WORKSPACE 16u /* a split partition had no workspace (never written) */
 #define PA_STATUS_WS_DIRTY 32u   /* a decode read a partial result no decode writes: its workspace
                                     was not zero-filled (or a call that timed out left it so) and
@@ -330,7 +330,11 @@ int pa_decode_step_fp8(void *out, const void *q, const void *k_new, const void *
  * a device share the array: calls that overlap on the GPU race.  The array
  * starts zero-filled and every call leaves it so; after a pa_get_status
  * that shows PA_STATUS_TIMEOUT or PA_STATUS_WS_DIRTY, the next call on that
- * device zeroes it first (a stream-ordered memset).
+ * device zeroes it first (a stream-ordered memset).  That clearing is made
+ * by the host call, so a CUDA graph that captured pa_decode_noalloc before
+ * such a status never makes it: its replays would merge partials the
+ * failed call left behind.  Re-capture such graphs after a direct call
+ * (the direct call clears the scratch).
  */
 #define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
 int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -348,6 +352,34 @@ int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void 
  * bits go to *bits when bits is not NULL.
  */
 int pa_get_status(void *stream, unsigned *bits);
+
+/*
+ * Failure-path tests of the kernels' bounded waits.  Every wait a kernel of
+ * this library makes (an mbarrier wait for an asynchronous copy, the merge
+ * launch's poll for partial results another grid writes) gives up after a
+ * time limit (2 s in the entry points above), sets PA_STATUS_TIMEOUT and
+ * lets the kernel return, so a lost copy or a missing partial never hangs the
+ * GPU.  These two calls make such a wait run out on purpose, with a short
+ * limit, so that a test can check the status and that the context stays
+ * usable.  Neither faults, traps or spins without bound.
+ *
+ * pa_test_wait_timeout: one warp waits, with the attention loop's bounded
+ * wait, on an mbarrier that nothing completes; after limit_ns (1 .. 2e9) it
+ * sets PA_STATUS_TIMEOUT.
+ *
+ * pa_test_merge_timeout: the merge launch of a pa_decode with these sizes,
+ * run alone, so no attention launch ever writes the partials it polls for;
+ * with a zero-filled workspace every CTA of a split sequence gives up after
+ * limit_ns and sets PA_STATUS_TIMEOUT, writing neither out nor the
+ * workspace.  context_lens is a device array as for pa_decode; at most 512
+ * sequences; n_q = 1, no window.
+ * Neither has a counterpart in the pages: they exist to test the library.
+ */
+int pa_test_wait_timeout(uint64_t limit_ns, void *stream);
+int pa_test_merge_timeout(void *out, const int32_t *context_lens, int max_context_len,
+                          int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                          int dtype, int split_ctas, void *workspace, size_t workspace_bytes,
+                          uint64_t limit_ns, void *stream);
 
 /* A static string naming a return code. */
 const char *pa_status_string(int code);

@@ -67,6 +67,7 @@ def lib():
                                             i32, i32, f32, i32, i32, vp, i32, vp]
             L.oracle_copy_blocks.argtypes = [vp, vp, vp, vp, vp, i32, ctypes.c_size_t, i32, i64]
             L.oracle_num_threads.restype = i32
+            L.oracle_set_num_threads.argtypes = [i32]
             _lib = L
     return _lib
 
@@ -74,6 +75,12 @@ def lib():
 def num_threads() -> int:
     """OpenMP threads the oracle's parallel loops use (OMP_NUM_THREADS or all cores)."""
     return int(lib().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Run the oracle's parallel loops on ``n`` threads from now on (results
+    do not depend on it: each output row is reduced by one thread)."""
+    lib().oracle_set_num_threads(int(n))
 
 
 def _u16(a: np.ndarray) -> np.ndarray:

@@ -428,3 +428,15 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* Threads of the parallel loops from now on (n >= 1); a harness setting, used
+ * to time the oracle on one core.  Results do not depend on it: every output
+ * row is reduced serially by one thread. */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

@@ -51,6 +51,9 @@ SIGNATURES = {
     "pa_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                            _i32, _i32, _f32, _i32, _i32, _i32, _i32, _u32, _vp], _i32),
     "pa_get_status": ([_vp, ctypes.POINTER(ctypes.c_uint)], _i32),
+    "pa_test_wait_timeout": ([ctypes.c_uint64, _vp], _i32),
+    "pa_test_merge_timeout": ([_vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz,
+                               ctypes.c_uint64, _vp], _i32),
 }
 
 _lock = threading.Lock()
@@ -448,6 +451,28 @@ def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
           block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
           float(scale), int(window), nq, _act_code(q.dtype), int(split_ctas),
           _flags(early_prologue), _stream(dev))
+
+
+def pa_test_wait_timeout(limit_ns: int, device=None) -> None:
+    """Failure-path test: one warp's bounded mbarrier wait on a barrier that
+    nothing completes gives up after ``limit_ns`` and sets PA_STATUS_TIMEOUT."""
+    _call(load().pa_test_wait_timeout, "pa_test_wait_timeout", int(limit_ns),
+          _stream(device or torch.cuda.current_device()))
+
+
+def pa_test_merge_timeout(out, context_lens, max_context_len: int, num_kv_heads: int,
+                          split_ctas: int, workspace, limit_ns: int) -> None:
+    """Failure-path test: pa_decode's merge launch alone (nothing writes the
+    partials it polls for) gives up after ``limit_ns`` and sets
+    PA_STATUS_TIMEOUT.  out [B][Hq][D] as for pa_decode."""
+    dev = out.device
+    _need(out, "out", (torch.float16, torch.bfloat16), 3, dev)
+    _need(context_lens, "context_lens", torch.int32, 1, dev)
+    B, Hq, D = out.shape
+    _call(load().pa_test_merge_timeout, "pa_test_merge_timeout",
+          _ptr(out), _ptr(context_lens), int(max_context_len), B, Hq, int(num_kv_heads), D,
+          _act_code(out.dtype), int(split_ctas), _ptr(workspace), _ws_bytes(workspace, dev),
+          int(limit_ns), _stream(dev))
 
 
 def pa_get_status(device=None) -> tuple[int, int]:

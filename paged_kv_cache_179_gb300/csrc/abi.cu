@@ -18,7 +18,6 @@ __device__ unsigned int g_pa_status_word;
 namespace pa {
 namespace {
 
-constexpr int kMaxDevices = 64;
 struct DeviceState {
   bool ready = false;
   unsigned* status = nullptr;
@@ -119,6 +118,7 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
   a.q_first = 0;
   a.early = (s.flags & PA_DECODE_EARLY_PROLOGUE) ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit_ns = kWaitLimitNs;
   a.k_pool_w = ap.k_pool;
   a.v_pool_w = ap.v_pool;
   a.k_scale_w = ap.k_scale;
@@ -185,7 +185,7 @@ const char* pa_status_string(int code) {
     case PA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
     case PA_ERR_CUDA: return "CUDA error";
     case PA_ERR_BOUNDS: return "a kernel skipped an out-of-range index";
-    case PA_ERR_TIMEOUT: return "an asynchronous-copy wait gave up";
+    case PA_ERR_TIMEOUT: return "a kernel's bounded wait gave up";
     case PA_ERR_SCRATCH_LIMIT: return "request exceeds the library's static scratch array";
     default: return "unknown status";
   }
@@ -425,6 +425,51 @@ int pa_decode_step_fp8(void* out, const void* q, const void* k_new, const void* 
   ap.v_scale = v_scale;
   return run_decode(s, out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
                     scale, true, dtype == PA_BF16, workspace, workspace_bytes, stream, ap);
+}
+
+int pa_test_wait_timeout(uint64_t limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > kWaitLimitNs) return PA_ERR_INVALID_ARG;
+  DeviceState* dev = nullptr;
+  if (int rc = device_state(&dev)) return rc;
+  return cuda_status(launch_wait_probe(dev->status, limit_ns, static_cast<cudaStream_t>(stream)));
+}
+
+int pa_test_merge_timeout(void* out, const int32_t* context_lens, int max_context_len,
+                          int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                          int dtype, int split_ctas, void* workspace, size_t workspace_bytes,
+                          uint64_t limit_ns, void* stream) {
+  if (!out || !context_lens || !workspace) return PA_ERR_INVALID_ARG;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+  if (limit_ns == 0 || limit_ns > kWaitLimitNs) return PA_ERR_INVALID_ARG;
+  if (num_seqs <= 0 || num_seqs > kMaxBatchPerLaunch || split_ctas <= 0 || max_context_len < 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_q_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (!aligned(out, 16) || !aligned(context_lens, 4) || !aligned(workspace, 256))
+    return PA_ERR_INVALID_ARG;
+  if (workspace_bytes < decode_workspace_bytes(num_seqs, num_q_heads, head_dim, split_ctas))
+    return PA_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  if (int rc = device_state(&dev)) return rc;
+  DecodeArgs a{};
+  a.out = out;
+  a.context_lens = context_lens;
+  a.status = dev->status;
+  a.mbs = (max_context_len + 15) / 16 > 0 ? (max_context_len + 15) / 16 : 1;
+  a.B = num_seqs;
+  a.Hq = num_q_heads;
+  a.Hkv = num_kv_heads;
+  a.group = num_q_heads / num_kv_heads;
+  a.D = head_dim;
+  a.max_context_len = max_context_len;
+  a.split_ctas = split_ctas;
+  a.n_q = 1;
+  a.q_tokens = 1;
+  a.wait_limit_ns = limit_ns;
+  decode_workspace_split(a, workspace);
+  return cuda_status(launch_merge_only(a, dtype == PA_BF16, static_cast<cudaStream_t>(stream)));
 }
 
 int pa_get_status(void* stream, unsigned* bits) {

@@ -55,9 +55,11 @@
 //
 // Bounds: block ids outside [0, num_blocks) and context lengths above their
 // bounds are never dereferenced; they set a status bit.  Every mbarrier wait
-// is bounded (kWaitLimit) and reports kStatusTimeout instead of hanging.
+// is bounded in time (DecodeArgs::wait_limit_ns) and reports kStatusTimeout
+// instead of hanging.
 #include <cfloat>
 #include <climits>
+#include <mutex>
 #include <type_traits>
 
 #include <cudaTypedefs.h>
@@ -909,7 +911,8 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     const int t_last = (APPEND && ((FP8 && ends_seg) || nt0.slot >= 0)) ? ch0.nb - 1 : -1;
     for (int t = 0; t < ch0.nb && !dead; ++t) {
       const int s = computed % STAGES;
-      if (!__all_sync(0xffffffffu, mbar_wait(sbar + 8 * s, (computed / STAGES) & 1))) {
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(sbar + 8 * s, (computed / STAGES) & 1, a.wait_limit_ns))) {
         if (lane == 0) atomicOr(a.status, kStatusTimeout);
         dead = true;
         break;
@@ -1043,7 +1046,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   if (dead) {
     // Wait (bounded) for this warp's copies still in flight.
     for (; computed < issued; ++computed)
-      (void)mbar_wait(sbar + 8 * (computed % STAGES), (computed / STAGES) & 1);
+      (void)mbar_wait(sbar + 8 * (computed % STAGES), (computed / STAGES) & 1, a.wait_limit_ns);
   }
 
   PA_TRACE_WARP(gw, 3, pa_now());
@@ -1191,13 +1194,13 @@ merge_kernel(const DecodeArgs a) {
             const uint64_t tl = global_ns();
             while (ld_relaxed_b32(first) == 0u) {
               __nanosleep(64);
-              if (global_ns() - tl > kPollLimitNs) {
+              if (global_ns() - tl > a.wait_limit_ns) {
                 fail = 1;
                 break;
               }
             }
           }
-          if (tid == 0 && global_ns() - t0 > kPollLimitNs) fail = 1;
+          if (tid == 0 && global_ns() - t0 > a.wait_limit_ns) fail = 1;
           __syncthreads();
           if (fail) break;
 #pragma unroll
@@ -1284,6 +1287,20 @@ cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, merge_kernel<D, BF16>, a);
 }
 
+// One warp: lane 0 sets up an mbarrier that nothing ever completes and waits
+// on it as the attention loop waits for its tiles (bounded by limit_ns), then
+// reports the timeout.  Used only to test that failure path.
+__global__ void wait_probe_kernel(unsigned* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), 0, limit_ns)) && threadIdx.x == 0)
+    atomicOr(status, kStatusTimeout);
+}
+
 // cuTensorMapEncodeTiled, from the driver (no link against libcuda).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
@@ -1347,15 +1364,26 @@ cudaError_t launch_one(const DecodeArgs& args, cudaStream_t s) {
   }
   const Layout lay = make_layout(TL::RING + TL::PAD, STAGES, a.B);
   auto* kern = decode_kernel<D, FP8, BF16, STAGES, APPEND, GENERAL, CTAS>;
-  static thread_local int last_smem[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (last_smem[dev & 63] != lay.total) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
+  // The dynamic shared-memory limit is an attribute of the function shared
+  // by every host thread: it is raised once per device, under a lock, to the
+  // layout of the largest batch a launch takes, so no thread ever lowers it
+  // below what another thread's launch asks for.
+  {
+    static std::mutex mu;
+    static bool raised[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    last_smem[dev & 63] = lay.total;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!raised[dev]) {
+      const int most = make_layout(TL::RING + TL::PAD, STAGES, kMaxBatchPerLaunch).total;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+      if (e != cudaSuccess) return e;
+      raised[dev] = true;
+    }
   }
+  cudaError_t e = cudaSuccess;
   if (a.early) {
     // a programmatic dependent launch: the prologue may overlap the previous
     // kernel on the stream, the rest waits for it (griddepcontrol.wait)
@@ -1439,6 +1467,16 @@ WsLayout ws_layout(int D, int split_ctas) {
   return l;
 }
 }  // namespace
+
+cudaError_t launch_merge_only(const DecodeArgs& a, bool bf16, cudaStream_t s) {
+  if (a.D == 128) return bf16 ? launch_merge<128, true>(a, s) : launch_merge<128, false>(a, s);
+  return bf16 ? launch_merge<64, true>(a, s) : launch_merge<64, false>(a, s);
+}
+
+cudaError_t launch_wait_probe(unsigned* status, uint64_t limit_ns, cudaStream_t s) {
+  wait_probe_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
 
 size_t decode_workspace_bytes(int B, int Hq, int D, int split_ctas) {
   if (B <= 0 || Hq <= 0 || D <= 0 || split_ctas <= 0) return 0;

@@ -27,7 +27,7 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
+using pa::kMaxDevices;
 std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 bool g_scratch_suspect[kMaxDevices] = {};
@@ -116,6 +116,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   a.q_first = 0;
   a.early = (flags & PA_DECODE_EARLY_PROLOGUE) ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit_ns = kWaitLimitNs;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   {
     // a status read saw a wait give up or a dirty workspace: partials may be

@@ -13,6 +13,16 @@ namespace pa {
 // the batch in shared memory; the host splits larger batches.
 constexpr int kMaxBatchPerLaunch = 512;
 
+// Devices the library keeps per-device state for (ordinals 0 .. 63).
+constexpr int kMaxDevices = 64;
+
+// Default time limit of every wait a kernel makes: an mbarrier wait for an
+// asynchronous copy, or the merge launch's poll for another grid's partial
+// results.  A wait that ends normally takes microseconds; one that reaches
+// the limit gives up, and the kernel sets kStatusTimeout and returns instead
+// of hanging.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
 // All pointers are device pointers; sizes were validated by the caller.
 struct DecodeArgs {
   // 16-bit pools: tensor maps of k_cache and v_cache that copy one
@@ -50,6 +60,7 @@ struct DecodeArgs {
   int q_first;                  // the first of them this launch serves
   int early;                    // programmatic dependent launch: prologue before griddepcontrol.wait
   float scale_log2;             // softmax scale * log2(e)
+  uint64_t wait_limit_ns;       // time limit of every wait (kWaitLimitNs unless a test shortens it)
 };
 
 int decode_default_ctas(bool fp8);   // CTAs a default launch uses for this pool type
@@ -59,6 +70,12 @@ size_t decode_workspace_bytes(int B, int Hq, int D, int split_ctas);
 void decode_workspace_split(DecodeArgs& a, void* ws);
 
 cudaError_t launch_decode(const DecodeArgs& a, bool fp8, bool bf16, cudaStream_t s);
+// The merge launch alone (no attention launch writes its partials): the
+// failure-path test of its bounded poll.
+cudaError_t launch_merge_only(const DecodeArgs& a, bool bf16, cudaStream_t s);
+// One warp waiting on an mbarrier that nothing completes, with the decode's
+// bounded wait: the failure-path test of that wait.
+cudaError_t launch_wait_probe(unsigned* status, uint64_t limit_ns, cudaStream_t s);
 
 cudaError_t launch_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                           const int64_t* slots, int T, int Hkv, int row_bytes, int block_size,

@@ -18,12 +18,9 @@ constexpr unsigned kStatusTimeout = 8u;    // an mbarrier wait hit its iteration
 constexpr unsigned kStatusNoWorkspace = 16u;  // a split partition found no workspace
 constexpr unsigned kStatusWsDirty = 32u;   // a partial no decode writes: workspace not zero-filled
 
-// Iteration limit of every mbarrier wait.  A wait that ends normally takes a
-// few microseconds.  Each try_wait suspends the thread for at most
-// kSuspendHintNs (it returns as soon as the phase completes), so a stuck wait
-// gives up after roughly kWaitLimit * kSuspendHintNs = 2 s and the kernel
-// reports kStatusTimeout instead of hanging.
-constexpr int kWaitLimit = 1 << 20;
+// Each mbarrier try_wait suspends the thread for at most kSuspendHintNs (it
+// returns as soon as the phase completes); waits are bounded in time by the
+// caller's limit (see mbar_wait).
 constexpr uint32_t kSuspendHintNs = 2000;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -54,10 +51,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (int it = 0; it < kWaitLimit; ++it)
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait for the phase with the given parity to complete: false when
+// limit_ns of %globaltimer time passed first.  The clock is read only once
+// the first try has failed.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  do {
     if (mbar_try_wait(bar, parity)) return true;
+  } while (global_ns() - t0 < limit_ns);
   return false;
 }
 
@@ -86,14 +93,6 @@ __device__ __forceinline__ uint4 ld_relaxed_v4(const void* p) {
                : "l"(p));
   return v;
 }
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-// Time limit of a wait for another grid's data: a wait that gives up
-// reports kStatusTimeout instead of hanging the kernel.
-constexpr uint64_t kPollLimitNs = 2000000000ull;
 
 // ------------------------------------------------------- bulk async copies
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {

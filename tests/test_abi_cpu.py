@@ -31,7 +31,7 @@ def header_functions():
 
 def test_header_and_binding_agree():
     names = header_functions()
-    assert len(names) == 15
+    assert len(names) == 17
     assert sorted(_abi.SIGNATURES) == names
 
 
@@ -105,6 +105,19 @@ def test_append_and_quantize_argument_errors(lib):
     assert q(None, None, FAKE, FAKE, FAKE, FAKE, 8, 2, 64, 16, None) == _abi.PA_ERR_INVALID_ARG
     assert q(FAKE, None, FAKE, None, FAKE, None, 8, 2, 64, 32, None) == _abi.PA_ERR_UNSUPPORTED
     assert lib.pa_e4m3_encode(FAKE, MISALIGNED, 10, None) == _abi.PA_ERR_INVALID_ARG
+
+
+def test_failure_path_hooks_check_their_limits(lib):
+    # a limit of 0 or above the 2 s default is refused before any CUDA call
+    assert lib.pa_test_wait_timeout(0, None) == _abi.PA_ERR_INVALID_ARG
+    assert lib.pa_test_wait_timeout(3_000_000_000, None) == _abi.PA_ERR_INVALID_ARG
+    m = lib.pa_test_merge_timeout
+    assert m(FAKE, FAKE, 128, 2, 8, 2, 64, 0, 8, FAKE, 1 << 20, 0, None) == _abi.PA_ERR_INVALID_ARG
+    assert m(FAKE, FAKE, 128, 2, 8, 2, 96, 0, 8, FAKE, 1 << 20, 1000, None) == \
+        _abi.PA_ERR_UNSUPPORTED
+    assert m(FAKE, FAKE, 128, 2, 8, 2, 64, 0, 8, FAKE, 16, 1000, None) == _abi.PA_ERR_WORKSPACE
+    assert m(FAKE, FAKE, 128, 513, 8, 2, 64, 0, 8, FAKE, 1 << 20, 1000, None) == \
+        _abi.PA_ERR_INVALID_ARG
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a CUDA device")
