@@ -733,7 +733,7 @@ def run_multiquery(args, dev):
     if w.kv == "fp8":
         raise SystemExit("--op multiquery runs on 16-bit pools")
     n = args.queries
-    per_pass = n if n * w.group <= 8 else 8 // w.group     # query tokens per launch pair
+    per_pass = n if n * w.group <= 32 else 32 // w.group   # query tokens per launch pair
     passes = -(-n // per_pass)
     lens = w.context_lens.cpu().numpy()
     g = torch.Generator(device=dev).manual_seed(args.seed + 17)
@@ -754,7 +754,8 @@ def run_multiquery(args, dev):
     steps = [DecodeStep(k_cache=kc, v_cache=vc, block_tables=w.block_tables,
                         context_lens=w.context_lens, max_context_len=w.max_context_len,
                         scale=w.scale, num_q_heads=w.Hq, split_ctas=args.splits,
-                        window=args.window, early_prologue=early) for kc, vc in pool_sets]
+                        window=args.window, early_prologue=early, queries_per_seq=n)
+             for kc, vc in pool_sets]
     step = steps[0]
     stream = torch.cuda.current_stream(dev)
     calls = [_abi.prepare(lambda st=st: st.decode(q, out), stream) for st in steps]

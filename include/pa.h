@@ -48,7 +48,8 @@
  *     dereferenced: the kernel skips the access and sets a bit in the
  *     library's device status word, which pa_get_status reads.
  *   - Supported now: head_dim 64 or 128, block_size 16, num_q_heads /
- *     num_kv_heads from 1 to 8.  Other shapes return PA_ERR_UNSUPPORTED.
+ *     num_kv_heads from 1 to 32 (multi-query attention included).  Other
+ *     shapes return PA_ERR_UNSUPPORTED.
  *   - Host state: for 16-bit pools the decode entry points encode TMA
  *     tensor maps of k_cache and v_cache (host memory, passed by value with
  *     the launch) and keep the last 40 per host thread, keyed by pool
@@ -194,8 +195,23 @@ int pa_decode_default_splits(int pool_type);
  * serves call after call, whatever their sizes, without clearing.  After a
  * call whose status shows PA_STATUS_TIMEOUT or PA_STATUS_WS_DIRTY, zero-fill
  * it again.  Calls that share a workspace must not overlap on the device.
+ *
+ * The size serves calls with up to 8 query rows per (sequence, kv head):
+ * queries_per_seq * (num_q_heads / num_kv_heads) <= 8.  Calls with more
+ * rows (query groups above 8, or several query tokens) hold 16 or 32 rows
+ * per partial and need pa_decode_workspace_size_rows.
  */
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int split_ctas);
+
+/*
+ * Bytes of decode workspace for calls with up to query_rows =
+ * queries_per_seq * (num_q_heads / num_kv_heads) query rows per (sequence,
+ * kv head): a launch holds 8, 16 or 32 rows per partial (the widest of its
+ * passes: at most 32 rows).  pa_decode_workspace_size(...) equals this with
+ * query_rows 8.  Otherwise as pa_decode_workspace_size.
+ */
+size_t pa_decode_workspace_size_rows(int num_seqs, int num_q_heads, int head_dim, int split_ctas,
+                                     int query_rows);
 
 /*
  * Paged GQA decode over a 16-bit pool.  For every sequence b and q head hq,
@@ -223,12 +239,14 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int
  *   query i sits at position L - n_q + i (its own token and those before it
  *   are in the cache) and attends causally, positions up to its own (within
  *   its window); a query before position 0 gets a zero output.  With
- *   n_q * (num_q_heads / num_kv_heads) <= 8 the K/V is read once for all
- *   queries; larger n_q (at most 1024) run as consecutive passes of
- *   8 / group tokens, each reading the K/V again (pa_decode_noalloc rejects
- *   them with PA_ERR_UNSUPPORTED);
- *   workspace: at least pa_decode_workspace_size(...) bytes, 256-byte
- *   aligned;
+ *   n_q * (num_q_heads / num_kv_heads) <= 32 query rows per (sequence, kv
+ *   head) the K/V is read once for all of them; larger n_q (at most 1024)
+ *   run as consecutive passes of 32 / group tokens, each reading the K/V
+ *   again (pa_decode_noalloc rejects more than 8 rows with
+ *   PA_ERR_UNSUPPORTED).  Launches with more than 8 rows hold two CTAs per
+ *   SM whatever the pool type (split_ctas 0 then means two per SM);
+ *   workspace: at least pa_decode_workspace_size_rows(..., query_rows) bytes
+ *   (pa_decode_workspace_size(...) when query_rows <= 8), 256-byte aligned;
  *   flags: 0, or PA_DECODE_EARLY_PROLOGUE: the attention launch becomes a
  *   programmatic dependent launch.  Its prologue (reading context_lens and
  *   block_tables, dividing the batch among the warps, reading each warp's

@@ -38,6 +38,7 @@ SIGNATURES = {
     "pa_e4m3_encode": ([_vp, _vp, _i64, _vp], _i32),
     "pa_copy_blocks": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp], _i32),
     "pa_decode_workspace_size": ([_i32, _i32, _i32, _i32], _sz),
+    "pa_decode_workspace_size_rows": ([_i32, _i32, _i32, _i32, _i32], _sz),
     "pa_decode_default_splits": ([_i32], _i32),
     "pa_decode": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                    _f32, _i32, _i32, _i32, _i32, _vp, _sz, _u32, _vp], _i32),
@@ -294,6 +295,14 @@ def pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, split_ctas=0) -> i
     return int(load().pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, split_ctas))
 
 
+def pa_decode_workspace_size_rows(num_seqs, num_q_heads, head_dim, split_ctas=0,
+                                  query_rows=8) -> int:
+    """Workspace bytes for calls with up to ``query_rows`` = queries_per_seq *
+    (num_q_heads / num_kv_heads) query rows per (sequence, kv head)."""
+    return int(load().pa_decode_workspace_size_rows(num_seqs, num_q_heads, head_dim, split_ctas,
+                                                    query_rows))
+
+
 def pa_decode_default_splits(pool_dtype=torch.float16) -> int:
     """CTAs a default (split_ctas=0) decode uses over pools of this dtype
     (torch.uint8 for E4M3 pools)."""
@@ -301,10 +310,12 @@ def pa_decode_default_splits(pool_dtype=torch.float16) -> int:
     return int(load().pa_decode_default_splits(code))
 
 
-def alloc_workspace(num_seqs, num_q_heads, head_dim, split_ctas, device):
+def alloc_workspace(num_seqs, num_q_heads, head_dim, split_ctas, device, query_rows=8):
     """Caller-owned workspace for pa_decode, zero-filled as the decode needs
-    it (each call leaves it zero-filled again)."""
-    n = pa_decode_workspace_size(num_seqs, num_q_heads, head_dim, split_ctas)
+    it (each call leaves it zero-filled again); ``query_rows``: the most
+    query rows per (sequence, kv head) of the calls it serves (queries per
+    sequence times the query group)."""
+    n = pa_decode_workspace_size_rows(num_seqs, num_q_heads, head_dim, split_ctas, query_rows)
     return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
 
 

@@ -65,7 +65,7 @@ int check_decode_shape(const DecodeShape& s, float scale) {
   if (s.D != 64 && s.D != 128) return PA_ERR_UNSUPPORTED;
   if (s.bs != 16) return PA_ERR_UNSUPPORTED;
   if (s.nq < 1 || s.nq > 1024) return PA_ERR_INVALID_ARG;
-  if (s.Hq / s.Hkv > 8) return PA_ERR_UNSUPPORTED;
+  if (s.Hq / s.Hkv > kMaxRowsPerLaunch) return PA_ERR_UNSUPPORTED;
   if (s.flags & ~PA_DECODE_EARLY_PROLOGUE) return PA_ERR_INVALID_ARG;
   if (s.B > 65535 || s.Hkv > 65535) return PA_ERR_UNSUPPORTED;
   return PA_OK;
@@ -82,20 +82,30 @@ struct AppendArgs {
   float* v_scale = nullptr;
 };
 
+// Query tokens one launch pair serves: all n_q when their n_q * G rows fit
+// kMaxRowsPerLaunch (the K/V is then read once for all of them), else as many
+// as fit, in consecutive passes.
+int tokens_per_pass(int nq, int group) {
+  return nq * group <= kMaxRowsPerLaunch ? nq : kMaxRowsPerLaunch / group;
+}
+
 int run_decode(DecodeShape s, void* out, const void* q, const void* k, const void* v,
                const float* ks, const float* vs, const int32_t* bt, const int32_t* cl,
                float scale, bool fp8, bool bf16, void* ws, size_t ws_bytes, void* stream,
                const AppendArgs& ap = AppendArgs()) {
   if (s.B == 0) return PA_OK;
+  const int group = s.Hq / s.Hkv;
+  const int per_pass = tokens_per_pass(s.nq, group);
+  const int rows = per_pass * group;   // query rows per (sequence, kv head) of the widest pass
   auto ws_ok = [&]() {   // every split needs one: its four warps divide the batch
-    const size_t need = decode_workspace_bytes(s.B, s.Hq, s.D, s.splits);
+    const size_t need = decode_workspace_bytes(s.B, s.Hq, s.D, s.splits, rows);
     return ws != nullptr && ws_bytes >= need && aligned(ws, 256);
   };
   if (s.splits > 0 && !ws_ok()) return PA_ERR_WORKSPACE;   // checked before touching CUDA
   DeviceState* dev = nullptr;
   if (int rc = device_state(&dev)) return rc;
   if (s.splits == 0) {
-    s.splits = decode_default_ctas(fp8);
+    s.splits = decode_default_ctas(fp8, rows);
     if (!ws_ok()) return PA_ERR_WORKSPACE;
   }
   DecodeArgs a{};
@@ -107,7 +117,7 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
   a.mbs = s.mbs;
   a.Hq = s.Hq;
   a.Hkv = s.Hkv;
-  a.group = s.Hq / s.Hkv;
+  a.group = group;
   a.D = s.D;
   a.num_blocks = s.NB;
   a.max_context_len = s.max_ctx;
@@ -139,15 +149,16 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
       c.v_new = static_cast<const uint8_t*>(ap.v_new) + b0 * new_row;
       c.slots = ap.slots + b0;
     }
-    decode_workspace_split(c, ws);
-    // One launch pair serves up to 8 query rows per (sequence, kv head):
-    // n_q tokens of a group of G heads fit when n_q * G <= 8 and the K/V is
-    // read once for all of them; more tokens run as consecutive passes of
-    // 8 / G tokens each, every pass reading the K/V again.
-    const int per_pass = s.nq * c.group <= 8 ? s.nq : 8 / c.group;
+    // One launch pair serves up to 32 query rows per (sequence, kv head)
+    // (the warps hold 1, 2 or 4 tiles of the MMA's 8 columns): n_q tokens of
+    // a group of G heads fit when n_q * G <= 32, and the K/V is read once for
+    // all of them; more tokens run as consecutive passes of 32 / G tokens,
+    // every pass reading the K/V again.
     for (int t0 = 0; t0 < s.nq; t0 += per_pass) {
       c.q_first = t0;
       c.n_q = s.nq - t0 < per_pass ? s.nq - t0 : per_pass;
+      c.rows = decode_rows(c.n_q * group);
+      decode_workspace_split(c, ws);
       if (cudaError_t e = launch_decode(c, fp8, bf16, static_cast<cudaStream_t>(stream)))
         return cuda_status(e);
     }
@@ -302,9 +313,16 @@ int pa_e4m3_encode(const float* x, uint8_t* codes, int64_t n, void* stream) {
 }
 
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_dim, int split_ctas) {
-  if (split_ctas < 0) return 0;
+  return pa_decode_workspace_size_rows(num_seqs, num_q_heads, head_dim, split_ctas, 8);
+}
+
+size_t pa_decode_workspace_size_rows(int num_seqs, int num_q_heads, int head_dim, int split_ctas,
+                                     int query_rows) {
+  if (split_ctas < 0 || query_rows <= 0) return 0;
   if (split_ctas == 0) split_ctas = decode_max_default_ctas();
-  return decode_workspace_bytes(num_seqs, num_q_heads, head_dim, split_ctas);
+  // the widest pass: at most kMaxRowsPerLaunch rows
+  const int rows = query_rows < kMaxRowsPerLaunch ? query_rows : kMaxRowsPerLaunch;
+  return decode_workspace_bytes(num_seqs, num_q_heads, head_dim, split_ctas, rows);
 }
 
 int pa_decode_default_splits(int pool_type) {
@@ -449,7 +467,7 @@ int pa_test_merge_timeout(void* out, const int32_t* context_lens, int max_contex
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (!aligned(out, 16) || !aligned(context_lens, 4) || !aligned(workspace, 256))
     return PA_ERR_INVALID_ARG;
-  if (workspace_bytes < decode_workspace_bytes(num_seqs, num_q_heads, head_dim, split_ctas))
+  if (workspace_bytes < decode_workspace_bytes(num_seqs, num_q_heads, head_dim, split_ctas, 8))
     return PA_ERR_WORKSPACE;
   DeviceState* dev = nullptr;
   if (int rc = device_state(&dev)) return rc;
@@ -467,6 +485,7 @@ int pa_test_merge_timeout(void* out, const int32_t* context_lens, int max_contex
   a.split_ctas = split_ctas;
   a.n_q = 1;
   a.q_tokens = 1;
+  a.rows = 8;
   a.wait_limit_ns = limit_ns;
   decode_workspace_split(a, workspace);
   return cuda_status(launch_merge_only(a, dtype == PA_BF16, static_cast<cudaStream_t>(stream)));

@@ -95,7 +95,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   unsigned* status = nullptr;
   if (int rc = device_status_word(&status)) return rc;
   const int splits = split_ctas == 0 ? decode_default_ctas(false) : split_ctas;
-  const size_t need = decode_workspace_bytes(num_seqs, num_q_heads, head_dim, splits);
+  const size_t need = decode_workspace_bytes(num_seqs, num_q_heads, head_dim, splits, 8);
   if (need == 0 || need > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_SCRATCH_LIMIT;
 
   DecodeArgs a{};
@@ -114,6 +114,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   a.n_q = queries_per_seq;
   a.q_tokens = queries_per_seq;
   a.q_first = 0;
+  a.rows = 8;
   a.early = (flags & PA_DECODE_EARLY_PROLOGUE) ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit_ns = kWaitLimitNs;

@@ -36,8 +36,8 @@ struct DecodeArgs {
   const float* v_scale;
   const int32_t* block_tables;  // [B][mbs]
   const int32_t* context_lens;  // [B]
-  float* ws_acc;                // [split_ctas*4][2][8][D] partial sums (unnormalised), and
-  float* ws_ml;                 // [split_ctas*4][2][8][2] partial (max, sum) in log2 units;
+  float* ws_acc;                // [split_ctas*4][2][rows][D] partial sums (unnormalised), and
+  float* ws_ml;                 // [split_ctas*4][2][rows][2] partial (max, sum) in log2 units;
                                 // both bit-inverted, zero when not written
   unsigned* status;             // device status word
   // fused append (pa_decode_step*): this step's new rows and where they go;
@@ -55,7 +55,8 @@ struct DecodeArgs {
   int max_context_len;
   int split_ctas;               // CTAs the batch's blocks are divided among
   int window;                   // sliding window in tokens (0: the whole context)
-  int n_q;                      // query tokens this launch serves (n_q * group <= 8)
+  int n_q;                      // query tokens this launch serves (n_q * group <= rows)
+  int rows;                     // query rows per (sequence, kv head) a launch holds: 8, 16 or 32
   int q_tokens;                 // query tokens per sequence in q and out
   int q_first;                  // the first of them this launch serves
   int early;                    // programmatic dependent launch: prologue before griddepcontrol.wait
@@ -63,13 +64,26 @@ struct DecodeArgs {
   uint64_t wait_limit_ns;       // time limit of every wait (kWaitLimitNs unless a test shortens it)
 };
 
-int decode_default_ctas(bool fp8);   // CTAs a default launch uses for this pool type
+// Largest query rows per (sequence, kv head) one launch serves: four tiles of
+// the MMA's 8 columns.
+constexpr int kMaxRowsPerLaunch = 32;
+// CTAs a default launch uses for this pool type and query rows per
+// (sequence, kv head)
+int decode_default_ctas(bool fp8, int rows = 1);
 int decode_max_default_ctas();       // the largest of those over pool types
-size_t decode_workspace_bytes(int B, int Hq, int D, int split_ctas);
-// Points a's workspace fields into ws, for a's sizes (a.split_ctas, a.B, a.D).
+// Rows per piece a launch serving `query_rows` rows holds: 8, 16 or 32.
+int decode_rows(int query_rows);
+// Workspace bytes for launches of up to `rows` query rows per (sequence, kv head).
+size_t decode_workspace_bytes(int B, int Hq, int D, int split_ctas, int rows);
+// Points a's workspace fields into ws, for a's sizes (a.split_ctas, a.D, a.rows).
 void decode_workspace_split(DecodeArgs& a, void* ws);
 
 cudaError_t launch_decode(const DecodeArgs& a, bool fp8, bool bf16, cudaStream_t s);
+// The launches with two and four tiles of query columns per warp (a.rows 16
+// and 32), each in a translation unit of its own.
+cudaError_t launch_decode_tiles2(const DecodeArgs& a, bool fp8, bool bf16, cudaStream_t s);
+cudaError_t launch_decode_tiles4_16bit(const DecodeArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_decode_tiles4_e4m3(const DecodeArgs& a, bool bf16, cudaStream_t s);
 // The merge launch alone (no attention launch writes its partials): the
 // failure-path test of its bounded poll.
 cudaError_t launch_merge_only(const DecodeArgs& a, bool bf16, cudaStream_t s);

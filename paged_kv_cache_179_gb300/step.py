@@ -22,7 +22,7 @@ class DecodeStep:
 
     def __init__(self, *, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
                  num_q_heads, k_scale=None, v_scale=None, split_ctas=0, window=0,
-                 early_prologue=False):
+                 early_prologue=False, queries_per_seq=1):
         self.kv = "fp8" if k_cache.dtype == torch.uint8 else "16"
         self.k_cache, self.v_cache = k_cache, v_cache
         self.k_scale, self.v_scale = k_scale, v_scale
@@ -32,13 +32,18 @@ class DecodeStep:
         self.B = int(block_tables.shape[0])
         self.Hq = int(num_q_heads)
         self.NB, self.Hkv, self.bs, self.D = (int(x) for x in k_cache.shape)
-        self.split_ctas = int(split_ctas) or _abi.pa_decode_default_splits(k_cache.dtype)
+        # query rows per (sequence, kv head) of a decode call: its query tokens
+        # (queries_per_seq; the fused step takes one) times the query group
+        rows = int(queries_per_seq) * (self.Hq // self.Hkv)
+        # more than 8 query rows: two CTAs per SM for every pool type
+        self.split_ctas = int(split_ctas) or _abi.pa_decode_default_splits(
+            k_cache.dtype if rows <= 8 else torch.float16)
         self.window = int(window)           # sliding window in tokens, 0 for the whole context
         # the attention launch's prologue may overlap the kernel before it on
         # the stream (which must then not write context_lens or block_tables)
         self.early_prologue = bool(early_prologue)
         self.workspace = _abi.alloc_workspace(self.B, self.Hq, self.D, self.split_ctas,
-                                              k_cache.device)
+                                              k_cache.device, query_rows=rows)
         self._bound = {}     # run_from_staging's bound steps
 
     def append(self, k_new, v_new, slot_mapping):

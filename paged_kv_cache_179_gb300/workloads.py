@@ -19,6 +19,7 @@ qwen2_5_7b         128   28/4      128   f16    lognormal(median 1024, sigma 1)
                                                 clipped to [1,8192]
 qwen2_5_7b_fp8     256   28/4      128   fp8    U[4096,32768]; K/V drawn fp16,
                                                 then quantised to E4M3 per page
+mqa_32x1           128   32/1      128   f16    as qwen2_5_7b (multi-query)
 =================  ====  ========  ====  =====  ==============================
 
 Generation order is fixed: context lengths, block tables, Q, the K/V pool,
@@ -49,6 +50,10 @@ CONFIGS = {
                        median=1024, sigma=1.0, lo=1, hi=8192),
     "qwen2_5_7b_fp8": dict(B=256, Hq=28, Hkv=4, D=128, dtype="f16", kv="fp8", lens="uniform",
                            lo=4096, hi=32768),
+    # multi-query attention: one kv head serves all 32 q heads (the pages'
+    # "GQA/MQA"), with the Qwen2.5-7B batch's lengths
+    "mqa_32x1": dict(B=128, Hq=32, Hkv=1, D=128, dtype="f16", kv="f16", lens="lognormal",
+                     median=1024, sigma=1.0, lo=1, hi=8192),
 }
 
 TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16}

@@ -31,7 +31,7 @@ def header_functions():
 
 def test_header_and_binding_agree():
     names = header_functions()
-    assert len(names) == 17
+    assert len(names) == 18
     assert sorted(_abi.SIGNATURES) == names
 
 
@@ -68,7 +68,8 @@ def test_decode_argument_errors(lib):
     assert _decode(lib, q=MISALIGNED) == _abi.PA_ERR_INVALID_ARG
     assert _decode(lib, D=96) == _abi.PA_ERR_UNSUPPORTED
     assert _decode(lib, bs=32, mbs=4) == _abi.PA_ERR_UNSUPPORTED
-    assert _decode(lib, Hq=18, Hkv=2) == _abi.PA_ERR_UNSUPPORTED    # group of 9
+    assert _decode(lib, Hq=66, Hkv=2) == _abi.PA_ERR_UNSUPPORTED    # group of 33
+    assert _decode(lib, Hq=32, Hkv=1, ws_bytes=16) == _abi.PA_ERR_WORKSPACE   # 32 rows: larger
     assert _decode(lib, ws=None) == _abi.PA_ERR_WORKSPACE
     assert _decode(lib, ws_bytes=16) == _abi.PA_ERR_WORKSPACE
     assert _decode(lib, ws=FAKE + 16) == _abi.PA_ERR_WORKSPACE      # not 256-aligned
@@ -86,6 +87,13 @@ def test_workspace_size_formula(lib):
     assert n == up(acc) + up(ml)
     assert lib.pa_decode_workspace_size(2, 8, 64, 1) > 0        # one CTA's 4 warps still split
     assert lib.pa_decode_workspace_size(2, 8, 64, -1) == 0      # invalid
+    # launches holding 16 or 32 query rows per (sequence, kv head)
+    f = lib.pa_decode_workspace_size_rows
+    assert f(2, 8, 64, 10, 8) == n
+    for qr, rows_per_piece in ((1, 8), (9, 16), (16, 16), (17, 32), (32, 32), (200, 32)):
+        r = 10 * 4 * 2 * rows_per_piece
+        assert f(2, 8, 64, 10, qr) == up(r * 64 * 4) + up(r * 2 * 4), qr
+    assert f(2, 8, 64, 10, 0) == 0
     # the size does not grow with the batch (launches of 512 sequences share it)
     assert lib.pa_decode_workspace_size(5000, 8, 64, 10) == \
         lib.pa_decode_workspace_size(2, 8, 64, 10)

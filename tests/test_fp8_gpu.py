@@ -174,8 +174,10 @@ def test_decode_fp8_small_matches_oracle(seed, B, Hq, Hkv, D, max_len, splits, d
 def test_fp8_full_batch_sampled_rows():
     """The 256-sequence E4M3 batch at full size, in the benchmark's launch
     configuration: quantise on the GPU (checked bit-exact on the sampled
-    sequences' pages), append + decode, and compare sampled sequences with the
-    oracle run from the fp16 source of those pages."""
+    sequences' pages), append + decode, and compare 32 sampled sequences --
+    the 8 longest (32k-token contexts split across many warps), the 8
+    shortest and 16 drawn at random -- with the oracle run from the fp16
+    source of those pages."""
     w = W.make_workload("qwen2_5_7b_fp8", seed=0, device="cuda")
     lens = w.context_lens.cpu().numpy()
     kc, vc, ks, vs = _quantized_on_gpu(w)
@@ -183,8 +185,11 @@ def test_fp8_full_batch_sampled_rows():
     out = torch.empty_like(w.q)
     step(w.q, w.k_new, w.v_new, w.slot_mapping, out)
     assert _abi.pa_get_status() == (0, 0)
-    order = np.argsort(lens)
-    rows = sorted({int(order[0]), int(order[-1]), 7, 100, 201})
+    order = np.argsort(lens, kind="stable")
+    rest = order[8:-8]
+    picked = np.random.default_rng(5).choice(rest, size=16, replace=False)
+    rows = sorted({int(x) for x in np.concatenate([order[:8], order[-8:], picked])})
+    assert len(rows) == 32
     tables = w.block_tables.cpu().numpy()
     sub_t, sub_l, (kp, vp) = W.extract_rows(tables, lens, rows, [w.k_cache, w.v_cache])
     # oracle side: quantise the fp16 source pages, then append the new tokens
@@ -211,3 +216,20 @@ def test_fp8_full_batch_sampled_rows():
     ref = oracle.decode_fp8(to_np16(w.q[rows]), kc_o, vc_o, ks_o, vs_o, sub_t, sub_l, w.scale)
     err = np.abs(out[rows].float().cpu().numpy() - ref).max()
     assert err <= TOL["fp8"], err
+
+
+def test_fp8_full_pool_quantiser_bit_exact():
+    """pa_quantize_fp8 over the whole E4M3 batch's pools (about 325k pages of
+    each of K and V), compared code for code and scale for scale with the
+    oracle's quantiser, in chunks of 32768 pages."""
+    w = W.make_workload("qwen2_5_7b_fp8", seed=1, device="cuda")
+    kc, vc, ks, vs = _quantized_on_gpu(w)
+    assert _abi.pa_get_status() == (0, 0)
+    chunk = 32768
+    for src, codes, scales in ((w.k_cache, kc, ks), (w.v_cache, vc, vs)):
+        for p0 in range(0, w.num_blocks, chunk):
+            p1 = min(w.num_blocks, p0 + chunk)
+            c_o, s_o = oracle.quantize_fp8(to_np16(src[p0:p1]))
+            assert np.array_equal(codes[p0:p1].cpu().numpy(), c_o), p0
+            assert np.array_equal(scales[p0:p1].cpu().numpy().view(np.uint32),
+                                  s_o.view(np.uint32)), p0

@@ -76,16 +76,18 @@ def test_multiquery_fp8_matches_oracle(nq, window, splits):
 
 
 @pytest.mark.parametrize("seed,nq,Hq,Hkv,window,splits", [
-    (10, 3, 28, 4, 0, 0),      # group 7: three passes of one token
-    (11, 5, 16, 4, 0, 9),      # group 4: passes of 2, 2 and 1 tokens
-    (12, 4, 28, 4, 50, 0)])    # with a sliding window
-def test_multiquery_beyond_eight_rows_runs_in_passes(seed, nq, Hq, Hkv, window, splits):
+    (10, 3, 28, 4, 0, 0),      # group 7: 21 rows, one pass of four column tiles
+    (11, 5, 16, 4, 0, 9),      # group 4: 20 rows, one pass
+    (12, 4, 28, 4, 50, 0),     # 28 rows with a sliding window
+    (13, 6, 28, 4, 0, 0),      # 42 rows: passes of 4 and 2 tokens
+    (14, 9, 16, 4, 30, 5)])    # 36 rows: passes of 8 and 1 tokens, windowed
+def test_multiquery_beyond_eight_rows(seed, nq, Hq, Hkv, window, splits):
     q, kp, vp, tables, lens = _case(seed, 5, nq, Hq, Hkv, 128, 600, torch.float16, True)
     scale = float(np.float32(1 / math.sqrt(128)))
     ref = oracle.decode(to_np16(q), to_np16(kp), to_np16(vp), tables.numpy(), lens.numpy(), scale,
                         window=window)
     out = torch.full_like(q, float("nan"), device="cuda")
-    ws = _abi.alloc_workspace(5, Hq, 128, splits, "cuda")
+    ws = _abi.alloc_workspace(5, Hq, 128, splits, "cuda", query_rows=nq * (Hq // Hkv))
     _abi.pa_decode(out, q.cuda(), kp.cuda(), vp.cuda(), tables.cuda(), lens.cuda(),
                    int(lens.max()), scale, splits, ws, window=window)
     assert _abi.pa_get_status() == (0, 0)

@@ -297,7 +297,9 @@ def _random_case(rng, B, Hq, Hkv, D, max_len, bf16=False, NB=None):
 
 @pytest.mark.parametrize("B,Hq,Hkv,D,bf16", [
     (3, 8, 2, 64, False), (2, 7, 1, 128, False), (4, 15, 5, 64, True), (2, 28, 4, 128, False),
-    (2, 12, 2, 128, False), (2, 4, 4, 64, True)])
+    (2, 12, 2, 128, False), (2, 4, 4, 64, True),
+    # multi-query and groups above 8 (one kv head for 16 or 32 q heads; groups of 12 and 20)
+    (2, 16, 1, 128, False), (2, 32, 1, 64, True), (3, 24, 2, 128, False), (2, 40, 2, 64, False)])
 def test_decode_matches_dense_softmax(B, Hq, Hkv, D, bf16):
     rng = np.random.default_rng(B * 100 + Hq)
     q, kp, vp, tables, lens = _random_case(rng, B, Hq, Hkv, D, 300, bf16)

@@ -93,8 +93,8 @@ def test_window_fused_step_appends_and_attends():
 
 def test_window_full_batch_sampled_rows():
     """The Qwen2.5-7B batch with a 1024-token window, the benchmark's launch
-    configuration; sampled sequences (shortest, longest and three others)
-    against the oracle on the blocks they read."""
+    configuration; 32 sampled sequences (the 8 shortest, the 8 longest and
+    16 drawn at random) against the oracle on the blocks they read."""
     w = W.make_workload("qwen2_5_7b", seed=0, device="cuda")
     window = 1024
     step = DecodeStep(k_cache=w.k_cache, v_cache=w.v_cache, block_tables=w.block_tables,
@@ -104,8 +104,10 @@ def test_window_full_batch_sampled_rows():
     step(w.q, w.k_new, w.v_new, w.slot_mapping, out)
     assert _abi.pa_get_status() == (0, 0)
     lens = w.context_lens.cpu().numpy()
-    order = np.argsort(lens)
-    rows = sorted({int(order[0]), int(order[-1]), 5, 64, 120})
+    order = np.argsort(lens, kind="stable")
+    picked = np.random.default_rng(6).choice(order[8:-8], size=16, replace=False)
+    rows = sorted({int(x) for x in np.concatenate([order[:8], order[-8:], picked])})
+    assert len(rows) == 32
     sub_t, sub_l, (kp, vp) = W.extract_rows(w.block_tables.cpu().numpy(), lens, rows,
                                             [w.k_cache, w.v_cache])
     ref = oracle.decode(to_np16(w.q[rows]), kp, vp, sub_t, sub_l, w.scale, window=window)

@@ -9,7 +9,8 @@ import torch
 from paged_kv_cache_179_gb300 import workloads as W
 
 
-@pytest.mark.parametrize("name", ["tiny", "smollm2_360m", "qwen2_5_1_5b", "qwen2_5_7b"])
+@pytest.mark.parametrize("name", ["tiny", "smollm2_360m", "qwen2_5_1_5b", "qwen2_5_7b",
+                                  "mqa_32x1"])
 def test_shapes_tables_and_slots(name):
     w = W.make_workload(name, seed=0)
     cfg = W.CONFIGS[name]
