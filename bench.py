@@ -489,10 +489,15 @@ def measure_e2e(args, run, dev):
                           split_ctas=args.splits, window=run.window,
                           early_prologue=run.early)
     h2d = d2h = 0
+    host_us = None
     if run.back_to_back:
+        pipe = StepPipeline(make_step, specs, out.shape, out.dtype, dev, depth=max(2, copies),
+                            handshake=args.handshake)
         mode = ("pipelined: uploads and read-backs on two copy streams, overlapping the "
-                f"steps ({max(2, copies)} slots)")
-        pipe = StepPipeline(make_step, specs, out.shape, out.dtype, dev, depth=max(2, copies))
+                f"steps ({max(2, copies)} slots), ordered by "
+                + ("a device-side handshake (the attention launch waits for its upload's word, "
+                   "the read-back for the step's done word; only kernels on the compute stream)"
+                   if pipe.uses_device_handshake(fused) else "stream events"))
         for st_ in pipe.stagings:
             for k in names:
                 st_.host[k].copy_(getattr(w, k).cpu())
@@ -502,8 +507,10 @@ def measure_e2e(args, run, dev):
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        t_host = time.perf_counter()
         for i in range(K):
             _, h2d, d2h = pipe.submit(fused=fused)
+        host_us = (time.perf_counter() - t_host) / K * 1e6
         pipe.finish()
         e1.record(stream)
         ev = [(e0, e1)]
@@ -524,6 +531,8 @@ def measure_e2e(args, run, dev):
             h2d, d2h = e2e_step.run_from_staging(staging, host_out, out, fused=fused)
             ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
+    if host_us is not None:
+        mode += f"; the host issues a step in {host_us:.1f} us"
     return sum(a.elapsed_time(b) for a, b in ev), h2d, d2h, mode
 
 
@@ -835,7 +844,8 @@ def describe(w, tokens):
 def kernel_sha() -> str:
     import hashlib
     h = hashlib.sha256()
-    for p in ("paged_kv_cache_179_gb300/csrc/decode.cu", "paged_kv_cache_179_gb300/csrc/pa_ptx.cuh",
+    for p in ("paged_kv_cache_179_gb300/csrc/decode_kernels.cuh",
+              "paged_kv_cache_179_gb300/csrc/decode.cu", "paged_kv_cache_179_gb300/csrc/pa_ptx.cuh",
               "paged_kv_cache_179_gb300/csrc/pa_launch.h", "paged_kv_cache_179_gb300/csrc/pa_e4m3.cuh"):
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
@@ -951,6 +961,10 @@ def main(argv=None):
                     help="all: the default single-GPU run also times the other four configs "
                          "(tiny, SmolLM2-360M, Qwen2.5-1.5B, E4M3 Qwen2.5-7B) one after another "
                          "and reports them under 'configs'")
+    ap.add_argument("--handshake", choices=["auto", "device", "events"], default="auto",
+                    help="how the pipelined end-to-end steps order their copies: a device-side "
+                         "handshake (auto: when the driver offers stream memory operations) or "
+                         "stream events")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-step-s", type=float, default=2.0)

@@ -332,6 +332,74 @@ int pa_decode_step_fp8(void *out, const void *q, const void *k_new, const void *
                        void *stream);
 
 /*
+ * Device-side ordering of a decode step against copies made on other
+ * streams, for serving loops that upload each step's inputs (q, new rows,
+ * slots, block tables, context lengths) and read its output back while the
+ * previous step still runs.  Ordering those copies with stream events puts
+ * waits and records between the kernels of consecutive steps on the compute
+ * stream, which keeps the next step's launch from overlapping the end of
+ * the previous one (PA_DECODE_EARLY_PROLOGUE); with this handshake the
+ * compute stream holds nothing but the steps' kernels:
+ *   - the copy stream uploads the step's inputs, then writes ready_value to
+ *     *ready with pa_stream_write_value (ordered after the upload);
+ *   - the step's attention launch waits, bounded by 2 s, until
+ *     (int32_t)(*ready - ready_value) >= 0 before it reads any input; a CTA
+ *     that gives up sets PA_STATUS_TIMEOUT and returns;
+ *   - once its output is complete, the step stores done_value to *done
+ *     (the merge launch's CTAs count themselves on *done_count, which must
+ *     be zero before the first step that uses it and is zero again after
+ *     each); a step that hit a timeout still stores it, so a stream waiting
+ *     on *done never waits forever (its pa_get_status shows the failure);
+ *   - the read-back stream waits with pa_stream_wait_value(..., done,
+ *     done_value) and copies the output; an upload that reuses the step's
+ *     input buffers waits on *done likewise.
+ * ready, done and done_count are device words, 4-byte aligned, owned by the
+ * caller; give each in-flight step its own (a ring of slots), with values
+ * that grow from step to step.
+ * No counterpart in the pages: host-device plumbing of a serving loop.
+ */
+typedef struct pa_step_sync {
+    const uint32_t *ready;
+    uint32_t *done;
+    uint32_t *done_count;
+    uint32_t ready_value;
+    uint32_t done_value;
+} pa_step_sync;
+
+/* pa_decode_step / pa_decode_step_fp8 with the handshake above (sync must
+ * not be NULL).  Results are those of the plain calls. */
+int pa_decode_step_synced(void *out, const void *q, const void *k_new, const void *v_new,
+                          void *k_cache, void *v_cache, const int64_t *slot_mapping,
+                          const int32_t *block_tables, int max_blocks_per_seq,
+                          const int32_t *context_lens, int max_context_len, int num_seqs,
+                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                          int num_blocks, float scale, int window_size, int dtype,
+                          int split_ctas, void *workspace, size_t workspace_bytes,
+                          unsigned flags, const pa_step_sync *sync, void *stream);
+int pa_decode_step_fp8_synced(void *out, const void *q, const void *k_new, const void *v_new,
+                              uint8_t *k_cache, uint8_t *v_cache, float *k_scale,
+                              float *v_scale, const int64_t *slot_mapping,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, int max_context_len, int num_seqs,
+                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                              int num_blocks, float scale, int window_size, int dtype,
+                              int split_ctas, void *workspace, size_t workspace_bytes,
+                              unsigned flags, const pa_step_sync *sync, void *stream);
+
+/*
+ * Stream-ordered 32-bit device-word operations (the driver's stream memory
+ * operations): pa_stream_write_value stores value to *addr once the work
+ * before it on stream has completed (its writes visible first);
+ * pa_stream_wait_value holds the work after it on stream until
+ * (int32_t)(*addr - value) >= 0.  addr is a 4-byte aligned device pointer.
+ * PA_ERR_UNSUPPORTED when the driver or device does not offer them.  Such a
+ * wait has no time limit of its own: wait only on words a step of this
+ * library (or the caller) is certain to write.
+ */
+int pa_stream_write_value(void *stream, uint32_t *addr, uint32_t value);
+int pa_stream_wait_value(void *stream, const uint32_t *addr, uint32_t value);
+
+/*
  * pa_decode without a caller-provided workspace, for callers that cannot
  * allocate device memory: code inside a host framework that owns all device
  * memory and forbids raw allocations, latency-critical loops where

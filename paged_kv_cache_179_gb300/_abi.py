@@ -51,6 +51,14 @@ SIGNATURES = {
                             _vp], _i32),
     "pa_decode_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                            _i32, _i32, _f32, _i32, _i32, _i32, _i32, _u32, _vp], _i32),
+    "pa_decode_step_synced": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32,
+                               _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _i32, _vp, _sz,
+                               _u32, _vp, _vp], _i32),
+    "pa_decode_step_fp8_synced": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp,
+                                   _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32,
+                                   _i32, _vp, _sz, _u32, _vp, _vp], _i32),
+    "pa_stream_write_value": ([_vp, _vp, _u32], _i32),
+    "pa_stream_wait_value": ([_vp, _vp, _u32], _i32),
     "pa_get_status": ([_vp, ctypes.POINTER(ctypes.c_uint)], _i32),
     "pa_test_wait_timeout": ([ctypes.c_uint64, _vp], _i32),
     "pa_test_merge_timeout": ([_vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz,
@@ -382,6 +390,37 @@ def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, cont
           _ptr(workspace), ws_bytes, _flags(early_prologue), _stream(dev))
 
 
+class StepSync(ctypes.Structure):
+    """pa_step_sync: the device words and values of one step's handshake with
+    the copies on other streams (see include/pa.h).  The entry points read
+    the values when they are called, so a bound call sees updated values."""
+    _fields_ = [("ready", ctypes.c_void_p), ("done", ctypes.c_void_p),
+                ("done_count", ctypes.c_void_p), ("ready_value", ctypes.c_uint32),
+                ("done_value", ctypes.c_uint32)]
+
+
+def _sync_ptr(sync):
+    return ctypes.c_void_p(ctypes.addressof(sync))
+
+
+def pa_stream_write_value(word, value: int, stream=None) -> None:
+    """Stream-ordered store of ``value`` into the device int32 tensor element
+    ``word`` (a 1-element view) on ``stream`` (default: the current stream)."""
+    _need(word, "word", (torch.int32,), None)
+    s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream(word.device)
+    _call(load().pa_stream_write_value, "pa_stream_write_value", s, _ptr(word),
+          int(value) & 0xffffffff)
+
+
+def pa_stream_wait_value(word, value: int, stream=None) -> None:
+    """Hold ``stream``'s later work until the device word reaches ``value``
+    (cyclic 32-bit comparison)."""
+    _need(word, "word", (torch.int32,), None)
+    s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream(word.device)
+    _call(load().pa_stream_wait_value, "pa_stream_wait_value", s, _ptr(word),
+          int(value) & 0xffffffff)
+
+
 def _ws_bytes(workspace, dev):
     if workspace is None:
         return 0
@@ -391,8 +430,10 @@ def _ws_bytes(workspace, dev):
 
 def pa_decode_step(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_tables,
                    context_lens, max_context_len: int, scale: float, split_ctas: int = 0,
-                   workspace=None, *, window: int = 0, early_prologue: bool = False) -> None:
-    """Append k_new/v_new at slot_mapping, then decode, in one launch (16-bit pools)."""
+                   workspace=None, *, window: int = 0, early_prologue: bool = False,
+                   sync: StepSync = None) -> None:
+    """Append k_new/v_new at slot_mapping, then decode, in one launch (16-bit
+    pools); with ``sync``, pa_decode_step_synced (device-side handshake)."""
     dev = q.device
     act = (torch.float16, torch.bfloat16)
     _need(q, "q", act, 3, dev)
@@ -408,18 +449,22 @@ def pa_decode_step(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_t
     NB, Hkv, bs, _ = k_cache.shape
     if k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape or slot_mapping.shape[0] != B:
         raise ValueError("shape mismatch")
-    _call(load().pa_decode_step, "pa_decode_step",
-          _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-          _ptr(slot_mapping), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
-          int(max_context_len), B, Hq, Hkv, D, bs, NB, float(scale), int(window),
-          _act_code(q.dtype), int(split_ctas), _ptr(workspace), _ws_bytes(workspace, dev),
-          _flags(early_prologue), _stream(dev))
+    args = (_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+            _ptr(slot_mapping), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+            int(max_context_len), B, Hq, Hkv, D, bs, NB, float(scale), int(window),
+            _act_code(q.dtype), int(split_ctas), _ptr(workspace), _ws_bytes(workspace, dev),
+            _flags(early_prologue))
+    if sync is None:
+        _call(load().pa_decode_step, "pa_decode_step", *args, _stream(dev))
+    else:
+        _call(load().pa_decode_step_synced, "pa_decode_step_synced", *args, _sync_ptr(sync),
+              _stream(dev))
 
 
 def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping,
                        block_tables, context_lens, max_context_len: int, scale: float,
                        split_ctas: int = 0, workspace=None, *, window: int = 0,
-                       early_prologue: bool = False) -> None:
+                       early_prologue: bool = False, sync: StepSync = None) -> None:
     """Append (E4M3-encode) k_new/v_new, then decode over the E4M3 pools, in one
     attention launch; q, k_new, v_new and out share one dtype (fp16 or bf16)."""
     dev = q.device
@@ -437,12 +482,16 @@ def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
     NB, Hkv, bs, _ = k_cache.shape
     if k_new.shape != (B, Hkv, D) or v_new.shape != k_new.shape or slot_mapping.shape[0] != B:
         raise ValueError("shape mismatch")
-    _call(load().pa_decode_step_fp8, "pa_decode_step_fp8",
-          _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-          _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), _ptr(block_tables),
-          block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
-          float(scale), int(window), _act_code(q.dtype), int(split_ctas), _ptr(workspace),
-          _ws_bytes(workspace, dev), _flags(early_prologue), _stream(dev))
+    args = (_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+            _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), _ptr(block_tables),
+            block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
+            float(scale), int(window), _act_code(q.dtype), int(split_ctas), _ptr(workspace),
+            _ws_bytes(workspace, dev), _flags(early_prologue))
+    if sync is None:
+        _call(load().pa_decode_step_fp8, "pa_decode_step_fp8", *args, _stream(dev))
+    else:
+        _call(load().pa_decode_step_fp8_synced, "pa_decode_step_fp8_synced", *args,
+              _sync_ptr(sync), _stream(dev))
 
 
 def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,

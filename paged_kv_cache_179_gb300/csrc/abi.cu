@@ -10,6 +10,8 @@
 #include <cmath>
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 #include "pa.h"
 #include "pa_launch.h"
 
@@ -92,7 +94,7 @@ int tokens_per_pass(int nq, int group) {
 int run_decode(DecodeShape s, void* out, const void* q, const void* k, const void* v,
                const float* ks, const float* vs, const int32_t* bt, const int32_t* cl,
                float scale, bool fp8, bool bf16, void* ws, size_t ws_bytes, void* stream,
-               const AppendArgs& ap = AppendArgs()) {
+               const AppendArgs& ap = AppendArgs(), const pa_step_sync* sync = nullptr) {
   if (s.B == 0) return PA_OK;
   const int group = s.Hq / s.Hkv;
   const int per_pass = tokens_per_pass(s.nq, group);
@@ -159,11 +161,53 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
       c.n_q = s.nq - t0 < per_pass ? s.nq - t0 : per_pass;
       c.rows = decode_rows(c.n_q * group);
       decode_workspace_split(c, ws);
+      // device-side handshake: the first attention launch waits for the
+      // upload, the last merge launch signals the call done
+      const bool first = b0 == 0 && t0 == 0;
+      const bool last = b0 + kMaxBatchPerLaunch >= s.B && t0 + per_pass >= s.nq;
+      c.ready = sync != nullptr && first ? sync->ready : nullptr;
+      c.ready_value = sync != nullptr ? sync->ready_value : 0u;
+      c.done = sync != nullptr && last ? sync->done : nullptr;
+      c.done_count = sync != nullptr && last ? sync->done_count : nullptr;
+      c.done_value = sync != nullptr ? sync->done_value : 0u;
       if (cudaError_t e = launch_decode(c, fp8, bf16, static_cast<cudaStream_t>(stream)))
         return cuda_status(e);
     }
   }
   return PA_OK;
+}
+
+bool sync_ok(const pa_step_sync* sync) {
+  if (sync == nullptr) return true;
+  return sync->ready != nullptr && sync->done != nullptr && sync->done_count != nullptr &&
+         aligned(sync->ready, 4) && aligned(sync->done, 4) && aligned(sync->done_count, 4);
+}
+
+// cuStreamWriteValue32 / cuStreamWaitValue32, from the driver (no link against libcuda).
+struct StreamMemOps {
+  PFN_cuStreamWriteValue32_v11070 write = nullptr;
+  PFN_cuStreamWaitValue32_v11070 wait = nullptr;
+};
+const StreamMemOps& stream_mem_ops() {
+  static const StreamMemOps ops = [] {
+    StreamMemOps o;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &f, 11070, cudaEnableDefault,
+                                         &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      o.write = reinterpret_cast<PFN_cuStreamWriteValue32_v11070>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &f, 11070, cudaEnableDefault,
+                                         &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      o.wait = reinterpret_cast<PFN_cuStreamWaitValue32_v11070>(f);
+    return o;
+  }();
+  return ops;
+}
+
+int cu_status(CUresult r) {
+  if (r == CUDA_SUCCESS) return PA_OK;
+  return r == CUDA_ERROR_NOT_SUPPORTED ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA;
 }
 
 }  // namespace
@@ -379,18 +423,28 @@ int pa_decode_fp8(void* out, const void* q, const uint8_t* k_cache, const uint8_
                     scale, true, dtype == PA_BF16, workspace, workspace_bytes, stream);
 }
 
-int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_new,
-                   void* k_cache, void* v_cache, const int64_t* slot_mapping,
-                   const int32_t* block_tables, int max_blocks_per_seq,
-                   const int32_t* context_lens, int max_context_len, int num_seqs,
-                   int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+}  // extern "C"
+
+namespace {
+
+int decode_step_16(void* out, const void* q, const void* k_new, const void* v_new, void* k_cache,
+                   void* v_cache, const int64_t* slot_mapping, const int32_t* block_tables,
+                   int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
+                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                    int num_blocks, float scale, int window_size, int dtype, int split_ctas,
-                   void* workspace, size_t workspace_bytes, unsigned flags, void* stream) {
-  if (num_seqs == 0) return PA_OK;
+                   void* workspace, size_t workspace_bytes, unsigned flags,
+                   const pa_step_sync* sync, void* stream) {
+  if (num_seqs == 0) {   // nothing to attend; a handshake still gets its done signal
+    if (sync == nullptr) return PA_OK;
+    if (!sync_ok(sync)) return PA_ERR_INVALID_ARG;
+    return cuda_status(launch_signal_done(sync->done, sync->done_value,
+                                          static_cast<cudaStream_t>(stream)));
+  }
   if (!out || !q || !k_new || !v_new || !k_cache || !v_cache || !slot_mapping ||
       !block_tables || !context_lens)
     return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+  if (!sync_ok(sync)) return PA_ERR_INVALID_ARG;
   DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                 num_blocks, max_blocks_per_seq, max_context_len, split_ctas, window_size};
   s.flags = flags;
@@ -407,22 +461,28 @@ int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_ne
   ap.k_pool = k_cache;
   ap.v_pool = v_cache;
   return run_decode(s, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens,
-                    scale, false, dtype == PA_BF16, workspace, workspace_bytes, stream, ap);
+                    scale, false, dtype == PA_BF16, workspace, workspace_bytes, stream, ap, sync);
 }
 
-int pa_decode_step_fp8(void* out, const void* q, const void* k_new, const void* v_new,
-                       uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
-                       const int64_t* slot_mapping, const int32_t* block_tables,
-                       int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
-                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                       int block_size, int num_blocks, float scale, int window_size, int dtype,
-                       int split_ctas, void* workspace, size_t workspace_bytes, unsigned flags,
-                       void* stream) {
-  if (num_seqs == 0) return PA_OK;
+int decode_step_e4m3(void* out, const void* q, const void* k_new, const void* v_new,
+                     uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
+                     const int64_t* slot_mapping, const int32_t* block_tables,
+                     int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
+                     int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                     int block_size, int num_blocks, float scale, int window_size, int dtype,
+                     int split_ctas, void* workspace, size_t workspace_bytes, unsigned flags,
+                     const pa_step_sync* sync, void* stream) {
+  if (num_seqs == 0) {   // nothing to attend; a handshake still gets its done signal
+    if (sync == nullptr) return PA_OK;
+    if (!sync_ok(sync)) return PA_ERR_INVALID_ARG;
+    return cuda_status(launch_signal_done(sync->done, sync->done_value,
+                                          static_cast<cudaStream_t>(stream)));
+  }
   if (!out || !q || !k_new || !v_new || !k_cache || !v_cache || !k_scale || !v_scale ||
       !slot_mapping || !block_tables || !context_lens)
     return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+  if (!sync_ok(sync)) return PA_ERR_INVALID_ARG;
   DecodeShape s{num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                 num_blocks, max_blocks_per_seq, max_context_len, split_ctas, window_size};
   s.flags = flags;
@@ -442,7 +502,89 @@ int pa_decode_step_fp8(void* out, const void* q, const void* k_new, const void* 
   ap.k_scale = k_scale;
   ap.v_scale = v_scale;
   return run_decode(s, out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
-                    scale, true, dtype == PA_BF16, workspace, workspace_bytes, stream, ap);
+                    scale, true, dtype == PA_BF16, workspace, workspace_bytes, stream, ap, sync);
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_new,
+                   void* k_cache, void* v_cache, const int64_t* slot_mapping,
+                   const int32_t* block_tables, int max_blocks_per_seq,
+                   const int32_t* context_lens, int max_context_len, int num_seqs,
+                   int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                   int num_blocks, float scale, int window_size, int dtype, int split_ctas,
+                   void* workspace, size_t workspace_bytes, unsigned flags, void* stream) {
+  return decode_step_16(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_tables,
+                        max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                        num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                        window_size, dtype, split_ctas, workspace, workspace_bytes, flags,
+                        nullptr, stream);
+}
+
+int pa_decode_step_synced(void* out, const void* q, const void* k_new, const void* v_new,
+                          void* k_cache, void* v_cache, const int64_t* slot_mapping,
+                          const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* context_lens, int max_context_len, int num_seqs,
+                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                          int num_blocks, float scale, int window_size, int dtype,
+                          int split_ctas, void* workspace, size_t workspace_bytes,
+                          unsigned flags, const pa_step_sync* sync, void* stream) {
+  if (sync == nullptr) return PA_ERR_INVALID_ARG;
+  return decode_step_16(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_tables,
+                        max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                        num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                        window_size, dtype, split_ctas, workspace, workspace_bytes, flags, sync,
+                        stream);
+}
+
+int pa_decode_step_fp8(void* out, const void* q, const void* k_new, const void* v_new,
+                       uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
+                       const int64_t* slot_mapping, const int32_t* block_tables,
+                       int max_blocks_per_seq, const int32_t* context_lens, int max_context_len,
+                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, int num_blocks, float scale, int window_size, int dtype,
+                       int split_ctas, void* workspace, size_t workspace_bytes, unsigned flags,
+                       void* stream) {
+  return decode_step_e4m3(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                          slot_mapping, block_tables, max_blocks_per_seq, context_lens,
+                          max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                          block_size, num_blocks, scale, window_size, dtype, split_ctas,
+                          workspace, workspace_bytes, flags, nullptr, stream);
+}
+
+int pa_decode_step_fp8_synced(void* out, const void* q, const void* k_new, const void* v_new,
+                              uint8_t* k_cache, uint8_t* v_cache, float* k_scale,
+                              float* v_scale, const int64_t* slot_mapping,
+                              const int32_t* block_tables, int max_blocks_per_seq,
+                              const int32_t* context_lens, int max_context_len, int num_seqs,
+                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                              int num_blocks, float scale, int window_size, int dtype,
+                              int split_ctas, void* workspace, size_t workspace_bytes,
+                              unsigned flags, const pa_step_sync* sync, void* stream) {
+  if (sync == nullptr) return PA_ERR_INVALID_ARG;
+  return decode_step_e4m3(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                          slot_mapping, block_tables, max_blocks_per_seq, context_lens,
+                          max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                          block_size, num_blocks, scale, window_size, dtype, split_ctas,
+                          workspace, workspace_bytes, flags, sync, stream);
+}
+
+int pa_stream_write_value(void* stream, uint32_t* addr, uint32_t value) {
+  if (addr == nullptr || !aligned(addr, 4)) return PA_ERR_INVALID_ARG;
+  const StreamMemOps& ops = stream_mem_ops();
+  if (ops.write == nullptr) return PA_ERR_UNSUPPORTED;
+  return cu_status(ops.write(static_cast<CUstream>(stream), reinterpret_cast<CUdeviceptr>(addr),
+                             value, CU_STREAM_WRITE_VALUE_DEFAULT));
+}
+
+int pa_stream_wait_value(void* stream, const uint32_t* addr, uint32_t value) {
+  if (addr == nullptr || !aligned(addr, 4)) return PA_ERR_INVALID_ARG;
+  const StreamMemOps& ops = stream_mem_ops();
+  if (ops.wait == nullptr) return PA_ERR_UNSUPPORTED;
+  return cu_status(ops.wait(static_cast<CUstream>(stream), reinterpret_cast<CUdeviceptr>(addr),
+                            value, CU_STREAM_WAIT_VALUE_GEQ));
 }
 
 int pa_test_wait_timeout(uint64_t limit_ns, void* stream) {

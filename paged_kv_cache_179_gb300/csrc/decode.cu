@@ -50,8 +50,20 @@ WsLayout ws_layout(int D, int split_ctas, int rows_per_piece) {
 }  // namespace
 
 cudaError_t launch_merge_only(const DecodeArgs& a, bool bf16, cudaStream_t s) {
-  if (a.D == 128) return bf16 ? launch_merge<128, true>(a, s) : launch_merge<128, false>(a, s);
-  return bf16 ? launch_merge<64, true>(a, s) : launch_merge<64, false>(a, s);
+  if (a.rows != 8) return cudaErrorInvalidValue;
+  if (a.D == 128) return bf16 ? launch_merge<128, true, 8>(a, s) : launch_merge<128, false, 8>(a, s);
+  return bf16 ? launch_merge<64, true, 8>(a, s) : launch_merge<64, false, 8>(a, s);
+}
+
+// A step with nothing to attend still signals its handshake's done word.
+__global__ void signal_done_kernel(uint32_t* done, uint32_t value) {
+  __threadfence_system();
+  st_release_sys_b32(done, value);
+}
+
+cudaError_t launch_signal_done(uint32_t* done, uint32_t value, cudaStream_t s) {
+  signal_done_kernel<<<1, 1, 0, s>>>(done, value);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_wait_probe(unsigned* status, uint64_t limit_ns, cudaStream_t s) {

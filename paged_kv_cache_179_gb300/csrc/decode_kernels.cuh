@@ -358,15 +358,16 @@ __device__ __forceinline__ void pv_tiles(WarpAcc<D> (&st)[NT], const uint32_t (&
       const uint32_t x01h = __byte_perm(word(v[0], ehi >> 2), word(v[1], ehi >> 2), sh);
       const uint32_t x23l = __byte_perm(word(v[2], elo >> 2), word(v[3], elo >> 2), sl);
       const uint32_t x23h = __byte_perm(word(v[2], ehi >> 2), word(v[3], ehi >> 2), sh);
+      // (the conversions and MMAs are volatile asm, issued in this order:
+      // with one tile each MMA follows its own four conversions)
       const uint32_t f0 = e4m3x2_to_f16x2(x01l), f1 = e4m3x2_to_f16x2(x01h);
       const uint32_t f2 = e4m3x2_to_f16x2(x23l), f3 = e4m3x2_to_f16x2(x23h);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) mma16816<false>(st[t].o[i], f0, f1, f2, f3, b0[t], b1[t]);
       const uint32_t g0 = e4m3x2_to_f16x2(x01l >> 16), g1 = e4m3x2_to_f16x2(x01h >> 16);
       const uint32_t g2 = e4m3x2_to_f16x2(x23l >> 16), g3 = e4m3x2_to_f16x2(x23h >> 16);
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        mma16816<false>(st[t].o[i], f0, f1, f2, f3, b0[t], b1[t]);
-        mma16816<false>(st[t].o[i + 1], g0, g1, g2, g3, b0[t], b1[t]);
-      }
+      for (int t = 0; t < NT; ++t) mma16816<false>(st[t].o[i + 1], g0, g1, g2, g3, b0[t], b1[t]);
     }
   }
 }
@@ -759,12 +760,12 @@ __device__ __forceinline__ float ws_dec(uint32_t u) { return __uint_as_float(~u)
 
 // Write a split piece's partial (unnormalised acc, running max, sum) of
 // query-column tile t to the workspace.
-template <int D, bool FP8>
+template <int D, bool FP8, int ROWS>
 __device__ __forceinline__ void store_partial(const WarpAcc<D>& st, const DecodeArgs& a, int w,
                                               int slot, int r, int c, float unboost, int t) {
   const int g0 = 8 * t + 2 * c, g1 = g0 + 1;
-  float* r0 = a.ws_acc + piece_row(w, slot, g0, a.rows) * D;
-  float* r1 = a.ws_acc + piece_row(w, slot, g1, a.rows) * D;
+  float* r0 = a.ws_acc + piece_row(w, slot, g0, ROWS) * D;
+  float* r1 = a.ws_acc + piece_row(w, slot, g1, ROWS) * D;
 #pragma unroll
   for (int i = 0; i < D / 16; i += 2) {
     const int dl = d_lo<D, FP8>(i, r), dh = d_hi<D, FP8>(i, r);
@@ -779,9 +780,9 @@ __device__ __forceinline__ void store_partial(const WarpAcc<D>& st, const Decode
   }
   if (r == 0) {
     if (g0 < a.n_q * a.group)
-      st_relaxed_v2(a.ws_ml + piece_row(w, slot, g0, a.rows) * 2, ws_enc(st.m0), ws_enc(st.l0));
+      st_relaxed_v2(a.ws_ml + piece_row(w, slot, g0, ROWS) * 2, ws_enc(st.m0), ws_enc(st.l0));
     if (g1 < a.n_q * a.group)
-      st_relaxed_v2(a.ws_ml + piece_row(w, slot, g1, a.rows) * 2, ws_enc(st.m1), ws_enc(st.l1));
+      st_relaxed_v2(a.ws_ml + piece_row(w, slot, g1, ROWS) * 2, ws_enc(st.m1), ws_enc(st.l1));
   }
 }
 
@@ -906,6 +907,29 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   int* misc = reinterpret_cast<int*>(smem + lay.misc);   // [0..3] warp sums of the scan
 
   PA_TRACE_ONLY(const unsigned long long t_entry = pa_now());
+  // ---- 0. with a device-side handshake, nothing of this step's inputs is
+  // read before the copy that uploads them has completed: thread 0 waits
+  // (bounded) for the word written after it.  A CTA that gives up reports
+  // the timeout and returns without touching anything.
+  if (a.ready != nullptr) {
+    if (tid == 0) {
+      bool ok = true;
+      if (static_cast<int>(ld_acquire_b32(a.ready) - a.ready_value) < 0) {
+        const uint64_t t0 = global_ns();
+        while (static_cast<int>(ld_acquire_b32(a.ready) - a.ready_value) < 0) {
+          __nanosleep(256);
+          if (global_ns() - t0 > a.wait_limit_ns) {
+            ok = false;
+            break;
+          }
+        }
+      }
+      misc[4] = ok;
+      if (!ok) atomicOr(a.status, kStatusTimeout);
+    }
+    __syncthreads();
+    if (!misc[4]) return;
+  }
   // ---- 1. blocks per sequence and their prefix sum (segments of Hkv * nblk)
   {
     const int per = (B + kThreads - 1) / kThreads;
@@ -1241,7 +1265,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         // combines its pieces as soon as all are written
 #pragma unroll
         for (int t = 0; t < NT; ++t)
-          store_partial<D, FP8>(st[t], a, gw, piece_no == 0 ? 0 : 1, r, c, unboost, t);
+          store_partial<D, FP8, ROWS>(st[t], a, gw, piece_no == 0 ? 0 : 1, r, c, unboost, t);
       }
       ++piece_no;
       PA_TRACE_ONLY(++tr_pieces; tr_split += !(s0 >= lo && s0 + nbk <= hi));
@@ -1325,7 +1349,7 @@ constexpr int kMergeThreads = 256;
 #endif
 constexpr int kMergeBatch = PA_MERGE_BATCH;
 
-template <int D, bool BF16>
+template <int D, bool BF16, int ROWS>
 __global__ void __launch_bounds__(kMergeThreads, 2)
 merge_kernel(const DecodeArgs a) {
   PA_TRACE_ONLY(const unsigned long long t_in = pa_now());
@@ -1387,7 +1411,7 @@ merge_kernel(const DecodeArgs a) {
     const bool row = g < a.n_q * G;
     // partial row of piece p for query row q
     auto prow = [&](int p, int q) {
-      return piece_row(w0 + p, p == 0 ? first_slot : 0, q, a.rows);
+      return piece_row(w0 + p, p == 0 ? first_slot : 0, q, ROWS);
     };
     float M = -INFINITY, S = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1402,12 +1426,12 @@ merge_kernel(const DecodeArgs a) {
       // p0 + k sits 16 rows after piece p0 + k - 1 (slot 0 of the next
       // worker), except that the segment's first piece may be its worker's
       // slot 1.
-      const int64_t rb = static_cast<int64_t>(w0 + p0) * 2 * a.rows + g;
+      const int64_t rb = static_cast<int64_t>(w0 + p0) * 2 * ROWS + g;
       const float* mlb = a.ws_ml + rb * 2;
       const float* vb = a.ws_acc + rb * D + 4 * d4;
-      const int s0x = p0 == 0 ? first_slot * a.rows : 0;
+      const int s0x = p0 == 0 ? first_slot * ROWS : 0;
       auto load = [&](int k) {
-        const int dr = k == 0 ? s0x : 2 * a.rows * k;
+        const int dr = k == 0 ? s0x : 2 * ROWS * k;
         ml[k] = ld_relaxed_v2(mlb + dr * 2);
         v[k] = ld_relaxed_v4(vb + static_cast<int64_t>(dr) * D);
       };
@@ -1513,11 +1537,29 @@ merge_kernel(const DecodeArgs a) {
     });
   }
   if (blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1 && tid == 0) griddep_wait();
+  // device-side handshake: the last merge CTA to finish, once the attention
+  // grid has completed (its own outputs written and visible), signals the
+  // step done; it does so even after a wait gave up, so that a copy waiting
+  // on the signal never waits forever (the status word carries the failure)
+  if (a.done != nullptr) {
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      if (atomicAdd(a.done_count, 1u) == gridDim.x * gridDim.y - 1) {
+        griddep_wait();
+        *a.done_count = 0u;
+        __threadfence_system();
+        st_release_sys_b32(a.done, a.done_value);
+      }
+    }
+  }
 }
 
 // The merge launch, allowed to be scheduled while the attention grid runs
 // (programmatic stream serialization).
-template <int D, bool BF16>
+// ROWS: the partials' rows per piece (a.rows; 8 per tile of query columns
+// the attention launch held).
+template <int D, bool BF16, int ROWS>
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   // one thread per (query row, 4 output columns), rounded up to whole warps:
@@ -1537,7 +1579,7 @@ cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_kernel<D, BF16>, a);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<D, BF16, ROWS>, a);
 }
 
 // cuTensorMapEncodeTiled, from the driver (no link against libcuda).
@@ -1644,7 +1686,7 @@ cudaError_t launch_one(const DecodeArgs& args, cudaStream_t s) {
   }
   if (e != cudaSuccess) return e;
   if (a.ws_acc == nullptr) return cudaSuccess;
-  return launch_merge<D, BF16>(a, s);
+  return launch_merge<D, BF16, 8 * NT>(a, s);
 }
 
 // Shared memory and registers per CTA are traded against resident CTAs per

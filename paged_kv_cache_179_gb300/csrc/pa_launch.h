@@ -62,6 +62,16 @@ struct DecodeArgs {
   int early;                    // programmatic dependent launch: prologue before griddepcontrol.wait
   float scale_log2;             // softmax scale * log2(e)
   uint64_t wait_limit_ns;       // time limit of every wait (kWaitLimitNs unless a test shortens it)
+  // device-side ordering against copies on other streams (null: none).  The
+  // attention launch waits (bounded) until *ready reaches ready_value before
+  // it reads anything; the merge launch's CTAs count themselves on
+  // *done_count and the last one, once the attention grid has completed,
+  // resets the count and stores done_value to *done.
+  const uint32_t* ready;
+  uint32_t* done;
+  uint32_t* done_count;
+  uint32_t ready_value;
+  uint32_t done_value;
 };
 
 // Largest query rows per (sequence, kv head) one launch serves: four tiles of
@@ -87,6 +97,9 @@ cudaError_t launch_decode_tiles4_e4m3(const DecodeArgs& a, bool bf16, cudaStream
 // The merge launch alone (no attention launch writes its partials): the
 // failure-path test of its bounded poll.
 cudaError_t launch_merge_only(const DecodeArgs& a, bool bf16, cudaStream_t s);
+// Stores value to *done (release, system scope): the handshake's done signal
+// of a step that launches nothing else.
+cudaError_t launch_signal_done(uint32_t* done, uint32_t value, cudaStream_t s);
 // One warp waiting on an mbarrier that nothing completes, with the decode's
 // bounded wait: the failure-path test of that wait.
 cudaError_t launch_wait_probe(unsigned* status, uint64_t limit_ns, cudaStream_t s);

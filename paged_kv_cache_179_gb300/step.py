@@ -8,6 +8,8 @@ attention output is copied back.
 """
 from __future__ import annotations
 
+import ctypes
+
 import torch
 
 from . import _abi
@@ -65,20 +67,22 @@ class DecodeStep:
                            self.split_ctas, self.workspace, window=self.window,
                            early_prologue=self.early_prologue)
 
-    def fused(self, q, k_new, v_new, slot_mapping, out):
+    def fused(self, q, k_new, v_new, slot_mapping, out, sync=None):
         """Append and decode in one launch (slot_mapping must hold each
-        sequence's position context_len - 1, as a decode step does)."""
+        sequence's position context_len - 1, as a decode step does); ``sync``
+        (an ``_abi.StepSync``) adds the device-side handshake with the copies
+        of a serving loop (``StepPipeline``)."""
         if self.kv == "fp8":
             _abi.pa_decode_step_fp8(out, q, k_new, v_new, self.k_cache, self.v_cache,
                                     self.k_scale, self.v_scale, slot_mapping, self.block_tables,
                                     self.context_lens, self.max_context_len, self.scale,
                                     self.split_ctas, self.workspace, window=self.window,
-                                    early_prologue=self.early_prologue)
+                                    early_prologue=self.early_prologue, sync=sync)
         else:
             _abi.pa_decode_step(out, q, k_new, v_new, self.k_cache, self.v_cache, slot_mapping,
                                 self.block_tables, self.context_lens, self.max_context_len,
                                 self.scale, self.split_ctas, self.workspace, window=self.window,
-                                early_prologue=self.early_prologue)
+                                early_prologue=self.early_prologue, sync=sync)
         return out
 
     @property
@@ -92,22 +96,27 @@ class DecodeStep:
         the 256-sequence E4M3 batch)."""
         return self.kv != "fp8"
 
-    def __call__(self, q, k_new, v_new, slot_mapping, out, fused=None):
-        """One step; ``fused`` None picks the faster form (``prefers_fused``)."""
+    def __call__(self, q, k_new, v_new, slot_mapping, out, fused=None, sync=None):
+        """One step; ``fused`` None picks the faster form (``prefers_fused``);
+        ``sync`` only with the fused form."""
         if fused is None:
             fused = self.prefers_fused
+        if sync is not None and not fused:
+            raise ValueError("the device-side handshake needs the fused step")
         if fused:
-            return self.fused(q, k_new, v_new, slot_mapping, out)
+            return self.fused(q, k_new, v_new, slot_mapping, out, sync=sync)
         self.append(k_new, v_new, slot_mapping)
         self.decode(q, out)
         return out
 
-    def bind(self, q, k_new, v_new, slot_mapping, out, fused=None, stream=None):
+    def bind(self, q, k_new, v_new, slot_mapping, out, fused=None, stream=None, sync=None):
         """The step on these tensors as a callable with its C-ABI arguments
         checked and marshalled once (``_abi.prepare``), launching on
         ``stream`` (default: the current stream at each call).  Each call
-        runs one step; refill the tensors in place between calls."""
-        return _abi.prepare(lambda: self(q, k_new, v_new, slot_mapping, out, fused=fused), stream)
+        runs one step; refill the tensors in place between calls (and
+        ``sync``'s values, which each call reads)."""
+        return _abi.prepare(lambda: self(q, k_new, v_new, slot_mapping, out, fused=fused,
+                                         sync=sync), stream)
 
     def capture(self, q, k_new, v_new, slot_mapping, out, fused=None, stream=None):
         """Record the step into a CUDA graph and return it (``torch.cuda.CUDAGraph``).
@@ -222,7 +231,8 @@ class StepPipeline:
     fills ``stagings[k].host`` before ``submit`` uses slot k (``slot()`` says
     which; ``wait_slot_free()`` waits until its last upload has finished)."""
 
-    def __init__(self, make_step, specs: dict, out_shape, out_dtype, device, depth: int = 2):
+    def __init__(self, make_step, specs: dict, out_shape, out_dtype, device, depth: int = 2,
+                 handshake: str = "auto"):
         self.depth = depth
         self.copy = torch.cuda.Stream(device)       # uploads
         self.back = torch.cuda.Stream(device)       # read-backs
@@ -236,8 +246,38 @@ class StepPipeline:
         self.uploaded = [torch.cuda.Event() for _ in range(depth)]    # the slot's upload done
         self.stepped = [torch.cuda.Event() for _ in range(depth)]     # the slot's step done
         self.read_back = [torch.cuda.Event() for _ in range(depth)]   # its output on the host
-        self.calls = {}        # (slot, fused) -> the bound step
+        self.calls = {}        # (slot, fused, device handshake) -> the bound step
         self.n = 0
+        # Device-side handshake (fused steps): per slot a "ready" word the
+        # upload stream sets after the upload, and a "done" word (with the
+        # merge launch's CTA count) the step sets when its output is complete;
+        # each in its own 32-byte sector.
+        self.words = torch.zeros(depth, 3, 8, dtype=torch.int32, device=device)
+        self.syncs = []
+        for k in range(depth):
+            sy = _abi.StepSync()
+            sy.ready = self.words[k, 0].data_ptr()
+            sy.done = self.words[k, 1].data_ptr()
+            sy.done_count = self.words[k, 2].data_ptr()
+            self.syncs.append(sy)
+        # the word operations of a submit, marshalled once: library entry
+        # points with the words' addresses and the streams' handles
+        lib = _abi.load()
+        self._write_word, self._wait_word = lib.pa_stream_write_value, lib.pa_stream_wait_value
+        self._ready_p = [ctypes.c_void_p(self.words[k, 0].data_ptr()) for k in range(depth)]
+        self._done_p = [ctypes.c_void_p(self.words[k, 1].data_ptr()) for k in range(depth)]
+        self._copy_h = ctypes.c_void_p(self.copy.cuda_stream)
+        self._back_h = ctypes.c_void_p(self.back.cuda_stream)
+        self.handshake = handshake
+        if handshake == "auto":
+            try:
+                _abi.pa_stream_write_value(self.words[0, 0, :1], 0, self.copy)
+                self.handshake = "device"
+            except _abi.PAError as e:
+                if e.code != _abi.PA_ERR_UNSUPPORTED:
+                    raise
+                self.handshake = "events"
+        self._fresh = True
 
     def slot(self) -> int:
         return self.n % self.depth
@@ -247,22 +287,34 @@ class StepPipeline:
         if self.n >= self.depth:
             self.uploaded[self.slot()].synchronize()
 
-    def _call(self, k, fused):
-        key = (k, fused)
+    def _call(self, k, fused, device):
+        key = (k, fused, device)
         if key not in self.calls:
             d = self.stagings[k].dev
             self.calls[key] = self.steps[k].bind(d["q"], d["k_new"], d["v_new"],
                                                  d["slot_mapping"], self.dev_out[k], fused=fused,
-                                                 stream=self.compute)
+                                                 stream=self.compute,
+                                                 sync=self.syncs[k] if device else None)
         return self.calls[key]
+
+    def uses_device_handshake(self, fused=None) -> bool:
+        """Whether submit(fused) orders its copies by the device-side handshake
+        (fused steps, where the driver offers stream memory operations)."""
+        if fused is None:
+            fused = self.steps[0].prefers_fused
+        return self.handshake == "device" and bool(fused)
 
     def submit(self, fused=None):
         """Upload the next slot's inputs, run its step, read its output back.
         Returns (slot, h2d bytes, d2h bytes); ``host_out[slot]`` holds the
         output once ``read_back[slot]`` has completed."""
+        if fused is None:
+            fused = self.steps[0].prefers_fused
+        if self.uses_device_handshake(fused):
+            return self._submit_device(fused)
         k = self.slot()
         reused = self.n >= self.depth
-        step = self._call(k, fused)
+        step = self._call(k, fused, False)
         self.compute.wait_stream(torch.cuda.current_stream())
         if reused:
             self.copy.wait_event(self.stepped[k])         # the slot's last step is done with it
@@ -281,7 +333,44 @@ class StepPipeline:
         self.n += 1
         return k, h2d, self.host_out[k].numel() * self.host_out[k].element_size()
 
+    def _submit_device(self, fused):
+        """submit() with the device-side handshake: the compute stream holds
+        only the steps' kernels (the attention launch waits on the device for
+        its upload; the read-back stream waits for the step's done word), so
+        consecutive steps overlap as they do without copies."""
+        k = self.slot()
+        reused = self.n >= self.depth
+        seq = (self.n + 1) & 0xffffffff
+        step = self._call(k, fused, True)
+        if self._fresh:       # order everything after the caller's earlier work, once
+            cur = torch.cuda.current_stream()
+            for st in (self.compute, self.copy, self.back):
+                st.wait_stream(cur)
+            self._fresh = False
+        if reused:
+            # the slot's last step is done with its inputs and its output was
+            # read back (that read-back waited for the step's done word)
+            self.copy.wait_event(self.read_back[k])
+        with torch.cuda.stream(self.copy):
+            h2d = self.stagings[k].upload()
+        rc = self._write_word(self._copy_h, self._ready_p[k], seq)
+        if rc:
+            raise _abi.PAError(rc, "pa_stream_write_value")
+        sy = self.syncs[k]
+        sy.ready_value = seq
+        sy.done_value = seq
+        step()
+        rc = self._wait_word(self._back_h, self._done_p[k], seq)
+        if rc:
+            raise _abi.PAError(rc, "pa_stream_wait_value")
+        with torch.cuda.stream(self.back):
+            self.host_out[k].copy_(self.dev_out[k], non_blocking=True)
+        self.read_back[k].record(self.back)
+        self.n += 1
+        return k, h2d, self.host_out[k].numel() * self.host_out[k].element_size()
+
     def finish(self):
         """Make the caller's stream wait for every step and copy submitted so far."""
         for st in (self.compute, self.copy, self.back):
             torch.cuda.current_stream().wait_stream(st)
+        self._fresh = True

@@ -31,7 +31,7 @@ def header_functions():
 
 def test_header_and_binding_agree():
     names = header_functions()
-    assert len(names) == 18
+    assert len(names) == 22
     assert sorted(_abi.SIGNATURES) == names
 
 
@@ -113,6 +113,14 @@ def test_append_and_quantize_argument_errors(lib):
     assert q(None, None, FAKE, FAKE, FAKE, FAKE, 8, 2, 64, 16, None) == _abi.PA_ERR_INVALID_ARG
     assert q(FAKE, None, FAKE, None, FAKE, None, 8, 2, 64, 32, None) == _abi.PA_ERR_UNSUPPORTED
     assert lib.pa_e4m3_encode(FAKE, MISALIGNED, 10, None) == _abi.PA_ERR_INVALID_ARG
+
+
+def test_handshake_argument_errors(lib):
+    # the synced step needs its sync words; stream word operations a 4-aligned word
+    args = [FAKE] * 8 + [8, FAKE, 128, 2, 8, 2, 64, 16, 32, 0.125, 0, 0, 8, FAKE, 1 << 20, 0]
+    assert lib.pa_decode_step_synced(*args, None, None) == _abi.PA_ERR_INVALID_ARG
+    assert lib.pa_stream_write_value(None, None, 1) == _abi.PA_ERR_INVALID_ARG
+    assert lib.pa_stream_wait_value(None, FAKE + 2, 1) == _abi.PA_ERR_INVALID_ARG
 
 
 def test_failure_path_hooks_check_their_limits(lib):

@@ -156,7 +156,8 @@ def test_run_from_staging_matches_device_call():
     assert torch.equal(kc.view(torch.int16), k2.view(torch.int16))
 
 
-def test_step_pipeline_overlapped_copies_match_direct_calls():
+@pytest.mark.parametrize("handshake", ["events", "device"])
+def test_step_pipeline_overlapped_copies_match_direct_calls(handshake):
     """StepPipeline: two slots with different queries, five steps submitted
     back to back; every read-back equals the step called directly on the
     same inputs (the appended rows are the same each step)."""
@@ -171,7 +172,8 @@ def test_step_pipeline_overlapped_copies_match_direct_calls():
         return DecodeStep(k_cache=kc, v_cache=vc, block_tables=st.dev["block_tables"],
                           context_lens=st.dev["context_lens"], max_context_len=w.max_context_len,
                           scale=w.scale, num_q_heads=w.Hq)
-    pipe = StepPipeline(make_step, specs, w.q.shape, w.q.dtype, "cuda")
+    pipe = StepPipeline(make_step, specs, w.q.shape, w.q.dtype, "cuda", handshake=handshake)
+    assert pipe.uses_device_handshake() == (handshake == "device")
     g = torch.Generator().manual_seed(1)
     qs = [torch.randn(w.q.shape, generator=g).to(w.q.dtype) for _ in range(2)]
     for k, st in enumerate(pipe.stagings):
@@ -226,13 +228,15 @@ def test_bound_step_records_once_and_matches_direct_calls():
         assert torch.equal(w.v_cache.view(torch.int16), v2.view(torch.int16))
 
 
-def test_step_pipeline_early_prologue_new_lengths_each_step():
+@pytest.mark.parametrize("handshake", ["events", "device"])
+def test_step_pipeline_early_prologue_new_lengths_each_step(handshake):
     """StepPipeline with the early prologue: every step uploads new context
     lengths and slots (one token more each step), so a prologue that read
     its slot's lengths before that upload had landed would attend the wrong
     contexts.  The uploads are ordered before the step by events, which the
     early prologue does not relax: the outputs and pools must equal plain
-    direct steps on the same inputs, step by step."""
+    direct steps on the same inputs, step by step.  With the device-side
+    handshake the attention launch itself waits for the upload's word."""
     from paged_kv_cache_179_gb300.step import StepPipeline
     STEPS = 6
     name = "qwen2_5_1_5b"
@@ -261,7 +265,8 @@ def test_step_pipeline_early_prologue_new_lengths_each_step():
         return DecodeStep(k_cache=kc, v_cache=vc, block_tables=st.dev["block_tables"],
                           context_lens=st.dev["context_lens"], max_context_len=max_ctx,
                           scale=w.scale, num_q_heads=w.Hq, early_prologue=True)
-    pipe = StepPipeline(make_step, specs, w.q.shape, w.q.dtype, "cuda")
+    pipe = StepPipeline(make_step, specs, w.q.shape, w.q.dtype, "cuda", handshake=handshake)
+    assert pipe.uses_device_handshake() == (handshake == "device")
     got = [None] * STEPS
     pending = None
     for n in range(STEPS):
