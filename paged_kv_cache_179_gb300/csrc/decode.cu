@@ -57,8 +57,7 @@ cudaError_t launch_merge_only(const DecodeArgs& a, bool bf16, cudaStream_t s) {
 
 // A step with nothing to attend still signals its handshake's done word.
 __global__ void signal_done_kernel(uint32_t* done, uint32_t value) {
-  __threadfence_system();
-  st_release_sys_b32(done, value);
+  st_release_gpu_b32(done, value);
 }
 
 cudaError_t launch_signal_done(uint32_t* done, uint32_t value, cudaStream_t s) {

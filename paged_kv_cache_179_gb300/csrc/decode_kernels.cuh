@@ -1540,7 +1540,9 @@ merge_kernel(const DecodeArgs a) {
   // device-side handshake: the last merge CTA to finish, once the attention
   // grid has completed (its own outputs written and visible), signals the
   // step done; it does so even after a wait gave up, so that a copy waiting
-  // on the signal never waits forever (the status word carries the failure)
+  // on the signal never waits forever (the status word carries the failure).
+  // Every reader of the signal and of the output (the stream waiting on it,
+  // the copy engine after it, later kernels) is on this GPU: gpu scope.
   if (a.done != nullptr) {
     __syncthreads();
     if (tid == 0) {
@@ -1548,8 +1550,8 @@ merge_kernel(const DecodeArgs a) {
       if (atomicAdd(a.done_count, 1u) == gridDim.x * gridDim.y - 1) {
         griddep_wait();
         *a.done_count = 0u;
-        __threadfence_system();
-        st_release_sys_b32(a.done, a.done_value);
+        __threadfence();
+        st_release_gpu_b32(a.done, a.done_value);
       }
     }
   }

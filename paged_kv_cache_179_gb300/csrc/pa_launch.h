@@ -97,7 +97,7 @@ cudaError_t launch_decode_tiles4_e4m3(const DecodeArgs& a, bool bf16, cudaStream
 // The merge launch alone (no attention launch writes its partials): the
 // failure-path test of its bounded poll.
 cudaError_t launch_merge_only(const DecodeArgs& a, bool bf16, cudaStream_t s);
-// Stores value to *done (release, system scope): the handshake's done signal
+// Stores value to *done (release, gpu scope): the handshake's done signal
 // of a step that launches nothing else.
 cudaError_t launch_signal_done(uint32_t* done, uint32_t value, cudaStream_t s);
 // One warp waiting on an mbarrier that nothing completes, with the decode's
