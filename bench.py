@@ -430,6 +430,7 @@ def measure_other_config(args, name, dev, clocks, peak):
     run.time_steps(args.steps)
     clocks.mark(f"{name}:end")
     run.time_decode(args.steps)
+    e2e_ms, h2d, d2h, e2e_mode = measure_e2e(args, run, dev)
     run.check()
     step_s = statistics.mean(run.step_ms) / 1e3
     dec_s = statistics.mean(run.dec_ms) / 1e3
@@ -444,6 +445,8 @@ def measure_other_config(args, name, dev, clocks, peak):
         "decode_us": run.decode_us(),
         "bytes_per_decode": kb, "hbm_gbs": round(kb / dec_s / 1e9, 1),
         "frac_of_peak": round(kb / dec_s / 1e9 / peak, 4),
+        "e2e": {"value": round(run.tokens * args.steps / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "mode": e2e_mode},
         "gpu_launches": run.launches_per_step * args.steps,
         "clocks_marks": (f"{name}:start", f"{name}:end"),
     }

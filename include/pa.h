@@ -387,6 +387,58 @@ int pa_decode_step_fp8_synced(void *out, const void *q, const void *k_new, const
                               unsigned flags, const pa_step_sync *sync, void *stream);
 
 /*
+ * One whole pipelined step of a serving loop in one call: the step's packed
+ * inputs uploaded from pinned host memory on copy_stream, the handshake's
+ * ready word written after them, the step (as pa_decode_step_synced /
+ * pa_decode_step_fp8_synced) launched on `stream`, and on back_stream a wait
+ * for the step's done word, the output copied to pinned host memory and
+ * `reuse_event` recorded.  When slot_reused is set, the upload first waits
+ * for `reuse_event` (the previous read-back of this slot, recorded by the
+ * call that used the slot before), so that neither the slot's inputs nor its
+ * output are overwritten while still in use.  The decode arguments (q,
+ * k_new, v_new, slot_mapping, block_tables, context_lens) point into the
+ * device buffer the upload fills.  Streams are cudaStream_t and the event a
+ * cudaEvent_t, passed as void*; all are the caller's.  If the step cannot
+ * be launched the call returns its error after the upload and before any
+ * wait on the done word (so nothing waits for a step that never ran).
+ * No counterpart in the pages: host-device plumbing of a serving loop, one
+ * library call per step instead of a dozen runtime calls.
+ */
+typedef struct pa_step_copies {
+    const void *host_in;     /* pinned host: the step's inputs, in_bytes */
+    void *dev_in;            /* device: where they are uploaded */
+    size_t in_bytes;
+    const void *dev_out;     /* device: the step's output, out_bytes */
+    void *host_out;          /* pinned host: where it is read back */
+    size_t out_bytes;
+    void *copy_stream;
+    void *back_stream;
+    void *reuse_event;
+    int slot_reused;
+} pa_step_copies;
+
+int pa_decode_step_pipelined(void *out, const void *q, const void *k_new, const void *v_new,
+                             void *k_cache, void *v_cache, const int64_t *slot_mapping,
+                             const int32_t *block_tables, int max_blocks_per_seq,
+                             const int32_t *context_lens, int max_context_len, int num_seqs,
+                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                             int num_blocks, float scale, int window_size, int dtype,
+                             int split_ctas, void *workspace, size_t workspace_bytes,
+                             unsigned flags, const pa_step_sync *sync,
+                             const pa_step_copies *io, void *stream);
+int pa_decode_step_fp8_pipelined(void *out, const void *q, const void *k_new, const void *v_new,
+                                 uint8_t *k_cache, uint8_t *v_cache, float *k_scale,
+                                 float *v_scale, const int64_t *slot_mapping,
+                                 const int32_t *block_tables, int max_blocks_per_seq,
+                                 const int32_t *context_lens, int max_context_len,
+                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int num_blocks, float scale, int window_size,
+                                 int dtype, int split_ctas, void *workspace,
+                                 size_t workspace_bytes, unsigned flags,
+                                 const pa_step_sync *sync, const pa_step_copies *io,
+                                 void *stream);
+
+/*
  * Stream-ordered 32-bit device-word operations (the driver's stream memory
  * operations): pa_stream_write_value stores value to *addr once the work
  * before it on stream has completed (its writes visible first);

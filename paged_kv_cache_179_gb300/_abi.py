@@ -57,6 +57,12 @@ SIGNATURES = {
     "pa_decode_step_fp8_synced": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp,
                                    _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32,
                                    _i32, _vp, _sz, _u32, _vp, _vp], _i32),
+    "pa_decode_step_pipelined": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32,
+                                  _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _i32,
+                                  _vp, _sz, _u32, _vp, _vp, _vp], _i32),
+    "pa_decode_step_fp8_pipelined": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                      _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32,
+                                      _i32, _i32, _vp, _sz, _u32, _vp, _vp, _vp], _i32),
     "pa_stream_write_value": ([_vp, _vp, _u32], _i32),
     "pa_stream_wait_value": ([_vp, _vp, _u32], _i32),
     "pa_get_status": ([_vp, ctypes.POINTER(ctypes.c_uint)], _i32),
@@ -399,6 +405,16 @@ class StepSync(ctypes.Structure):
                 ("done_value", ctypes.c_uint32)]
 
 
+class StepCopies(ctypes.Structure):
+    """pa_step_copies: the host<->device copies of one pipelined step (see
+    include/pa.h); ``slot_reused`` is read at each call."""
+    _fields_ = [("host_in", ctypes.c_void_p), ("dev_in", ctypes.c_void_p),
+                ("in_bytes", ctypes.c_size_t), ("dev_out", ctypes.c_void_p),
+                ("host_out", ctypes.c_void_p), ("out_bytes", ctypes.c_size_t),
+                ("copy_stream", ctypes.c_void_p), ("back_stream", ctypes.c_void_p),
+                ("reuse_event", ctypes.c_void_p), ("slot_reused", ctypes.c_int)]
+
+
 def _sync_ptr(sync):
     return ctypes.c_void_p(ctypes.addressof(sync))
 
@@ -431,9 +447,11 @@ def _ws_bytes(workspace, dev):
 def pa_decode_step(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_tables,
                    context_lens, max_context_len: int, scale: float, split_ctas: int = 0,
                    workspace=None, *, window: int = 0, early_prologue: bool = False,
-                   sync: StepSync = None) -> None:
+                   sync: StepSync = None, copies: StepCopies = None) -> None:
     """Append k_new/v_new at slot_mapping, then decode, in one launch (16-bit
-    pools); with ``sync``, pa_decode_step_synced (device-side handshake)."""
+    pools); with ``sync``, pa_decode_step_synced (device-side handshake); with
+    ``copies`` too, pa_decode_step_pipelined (the step's upload and read-back
+    in the same call)."""
     dev = q.device
     act = (torch.float16, torch.bfloat16)
     _need(q, "q", act, 3, dev)
@@ -456,15 +474,19 @@ def pa_decode_step(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_t
             _flags(early_prologue))
     if sync is None:
         _call(load().pa_decode_step, "pa_decode_step", *args, _stream(dev))
-    else:
+    elif copies is None:
         _call(load().pa_decode_step_synced, "pa_decode_step_synced", *args, _sync_ptr(sync),
               _stream(dev))
+    else:
+        _call(load().pa_decode_step_pipelined, "pa_decode_step_pipelined", *args,
+              _sync_ptr(sync), _sync_ptr(copies), _stream(dev))
 
 
 def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping,
                        block_tables, context_lens, max_context_len: int, scale: float,
                        split_ctas: int = 0, workspace=None, *, window: int = 0,
-                       early_prologue: bool = False, sync: StepSync = None) -> None:
+                       early_prologue: bool = False, sync: StepSync = None,
+                       copies: StepCopies = None) -> None:
     """Append (E4M3-encode) k_new/v_new, then decode over the E4M3 pools, in one
     attention launch; q, k_new, v_new and out share one dtype (fp16 or bf16)."""
     dev = q.device
@@ -489,9 +511,12 @@ def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
             _ws_bytes(workspace, dev), _flags(early_prologue))
     if sync is None:
         _call(load().pa_decode_step_fp8, "pa_decode_step_fp8", *args, _stream(dev))
-    else:
+    elif copies is None:
         _call(load().pa_decode_step_fp8_synced, "pa_decode_step_fp8_synced", *args,
               _sync_ptr(sync), _stream(dev))
+    else:
+        _call(load().pa_decode_step_fp8_pipelined, "pa_decode_step_fp8_pipelined", *args,
+              _sync_ptr(sync), _sync_ptr(copies), _stream(dev))
 
 
 def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,

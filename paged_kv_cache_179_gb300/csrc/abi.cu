@@ -571,6 +571,95 @@ int pa_decode_step_fp8_synced(void* out, const void* q, const void* k_new, const
                           workspace, workspace_bytes, flags, sync, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+bool copies_ok(const pa_step_copies* io) {
+  return io != nullptr && io->host_in != nullptr && io->dev_in != nullptr &&
+         io->dev_out != nullptr && io->host_out != nullptr && io->reuse_event != nullptr &&
+         io->in_bytes > 0 && io->out_bytes > 0;
+}
+
+// The copies before a pipelined step: wait for the slot's last read-back
+// (when reused), upload, then the ready word.
+int upload_and_signal(const pa_step_copies* io, const pa_step_sync* sync) {
+  const cudaStream_t cs = static_cast<cudaStream_t>(io->copy_stream);
+  if (io->slot_reused &&
+      cudaStreamWaitEvent(cs, static_cast<cudaEvent_t>(io->reuse_event), 0) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaMemcpyAsync(io->dev_in, io->host_in, io->in_bytes, cudaMemcpyHostToDevice, cs) !=
+      cudaSuccess)
+    return PA_ERR_CUDA;
+  const StreamMemOps& ops = stream_mem_ops();
+  if (ops.write == nullptr) return PA_ERR_UNSUPPORTED;
+  return cu_status(ops.write(static_cast<CUstream>(cs),
+                             reinterpret_cast<CUdeviceptr>(sync->ready), sync->ready_value,
+                             CU_STREAM_WRITE_VALUE_DEFAULT));
+}
+
+// The copies after a launched step: wait for its done word, read the output
+// back, record the slot's event.
+int wait_and_read_back(const pa_step_copies* io, const pa_step_sync* sync) {
+  const cudaStream_t bs = static_cast<cudaStream_t>(io->back_stream);
+  const StreamMemOps& ops = stream_mem_ops();
+  if (ops.wait == nullptr) return PA_ERR_UNSUPPORTED;
+  if (int rc = cu_status(ops.wait(static_cast<CUstream>(bs),
+                                  reinterpret_cast<CUdeviceptr>(sync->done), sync->done_value,
+                                  CU_STREAM_WAIT_VALUE_GEQ)))
+    return rc;
+  if (cudaMemcpyAsync(io->host_out, io->dev_out, io->out_bytes, cudaMemcpyDeviceToHost, bs) !=
+      cudaSuccess)
+    return PA_ERR_CUDA;
+  return cuda_status(cudaEventRecord(static_cast<cudaEvent_t>(io->reuse_event), bs));
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_decode_step_pipelined(void* out, const void* q, const void* k_new, const void* v_new,
+                             void* k_cache, void* v_cache, const int64_t* slot_mapping,
+                             const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* context_lens, int max_context_len, int num_seqs,
+                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                             int num_blocks, float scale, int window_size, int dtype,
+                             int split_ctas, void* workspace, size_t workspace_bytes,
+                             unsigned flags, const pa_step_sync* sync,
+                             const pa_step_copies* io, void* stream) {
+  if (sync == nullptr || !sync_ok(sync) || !copies_ok(io)) return PA_ERR_INVALID_ARG;
+  if (int rc = upload_and_signal(io, sync)) return rc;
+  if (int rc = decode_step_16(out, q, k_new, v_new, k_cache, v_cache, slot_mapping,
+                              block_tables, max_blocks_per_seq, context_lens, max_context_len,
+                              num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                              num_blocks, scale, window_size, dtype, split_ctas, workspace,
+                              workspace_bytes, flags, sync, stream))
+    return rc;
+  return wait_and_read_back(io, sync);
+}
+
+int pa_decode_step_fp8_pipelined(void* out, const void* q, const void* k_new, const void* v_new,
+                                 uint8_t* k_cache, uint8_t* v_cache, float* k_scale,
+                                 float* v_scale, const int64_t* slot_mapping,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* context_lens, int max_context_len,
+                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int num_blocks, float scale, int window_size,
+                                 int dtype, int split_ctas, void* workspace,
+                                 size_t workspace_bytes, unsigned flags,
+                                 const pa_step_sync* sync, const pa_step_copies* io,
+                                 void* stream) {
+  if (sync == nullptr || !sync_ok(sync) || !copies_ok(io)) return PA_ERR_INVALID_ARG;
+  if (int rc = upload_and_signal(io, sync)) return rc;
+  if (int rc = decode_step_e4m3(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                                slot_mapping, block_tables, max_blocks_per_seq, context_lens,
+                                max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                block_size, num_blocks, scale, window_size, dtype, split_ctas,
+                                workspace, workspace_bytes, flags, sync, stream))
+    return rc;
+  return wait_and_read_back(io, sync);
+}
+
 int pa_stream_write_value(void* stream, uint32_t* addr, uint32_t value) {
   if (addr == nullptr || !aligned(addr, 4)) return PA_ERR_INVALID_ARG;
   const StreamMemOps& ops = stream_mem_ops();

@@ -67,7 +67,7 @@ class DecodeStep:
                            self.split_ctas, self.workspace, window=self.window,
                            early_prologue=self.early_prologue)
 
-    def fused(self, q, k_new, v_new, slot_mapping, out, sync=None):
+    def fused(self, q, k_new, v_new, slot_mapping, out, sync=None, copies=None):
         """Append and decode in one launch (slot_mapping must hold each
         sequence's position context_len - 1, as a decode step does); ``sync``
         (an ``_abi.StepSync``) adds the device-side handshake with the copies
@@ -77,12 +77,13 @@ class DecodeStep:
                                     self.k_scale, self.v_scale, slot_mapping, self.block_tables,
                                     self.context_lens, self.max_context_len, self.scale,
                                     self.split_ctas, self.workspace, window=self.window,
-                                    early_prologue=self.early_prologue, sync=sync)
+                                    early_prologue=self.early_prologue, sync=sync,
+                                    copies=copies)
         else:
             _abi.pa_decode_step(out, q, k_new, v_new, self.k_cache, self.v_cache, slot_mapping,
                                 self.block_tables, self.context_lens, self.max_context_len,
                                 self.scale, self.split_ctas, self.workspace, window=self.window,
-                                early_prologue=self.early_prologue, sync=sync)
+                                early_prologue=self.early_prologue, sync=sync, copies=copies)
         return out
 
     @property
@@ -268,6 +269,22 @@ class StepPipeline:
         self._done_p = [ctypes.c_void_p(self.words[k, 1].data_ptr()) for k in range(depth)]
         self._copy_h = ctypes.c_void_p(self.copy.cuda_stream)
         self._back_h = ctypes.c_void_p(self.back.cuda_stream)
+        # the copies of each slot's pipelined step, for the one-call form
+        # (pa_decode_step_pipelined): the slot's buffers, the two copy
+        # streams and the slot's read-back event (recorded once here so that
+        # its handle exists)
+        self.copies = []
+        for k in range(depth):
+            st, io = self.stagings[k], _abi.StepCopies()
+            io.host_in, io.dev_in, io.in_bytes = (st.host_buf.data_ptr(), st.dev_buf.data_ptr(),
+                                                  st.nbytes)
+            io.dev_out, io.host_out = self.dev_out[k].data_ptr(), self.host_out[k].data_ptr()
+            io.out_bytes = self.dev_out[k].numel() * self.dev_out[k].element_size()
+            io.copy_stream, io.back_stream = self.copy.cuda_stream, self.back.cuda_stream
+            self.read_back[k].record(self.back)
+            io.reuse_event = self.read_back[k].cuda_event
+            io.slot_reused = 0
+            self.copies.append(io)
         self.handshake = handshake
         if handshake == "auto":
             try:
@@ -285,16 +302,24 @@ class StepPipeline:
     def wait_slot_free(self):
         """Block the host until the next slot's host buffer may be refilled."""
         if self.n >= self.depth:
-            self.uploaded[self.slot()].synchronize()
+            if self.uses_device_handshake():   # the one-call form records only the read-back
+                self.read_back[self.slot()].synchronize()
+            else:
+                self.uploaded[self.slot()].synchronize()
 
     def _call(self, k, fused, device):
         key = (k, fused, device)
         if key not in self.calls:
             d = self.stagings[k].dev
-            self.calls[key] = self.steps[k].bind(d["q"], d["k_new"], d["v_new"],
-                                                 d["slot_mapping"], self.dev_out[k], fused=fused,
-                                                 stream=self.compute,
-                                                 sync=self.syncs[k] if device else None)
+            if device:   # the whole pipelined step, copies included, in one library call
+                st, out = self.steps[k], self.dev_out[k]
+                self.calls[key] = _abi.prepare(
+                    lambda: st.fused(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], out,
+                                     sync=self.syncs[k], copies=self.copies[k]), self.compute)
+            else:
+                self.calls[key] = self.steps[k].bind(d["q"], d["k_new"], d["v_new"],
+                                                     d["slot_mapping"], self.dev_out[k],
+                                                     fused=fused, stream=self.compute)
         return self.calls[key]
 
     def uses_device_handshake(self, fused=None) -> bool:
@@ -334,12 +359,13 @@ class StepPipeline:
         return k, h2d, self.host_out[k].numel() * self.host_out[k].element_size()
 
     def _submit_device(self, fused):
-        """submit() with the device-side handshake: the compute stream holds
-        only the steps' kernels (the attention launch waits on the device for
-        its upload; the read-back stream waits for the step's done word), so
-        consecutive steps overlap as they do without copies."""
+        """submit() with the device-side handshake, as one library call
+        (pa_decode_step_pipelined): the upload and the ready word on the copy
+        stream, the step's kernels alone on the compute stream (the attention
+        launch waits on the device for its upload), the wait for the step's
+        done word and the read-back on the read-back stream, so consecutive
+        steps overlap as they do without copies."""
         k = self.slot()
-        reused = self.n >= self.depth
         seq = (self.n + 1) & 0xffffffff
         step = self._call(k, fused, True)
         if self._fresh:       # order everything after the caller's earlier work, once
@@ -347,27 +373,13 @@ class StepPipeline:
             for st in (self.compute, self.copy, self.back):
                 st.wait_stream(cur)
             self._fresh = False
-        if reused:
-            # the slot's last step is done with its inputs and its output was
-            # read back (that read-back waited for the step's done word)
-            self.copy.wait_event(self.read_back[k])
-        with torch.cuda.stream(self.copy):
-            h2d = self.stagings[k].upload()
-        rc = self._write_word(self._copy_h, self._ready_p[k], seq)
-        if rc:
-            raise _abi.PAError(rc, "pa_stream_write_value")
-        sy = self.syncs[k]
+        sy, io = self.syncs[k], self.copies[k]
         sy.ready_value = seq
         sy.done_value = seq
+        io.slot_reused = 1 if self.n >= self.depth else 0
         step()
-        rc = self._wait_word(self._back_h, self._done_p[k], seq)
-        if rc:
-            raise _abi.PAError(rc, "pa_stream_wait_value")
-        with torch.cuda.stream(self.back):
-            self.host_out[k].copy_(self.dev_out[k], non_blocking=True)
-        self.read_back[k].record(self.back)
         self.n += 1
-        return k, h2d, self.host_out[k].numel() * self.host_out[k].element_size()
+        return k, io.in_bytes, io.out_bytes
 
     def finish(self):
         """Make the caller's stream wait for every step and copy submitted so far."""

@@ -31,7 +31,7 @@ def header_functions():
 
 def test_header_and_binding_agree():
     names = header_functions()
-    assert len(names) == 22
+    assert len(names) == 24
     assert sorted(_abi.SIGNATURES) == names
 
 
@@ -119,6 +119,13 @@ def test_handshake_argument_errors(lib):
     # the synced step needs its sync words; stream word operations a 4-aligned word
     args = [FAKE] * 8 + [8, FAKE, 128, 2, 8, 2, 64, 16, 32, 0.125, 0, 0, 8, FAKE, 1 << 20, 0]
     assert lib.pa_decode_step_synced(*args, None, None) == _abi.PA_ERR_INVALID_ARG
+    # the pipelined step needs both its sync words and its copies
+    sync = _abi.StepSync(FAKE, FAKE, FAKE, 1, 1)
+    sp = ctypes.c_void_p(ctypes.addressof(sync))
+    assert lib.pa_decode_step_pipelined(*args, sp, None, None) == _abi.PA_ERR_INVALID_ARG
+    io = _abi.StepCopies(FAKE, FAKE, 0, FAKE, FAKE, 64, None, None, FAKE, 0)   # no input bytes
+    iop = ctypes.c_void_p(ctypes.addressof(io))
+    assert lib.pa_decode_step_pipelined(*args, sp, iop, None) == _abi.PA_ERR_INVALID_ARG
     assert lib.pa_stream_write_value(None, None, 1) == _abi.PA_ERR_INVALID_ARG
     assert lib.pa_stream_wait_value(None, FAKE + 2, 1) == _abi.PA_ERR_INVALID_ARG
 
