@@ -5,11 +5,13 @@ stream writes after the step's inputs, and signals a second word once its
 output is complete, so that a serving loop's compute stream holds only the
 steps' kernels.  The pipelined end-to-end tests (test_step_gpu.py) check its
 results step by step; these check the pieces: stream-ordered word writes and
-waits, the done signal of a step with nothing to attend, and a step whose
-upload never arrives: its attention launch gives up after the 2 s limit,
-reports a timeout, and the step still signals done, so a stream waiting on
-it never waits forever.
+waits, the done signal of a step with nothing to attend, a step whose upload
+never arrives (its attention launch gives up after the 2 s limit, reports a
+timeout, and the step still signals done, so a stream waiting on it never
+waits forever), the one-call pipelined step over E4M3 pools, and a
+pipelined call whose step is refused (it queues no wait for a done word).
 """
+import ctypes
 import time
 
 import pytest
@@ -126,3 +128,105 @@ def test_synced_call_argument_checks():
                             w.slot_mapping, w.block_tables, w.context_lens, w.max_context_len,
                             w.scale, 4, ws, sync=bad)
     assert e.value.code == _abi.PA_ERR_INVALID_ARG
+
+
+def test_pipelined_fp8_steps_match_direct_calls():
+    """StepPipeline over E4M3 pools with fused steps, each step one library
+    call (pa_decode_step_fp8_pipelined): every step uploads new lengths,
+    slots, rows and queries; outputs, codes and page scales must equal the
+    same fused steps called directly, step by step."""
+    from paged_kv_cache_179_gb300.step import StepPipeline
+    STEPS = 5
+    name = "qwen2_5_1_5b"
+    B = W.CONFIGS[name]["B"]
+    g = torch.Generator().manual_seed(21)
+    lens0 = (torch.randint(2, 60, (B,), generator=g) * 16
+             + torch.randint(1, 16 - STEPS + 1, (B,), generator=g))
+    w = W.make_workload(name, seed=5, lens_override=lens0.tolist())
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    specs = {k: (getattr(w, k).shape, getattr(w, k).dtype) for k in names}
+    kp, vp = w.k_cache.cuda(), w.v_cache.cuda()
+    kc = torch.empty(kp.shape, dtype=torch.uint8, device="cuda")
+    vc = torch.empty_like(kc)
+    ks = torch.empty(w.num_blocks, w.Hkv, dtype=torch.float32, device="cuda")
+    vs = torch.empty_like(ks)
+    _abi.pa_quantize_fp8(kp, vp, kc, vc, ks, vs)
+    ref_pools = [t.clone() for t in (kc, vc, ks, vs)]
+    max_ctx = int(lens0.max()) + STEPS
+    tables = w.block_tables
+    inputs = []
+    for n in range(STEPS):
+        lens = (lens0 + n).to(torch.int32)
+        last = lens.to(torch.int64) - 1
+        slots = tables[torch.arange(B), last // 16].to(torch.int64) * 16 + last % 16
+        inputs.append(dict(q=torch.randn(w.q.shape, generator=g).to(w.q.dtype),
+                           k_new=torch.randn(w.k_new.shape, generator=g).to(w.q.dtype),
+                           v_new=torch.randn(w.k_new.shape, generator=g).to(w.q.dtype),
+                           slot_mapping=slots, block_tables=tables, context_lens=lens))
+
+    def make_step(st):
+        return DecodeStep(k_cache=kc, v_cache=vc, k_scale=ks, v_scale=vs,
+                          block_tables=st.dev["block_tables"],
+                          context_lens=st.dev["context_lens"], max_context_len=max_ctx,
+                          scale=w.scale, num_q_heads=w.Hq, early_prologue=True)
+    pipe = StepPipeline(make_step, specs, w.q.shape, w.q.dtype, "cuda")
+    assert pipe.uses_device_handshake(fused=True)
+    got = []
+    for n in range(STEPS):
+        pipe.wait_slot_free()
+        for k in names:
+            pipe.stagings[pipe.slot()].host[k].copy_(inputs[n][k])
+        slot, _, _ = pipe.submit(fused=True)
+        pipe.read_back[slot].synchronize()
+        got.append(pipe.host_out[slot].clone())
+    pipe.finish()
+    torch.cuda.synchronize()
+    assert _abi.pa_get_status() == (0, 0)
+
+    rk, rv, rks, rvs = ref_pools
+    lens_d = torch.empty(B, dtype=torch.int32, device="cuda")
+    ref_step = DecodeStep(k_cache=rk, v_cache=rv, k_scale=rks, v_scale=rvs,
+                          block_tables=tables.cuda(), context_lens=lens_d,
+                          max_context_len=max_ctx, scale=w.scale, num_q_heads=w.Hq)
+    for n in range(STEPS):
+        lens_d.copy_(inputs[n]["context_lens"])
+        r = torch.empty_like(w.q, device="cuda")
+        d = {k: inputs[n][k].cuda() for k in ("q", "k_new", "v_new", "slot_mapping")}
+        ref_step.fused(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], r)
+        assert torch.equal(got[n].view(torch.int16), r.cpu().view(torch.int16)), n
+    for a, b in zip((kc, vc, ks, vs), (rk, rv, rks, rvs)):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+def test_pipelined_step_refused_launch_queues_no_wait():
+    """A pipelined call whose step cannot be launched (here: q heads not a
+    multiple of kv heads) returns the error after its upload and before it
+    queues the wait for a done word that would never come: the read-back
+    stream stays free."""
+    w = to_cuda(W.make_workload("tiny", seed=1))
+    words = torch.zeros(32, dtype=torch.int32, device="cuda")
+    sy = _sync(words, 1, 1)
+    host_in = torch.zeros(4096, dtype=torch.uint8).pin_memory()
+    dev_in = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(w.q)
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    copy, back = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = torch.cuda.Event()
+    ev.record(back)
+    io = _abi.StepCopies(host_in.data_ptr(), dev_in.data_ptr(), 4096, out.data_ptr(),
+                         host_out.data_ptr(), out.numel() * out.element_size(),
+                         copy.cuda_stream, back.cuda_stream, ev.cuda_event, 0)
+    ws = _abi.alloc_workspace(w.B, w.Hq, w.D, 4, "cuda")
+    lib = _abi.load()
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    rc = lib.pa_decode_step_pipelined(
+        P(out), P(w.q), P(w.k_new), P(w.v_new), P(w.k_cache), P(w.v_cache), P(w.slot_mapping),
+        P(w.block_tables), w.block_tables.shape[1], P(w.context_lens), w.max_context_len, w.B,
+        w.Hq - 1, w.Hkv, w.D, 16, w.num_blocks, w.scale, 0, 0, 4, P(ws),
+        ws.numel(), 0, ctypes.c_void_p(ctypes.addressof(sy)),
+        ctypes.c_void_p(ctypes.addressof(io)), None)
+    assert rc == _abi.PA_ERR_INVALID_ARG
+    back.synchronize()                     # nothing waits on the done word
+    copy.synchronize()
+    assert int(words[0]) == 1              # the upload's ready word was written
+    assert int(words[8]) == 0              # no step, no done signal
