@@ -645,6 +645,8 @@ def run_ours(args, rank, world, dev):
         "e2e": {"value": round(tokens_all * K / (e2e_ms_max / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "mode": e2e_mode},
         "gpu_launches": run.launches_per_step * K,
+        "device": {"name": torch.cuda.get_device_name(dev),
+                   "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count},
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_baseline(w, run.pools, args.cpu_budget, args.window)
