@@ -21,8 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpa.so")
 SOURCES = ["abi.cu", "append.cu", "quantize.cu", "decode.cu", "decode_t2.cu",
-           "decode_t4_16bit.cu", "decode_t4_e4m3.cu", "noalloc.cu", "copy.cu"]
-HEADERS = ["pa_launch.h", "pa_ptx.cuh", "pa_e4m3.cuh", "decode_kernels.cuh"]
+           "decode_t4_16bit.cu", "decode_t4_e4m3.cu", "decode_tc.cu", "noalloc.cu", "copy.cu"]
+HEADERS = ["pa_launch.h", "pa_ptx.cuh", "pa_e4m3.cuh", "pa_tc.cuh", "decode_kernels.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

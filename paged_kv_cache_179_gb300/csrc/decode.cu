@@ -89,6 +89,7 @@ void decode_workspace_split(DecodeArgs& a, void* ws) {
 
 cudaError_t launch_decode(const DecodeArgs& a, bool fp8, bool bf16, cudaStream_t s) {
   if (a.rows == 8) return launch_nt<1>(a, fp8, bf16, s);
+  if (decode_tc_eligible(a, fp8)) return launch_decode_tc(a, bf16, s);
   if (a.rows == 16) return launch_decode_tiles2(a, fp8, bf16, s);
   if (a.rows == 32)
     return fp8 ? launch_decode_tiles4_e4m3(a, bf16, s) : launch_decode_tiles4_16bit(a, bf16, s);

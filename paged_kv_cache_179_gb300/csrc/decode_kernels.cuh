@@ -490,7 +490,7 @@ __device__ __forceinline__ void attend_block_mt(WarpAcc<D> (&st)[NT], uint32_t q
 // of a segment is one context partition ("piece").  A segment inside one
 // worker's range is attended whole; one that crosses ranges is split into
 // pieces whose partial results are merged.  A worker walks its range in
-// chunks of at most kChunk blocks, one block id per lane.
+// chunks of at most kChunk blocks (CH), one block id per lane.
 constexpr int kChunk = 32;
 
 struct Chunk {
@@ -508,6 +508,7 @@ __device__ __forceinline__ int worker_of(int64_t x, int64_t W, int64_t N) {
   return static_cast<int>(((x + 1) * N - 1) / W);
 }
 
+template <int CH = kChunk>
 __device__ __forceinline__ Chunk first_chunk(int64_t lo, int64_t hi, const int* pf, int B,
                                              int Hkv) {
   Chunk x{0, 0, 0, 0};
@@ -523,10 +524,11 @@ __device__ __forceinline__ Chunk first_chunk(int64_t lo, int64_t hi, const int* 
   x.h = static_cast<int>((lo - pf[l]) / nbk);
   const int64_t s0 = pf[l] + static_cast<int64_t>(x.h) * nbk;
   x.cb0 = static_cast<int>(lo - s0);
-  x.nb = static_cast<int>(min(static_cast<int64_t>(kChunk), min(hi, s0 + nbk) - lo));
+  x.nb = static_cast<int>(min(static_cast<int64_t>(CH), min(hi, s0 + nbk) - lo));
   return x;
 }
 
+template <int CH = kChunk>
 __device__ __forceinline__ Chunk next_chunk(const Chunk& x, int64_t hi, const int* pf, int B,
                                             int Hkv) {
   Chunk y{0, 0, 0, 0};
@@ -535,7 +537,7 @@ __device__ __forceinline__ Chunk next_chunk(const Chunk& x, int64_t hi, const in
   int64_t s0 = pf[x.b] + static_cast<int64_t>(x.h) * nbk;
   const int pend = static_cast<int>(min(hi, s0 + nbk) - s0);
   const int n0 = x.cb0 + x.nb;
-  if (n0 < pend) return Chunk{x.b, x.h, n0, min(kChunk, pend - n0)};
+  if (n0 < pend) return Chunk{x.b, x.h, n0, min(CH, pend - n0)};
   int b = x.b, h = x.h + 1;
   if (h == Hkv) {
     h = 0;
@@ -546,7 +548,7 @@ __device__ __forceinline__ Chunk next_chunk(const Chunk& x, int64_t hi, const in
   nbk = seg_blocks(pf, b, Hkv);
   s0 = pf[b] + static_cast<int64_t>(h) * nbk;
   if (s0 >= hi) return y;
-  return Chunk{b, h, 0, static_cast<int>(min(static_cast<int64_t>(kChunk), min(hi, s0 + nbk) - s0))};
+  return Chunk{b, h, 0, static_cast<int>(min(static_cast<int64_t>(CH), min(hi, s0 + nbk) - s0))};
 }
 
 // The first block a sequence of L tokens attends: with a sliding window of
@@ -567,6 +569,13 @@ __device__ __forceinline__ int launch_len(const DecodeArgs& a, int raw) {
 // Blocks per kv head a sequence of launch length L puts in the block stream.
 __device__ __forceinline__ int stream_blocks(const DecodeArgs& a, int L) {
   return L > 0 ? ((L + 15) >> 4) - window_first_block(L, a.window, a.n_q) : 0;
+}
+// Units per kv head it puts in the stream the workers share: its blocks,
+// after a.seg_cost units that stand for a segment's fixed cost (a launch
+// whose workers pay one per segment evens out the cost, not the blocks).
+__device__ __forceinline__ int stream_units(const DecodeArgs& a, int L) {
+  const int n = stream_blocks(a, L);
+  return n > 0 ? n + a.seg_cost : 0;
 }
 
 // This lane's block id of chunk x (lane t holds block cb0 + t of the
@@ -1366,7 +1375,7 @@ merge_kernel(const DecodeArgs a) {
   // ---- the block stream: its length W and the start of sequence b's segments
   int before = 0, total = 0;
   for (int i = tid; i < a.B; i += blockDim.x) {
-    const int n = stream_blocks(a, launch_len(a, __ldg(a.context_lens + i))) * Hkv;
+    const int n = stream_units(a, launch_len(a, __ldg(a.context_lens + i))) * Hkv;
     total += n;
     before += i < b ? n : 0;
   }
@@ -1390,10 +1399,14 @@ merge_kernel(const DecodeArgs a) {
   int w0 = 0, np = 0, first_slot = 0;
   if (nbk > 0) {
     const int64_t W = total;
-    const int64_t NW = min(static_cast<int64_t>(a.split_ctas) * kWarps, W);
-    const int64_t s0 = before + static_cast<int64_t>(h) * nbk;
-    w0 = worker_of(s0, W, NW);
-    np = worker_of(s0 + nbk - 1, W, NW) - w0 + 1;
+    const int64_t NW = min(a.workers > 0 ? static_cast<int64_t>(a.workers)
+                                         : static_cast<int64_t>(a.split_ctas) * kWarps,
+                           W);
+    // the segment's units start at s0, its blocks at sb (after seg_cost units)
+    const int64_t s0 = before + static_cast<int64_t>(h) * (nbk + a.seg_cost);
+    const int64_t sb = s0 + a.seg_cost;
+    w0 = worker_of(sb, W, NW);
+    np = worker_of(sb + nbk - 1, W, NW) - w0 + 1;
     first_slot = s0 > worker_lo(w0, W, NW) ? 1 : 0;   // the segment is w0's last piece
   }
   PA_TRACE_ONLY(if (tid == 0 && blockIdx.x < 16384) {

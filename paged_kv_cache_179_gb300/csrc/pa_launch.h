@@ -54,6 +54,9 @@ struct DecodeArgs {
   int num_blocks;
   int max_context_len;
   int split_ctas;               // CTAs the batch's blocks are divided among
+  int workers;                  // workers they are divided among (0: split_ctas x 4 warps)
+  int seg_cost;                 // units each non-empty segment adds before its blocks in the
+                                // stream the workers share (0: the stream is blocks alone)
   int window;                   // sliding window in tokens (0: the whole context)
   int n_q;                      // query tokens this launch serves (n_q * group <= rows)
   int rows;                     // query rows per (sequence, kv head) a launch holds: 8, 16 or 32
@@ -94,6 +97,11 @@ cudaError_t launch_decode(const DecodeArgs& a, bool fp8, bool bf16, cudaStream_t
 cudaError_t launch_decode_tiles2(const DecodeArgs& a, bool fp8, bool bf16, cudaStream_t s);
 cudaError_t launch_decode_tiles4_16bit(const DecodeArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_decode_tiles4_e4m3(const DecodeArgs& a, bool bf16, cudaStream_t s);
+// The launch on the fifth-generation tensor cores (decode_tc.cu) for 17 to
+// 32 query rows per (sequence, kv head) over 16-bit pools at head_dim 128;
+// launch_decode takes it whenever decode_tc_eligible holds.
+bool decode_tc_eligible(const DecodeArgs& a, bool fp8);
+cudaError_t launch_decode_tc(const DecodeArgs& a, bool bf16, cudaStream_t s);
 // The merge launch alone (no attention launch writes its partials): the
 // failure-path test of its bounded poll.
 cudaError_t launch_merge_only(const DecodeArgs& a, bool bf16, cudaStream_t s);
