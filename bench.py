@@ -817,8 +817,12 @@ def run_multiquery(args, dev):
                               else "plain launches"),
                    **({"window": args.window} if args.window else {})},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
-                     "kernel": "decode_kernel (general masks), then merge_kernel",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": (load_traffic(f"{args.config}:q{n}", step.split_ctas)
+                                 if passes == 1 and not args.window else None),
+                     "kernel": (("decode_tc_kernel (tcgen05: 17-32 query rows per kv head)"
+                                 if w.D == 128 and per_pass * w.group > 16
+                                 else "decode_kernel (general masks)") + ", then merge_kernel"),
                      "bytes_per_launch": moved, "peak_source": peak_kind},
         "decode_us": {"mean": round(t * 1e6, 2),
                       "timing": ("K decodes back to back between two events" if back_to_back
@@ -851,7 +855,8 @@ def kernel_sha() -> str:
     h = hashlib.sha256()
     for p in ("paged_kv_cache_179_gb300/csrc/decode_kernels.cuh",
               "paged_kv_cache_179_gb300/csrc/decode.cu", "paged_kv_cache_179_gb300/csrc/pa_ptx.cuh",
-              "paged_kv_cache_179_gb300/csrc/pa_launch.h", "paged_kv_cache_179_gb300/csrc/pa_e4m3.cuh"):
+              "paged_kv_cache_179_gb300/csrc/pa_launch.h", "paged_kv_cache_179_gb300/csrc/pa_e4m3.cuh",
+              "paged_kv_cache_179_gb300/csrc/decode_tc.cu", "paged_kv_cache_179_gb300/csrc/pa_tc.cuh"):
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

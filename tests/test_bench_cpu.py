@@ -67,6 +67,9 @@ def test_committed_traffic_figures_are_consistent():
     for name, e in t.items():
         if name.startswith("_"):
             continue
-        assert name in W.CONFIGS
+        # "config" (the decode step) or "config:qN" (N query tokens per sequence)
+        config, _, queries = name.partition(":")
+        assert config in W.CONFIGS
+        assert queries == "" or (queries.startswith("q") and int(queries[1:]) >= 2)
         assert e["bytes_per_launch"] == e["read"] + e["write"]
         assert len(e["kernel_sha"]) == 16
