@@ -801,6 +801,7 @@ def run_multiquery(args, dev):
     achieved = moved / t / 1e9
     peak, peak_kind = measured_peaks()
     att = int(attended(lens, args.window).sum())
+    on_tc = w.D == 128 and per_pass * w.group > 16   # the tensor-core launch serves this pass
     return {
         "metric": "multi-token paged decode: attended (query token, KV token) pairs/s",
         "impl": "ours", "value": round(att * n / t, 1), "unit": "pairs/s", "n_gpus": 1,
@@ -818,11 +819,11 @@ def run_multiquery(args, dev):
                    **({"window": args.window} if args.window else {})},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": (load_traffic(f"{args.config}:q{n}", step.split_ctas)
+                     "traffic": (load_traffic(f"{args.config}:q{n}", step.split_ctas, tc=on_tc)
                                  if passes == 1 and not args.window else None),
                      "kernel": (("decode_tc_kernel (tcgen05: 17-32 query rows per kv head)"
-                                 if w.D == 128 and per_pass * w.group > 16
-                                 else "decode_kernel (general masks)") + ", then merge_kernel"),
+                                 if on_tc else "decode_kernel (general masks)")
+                                + ", then merge_kernel"),
                      "bytes_per_launch": moved, "peak_source": peak_kind},
         "decode_us": {"mean": round(t * 1e6, 2),
                       "timing": ("K decodes back to back between two events" if back_to_back
@@ -850,19 +851,22 @@ def describe(w, tokens):
             f"{tokens} attended tokens (max {w.max_context_len}), {w.num_blocks}-block pool")
 
 
-def kernel_sha() -> str:
+_DECODE_SOURCES = ("decode_kernels.cuh", "decode.cu", "pa_ptx.cuh", "pa_launch.h", "pa_e4m3.cuh")
+_TC_SOURCES = _DECODE_SOURCES + ("decode_tc.cu", "pa_tc.cuh")
+
+
+def kernel_sha(tc: bool = False) -> str:
+    """sha256 prefix of the sources of the decode launch (decode_kernel and the
+    merge), or with ``tc`` of the tensor-core launch as well."""
     import hashlib
     h = hashlib.sha256()
-    for p in ("paged_kv_cache_179_gb300/csrc/decode_kernels.cuh",
-              "paged_kv_cache_179_gb300/csrc/decode.cu", "paged_kv_cache_179_gb300/csrc/pa_ptx.cuh",
-              "paged_kv_cache_179_gb300/csrc/pa_launch.h", "paged_kv_cache_179_gb300/csrc/pa_e4m3.cuh",
-              "paged_kv_cache_179_gb300/csrc/decode_tc.cu", "paged_kv_cache_179_gb300/csrc/pa_tc.cuh"):
-        with open(os.path.join(ROOT, p), "rb") as f:
+    for name in (_TC_SOURCES if tc else _DECODE_SOURCES):
+        with open(os.path.join(ROOT, "paged_kv_cache_179_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def load_traffic(config, splits):
+def load_traffic(config, splits, tc: bool = False):
     """DRAM bytes per decode call from the committed ncu summary, when it
     matches this workload, CTA split and kernel source (else null)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -870,7 +874,7 @@ def load_traffic(config, splits):
         with open(path) as f:
             t = json.load(f)
         e = t.get(config)
-        if e and e.get("split_ctas") == splits and e.get("kernel_sha") == kernel_sha():
+        if e and e.get("split_ctas") == splits and e.get("kernel_sha") == kernel_sha(tc):
             return e.get("bytes_per_launch")
     except (OSError, ValueError):
         pass

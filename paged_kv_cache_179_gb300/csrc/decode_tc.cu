@@ -100,7 +100,7 @@ enum : int {
 // buffers and P (swizzled operands), then the small state.  The host sizes
 // the launch with the same function (plus 1024 bytes to align the base).
 struct TcLayout {
-  int q, p, bars, meta, flags, red, red2, mcol, colf, rowoff, misc, pf, len, total;
+  int q, p, bars, meta, flags, red, red2, mcol, colf, einv, rowoff, misc, pf, len, total;
 };
 template <int R>
 __host__ __device__ inline TcLayout tc_layout(int B) {
@@ -115,6 +115,7 @@ __host__ __device__ inline TcLayout tc_layout(int B) {
   l.red2 = o;  o += 4 * R * 4;
   l.mcol = o;  o += R * 4;
   l.colf = o;  o += R * 4;
+  l.einv = o;  o += R * 4;
   l.rowoff = o; o += R * 4;
   l.misc = o;  o += 16;
   l.pf = o;    o += round16((B + 1) * 4);
@@ -275,6 +276,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
   float* red2 = reinterpret_cast<float*>(smem + lay.red2); // [group][4][R/2] column sums
   float* mcol = reinterpret_cast<float*>(smem + lay.mcol); // [R] running max per row (log2 units)
   float* colf = reinterpret_cast<float*>(smem + lay.colf); // [R] per-row factor
+  float* einv = reinterpret_cast<float*>(smem + lay.einv); // [R] a finished piece's 1 / sum
   int* rowoff = reinterpret_cast<int*>(smem + lay.rowoff); // [R] output row offsets
   int* misc = reinterpret_cast<int*>(smem + lay.misc);     // [0] tmem base [1] dead [2] ready ok
   int* pf = reinterpret_cast<int*>(smem + lay.pf);
@@ -712,9 +714,39 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
     uint32_t sw[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) sw[j] = static_cast<uint32_t>(((((t >> 3) & 7) ^ j)) << 4);
+    bool bad = false;                     // this warp saw a wait give up
+    // a finished piece whose O^T is still to be read and stored
+    struct Epilogue {
+      int b, h, slot, chunk;
+      bool whole, pending;
+    } epi{0, 0, 0, 0, false, false};
+    // O^T of the finished piece, once its last PV product is done: the
+    // group's rows, as outputs (times the owner's 1 / sum) or as partials
+    auto store_piece = [&]() {
+      epi.pending = false;
+      const int q_end = min(c0 + RH, live);
+      if (bad || c0 >= q_end) return;
+      tc_fence_after();
+      uint16_t* out = static_cast<uint16_t*>(a.out) +
+                      (static_cast<int64_t>(epi.b) * a.q_tokens + a.q_first) * Hq * 128 +
+                      static_cast<int64_t>(epi.h) * G * 128 + t;
+      float* ws = a.ws_acc + piece_row(cta, epi.slot, 0, R) * 128 + t;
+      float o[RH];
+      tmem_ld<RH>(tl + kTcSBufs * R + c0, o);
+      tmem_wait_ld();
+#pragma unroll
+      for (int r = 0; r < RH; ++r) {
+        const int q = c0 + r;
+        if (q >= q_end) break;
+        if (epi.whole)
+          out[rowoff[q]] = static_cast<uint16_t>(pack2<BF16>(o[r] * einv[q], 0.f) & 0xFFFFu);
+        else
+          st_relaxed_b32(ws + q * 128, ws_enc(o[r]));
+      }
+      tc_fence_before();
+    };
     Chunk x = tc_first<kTcBlocks>(lo, hi, pf, B, Hkv, C);
     int i = 0, piece_no = 0;
-    bool bad = false;                     // this warp saw a wait give up
     while (x.nb > 0) {
       const int s = i % kTcStages;
       const int sb = i % kTcSBufs;
@@ -805,6 +837,8 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
       }
       // P (single buffer): the previous PV product must be done reading it
       if (i > 0 && !o_ready) bad |= !tc_wait_warp(bar(kBarODone), (i - 1) & 1, dead, a);
+      // the previous piece's O^T (before this chunk's PV product replaces it)
+      if (epi.pending) store_piece();
 #pragma unroll
       for (int r = 0; r < RH; r += 2) {
         const float p0 = fast_exp2(fmaf(v[r], sl2, -mo[r]));
@@ -839,59 +873,50 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
       if (lane == 0) mbar_arrive(bar(kBarPFull));
 
       if (plast) {
-        // ---- the piece's result for the group's rows.  Row sums: each
-        // warp's, then the row owner's total, its reciprocal and the row's
-        // output offset (or the partial's max and sum); then O^T once the
-        // piece's last PV is done, four columns at a time.
+        // ---- the piece's result for the group's rows, first half: row
+        // sums (each warp's, then the row owner's total: its reciprocal, or
+        // the partial's max and sum).  O^T is read in the next chunk, once
+        // the piece's last PV product is done (it is waited for there
+        // anyway), so the warps never wait for it here.
         float c[RH];
 #pragma unroll
         for (int r = 0; r < RH; ++r) c[r] = l[r];
         const float cs = warp_columns<RH, false>(c, lane);
         if (lane < RH) gred2[wq * RH + lane] = cs;
-        bad |= !tc_wait_warp(bar(kBarODone), i & 1, dead, a);
         named_bar_sync(bar_id, 128);
-        const bool whole = wh.whole;
-        const int slot = piece_no == 0 ? 0 : 1;
-        const bool keep = whole || a.ws_acc != nullptr;
-        if (!whole && a.ws_acc == nullptr && t == 0) atomicOr(a.status, kStatusNoWorkspace);
+        epi.b = x.b;
+        epi.h = x.h;
+        epi.whole = wh.whole;
+        epi.slot = piece_no == 0 ? 0 : 1;
+        epi.chunk = i;
+        epi.pending = true;
+        if (!epi.whole && a.ws_acc == nullptr) {
+          if (t == 0) atomicOr(a.status, kStatusNoWorkspace);
+          epi.pending = false;
+        }
         const int q_end = min(c0 + RH, live);
-        if (t < RH && c0 + t < q_end && keep) {
+        if (t < RH && c0 + t < q_end && epi.pending) {
           const int q = c0 + t;
           const float sum = (gred2[t] + gred2[RH + t]) + (gred2[2 * RH + t] + gred2[3 * RH + t]);
-          if (whole) {
-            colf[q] = sum > 0.f ? __frcp_rn(sum) : 0.f;
+          if (epi.whole) {
+            einv[q] = sum > 0.f ? __frcp_rn(sum) : 0.f;
           } else if (!bad) {
             // a split segment: the merge launch combines its pieces
-            st_relaxed_v2(a.ws_ml + piece_row(cta, slot, q, R) * 2, ws_enc(mcol[q]), ws_enc(sum));
+            st_relaxed_v2(a.ws_ml + piece_row(cta, epi.slot, q, R) * 2, ws_enc(mcol[q]),
+                          ws_enc(sum));
           }
         }
-        named_bar_sync(bar_id, 128);
-        if (!bad && keep) {
-          tc_fence_after();
-          uint16_t* out = static_cast<uint16_t*>(a.out) +
-                          (static_cast<int64_t>(x.b) * a.q_tokens + a.q_first) * Hq * 128 +
-                          static_cast<int64_t>(x.h) * G * 128 + t;
-          float* ws = a.ws_acc + piece_row(cta, slot, 0, R) * 128 + t;
-          float o[RH];
-          tmem_ld<RH>(tl + kTcSBufs * R + c0, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int r = 0; r < RH; ++r) {
-            const int q = c0 + r;
-            if (q >= q_end) break;
-            if (whole)
-              out[rowoff[q]] = static_cast<uint16_t>(pack2<BF16>(o[r] * colf[q], 0.f) & 0xFFFFu);
-            else
-              st_relaxed_b32(ws + q * 128, ws_enc(o[r]));
-          }
-        }
-        tc_fence_before();
         ++piece_no;
         reset_rows();
         if (t < RH) mcol[c0 + t] = -INFINITY;
       }
       x = tc_next<kTcBlocks>(x, hi, pf, B, Hkv, C);
       ++i;
+    }
+    if (epi.pending) {                    // the last piece: its O^T once its PV is done
+      bad |= !tc_wait_warp(bar(kBarODone), epi.chunk & 1, dead, a);
+      named_bar_sync(bar_id, 128);        // the owners' reciprocals are visible
+      store_piece();
     }
   }
   // ---- teardown: every role has left its loop with nothing in flight

@@ -53,11 +53,11 @@ def test_traffic_used_only_for_its_sources(tmp_path, monkeypatch):
     entry = {"split_ctas": 304, "kernel_sha": "abc", "bytes_per_launch": 123}
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"cfg": entry}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "kernel_sha", lambda: "abc")
+    monkeypatch.setattr(bench, "kernel_sha", lambda tc=False: "abc")
     assert bench.load_traffic("cfg", 304) == 123
     assert bench.load_traffic("cfg", 456) is None         # another CTA split
     assert bench.load_traffic("other", 304) is None
-    monkeypatch.setattr(bench, "kernel_sha", lambda: "def")
+    monkeypatch.setattr(bench, "kernel_sha", lambda tc=False: "def")
     assert bench.load_traffic("cfg", 304) is None         # the kernel changed since
 
 
