@@ -244,7 +244,11 @@ size_t pa_decode_workspace_size_rows(int num_seqs, int num_q_heads, int head_dim
  *   run as consecutive passes of 32 / group tokens, each reading the K/V
  *   again (pa_decode_noalloc rejects more than 8 rows with
  *   PA_ERR_UNSUPPORTED).  Launches with more than 8 rows hold two CTAs per
- *   SM whatever the pool type (split_ctas 0 then means two per SM);
+ *   SM whatever the pool type (split_ctas 0 then means two per SM).  Over
+ *   16-bit pools at head_dim 128, a launch with 17 to 32 rows runs its
+ *   products on the fifth-generation tensor cores instead (tcgen05, one CTA
+ *   of ten warps per SM): the batch is then divided among min(SMs,
+ *   4 * split_ctas) CTAs, with the same workspace and merge;
  *   workspace: at least pa_decode_workspace_size_rows(..., query_rows) bytes
  *   (pa_decode_workspace_size(...) when query_rows <= 8), 256-byte aligned;
  *   flags: 0, or PA_DECODE_EARLY_PROLOGUE: the attention launch becomes a

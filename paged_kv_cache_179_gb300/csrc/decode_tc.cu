@@ -380,11 +380,10 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
   tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
 
-  // the piece a chunk belongs to: its segment's first block in the stream
-  // (s0), its blocks (nbk) and where the piece ends (pend, from s0)
-  // (s0: the first unit of its blocks, nbk: its blocks, pend: where the
-  // piece ends, in blocks from the segment's first; whole: the segment's
-  // blocks all lie in this worker's range)
+  // the piece a chunk belongs to -- s0: the first unit of its segment's
+  // blocks, nbk: the segment's blocks, pend: where the piece ends, in blocks
+  // from the segment's first; whole: the segment's blocks all lie in this
+  // worker's range
   struct Where {
     int nbk, pend;
     int64_t s0;
