@@ -336,8 +336,33 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
   }
   const int64_t W = pf[B];
   const int cta = blockIdx.x;
+  const int C = a.seg_cost;
+  const int64_t NW = min(static_cast<int64_t>(gridDim.x), W);   // never more workers than units
+  const int64_t lo = worker_lo(cta, W, NW), hi = worker_lo(cta + 1, W, NW);
+  auto first_block = [&](int b) {   // the segment's first block in the sequence
+    return a.window > 0 ? window_first_block(len[b], a.window, a.n_q) : 0;
+  };
   griddep_launch_dependents();
-  if (a.early) griddep_wait();
+  if (a.early) {
+    // With an early prologue, while the kernel before ends: ask L2 for this
+    // worker's first 16 K/V tiles and its first piece's query rows (a
+    // prefetch reads nothing into the SM, so what that kernel writes before
+    // it completes is still what the copies read; the block ids come from
+    // the tables, which that kernel does not write).
+    if (warp == kTcCopyWarp && cta < NW) {
+      const Chunk c = tc_first<kChunk>(lo, hi, pf, B, Hkv, C);
+      if (c.nb > 0) {
+        const int id = load_chunk_id(a, c, first_block(c.b), lane);
+        if (lane < min(c.nb, 16) && id >= 0 && id < a.num_blocks) {
+          const int64_t tile = static_cast<int64_t>(id) * Hkv + c.h;
+          prefetch_l2(static_cast<const uint8_t*>(a.k_cache) + tile * 4096, 4096);
+          prefetch_l2(static_cast<const uint8_t*>(a.v_cache) + tile * 4096, 4096);
+        }
+        prefetch_query_l2<128>(a, c.b, c.h, lane);
+      }
+    }
+    griddep_wait();
+  }
   // sequences with nothing to attend: a zero output (the softmax warps)
   if (warp < 4 * kTcGroups) {
     for (int b = cta * 4 * kTcGroups + warp; b < B;
@@ -350,11 +375,8 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
       for (int i = lane; i < a.n_q * Hq * 128; i += 32) o[i] = 0;
     }
   }
-  // ---- 2. this CTA's share of the block stream (never more workers than blocks)
-  const int C = a.seg_cost;
-  const int64_t NW = min(static_cast<int64_t>(gridDim.x), W);
+  // ---- 2. this CTA's share of the stream
   if (cta >= NW) return;
-  const int64_t lo = worker_lo(cta, W, NW), hi = worker_lo(cta + 1, W, NW);
 
   if (tid == 0) {
     for (int i = 0; i < kBarCount; ++i) {
@@ -396,9 +418,6 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
     w.pend = static_cast<int>(min(hi, w.s0 + w.nbk) - w.s0);
     w.whole = w.s0 >= lo && w.s0 + w.nbk <= hi;
     return w;
-  };
-  auto first_block = [&](int b) {   // the segment's first block in the sequence
-    return a.window > 0 ? window_first_block(len[b], a.window, a.n_q) : 0;
   };
 
   if (warp == kTcCopyWarp) {
