@@ -261,6 +261,7 @@ def reduce_over_ranks(step_ms: float, e2e_ms: float, tokens: int, world: int, de
 
 # ---------------------------------------------------------------- our arm
 OTHER_CONFIGS = ("tiny", "smollm2_360m", "qwen2_5_1_5b", "qwen2_5_7b_fp8")
+MULTIQUERY_RUNS = (("qwen2_5_7b", 4), ("mqa_32x1", 1))
 
 
 class ConfigRun:
@@ -666,12 +667,37 @@ def run_ours(args, rank, world, dev):
         for name in OTHER_CONFIGS:
             others[name] = measure_other_config(args, name, dev, clocks, peak)
             line["gpu_launches_all_configs"] += others[name]["gpu_launches"]
+        # several query rows per (sequence, kv head), decode only: 4 draft
+        # tokens on the 7B batch (28 rows) and multi-query attention (32
+        # heads on one kv head), both on the tensor-core launch
+        multi = {}
+        for name, n in MULTIQUERY_RUNS:
+            sub = argparse.Namespace(**vars(args))
+            sub.config, sub.queries = name, n
+            clocks.mark(f"{name}:q{n}:start")
+            r = run_multiquery(sub, dev)
+            clocks.mark(f"{name}:q{n}:end")
+            multi[f"{name}:q{n}"] = {
+                "workload": r["config"]["workload"], "queries_per_seq": n,
+                "metric": r["metric"], "value": r["value"], "unit": r["unit"],
+                "decode_us": r["decode_us"], "split_ctas": r["config"]["split_ctas"],
+                "l2": r["config"]["l2"], "launch": r["config"]["launch"],
+                "roofline": r["roofline"], "gpu_launches": r["gpu_launches"],
+                "clocks_marks": (f"{name}:q{n}:start", f"{name}:q{n}:end")}
+            line["gpu_launches_all_configs"] += r["gpu_launches"]
+            gc.collect()
+            torch.cuda.synchronize(dev)
+            torch.cuda.empty_cache()
     line["clocks"] = clocks.stop()
     if others:
         for name, e in others.items():
             start, end = e.pop("clocks_marks")
             e["clocks"] = clocks.summary(start, end, before=start)
         line["configs"] = others
+        for name, e in multi.items():
+            start, end = e.pop("clocks_marks")
+            e["clocks"] = clocks.summary(start, end, before=start)
+        line["multiquery"] = multi
     return line
 
 
@@ -974,7 +1000,9 @@ def main(argv=None):
     ap.add_argument("--configs", choices=["all", "none"], default="all",
                     help="all: the default single-GPU run also times the other four configs "
                          "(tiny, SmolLM2-360M, Qwen2.5-1.5B, E4M3 Qwen2.5-7B) one after another "
-                         "and reports them under 'configs'")
+                         "and reports them under 'configs', and two batches with several "
+                         "query rows per kv head (4 query tokens on the 7B batch, MQA 32 x 1) "
+                         "under 'multiquery'")
     ap.add_argument("--handshake", choices=["auto", "device", "events"], default="auto",
                     help="how the pipelined end-to-end steps order their copies: a device-side "
                          "handshake (auto: when the driver offers stream memory operations) or "
