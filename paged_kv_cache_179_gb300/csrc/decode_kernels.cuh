@@ -1319,9 +1319,12 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
 
   if constexpr (NT > 1) cp_async_wait_all();   // no query-buffer copy outlives the warp
   if (dead) {
-    // Wait (bounded) for this warp's copies still in flight.
+    // Wait (bounded, never shorter than the default limit, whatever a test
+    // set) for this warp's copies still in flight: none may land in shared
+    // memory after the CTA has left it.
+    const uint64_t drain = a.wait_limit_ns > kWaitLimitNs ? a.wait_limit_ns : kWaitLimitNs;
     for (; computed < issued; ++computed)
-      (void)mbar_wait(sbar + 8 * (computed % STAGES), (computed / STAGES) & 1, a.wait_limit_ns);
+      (void)mbar_wait(sbar + 8 * (computed % STAGES), (computed / STAGES) & 1, drain);
   }
 
   PA_TRACE_WARP(gw, 3, pa_now());

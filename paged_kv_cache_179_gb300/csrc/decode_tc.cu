@@ -37,8 +37,12 @@
 //    written.  Warps 0-7 run the softmax in two warpgroups, each on 16 of the
 //    query rows, thread t of a group on tensor-memory lane t: token t of the
 //    chunk for S, head_dim element t for O.  They read S^T with tcgen05.ld,
-//    mask it, exponentiate, write P and keep per-thread row sums; at a piece's
-//    end they read O^T and store the output or the split piece's partial.
+//    mask it, exponentiate, write P and keep per-thread row sums.  At a
+//    piece's last chunk they reduce the row sums; its O^T is read and stored
+//    (the output, or the split piece's partial) in the next chunk, once the
+//    piece's last PV product is done, which that chunk waits for anyway.
+//  * With an early prologue, the TMA warp asks L2 for its first 16 K/V tiles
+//    and first query rows while the kernel before ends.
 //  * The softmax offset of a query row moves only when a score of the chunk
 //    exceeds it by more than kTcSlack (log2 units).  Then the group's four
 //    warps reduce the exact running maximum, scale the row sums and O^T (in
@@ -512,11 +516,13 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
       if (n32.nb > 0 && n32.cb0 == 0) prefetch_query_l2<128>(a, n32.b, n32.h, lane);
     }
     if (ok && v_done < i) issue_v();      // the last chunk's V
-    // no copy outlives the CTA: wait (bounded) for each buffer's last fill
+    // no copy outlives the CTA: wait (bounded, never shorter than the
+    // default limit, whatever a test set) for each buffer's last fill
     const uint64_t t0 = global_ns();
+    const uint64_t drain = a.wait_limit_ns > kWaitLimitNs ? a.wait_limit_ns : kWaitLimitNs;
     auto settle = [&](uint32_t b, int fills) {
       if (fills <= 0) return;
-      while (!mbar_try_wait(b, (fills - 1) & 1) && global_ns() - t0 < a.wait_limit_ns) {
+      while (!mbar_try_wait(b, (fills - 1) & 1) && global_ns() - t0 < drain) {
       }
     };
     if (lane == 0) {
@@ -687,12 +693,14 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
       __nanosleep(32);
     }
     (void)ok;
-    // no MMA outlives the CTA: wait (bounded) for all of them
+    // no MMA outlives the CTA: wait (bounded, never shorter than the
+    // default limit) for all of them
     if (issued) {
       if (lane == 0) {
         umma_commit(bar(kBarFin));
         const uint64_t t0 = global_ns();
-        while (!mbar_try_wait(bar(kBarFin), 0) && global_ns() - t0 < a.wait_limit_ns) {
+        const uint64_t drain = a.wait_limit_ns > kWaitLimitNs ? a.wait_limit_ns : kWaitLimitNs;
+        while (!mbar_try_wait(bar(kBarFin), 0) && global_ns() - t0 < drain) {
         }
       }
       __syncwarp();
