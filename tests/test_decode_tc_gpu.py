@@ -5,8 +5,10 @@ query groups of 20).  The general cases of that row range run in
 test_query_tiles_gpu.py and test_multiquery_gpu.py; these add the full-size
 batches on sampled sequences, the fused append + decode step in bf16 with an
 early prologue, the device-side handshake (equal results, and an upload
-that never arrives), empty and one-token contexts, a bad block id, and
-run-to-run determinism -- every result against the fp64 oracle.
+that never arrives), empty and one-token contexts, a bad block id,
+run-to-run determinism, and a sweep over 17 to 32 rows (odd groups, up to
+32 query tokens, windows, NaN in unused pool rows) -- every result against
+the fp64 oracle.
 """
 import math
 import time
@@ -213,3 +215,55 @@ def test_results_are_deterministic():
     assert _abi.pa_get_status() == (0, 0)
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
     assert torch.equal(outs[0].view(torch.int16), outs[2].view(torch.int16))
+
+
+def _rows_case(seed, B, nq, G, D, max_len, dtype):
+    g = torch.Generator().manual_seed(seed)
+    lens = torch.randint(max(1, nq), max_len + 1, (B,), generator=g).to(torch.int32)
+    nblk = (lens + 15) // 16
+    NB = int(nblk.sum()) + 3
+    perm = torch.randperm(NB, generator=g).to(torch.int32)
+    tables = torch.full((B, int(nblk.max())), -1, dtype=torch.int32)
+    c = 0
+    for b in range(B):
+        tables[b, :nblk[b]] = perm[c:c + nblk[b]]
+        c += int(nblk[b])
+    Hkv = 2
+    shape = (B, G * Hkv, D) if nq == 1 else (B, nq, G * Hkv, D)
+    q = torch.randn(*shape, generator=g).to(dtype)
+    kp = torch.randn(NB, Hkv, 16, D, generator=g).to(dtype)
+    vp = torch.randn(NB, Hkv, 16, D, generator=g).to(dtype)
+    # rows past each context's end hold NaN: they must not reach any output
+    for b in range(B):
+        L = int(lens[b])
+        if L % 16:
+            blk = int(tables[b, L // 16])
+            kp[blk, :, L % 16:] = float("nan")
+            vp[blk, :, L % 16:] = float("nan")
+    return q, kp, vp, tables, lens
+
+
+# (n_q, G): 17 to 32 rows per kv head, odd groups, dead columns, several
+# tokens (causal among them), windows shorter than a block and than a chunk
+@pytest.mark.parametrize("seed,nq,G,window,splits,dtype", [
+    (80, 1, 17, 0, 0, torch.float16), (81, 1, 23, 0, 5, torch.bfloat16),
+    (82, 1, 31, 0, 2, torch.float16), (83, 3, 6, 0, 0, torch.float16),
+    (84, 2, 9, 0, 11, torch.bfloat16), (85, 5, 5, 0, 0, torch.float16),
+    (86, 8, 4, 0, 3, torch.float16), (87, 4, 8, 7, 0, torch.bfloat16),
+    (88, 2, 13, 130, 9, torch.float16), (89, 3, 9, 300, 0, torch.float16),
+    (90, 32, 1, 0, 0, torch.float16), (91, 16, 2, 50, 6, torch.bfloat16)])
+def test_row_counts_17_to_32_match_oracle(seed, nq, G, window, splits, dtype):
+    B, D = 5, 128
+    q, kp, vp, tables, lens = _rows_case(seed, B, nq, G, D, 900, dtype)
+    Hq = G * 2
+    scale = float(np.float32(1 / math.sqrt(D)))
+    bf16 = dtype == torch.bfloat16
+    ref = oracle.decode(to_np16(q), to_np16(kp), to_np16(vp), tables.numpy(), lens.numpy(), scale,
+                        bf16=bf16, window=window)
+    out = torch.full_like(q, float("nan"), device="cuda")
+    ws = _abi.alloc_workspace(B, Hq, D, splits, "cuda", query_rows=nq * G)
+    _abi.pa_decode(out, q.cuda(), kp.cuda(), vp.cuda(), tables.cuda(), lens.cuda(),
+                   int(lens.max()), scale, splits, ws, window=window)
+    assert _abi.pa_get_status() == (0, 0)
+    assert max_err(out, ref) <= TOL["bf16" if bf16 else "f16"]
+    assert int(ws.count_nonzero()) == 0     # the merge left the workspace zero-filled
