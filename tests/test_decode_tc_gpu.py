@@ -267,3 +267,34 @@ def test_row_counts_17_to_32_match_oracle(seed, nq, G, window, splits, dtype):
     assert _abi.pa_get_status() == (0, 0)
     assert max_err(out, ref) <= TOL["bf16" if bf16 else "f16"]
     assert int(ws.count_nonzero()) == 0     # the merge left the workspace zero-filled
+
+
+def test_contexts_shorter_than_the_query_tokens():
+    # 8 query tokens x a group of 4 = 32 rows; queries before position 0 see
+    # nothing and return zeros, the rest attend causally what exists
+    B, nq, G, Hkv, D = 6, 8, 4, 2, 128
+    lens = [1, 3, 7, 8, 9, 200]
+    g = torch.Generator().manual_seed(95)
+    lt = torch.tensor(lens, dtype=torch.int32)
+    nblk = (lt + 15) // 16
+    NB = int(nblk.sum()) + 2
+    perm = torch.randperm(NB, generator=g).to(torch.int32)
+    tables = torch.full((B, int(nblk.max())), -1, dtype=torch.int32)
+    c = 0
+    for b in range(B):
+        tables[b, :nblk[b]] = perm[c:c + nblk[b]]
+        c += int(nblk[b])
+    q = torch.randn(B, nq, G * Hkv, D, generator=g).half()
+    kp = torch.randn(NB, Hkv, 16, D, generator=g).half()
+    vp = torch.randn(NB, Hkv, 16, D, generator=g).half()
+    scale = float(np.float32(1 / math.sqrt(D)))
+    ref = oracle.decode(to_np16(q), to_np16(kp), to_np16(vp), tables.numpy(), lt.numpy(), scale)
+    out = torch.full_like(q, float("nan"), device="cuda")
+    ws = _abi.alloc_workspace(B, G * Hkv, D, 3, "cuda", query_rows=nq * G)
+    _abi.pa_decode(out, q.cuda(), kp.cuda(), vp.cuda(), tables.cuda(), lt.cuda(), 200, scale, 3, ws)
+    assert _abi.pa_get_status() == (0, 0)
+    got = out.float().cpu().numpy()
+    for b, L in enumerate(lens):
+        if L < nq:
+            assert np.all(got[b, :nq - L] == 0)     # the queries before position 0
+    assert np.abs(got - ref).max() <= TOL["f16"]
