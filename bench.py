@@ -480,18 +480,24 @@ def measure_e2e(args, run, dev):
     made = []
     fused, copies = run.fused, run.copies
 
+    shared_ws = []
+
     def make_step(staging):
         ps = run.pool_sets[len(made) % copies]
         made.append(staging)
         # the pipeline orders each step after its upload and after the last
         # read-back of its slot by events; with those between two steps the
         # attention launch starts once the previous merge has completed, early
-        # prologue or not (a full dependency, which it does not relax)
-        return DecodeStep(**ps, block_tables=staging.dev["block_tables"],
-                          context_lens=staging.dev["context_lens"],
-                          max_context_len=w.max_context_len, scale=w.scale, num_q_heads=w.Hq,
-                          split_ctas=args.splits, window=run.window,
-                          early_prologue=run.early)
+        # prologue or not (a full dependency, which it does not relax).  The
+        # slots' steps run one after another, so they share one workspace.
+        st = DecodeStep(**ps, block_tables=staging.dev["block_tables"],
+                        context_lens=staging.dev["context_lens"],
+                        max_context_len=w.max_context_len, scale=w.scale, num_q_heads=w.Hq,
+                        split_ctas=args.splits, window=run.window,
+                        early_prologue=run.early,
+                        workspace=shared_ws[0] if shared_ws else None)
+        shared_ws[:1] = [st.workspace]
+        return st
     h2d = d2h = 0
     host_us = None
     if run.back_to_back:

@@ -24,7 +24,7 @@ class DecodeStep:
 
     def __init__(self, *, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
                  num_q_heads, k_scale=None, v_scale=None, split_ctas=0, window=0,
-                 early_prologue=False, queries_per_seq=1):
+                 early_prologue=False, queries_per_seq=1, workspace=None):
         self.kv = "fp8" if k_cache.dtype == torch.uint8 else "16"
         self.k_cache, self.v_cache = k_cache, v_cache
         self.k_scale, self.v_scale = k_scale, v_scale
@@ -44,8 +44,19 @@ class DecodeStep:
         # the attention launch's prologue may overlap the kernel before it on
         # the stream (which must then not write context_lens or block_tables)
         self.early_prologue = bool(early_prologue)
-        self.workspace = _abi.alloc_workspace(self.B, self.Hq, self.D, self.split_ctas,
-                                              k_cache.device, query_rows=rows)
+        # The split-K workspace: zero-filled, left zero-filled by every call.
+        # Steps that run one after another on one stream (the slots of a
+        # StepPipeline) may share one (``workspace``: a uint8 device tensor of
+        # at least pa_decode_workspace_size_rows bytes), which keeps it hot in
+        # L2 for all of them.
+        need = _abi.pa_decode_workspace_size_rows(self.B, self.Hq, self.D, self.split_ctas, rows)
+        if workspace is not None:
+            if workspace.numel() * workspace.element_size() < need or workspace.device != k_cache.device:
+                raise ValueError(f"workspace too small or on another device: {need} bytes needed")
+            self.workspace = workspace
+        else:
+            self.workspace = _abi.alloc_workspace(self.B, self.Hq, self.D, self.split_ctas,
+                                                  k_cache.device, query_rows=rows)
         self._bound = {}     # run_from_staging's bound steps
 
     def append(self, k_new, v_new, slot_mapping):
@@ -228,7 +239,9 @@ class StepPipeline:
     full dependency, which the early prologue does not relax).
 
     ``make_step(staging)`` builds the DecodeStep for one staging (bound to its
-    device block_tables and context_lens; the pools are shared).  The caller
+    device block_tables and context_lens; the pools are shared, and the steps
+    may share one workspace: they run one after another on the compute
+    stream).  The caller
     fills ``stagings[k].host`` before ``submit`` uses slot k (``slot()`` says
     which; ``wait_slot_free()`` waits until its last upload has finished)."""
 

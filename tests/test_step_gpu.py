@@ -228,15 +228,17 @@ def test_bound_step_records_once_and_matches_direct_calls():
         assert torch.equal(w.v_cache.view(torch.int16), v2.view(torch.int16))
 
 
-@pytest.mark.parametrize("handshake", ["events", "device"])
-def test_step_pipeline_early_prologue_new_lengths_each_step(handshake):
+@pytest.mark.parametrize("handshake,shared", [("events", False), ("device", False),
+                                              ("events", True), ("device", True)])
+def test_step_pipeline_early_prologue_new_lengths_each_step(handshake, shared):
     """StepPipeline with the early prologue: every step uploads new context
     lengths and slots (one token more each step), so a prologue that read
     its slot's lengths before that upload had landed would attend the wrong
     contexts.  The uploads are ordered before the step by events, which the
     early prologue does not relax: the outputs and pools must equal plain
     direct steps on the same inputs, step by step.  With the device-side
-    handshake the attention launch itself waits for the upload's word."""
+    handshake the attention launch itself waits for the upload's word.
+    ``shared``: both slots' steps use one split-K workspace."""
     from paged_kv_cache_179_gb300.step import StepPipeline
     STEPS = 6
     name = "qwen2_5_1_5b"
@@ -261,12 +263,18 @@ def test_step_pipeline_early_prologue_new_lengths_each_step(handshake):
                            v_new=torch.randn(w.k_new.shape, generator=g).to(w.q.dtype),
                            slot_mapping=slots, block_tables=tables, context_lens=lens))
 
+    made = []
+
     def make_step(st):
-        return DecodeStep(k_cache=kc, v_cache=vc, block_tables=st.dev["block_tables"],
-                          context_lens=st.dev["context_lens"], max_context_len=max_ctx,
-                          scale=w.scale, num_q_heads=w.Hq, early_prologue=True)
+        s = DecodeStep(k_cache=kc, v_cache=vc, block_tables=st.dev["block_tables"],
+                       context_lens=st.dev["context_lens"], max_context_len=max_ctx,
+                       scale=w.scale, num_q_heads=w.Hq, early_prologue=True,
+                       workspace=made[0].workspace if shared and made else None)
+        made.append(s)
+        return s
     pipe = StepPipeline(make_step, specs, w.q.shape, w.q.dtype, "cuda", handshake=handshake)
     assert pipe.uses_device_handshake() == (handshake == "device")
+    assert (made[0].workspace.data_ptr() == made[1].workspace.data_ptr()) == shared
     got = [None] * STEPS
     pending = None
     for n in range(STEPS):
@@ -297,3 +305,19 @@ def test_step_pipeline_early_prologue_new_lengths_each_step(handshake):
         ref_step(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], r)
         assert torch.equal(got[n].view(torch.int16), r.cpu().view(torch.int16)), n
     assert torch.equal(kc.view(torch.int16), k2.view(torch.int16))
+
+
+def test_step_rejects_a_workspace_too_small():
+    """DecodeStep(workspace=...): a buffer smaller than the launch's split-K
+    workspace is refused before anything runs."""
+    w = to_cuda(W.make_workload("qwen2_5_1_5b", seed=12))
+    kw = dict(k_cache=w.k_cache, v_cache=w.v_cache, block_tables=w.block_tables,
+              context_lens=w.context_lens, max_context_len=w.max_context_len,
+              scale=w.scale, num_q_heads=w.Hq)
+    full = DecodeStep(**kw)
+    n = full.workspace.numel() * full.workspace.element_size()
+    assert n > 4096
+    with pytest.raises(ValueError):
+        DecodeStep(**kw, workspace=torch.zeros(n - 16, dtype=torch.uint8, device="cuda"))
+    ok = DecodeStep(**kw, workspace=full.workspace)
+    assert ok.workspace.data_ptr() == full.workspace.data_ptr()
