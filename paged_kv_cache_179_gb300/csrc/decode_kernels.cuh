@@ -1337,12 +1337,22 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
 // ------------------------------------------------------------ merge launch
 // The log-sum-exp merge of each split segment's pieces:
 //   out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p
-// (log2 units).  One CTA per (sequence, kv head, chunk of query rows: 8 at
-// head_dim 128, 16 at 64); thread (g, d4) owns output columns 4*d4 ..
-// 4*d4+3 of query row g and folds the pieces in worker order, kMergeBatch at
-// a time (their loads in flight together), rescaling its running state to
-// each batch's maximum: a fixed order, so results are deterministic.
-// Segments attended whole by one worker are skipped.
+// (log2 units).  One CTA per (sequence, kv head, run of query rows); thread
+// (j, g, d4) owns output columns 4*d4 .. 4*d4+3 of query row g within piece
+// group j.  The segment's pieces are dealt in rounds of groups x kMergeBatch:
+// group j takes pieces j*kMergeBatch .. of each round, so a round has the
+// loads of up to 16 pieces in flight at once (a round costs about one L2
+// round trip, however many of its pieces a thread folds).  Each group folds
+// its pieces in order, rescaling its running state to each batch's maximum;
+// at the end group 0 folds the other groups' states in group order: a fixed
+// order, so results are deterministic.  Segments attended whole by one
+// worker are skipped.
+//
+// The number of groups is the launch's (launch_merge): several only for
+// partials of 8 rows (16 or 32 rows fill a CTA already, and their workers
+// hold long shares, so few pieces), and only while the grid stays small
+// (a batch of few sequences and kv heads, whose segments are split into
+// many short pieces); the kernel reads it from its shape.
 //
 // The launch runs beside the attention grid: it is scheduled once every
 // attention CTA has passed its prologue, so it never holds resources an
@@ -1350,16 +1360,24 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
 // context lengths, as each attention CTA did, and reads its pieces as they
 // are written (a zero word is a partial not written yet): a segment is
 // merged as soon as its last piece lands, and only the segments of the last
-// warps to finish are merged after the attention ends.  While a batch is
-// incomplete, warp 0 polls the first word of each missing piece, so waiting
-// costs one load per piece per poll.  The CTA zeroes the partials it read.
-// The last CTA ends with griddepcontrol.wait: the launch completes after the
-// attention grid has completed and its writes are visible.
+// warps to finish are merged after the attention ends.  While a round is
+// incomplete, warp 0 polls the first word of each missing piece (lane j:
+// piece j of the round), so waiting costs one load per piece per poll.  The
+// CTA zeroes the partials it read.  The last CTA ends with
+// griddepcontrol.wait: the launch completes after the attention grid has
+// completed and its writes are visible.
+//
+// A CTA has at most kMergeThreads threads and registers for two per SM, so
+// that one fits beside an attention CTA that has not finished.
 constexpr int kMergeThreads = 256;
 #ifndef PA_MERGE_BATCH
 #define PA_MERGE_BATCH 8
 #endif
-constexpr int kMergeBatch = PA_MERGE_BATCH;
+constexpr int kMergeBatch = PA_MERGE_BATCH;       // pieces a thread loads at once
+constexpr int kMergeMaxGroups = 2;
+static_assert(kMergeMaxGroups * kMergeBatch <= 32, "one poll lane per piece of a round");
+// merge CTAs per SM the launch keeps to when it chooses several groups
+constexpr int kMergeCtasPerSm = 4;
 
 template <int D, bool BF16, int ROWS>
 __global__ void __launch_bounds__(kMergeThreads, 2)
@@ -1368,9 +1386,14 @@ merge_kernel(const DecodeArgs a) {
   // a decode launched after this one with an early prologue may start now:
   // it waits for this launch to complete before touching what it writes
   griddep_launch_dependents();
+  constexpr int COLS = D / 4;
+  constexpr int RG = kMergeThreads / (2 * COLS);   // rows per CTA at most, with 2+ groups
   __shared__ int red[kMergeThreads / 32][2];
   __shared__ unsigned want;
   __shared__ int fail;
+  // the running state of groups 1.. at the end, for group 0 to fold
+  __shared__ float gm[kMergeMaxGroups][RG], gs[kMergeMaxGroups][RG];
+  __shared__ float4 gacc[kMergeMaxGroups - 1][RG][COLS];
   const int Hkv = a.Hkv, G = a.group;
   const int b = blockIdx.x / Hkv, h = blockIdx.x - b * Hkv;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -1420,32 +1443,42 @@ merge_kernel(const DecodeArgs a) {
   });
 
   if (np > 1) {                                  // a split segment (np is CTA-uniform)
-    constexpr int COLS = D / 4;
-    constexpr int RPC = kMergeThreads / COLS;      // query rows per CTA
-    const int g0 = static_cast<int>(blockIdx.y) * RPC;   // this CTA's first query row
-    const int g = g0 + tid / COLS, d4 = tid % COLS;      // g: the thread's query row
-    const bool row = g < a.n_q * G;
+    // this launch's rows per CTA and piece groups: the live rows are spread
+    // evenly over grid y, each row takes D/4 threads per group (the block is
+    // rounded up to whole warps; threads past the groups hold no row)
+    const int live = a.n_q * G;
+    const int rows = (live + static_cast<int>(gridDim.y) - 1) / static_cast<int>(gridDim.y);
+    const int groups = a.merge_groups > 0 ? a.merge_groups : 1;
+    const int grp = tid / (rows * COLS);                 // the thread's piece group
+    const int rl = (tid - grp * rows * COLS) / COLS;     // its row within the CTA
+    const int d4 = tid % COLS;
+    const int g0 = static_cast<int>(blockIdx.y) * rows;  // the CTA's first query row
+    const int g = g0 + rl;                               // the thread's query row
+    const bool row = grp < groups && g < live;
     // partial row of piece p for query row q
     auto prow = [&](int p, int q) {
       return piece_row(w0 + p, p == 0 ? first_slot : 0, q, ROWS);
     };
+    const int kRound = groups * kMergeBatch;
     float M = -INFINITY, S = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     bool dirty = false;
     PA_TRACE_ONLY(int tr_waits = 0);
-    for (int p0 = 0; p0 < np; p0 += kMergeBatch) {
-      const int pn = min(kMergeBatch, np - p0);
+    for (int p0 = 0; p0 < np; p0 += kRound) {
+      const int pr = min(kRound, np - p0);               // pieces of the round
+      const int pg = p0 + grp * kMergeBatch;             // the group's first piece
+      const int pn = max(0, min(kMergeBatch, np - pg));  // and its pieces in the round
       uint2 ml[kMergeBatch];
       uint4 v[kMergeBatch];
       // Issue every load of the batch before looking at any (they are in
-      // flight together); then note the pieces not yet seen whole.  Piece
-      // p0 + k sits 16 rows after piece p0 + k - 1 (slot 0 of the next
-      // worker), except that the segment's first piece may be its worker's
-      // slot 1.
-      const int64_t rb = static_cast<int64_t>(w0 + p0) * 2 * ROWS + g;
+      // flight together, with the other groups'); then note the pieces not
+      // yet seen whole.  Piece pg + k sits 2 ROWS rows after piece pg + k - 1
+      // (slot 0 of the next worker), except that the segment's first piece
+      // may be its worker's slot 1.
+      const int64_t rb = static_cast<int64_t>(w0 + pg) * 2 * ROWS + g;
       const float* mlb = a.ws_ml + rb * 2;
       const float* vb = a.ws_acc + rb * D + 4 * d4;
-      const int s0x = p0 == 0 ? first_slot * ROWS : 0;
+      const int s0x = pg == 0 ? first_slot * ROWS : 0;
       auto load = [&](int k) {
         const int dr = k == 0 ? s0x : 2 * ROWS * k;
         ml[k] = ld_relaxed_v2(mlb + dr * 2);
@@ -1466,17 +1499,17 @@ merge_kernel(const DecodeArgs a) {
         if (mine >> k & 1u) load(k);
       unsigned missing = missing_of(mine);       // pieces this thread has not seen whole
       if (__syncthreads_or(missing != 0u)) {
-        // wait for the batch's missing pieces (bounded), then read them again
+        // wait for the round's missing pieces (bounded), then read them again
         const uint64_t t0 = tid == 0 ? global_ns() : 0;
         for (;;) {
           if (tid == 0) want = 0u;
           __syncthreads();
-          if (missing) atomicOr(&want, missing);
+          if (missing) atomicOr(&want, missing << (grp * kMergeBatch));
           __syncthreads();
           const unsigned need = want;
           if (need == 0u) break;
           PA_TRACE_ONLY(++tr_waits);
-          if (tid < 32 && lane < pn && (need >> lane & 1u)) {
+          if (tid < 32 && lane < pr && (need >> lane & 1u)) {
             const uint32_t* first =
                 reinterpret_cast<const uint32_t*>(a.ws_ml + prow(p0 + lane, g0) * 2);
             const uint64_t tl = global_ns();
@@ -1498,7 +1531,7 @@ merge_kernel(const DecodeArgs a) {
         }
         if (fail) break;                         // (uniform: read after a barrier)
       }
-      if (!row) continue;
+      if (!row || pn == 0) continue;
       float mk[kMergeBatch];
       float mb = M;
 #pragma unroll
@@ -1530,21 +1563,52 @@ merge_kernel(const DecodeArgs a) {
     }
     if (fail) {
       if (tid == 0) atomicOr(a.status, kStatusTimeout);
-    } else if (row) {
-      if (dirty) atomicOr(a.status, kStatusWsDirty);
-      const float inv = S > 0.f ? 1.f / S : 0.f;
-      uint2 o;
-      o.x = pack2<BF16>(acc.x * inv, acc.y * inv);
-      o.y = pack2<BF16>(acc.z * inv, acc.w * inv);
-      uint16_t* out = static_cast<uint16_t*>(a.out) +
-                      ((static_cast<int64_t>(b) * a.q_tokens + a.q_first + g / G) * a.Hq +
-                       h * G + g % G) * D;
-      *reinterpret_cast<uint2*>(out + 4 * d4) = o;
-      // leave the workspace zero-filled for the next call
-      for (int p = 0; p < np; ++p) {
-        const int64_t r = prow(p, g);
-        __stcg(reinterpret_cast<uint4*>(a.ws_acc + r * D) + d4, make_uint4(0u, 0u, 0u, 0u));
-        if (d4 == 0) __stcg(reinterpret_cast<uint2*>(a.ws_ml + r * 2), make_uint2(0u, 0u));
+    } else {
+      // group 0 folds the other groups' states, in group order
+      if (row && grp > 0) {
+        gacc[grp - 1][rl][d4] = acc;
+        if (d4 == 0) {
+          gm[grp][rl] = M;
+          gs[grp][rl] = S;
+        }
+      }
+      __syncthreads();
+      if (row && grp == 0) {
+        for (int j = 1; j < groups; ++j) {
+          const float mj = gm[j][rl];
+          const float mb = fmaxf(M, mj);
+          if (mb == -INFINITY) continue;         // neither has attended anything
+          const float k0 = fast_exp2(M - mb), k1 = fast_exp2(mj - mb);
+          const float4 aj = gacc[j - 1][rl][d4];
+          S = S * k0 + gs[j][rl] * k1;
+          acc.x = acc.x * k0 + aj.x * k1;
+          acc.y = acc.y * k0 + aj.y * k1;
+          acc.z = acc.z * k0 + aj.z * k1;
+          acc.w = acc.w * k0 + aj.w * k1;
+          M = mb;
+        }
+        const float inv = S > 0.f ? 1.f / S : 0.f;
+        uint2 o;
+        o.x = pack2<BF16>(acc.x * inv, acc.y * inv);
+        o.y = pack2<BF16>(acc.z * inv, acc.w * inv);
+        uint16_t* out = static_cast<uint16_t*>(a.out) +
+                        ((static_cast<int64_t>(b) * a.q_tokens + a.q_first + g / G) * a.Hq +
+                         h * G + g % G) * D;
+        *reinterpret_cast<uint2*>(out + 4 * d4) = o;
+      }
+      if (row) {
+        if (dirty) atomicOr(a.status, kStatusWsDirty);
+        // leave the workspace zero-filled for the next call: each thread the
+        // pieces its group read
+        for (int p0 = 0; p0 < np; p0 += kRound) {
+          const int pg = p0 + grp * kMergeBatch;
+          const int pn = min(kMergeBatch, np - pg);
+          for (int k = 0; k < pn; ++k) {
+            const int64_t r = prow(pg + k, g);
+            __stcg(reinterpret_cast<uint4*>(a.ws_acc + r * D) + d4, make_uint4(0u, 0u, 0u, 0u));
+            if (d4 == 0) __stcg(reinterpret_cast<uint2*>(a.ws_ml + r * 2), make_uint2(0u, 0u));
+          }
+        }
       }
     }
     PA_TRACE_ONLY(if (tid == 0 && blockIdx.x < 16384) {
@@ -1578,18 +1642,30 @@ merge_kernel(const DecodeArgs a) {
 // ROWS: the partials' rows per piece (a.rows; 8 per tile of query columns
 // the attention launch held).
 template <int D, bool BF16, int ROWS>
-cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t s) {
+cudaError_t launch_merge(const DecodeArgs& args, cudaStream_t s) {
+  DecodeArgs a = args;
   cudaLaunchConfig_t cfg = {};
-  // one thread per (query row, 4 output columns), rounded up to whole warps:
-  // no idle warps, so more CTAs fit an SM at once; rows beyond one CTA's
-  // kMergeThreads threads go to further CTAs (grid y)
-  constexpr int RPC = kMergeThreads / (D / 4);
+  // D/4 threads per query row and group, at most kMergeThreads per CTA; the
+  // live rows spread evenly over the CTAs of a (sequence, kv head) (grid y).
+  // Groups: for partials of 8 rows, the most (2 or 1) that keep the grid
+  // within kMergeCtasPerSm CTAs per SM; more CTAs than the SMs take in as
+  // attention CTAs leave would hold back the next launch's start.
+  constexpr int COLS = D / 4;
   const int live = a.n_q * a.group;
-  const int chunks = (live + RPC - 1) / RPC;
-  cfg.gridDim = dim3(static_cast<unsigned>(a.B) * static_cast<unsigned>(a.Hkv),
-                     static_cast<unsigned>(chunks));
-  const int threads = ((live < RPC ? live : RPC) * (D / 4) + 31) & ~31;
-  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  const int64_t pairs = static_cast<int64_t>(a.B) * a.Hkv;
+  auto chunks_for = [&](int groups) {
+    const int rpc = kMergeThreads / (groups * COLS);
+    return (live + rpc - 1) / rpc;
+  };
+  int groups = ROWS <= 8 ? kMergeMaxGroups : 1;
+  const int64_t budget = static_cast<int64_t>(device_sm_count()) * kMergeCtasPerSm;
+  while (groups > 1 && pairs * chunks_for(groups) > budget) groups /= 2;
+  const int chunks = chunks_for(groups);
+  const int rows = (live + chunks - 1) / chunks;
+  a.merge_groups = groups;
+  cfg.gridDim = dim3(static_cast<unsigned>(pairs), static_cast<unsigned>(chunks));
+  // whole warps (the length scan shuffles over full warps)
+  cfg.blockDim = dim3(static_cast<unsigned>((rows * groups * COLS + 31) & ~31));
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

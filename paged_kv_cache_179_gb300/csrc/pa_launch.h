@@ -60,6 +60,7 @@ struct DecodeArgs {
   int window;                   // sliding window in tokens (0: the whole context)
   int n_q;                      // query tokens this launch serves (n_q * group <= rows)
   int rows;                     // query rows per (sequence, kv head) a launch holds: 8, 16 or 32
+  int merge_groups;             // piece groups per merge CTA (set by the merge launch)
   int q_tokens;                 // query tokens per sequence in q and out
   int q_first;                  // the first of them this launch serves
   int early;                    // programmatic dependent launch: prologue before griddepcontrol.wait
