@@ -113,6 +113,25 @@ def test_split_invariance():
         assert (o - outs[0]).abs().max().item() <= 2 * TOL["f16"]
 
 
+@pytest.mark.parametrize("splits", [1, 4, 5, 8, 9, 12, 16, 17, 20])
+def test_merge_rounds_match_oracle(splits):
+    """One sequence of 4096 tokens on two kv heads, split over 4 x splits
+    warps: each segment comes in about 2 x splits pieces, so the merge's
+    rounds (two piece groups of 8 when its grid is small) are crossed at
+    every boundary -- part-full groups, an empty second group, several
+    rounds.  Equal to the oracle, and the workspace left zero-filled."""
+    w = W.make_workload("qwen2_5_1_5b", seed=21, lens_override=[4096])
+    ref = oracle_step(w)
+    to_cuda(w)
+    step = _step_for(w, splits)
+    out = torch.empty_like(w.q)
+    step(w.q, w.k_new, w.v_new, w.slot_mapping, out)
+    assert _abi.pa_get_status() == (0, 0)
+    assert max_err(out, ref) <= TOL["f16"]
+    torch.cuda.synchronize()
+    assert int(step.workspace.count_nonzero()) == 0
+
+
 def test_deterministic():
     w = to_cuda(W.make_workload("qwen2_5_7b", seed=0))
     step = _step_for(w)
