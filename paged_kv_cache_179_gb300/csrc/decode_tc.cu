@@ -68,13 +68,27 @@
 namespace pa {
 namespace {
 
-constexpr int kTcStages = 3;             // chunk stages in the ring
+// Slots of a chunk's K (scores) and of its V (PV product), 32 KB each, 192
+// KB in all.  A K slot is free once the chunk's scores are computed; a V
+// slot is held longer (until the chunk's P is written and its PV product
+// done), so V gets more of them.
+#ifndef PA_TC_KSTAGES
+#define PA_TC_KSTAGES 3
+#endif
+#ifndef PA_TC_VSTAGES
+#define PA_TC_VSTAGES 3
+#endif
+constexpr int kTcKStages = PA_TC_KSTAGES;
+constexpr int kTcVStages = PA_TC_VSTAGES;
+static_assert(kTcKStages >= 2 && kTcVStages >= 2 && kTcKStages + kTcVStages <= 6,
+              "the slots fit 192 KB");
 constexpr int kTcBlocks = 8;             // blocks per chunk: 128 tokens, the MMA's M
 constexpr int kTcGroups = 2;             // softmax warpgroups, each on half of the query rows
 constexpr int kTcThreads = 320;          // warps 0-7 softmax, 8 copies, 9 MMA
 constexpr int kTcCopyWarp = 8, kTcMmaWarp = 9;
 constexpr int kTcHalf = 128 * 128;       // one half (64 of head_dim) of one chunk tensor: 16 KB
-constexpr int kTcStage = 4 * kTcHalf;    // K and V of one chunk: 64 KB
+constexpr int kTcSlot = 2 * kTcHalf;     // K or V of one chunk: 32 KB
+constexpr int kTcVRing = kTcKStages * kTcSlot;   // the V slots follow the K slots
 constexpr float kTcSlack = 8.f;          // log2 units
 constexpr int kTcSBufs = 3;              // S buffers in tensor memory
 constexpr uint32_t kTcCols = 128;        // tensor-memory columns: S x 3, O (R x 4 <= 128)
@@ -85,11 +99,11 @@ constexpr int kTcSegCost = 10;
 
 // mbarriers
 enum : int {
-  kBarKFull = 0,                         // [3] a stage's K copies landed
-  kBarKEmpty = kBarKFull + kTcStages,    // [3] its scores are computed: the K slot is free
-  kBarVFull = kBarKEmpty + kTcStages,    // [3] a stage's V copies landed
-  kBarVEmpty = kBarVFull + kTcStages,    // [3] its PV product is done: the V slot is free
-  kBarQFull = kBarVEmpty + kTcStages,    // [2] a query buffer's copies landed
+  kBarKFull = 0,                         // [K] a slot's K copies landed
+  kBarKEmpty = kBarKFull + kTcKStages,   // [K] its scores are computed: the K slot is free
+  kBarVFull = kBarKEmpty + kTcKStages,   // [V] a slot's V copies landed
+  kBarVEmpty = kBarVFull + kTcVStages,   // [V] its PV product is done: the V slot is free
+  kBarQFull = kBarVEmpty + kTcVStages,   // [2] a query buffer's copies landed
   kBarQEmpty = kBarQFull + 2,            // [2] a query buffer's last MMA is done
   kBarSFull = kBarQEmpty + 2,            // [3] an S buffer holds a chunk's scores (and
                                          //     its mask is in wmeta): 2 arrivals
@@ -109,11 +123,11 @@ struct TcLayout {
 template <int R>
 __host__ __device__ inline TcLayout tc_layout(int B) {
   TcLayout l{};
-  int o = kTcStages * kTcStage;
+  int o = (kTcKStages + kTcVStages) * kTcSlot;
   l.q = o;     o += 2 * R * 256;
   l.p = o;     o += R * 256;
   l.bars = o;  o += round16(kBarCount * 8);
-  l.meta = o;  o += round16((kTcStages + kTcSBufs) * 8);
+  l.meta = o;  o += round16((kTcKStages + kTcSBufs) * 8);
   l.flags = o; o += kTcGroups * 2 * 4 * 4;
   l.red = o;   o += 4 * R * 4;
   l.red2 = o;  o += 4 * R * 4;
@@ -273,8 +287,8 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
   const uint32_t base = smem_u32(smem);
   const uint32_t ring = base, qbuf0 = base + lay.q, pbuf = base + lay.p;
   auto bar = [&](int i) { return base + lay.bars + 8u * static_cast<uint32_t>(i); };
-  int2* meta = reinterpret_cast<int2*>(smem + lay.meta);   // per stage: valid blocks, last id
-  int2* wmeta = meta + kTcStages;                          // per S buffer: the same, for the softmax
+  int2* meta = reinterpret_cast<int2*>(smem + lay.meta);   // per K slot: valid blocks, last id
+  int2* wmeta = meta + kTcKStages;                         // per S buffer: the same, for the softmax
   int* flags = reinterpret_cast<int*>(smem + lay.flags);   // [group][2][4] per-chunk votes
   float* red = reinterpret_cast<float*>(smem + lay.red);   // [group][4][R/2] column maxima
   float* red2 = reinterpret_cast<float*>(smem + lay.red2); // [group][4][R/2] column sums
@@ -441,15 +455,15 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
     unsigned v_valid = 0;
     bool ok = true;
     auto issue_v = [&]() {                // V copies of chunk v_done (< i)
-      const int vs = v_done % kTcStages;
-      if (v_done >= kTcStages &&
-          !tc_wait_warp(bar(kBarVEmpty + vs), (v_done / kTcStages - 1) & 1, dead, a))
+      const int vs = v_done % kTcVStages;
+      if (v_done >= kTcVStages &&
+          !tc_wait_warp(bar(kBarVEmpty + vs), (v_done / kTcVStages - 1) & 1, dead, a))
         return false;
       if (lane == 0)
         mbar_arrive_expect_tx(bar(kBarVFull + vs), static_cast<uint32_t>(__popc(v_valid)) * 4096u);
       __syncwarp();
       if (v_tile >= 0) {
-        const uint32_t vd = ring + vs * kTcStage + 2 * kTcHalf + lane * 2048;
+        const uint32_t vd = ring + kTcVRing + vs * kTcSlot + lane * 2048;
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb)
           tensor3_g2s(vd + hb * kTcHalf, &a.tm_v, 64 * hb, 0, v_tile, bar(kBarVFull + vs), pol);
@@ -460,9 +474,9 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
     while (ok && c32.nb > 0) {
       for (int k = 0; k < c32.nb; k += kTcBlocks) {
         const int nb = min(kTcBlocks, c32.nb - k);
-        const int s = i % kTcStages;
-        if (i >= kTcStages &&
-            !tc_wait_warp(bar(kBarKEmpty + s), (i / kTcStages - 1) & 1, dead, a)) {
+        const int s = i % kTcKStages;
+        if (i >= kTcKStages &&
+            !tc_wait_warp(bar(kBarKEmpty + s), (i / kTcKStages - 1) & 1, dead, a)) {
           ok = false;
           break;
         }
@@ -496,7 +510,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
         }
         __syncwarp();
         if (okid) {
-          const uint32_t kd = ring + s * kTcStage + lane * 2048;
+          const uint32_t kd = ring + s * kTcSlot + lane * 2048;
 #pragma unroll
           for (int hb = 0; hb < 2; ++hb)
             tensor3_g2s(kd + hb * kTcHalf, &a.tm_k, 64 * hb, 0, tile, bar(kBarKFull + s), pol);
@@ -526,10 +540,10 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
       }
     };
     if (lane == 0) {
-      for (int st = 0; st < kTcStages; ++st) {
-        settle(bar(kBarKFull + st), (i - st + kTcStages - 1) / kTcStages);
-        settle(bar(kBarVFull + st), (v_done - st + kTcStages - 1) / kTcStages);
-      }
+      for (int st = 0; st < kTcKStages; ++st)
+        settle(bar(kBarKFull + st), (i - st + kTcKStages - 1) / kTcKStages);
+      for (int st = 0; st < kTcVStages; ++st)
+        settle(bar(kBarVFull + st), (v_done - st + kTcVStages - 1) / kTcVStages);
       for (int j = 0; j < 2; ++j) settle(bar(kBarQFull + j), (piece - j + 1) / 2);
     }
     __syncwarp();
@@ -548,7 +562,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
     // operand descriptors of stage 0, query buffer 0 and P; a stage, buffer or
     // K step moves the start address (field bits 0-13, address / 16) only
     const uint64_t dk0 = umma_desc_sw128(ring, 16, 1024);
-    const uint64_t dv0 = umma_desc_sw128(ring + 2 * kTcHalf, kTcHalf, 1024);
+    const uint64_t dv0 = umma_desc_sw128(ring + kTcVRing, kTcHalf, 1024);
     const uint64_t dq0 = umma_desc_sw128(qbuf0, 16, 1024);
     const uint64_t dp = umma_desc_sw128(pbuf, 16, 1024);
     auto ready = [&](int b, int parity) {   // a phase complete (decided by lane 0)
@@ -566,7 +580,11 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
     Chunk x = tc_first<kTcBlocks>(lo, hi, pf, B, Hkv, C);
     int qi = 0, pi = 0, piece = -1;
     // per scored chunk (qi & 3) until its PV product: whether it starts a
-    // piece, and the fused append's V row for its tile (-1: none)
+    // piece, and the fused append's V row for its tile (-1: none).  A ring
+    // of 4, so chunk qi is scored only once chunk qi-4's PV product is
+    // issued (its S buffer alone would allow it earlier: that needs only the
+    // PV product of chunk qi-5 done, while chunk qi-4's V tile may not have
+    // landed).
     unsigned firsts = 0u;
     int vrows[4] = {-1, -1, -1, -1};
     uint2 vvals[4];
@@ -574,17 +592,17 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
     uint64_t idle_since = 0;
     for (;;) {
       bool did = false;
-      if (pi < qi && ready(kBarPFull, pi) && ready(kBarVFull + pi % kTcStages, pi / kTcStages)) {
-        const int ps = pi % kTcStages;
+      if (pi < qi && ready(kBarPFull, pi) && ready(kBarVFull + pi % kTcVStages, pi / kTcVStages)) {
+        const int ps = pi % kTcVStages;
         if (vrows[pi & 3] >= 0) {           // fused append: the new V row into the tile
-          *reinterpret_cast<uint2*>(smem + ps * kTcStage + 2 * kTcHalf + vrows[pi & 3]) =
+          *reinterpret_cast<uint2*>(smem + kTcVRing + ps * kTcSlot + vrows[pi & 3]) =
               vvals[pi & 3];
           fence_proxy_async_smem();
           __syncwarp();
         }
         tc_fence_after();
         if (lane == 0) {
-          const uint64_t dv = dv0 + static_cast<uint64_t>(ps * (kTcStage >> 4));
+          const uint64_t dv = dv0 + static_cast<uint64_t>(ps * (kTcSlot >> 4));
           const bool first = (firsts >> (pi & 3)) & 1u;
 #pragma unroll
           for (int k = 0; k < 8; ++k)   // 16 tokens a step
@@ -597,11 +615,11 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
         __syncwarp();
         ++pi;
         did = true;
-      } else if (x.nb > 0) {
-        const int s = qi % kTcStages, sbuf = qi % kTcSBufs;
+      } else if (x.nb > 0 && qi - pi < 4) {
+        const int s = qi % kTcKStages, sbuf = qi % kTcSBufs;
         const bool pfirst = qi == 0 || x.cb0 == 0;
         const int np = pfirst ? piece + 1 : piece;
-        if (ready(kBarKFull + s, qi / kTcStages) &&
+        if (ready(kBarKFull + s, qi / kTcKStages) &&
             (qi < kTcSBufs || ready(kBarSFree + sbuf, qi / kTcSBufs - 1)) &&
             (!pfirst || ready(kBarQFull + (np & 1), np >> 1))) {
           piece = np;
@@ -636,7 +654,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
                 const int tok = (x.nb - 1) * 16 + row;
                 const int c = (lane & 15) >> 1;
                 vrow = (lane >> 4) * kTcHalf + tok * 128 + ((c ^ (tok & 7)) << 4) + (lane & 1) * 8;
-                *reinterpret_cast<uint2*>(smem + s * kTcStage + vrow) = kv;
+                *reinterpret_cast<uint2*>(smem + s * kTcSlot + vrow) = kv;
                 fence_proxy_async_smem();
               }
             }
@@ -650,7 +668,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
           }
           tc_fence_after();
           if (lane == 0) {
-            const uint64_t dk = dk0 + static_cast<uint64_t>(s * (kTcStage >> 4));
+            const uint64_t dk = dk0 + static_cast<uint64_t>(s * (kTcSlot >> 4));
             const uint64_t dq = dq0 + static_cast<uint64_t>((piece & 1) * (R * 256 >> 4));
 #pragma unroll
             for (int k = 0; k < 8; ++k)   // 16 of head_dim a step
@@ -774,7 +792,7 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
     Chunk x = tc_first<kTcBlocks>(lo, hi, pf, B, Hkv, C);
     int i = 0, piece_no = 0;
     while (x.nb > 0) {
-      const int s = i % kTcStages;
+      const int vs = i % kTcVStages;       // the chunk's V slot
       const int sb = i % kTcSBufs;
       bad |= !tc_wait_warp(bar(kBarSFull + sb), (i / kTcSBufs) & 1, dead, a);
       const Where wh = where(x);
@@ -883,9 +901,9 @@ decode_tc_kernel(const __grid_constant__ TcArgs ta) {
       if (g == 0 && __any_sync(0xffffffffu, !data)) {
         // a token without data: its V row (either half) to zero, once the
         // chunk's V copies have landed
-        bad |= !tc_wait_warp(bar(kBarVFull + s), (i / kTcStages) & 1, dead, a);
+        bad |= !tc_wait_warp(bar(kBarVFull + vs), (i / kTcVStages) & 1, dead, a);
         if (!data && !bad) {
-          const uint32_t vrow = ring + s * kTcStage + 2 * kTcHalf + t * 128;
+          const uint32_t vrow = ring + kTcVRing + vs * kTcSlot + t * 128;
 #pragma unroll
           for (int hb = 0; hb < 2; ++hb)
 #pragma unroll
