@@ -1348,11 +1348,12 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
 // order, so results are deterministic.  Segments attended whole by one
 // worker are skipped.
 //
-// The number of groups is the launch's (launch_merge): several only for
+// The number of groups is the launch's (launch_merge): two only for
 // partials of 8 rows (16 or 32 rows fill a CTA already, and their workers
 // hold long shares, so few pieces), and only while the grid stays small
 // (a batch of few sequences and kv heads, whose segments are split into
-// many short pieces); the kernel reads it from its shape.
+// many short pieces).  The kernel reads it from DecodeArgs::merge_groups and
+// its rows per CTA from its grid.
 //
 // The launch runs beside the attention grid: it is scheduled once every
 // attention CTA has passed its prologue, so it never holds resources an
