@@ -313,14 +313,18 @@ class ConfigRun:
         self.back_to_back = l2_mode in ("none", "rotate")
         # the timed steps: nothing between them writes context_lens or
         # block_tables, so the attention launch may start its prologue while
-        # the previous step's merge finishes (PA_DECODE_EARLY_PROLOGUE).  Steps
-        # that each follow an L2-evicting kernel (not one of ours, which would
-        # let the launch start early) gain nothing by it, and launch plainly.
-        self.early = args.early_prologue == "on" and self.back_to_back
+        # the previous step's merge finishes (PA_DECODE_EARLY_PROLOGUE); and
+        # the kernels between them write the pools only in each sequence's
+        # last block (the previous step's append), so it may also start its
+        # first K/V copies then (PA_DECODE_EARLY_COPIES).  Steps that each
+        # follow an L2-evicting kernel (not one of ours, which would let the
+        # launch start early) gain nothing by it, and launch plainly.
+        self.early = args.early_prologue in ("on", "copies") and self.back_to_back
+        self.early_copies = self.early and args.early_prologue == "copies"
         self.steps = [DecodeStep(**ps, block_tables=w.block_tables, context_lens=w.context_lens,
                                  max_context_len=w.max_context_len, scale=w.scale,
                                  num_q_heads=w.Hq, split_ctas=args.splits, window=window,
-                                 early_prologue=self.early)
+                                 early_prologue=self.early, early_copies=self.early_copies)
                       for ps in self.pool_sets]
         self.step = self.steps[0]
         self.flush_buf = torch.ones(max(2 * l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
@@ -403,9 +407,12 @@ class ConfigRun:
                 if self.fused else "append launch, then attention and merge launches")
 
     def describe_launch(self):
+        if not self.early:
+            return "plain launches"
         return ("attention launch with an early prologue (PA_DECODE_EARLY_PROLOGUE: it may "
-                "start while the previous step's merge finishes)" if self.early
-                else "plain launches")
+                "start while the previous step's merge finishes"
+                + ("; PA_DECODE_EARLY_COPIES: its first K/V copies, of blocks before each "
+                   "sequence's last two, start then too)" if self.early_copies else ")"))
 
     def decode_us(self):
         d = self.dec_ms
@@ -494,7 +501,7 @@ def measure_e2e(args, run, dev):
                         context_lens=staging.dev["context_lens"],
                         max_context_len=w.max_context_len, scale=w.scale, num_q_heads=w.Hq,
                         split_ctas=args.splits, window=run.window,
-                        early_prologue=run.early,
+                        early_prologue=run.early, early_copies=run.early_copies,
                         workspace=shared_ws[0] if shared_ws else None)
         shared_ws[:1] = [st.workspace]
         return st
@@ -794,13 +801,15 @@ def run_multiquery(args, dev):
     copies = 1 if ab["kv"] >= 3 * l2 else -(-3 * l2 // max(ab["kv"], 1))
     back_to_back = copies <= 16
     copies = copies if back_to_back else 1
-    early = args.early_prologue == "on" and back_to_back   # as for the decode step
+    early = args.early_prologue in ("on", "copies") and back_to_back   # as for the decode step
+    early_copies = early and args.early_prologue == "copies"   # nothing writes the pools here
     pool_sets = [(w.k_cache, w.v_cache)] + [(w.k_cache.clone(), w.v_cache.clone())
                                            for _ in range(copies - 1)]
     steps = [DecodeStep(k_cache=kc, v_cache=vc, block_tables=w.block_tables,
                         context_lens=w.context_lens, max_context_len=w.max_context_len,
                         scale=w.scale, num_q_heads=w.Hq, split_ctas=args.splits,
-                        window=args.window, early_prologue=early, queries_per_seq=n)
+                        window=args.window, early_prologue=early, early_copies=early_copies,
+                        queries_per_seq=n)
              for kc, vc in pool_sets]
     step = steps[0]
     stream = torch.cuda.current_stream(dev)
@@ -846,8 +855,9 @@ def run_multiquery(args, dev):
                    "split_ctas": step.split_ctas,
                    "l2": (describe_l2("rotate" if copies > 1 else "none", ab["kv"], l2, copies)
                           if back_to_back else describe_l2("read", ab["kv"], l2)),
-                   "launch": ("attention launch with an early prologue" if early
-                              else "plain launches"),
+                   "launch": ("plain launches" if not early else
+                              "attention launch with an early prologue"
+                              + (" and early K/V copies" if early_copies else "")),
                    **({"window": args.window} if args.window else {})},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -1000,9 +1010,10 @@ def main(argv=None):
     ap.add_argument("--copy-pairs", type=int, default=8192)
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window in tokens (0: each sequence attends its whole context)")
-    ap.add_argument("--early-prologue", choices=["on", "off"], default="on",
-                    help="steps with PA_DECODE_EARLY_PROLOGUE (the device-timed steps and the "
-                         "pipelined end-to-end run)")
+    ap.add_argument("--early-prologue", choices=["copies", "on", "off"], default="copies",
+                    help="steps with PA_DECODE_EARLY_PROLOGUE (on), with PA_DECODE_EARLY_COPIES "
+                         "as well (copies), or neither (off): the device-timed steps and the "
+                         "pipelined end-to-end run")
     ap.add_argument("--configs", choices=["all", "none"], default="all",
                     help="all: the default single-GPU run also times the other four configs "
                          "(tiny, SmolLM2-360M, Qwen2.5-1.5B, E4M3 Qwen2.5-7B) one after another "

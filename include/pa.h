@@ -94,6 +94,7 @@ enum {
 
 /* Decode flags (the flags argument of the decode entry points). */
 #define PA_DECODE_EARLY_PROLOGUE 1u   /* the prologue may overlap the previous kernel: see pa_decode */
+#define PA_DECODE_EARLY_COPIES 2u     /* with EARLY_PROLOGUE: first K/V copies before the wait, see pa_decode */
 
 /*
  * Append: for each token i with s = slot_mapping[i] >= 0 and each kv head h,
@@ -263,6 +264,16 @@ size_t pa_decode_workspace_size_rows(int num_seqs, int num_q_heads, int head_dim
  *   only when the kernel just before the call on the stream does not write
  *   context_lens or block_tables (for example, when they are uploaded by a
  *   copy before the forward pass).  Results are the same either way.
+ *   PA_DECODE_EARLY_COPIES (only together with PA_DECODE_EARLY_PROLOGUE;
+ *   alone: PA_ERR_INVALID_ARG) lets the prologue go further on the mma.sync
+ *   launch (up to 16 query rows per kv head): before waiting, each warp
+ *   copies into shared memory its first K/V tiles that lie wholly before its
+ *   sequence's last two blocks.  Set it only when, besides the above, the
+ *   kernels before the call on the stream write nothing in the pools this
+ *   call reads except in each sequence's last two blocks -- as the previous
+ *   decode step of the same batch does (its append, E4M3 re-scales
+ *   included), or an append of up to 17 draft tokens -- and write no page
+ *   scale of another block.  Results are the same either way.
  * Source: rvLLM, CUDA Kernels table, "PagedAttention V2" (block-table
  * indirection, online softmax); LLM Serving Kernels, Projects table, row 04;
  * rvllm (small engine), How it's put together (GQA, read_blocks).

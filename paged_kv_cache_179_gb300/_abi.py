@@ -24,6 +24,7 @@ PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_LEN, PA_STATUS_BAD_SLOT, PA_STATUS_TIMEOUT = 
 PA_STATUS_NO_WORKSPACE = 16
 PA_STATUS_WS_DIRTY = 32
 PA_DECODE_EARLY_PROLOGUE = 1
+PA_DECODE_EARLY_COPIES = 2
 
 # (name, argtypes, restype) of every exported entry point
 _vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
@@ -193,8 +194,11 @@ def _need(t, name, dtype=None, ndim=None, device=None):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
-def _flags(early_prologue: bool) -> int:
-    return PA_DECODE_EARLY_PROLOGUE if early_prologue else 0
+def _flags(early_prologue: bool, early_copies: bool = False) -> int:
+    if early_copies and not early_prologue:
+        raise ValueError("early_copies needs early_prologue")
+    return ((PA_DECODE_EARLY_PROLOGUE if early_prologue else 0) |
+            (PA_DECODE_EARLY_COPIES if early_copies else 0))
 
 
 def _act_code(dtype) -> int:
@@ -348,10 +352,13 @@ def _decode_common(out, q, block_tables, context_lens, dev):
 
 def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
               scale: float, split_ctas: int = 0, workspace=None, *, window: int = 0,
-              early_prologue: bool = False) -> None:
+              early_prologue: bool = False, early_copies: bool = False) -> None:
     """out[b][hq] = softmax(scale q.K) V over each sequence's blocks (16-bit pools).
     early_prologue: PA_DECODE_EARLY_PROLOGUE (the kernel before this call on
-    the stream must not write context_lens or block_tables)."""
+    the stream must not write context_lens or block_tables).
+    early_copies: PA_DECODE_EARLY_COPIES as well (the kernels before it must
+    also write nothing in the pools except in each sequence's last two
+    blocks, as the previous decode step of the same batch does)."""
     dev = q.device
     act = (torch.float16, torch.bfloat16)
     _need(q, "q", act, None, dev)
@@ -368,12 +375,12 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context_
           _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
           block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
           float(scale), int(window), nq, _act_code(q.dtype), int(split_ctas), _ptr(workspace),
-          ws_bytes, _flags(early_prologue), _stream(dev))
+          ws_bytes, _flags(early_prologue, early_copies), _stream(dev))
 
 
 def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
                   max_context_len: int, scale: float, split_ctas: int = 0, workspace=None, *,
-                  window: int = 0, early_prologue: bool = False) -> None:
+                  window: int = 0, early_prologue: bool = False, early_copies: bool = False) -> None:
     """As pa_decode over E4M3 pools with per-(block, kv head) fp32 scales; q/out
     fp16 or bf16."""
     dev = q.device
@@ -393,7 +400,7 @@ def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, cont
           _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
           _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), int(max_context_len), B,
           Hq, Hkv, D, bs, NB, float(scale), int(window), nq, _act_code(q.dtype), int(split_ctas),
-          _ptr(workspace), ws_bytes, _flags(early_prologue), _stream(dev))
+          _ptr(workspace), ws_bytes, _flags(early_prologue, early_copies), _stream(dev))
 
 
 class StepSync(ctypes.Structure):
@@ -446,7 +453,7 @@ def _ws_bytes(workspace, dev):
 
 def pa_decode_step(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_tables,
                    context_lens, max_context_len: int, scale: float, split_ctas: int = 0,
-                   workspace=None, *, window: int = 0, early_prologue: bool = False,
+                   workspace=None, *, window: int = 0, early_prologue: bool = False, early_copies: bool = False,
                    sync: StepSync = None, copies: StepCopies = None) -> None:
     """Append k_new/v_new at slot_mapping, then decode, in one launch (16-bit
     pools); with ``sync``, pa_decode_step_synced (device-side handshake); with
@@ -471,7 +478,7 @@ def pa_decode_step(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_t
             _ptr(slot_mapping), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
             int(max_context_len), B, Hq, Hkv, D, bs, NB, float(scale), int(window),
             _act_code(q.dtype), int(split_ctas), _ptr(workspace), _ws_bytes(workspace, dev),
-            _flags(early_prologue))
+            _flags(early_prologue, early_copies))
     if sync is None:
         _call(load().pa_decode_step, "pa_decode_step", *args, _stream(dev))
     elif copies is None:
@@ -485,7 +492,7 @@ def pa_decode_step(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_t
 def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping,
                        block_tables, context_lens, max_context_len: int, scale: float,
                        split_ctas: int = 0, workspace=None, *, window: int = 0,
-                       early_prologue: bool = False, sync: StepSync = None,
+                       early_prologue: bool = False, early_copies: bool = False, sync: StepSync = None,
                        copies: StepCopies = None) -> None:
     """Append (E4M3-encode) k_new/v_new, then decode over the E4M3 pools, in one
     attention launch; q, k_new, v_new and out share one dtype (fp16 or bf16)."""
@@ -508,7 +515,7 @@ def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
             _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), _ptr(block_tables),
             block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
             float(scale), int(window), _act_code(q.dtype), int(split_ctas), _ptr(workspace),
-            _ws_bytes(workspace, dev), _flags(early_prologue))
+            _ws_bytes(workspace, dev), _flags(early_prologue, early_copies))
     if sync is None:
         _call(load().pa_decode_step_fp8, "pa_decode_step_fp8", *args, _stream(dev))
     elif copies is None:
@@ -521,7 +528,7 @@ def pa_decode_step_fp8(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
 
 def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
                       max_context_len: int, scale: float, split_ctas: int = 0,
-                      window: int = 0, early_prologue: bool = False) -> None:
+                      window: int = 0, early_prologue: bool = False, early_copies: bool = False) -> None:
     """pa_decode with the library's static scratch instead of a workspace (allocates nothing)."""
     dev = q.device
     act = (torch.float16, torch.bfloat16)
@@ -535,7 +542,7 @@ def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
           _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
           block_tables.shape[1], _ptr(context_lens), int(max_context_len), B, Hq, Hkv, D, bs, NB,
           float(scale), int(window), nq, _act_code(q.dtype), int(split_ctas),
-          _flags(early_prologue), _stream(dev))
+          _flags(early_prologue, early_copies), _stream(dev))
 
 
 def pa_test_wait_timeout(limit_ns: int, device=None) -> None:

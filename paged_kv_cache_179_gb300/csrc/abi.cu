@@ -68,7 +68,9 @@ int check_decode_shape(const DecodeShape& s, float scale) {
   if (s.bs != 16) return PA_ERR_UNSUPPORTED;
   if (s.nq < 1 || s.nq > 1024) return PA_ERR_INVALID_ARG;
   if (s.Hq / s.Hkv > kMaxRowsPerLaunch) return PA_ERR_UNSUPPORTED;
-  if (s.flags & ~PA_DECODE_EARLY_PROLOGUE) return PA_ERR_INVALID_ARG;
+  if (s.flags & ~(PA_DECODE_EARLY_PROLOGUE | PA_DECODE_EARLY_COPIES)) return PA_ERR_INVALID_ARG;
+  if ((s.flags & PA_DECODE_EARLY_COPIES) && !(s.flags & PA_DECODE_EARLY_PROLOGUE))
+    return PA_ERR_INVALID_ARG;
   if (s.B > 65535 || s.Hkv > 65535) return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
@@ -129,6 +131,7 @@ int run_decode(DecodeShape s, void* out, const void* q, const void* k, const voi
   a.q_tokens = s.nq;
   a.q_first = 0;
   a.early = (s.flags & PA_DECODE_EARLY_PROLOGUE) ? 1 : 0;
+  a.early_copies = (s.flags & PA_DECODE_EARLY_COPIES) ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit_ns = kWaitLimitNs;
   a.k_pool_w = ap.k_pool;

@@ -975,7 +975,9 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   // ---- 2. the previous kernel on the stream.  With an early prologue this
   // launch may have started before it finished: the prologue above and the
   // block-table reads below touch only what that kernel does not write
-  // (context_lens, block_tables); everything else waits for it here.
+  // (context_lens, block_tables); everything else waits for it here, except,
+  // with early copies, the first K/V tiles of blocks before a sequence's last
+  // two (which that kernel leaves alone, by the flag's contract).
   // Then sequences with nothing to attend get a zero output (one warp each).
   auto after_previous_kernel = [&]() {
     if (a.early) griddep_wait();
@@ -1038,6 +1040,62 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       prefetch_l2(static_cast<const uint8_t*>(a.v_cache) + tile * TL::BYTES, TL::BYTES);
     }
   }
+  const uint8_t* kbase = static_cast<const uint8_t*>(a.k_cache);
+  const uint8_t* vbase = static_cast<const uint8_t*>(a.v_cache);
+  const uint64_t pol = l2_policy_evict_first();
+  bool dead = false;            // a wait timed out: stop touching the pipeline
+  int issued = 0, computed = 0;
+  int ic = 0, it = 0;           // fetch cursor: chunk k+ic (ic in {0,1}), block it
+
+  // Keeps STAGES copies in flight.  pre: before the wait for the previous
+  // kernel (PA_DECODE_EARLY_COPIES), which may still write each sequence's
+  // last two blocks: stop at the first block that is one of them.
+  auto top_up = [&](bool pre) {
+    while (!dead && issued - computed < STAGES) {
+      const Chunk& x = ic == 0 ? ch0 : ch1;
+      if (x.nb == 0) return;
+      if (it >= x.nb) {
+        if (ic == 1) return;    // never more than one chunk ahead
+        ic = 1;
+        it = 0;
+        continue;
+      }
+      if (pre) {
+        const int Ls = len[x.b];
+        const int blk = (GENERAL ? window_first_block(Ls, a.window, a.n_q) : 0) + x.cb0 + it;
+        if (blk + 2 >= (Ls + 15) / 16) return;
+      }
+      const int id = __shfl_sync(0xffffffffu, ic == 0 ? id0 : id1, it);
+      const int s = issued % STAGES;
+      const uint32_t bar = sbar + 8 * s;
+      if (lane == 0) {
+        if (id >= 0 && id < a.num_blocks) {
+          const int64_t tile = static_cast<int64_t>(id) * Hkv + x.h;
+          mbar_arrive_expect_tx(bar, 2 * TL::BYTES);
+          if constexpr (TL::SWZ) {
+            // boxes of 64 elements x 16 rows: D / 64 per tile
+            const uint32_t kd = ring + s * TL::SLOT, vd = kd + TL::BYTES;
+            const int ti = static_cast<int>(tile);
+#pragma unroll
+            for (int hb = 0; hb < D / 64; ++hb) {
+              tensor3_g2s(kd + hb * 2048, &a.tm_k, 64 * hb, 0, ti, bar, pol);
+              tensor3_g2s(vd + hb * 2048, &a.tm_v, 64 * hb, 0, ti, bar, pol);
+            }
+          } else {
+            bulk_g2s(ring + s * TL::SLOT, kbase + tile * TL::BYTES, TL::BYTES, bar, pol);
+            bulk_g2s(ring + s * TL::SLOT + TL::BYTES, vbase + tile * TL::BYTES, TL::BYTES, bar,
+                     pol);
+          }
+        } else {
+          atomicOr(a.status, kStatusBadBlock);
+          mbar_arrive(bar);
+        }
+      }
+      ++issued;
+      ++it;
+    }
+  };
+  if (a.early && a.early_copies) top_up(true);
   after_previous_kernel();
   float ks0 = 1.f, vs0 = 1.f, ks1 = 1.f, vs1 = 1.f;   // E4M3 page scales of chunks k, k+1
   if constexpr (FP8) {
@@ -1080,55 +1138,8 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     }
   };
   prefetch_next_query(ch0.b, ch0.h);
+  top_up(false);
 
-  const uint8_t* kbase = static_cast<const uint8_t*>(a.k_cache);
-  const uint8_t* vbase = static_cast<const uint8_t*>(a.v_cache);
-  const uint64_t pol = l2_policy_evict_first();
-  bool dead = false;            // a wait timed out: stop touching the pipeline
-  int issued = 0, computed = 0;
-  int ic = 0, it = 0;           // fetch cursor: chunk k+ic (ic in {0,1}), block it
-
-  auto top_up = [&]() {
-    while (!dead && issued - computed < STAGES) {
-      const Chunk& x = ic == 0 ? ch0 : ch1;
-      if (x.nb == 0) return;
-      if (it >= x.nb) {
-        if (ic == 1) return;    // never more than one chunk ahead
-        ic = 1;
-        it = 0;
-        continue;
-      }
-      const int id = __shfl_sync(0xffffffffu, ic == 0 ? id0 : id1, it);
-      const int s = issued % STAGES;
-      const uint32_t bar = sbar + 8 * s;
-      if (lane == 0) {
-        if (id >= 0 && id < a.num_blocks) {
-          const int64_t tile = static_cast<int64_t>(id) * Hkv + x.h;
-          mbar_arrive_expect_tx(bar, 2 * TL::BYTES);
-          if constexpr (TL::SWZ) {
-            // boxes of 64 elements x 16 rows: D / 64 per tile
-            const uint32_t kd = ring + s * TL::SLOT, vd = kd + TL::BYTES;
-            const int ti = static_cast<int>(tile);
-#pragma unroll
-            for (int hb = 0; hb < D / 64; ++hb) {
-              tensor3_g2s(kd + hb * 2048, &a.tm_k, 64 * hb, 0, ti, bar, pol);
-              tensor3_g2s(vd + hb * 2048, &a.tm_v, 64 * hb, 0, ti, bar, pol);
-            }
-          } else {
-            bulk_g2s(ring + s * TL::SLOT, kbase + tile * TL::BYTES, TL::BYTES, bar, pol);
-            bulk_g2s(ring + s * TL::SLOT + TL::BYTES, vbase + tile * TL::BYTES, TL::BYTES, bar,
-                     pol);
-          }
-        } else {
-          atomicOr(a.status, kStatusBadBlock);
-          mbar_arrive(bar);
-        }
-      }
-      ++issued;
-      ++it;
-    }
-  };
-  top_up();
   PA_TRACE_WARP(gw, 0, t_entry);
   PA_TRACE_ONLY(int tr_pieces = 0; int tr_split = 0);
 
@@ -1237,7 +1248,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       }
       __syncwarp();
       ++computed;
-      top_up();
+      top_up(false);
     }
 
     // ---- does this chunk end its piece?  Then the warp's result is final.
@@ -1313,7 +1324,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       }
       prefetch_next_query(ch0.b, ch0.h);
     }
-    top_up();
+    top_up(false);
   }
   PA_TRACE_WARP(gw, 2, pa_now());
 

@@ -75,7 +75,9 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
     return PA_ERR_INVALID_ARG;
   if (num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 || split_ctas < 0 ||
-      window_size < 0 || queries_per_seq < 1 || (flags & ~PA_DECODE_EARLY_PROLOGUE) != 0)
+      window_size < 0 || queries_per_seq < 1 ||
+      (flags & ~(PA_DECODE_EARLY_PROLOGUE | PA_DECODE_EARLY_COPIES)) != 0 ||
+      ((flags & PA_DECODE_EARLY_COPIES) && !(flags & PA_DECODE_EARLY_PROLOGUE)))
     return PA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(max_context_len) >
       static_cast<int64_t>(max_blocks_per_seq) * block_size)
@@ -116,6 +118,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   a.q_first = 0;
   a.rows = 8;
   a.early = (flags & PA_DECODE_EARLY_PROLOGUE) ? 1 : 0;
+  a.early_copies = (flags & PA_DECODE_EARLY_COPIES) ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit_ns = kWaitLimitNs;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);

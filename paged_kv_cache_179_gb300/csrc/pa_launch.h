@@ -64,6 +64,7 @@ struct DecodeArgs {
   int q_tokens;                 // query tokens per sequence in q and out
   int q_first;                  // the first of them this launch serves
   int early;                    // programmatic dependent launch: prologue before griddepcontrol.wait
+  int early_copies;             // with early: first K/V copies (not of the last two blocks) before it
   float scale_log2;             // softmax scale * log2(e)
   uint64_t wait_limit_ns;       // time limit of every wait (kWaitLimitNs unless a test shortens it)
   // device-side ordering against copies on other streams (null: none).  The

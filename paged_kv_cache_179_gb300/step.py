@@ -24,7 +24,7 @@ class DecodeStep:
 
     def __init__(self, *, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
                  num_q_heads, k_scale=None, v_scale=None, split_ctas=0, window=0,
-                 early_prologue=False, queries_per_seq=1, workspace=None):
+                 early_prologue=False, queries_per_seq=1, workspace=None, early_copies=False):
         self.kv = "fp8" if k_cache.dtype == torch.uint8 else "16"
         self.k_cache, self.v_cache = k_cache, v_cache
         self.k_scale, self.v_scale = k_scale, v_scale
@@ -44,6 +44,11 @@ class DecodeStep:
         # the attention launch's prologue may overlap the kernel before it on
         # the stream (which must then not write context_lens or block_tables)
         self.early_prologue = bool(early_prologue)
+        # PA_DECODE_EARLY_COPIES: the kernels before each call write the pools
+        # only in each sequence's last two blocks (the previous step's append)
+        self.early_copies = bool(early_copies)
+        if self.early_copies and not self.early_prologue:
+            raise ValueError("early_copies needs early_prologue")
         # The split-K workspace: zero-filled, left zero-filled by every call.
         # Steps that run one after another on one stream (the slots of a
         # StepPipeline) may share one (``workspace``: a uint8 device tensor of
@@ -71,12 +76,12 @@ class DecodeStep:
             _abi.pa_decode_fp8(out, q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
                                self.block_tables, self.context_lens, self.max_context_len,
                                self.scale, self.split_ctas, self.workspace, window=self.window,
-                               early_prologue=self.early_prologue)
+                               early_prologue=self.early_prologue, early_copies=self.early_copies)
         else:
             _abi.pa_decode(out, q, self.k_cache, self.v_cache, self.block_tables,
                            self.context_lens, self.max_context_len, self.scale,
                            self.split_ctas, self.workspace, window=self.window,
-                           early_prologue=self.early_prologue)
+                           early_prologue=self.early_prologue, early_copies=self.early_copies)
 
     def fused(self, q, k_new, v_new, slot_mapping, out, sync=None, copies=None):
         """Append and decode in one launch (slot_mapping must hold each
@@ -88,13 +93,15 @@ class DecodeStep:
                                     self.k_scale, self.v_scale, slot_mapping, self.block_tables,
                                     self.context_lens, self.max_context_len, self.scale,
                                     self.split_ctas, self.workspace, window=self.window,
-                                    early_prologue=self.early_prologue, sync=sync,
+                                    early_prologue=self.early_prologue,
+                                    early_copies=self.early_copies, sync=sync,
                                     copies=copies)
         else:
             _abi.pa_decode_step(out, q, k_new, v_new, self.k_cache, self.v_cache, slot_mapping,
                                 self.block_tables, self.context_lens, self.max_context_len,
                                 self.scale, self.split_ctas, self.workspace, window=self.window,
-                                early_prologue=self.early_prologue, sync=sync, copies=copies)
+                                early_prologue=self.early_prologue,
+                                early_copies=self.early_copies, sync=sync, copies=copies)
         return out
 
     @property

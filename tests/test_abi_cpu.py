@@ -153,3 +153,14 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises(ValueError):
         _abi.pa_decode(t, t, t, t, torch.zeros(2, 4, dtype=torch.int32),
                        torch.zeros(2, dtype=torch.int32), 64, 0.125, 64)
+
+
+def test_early_copies_need_the_early_prologue():
+    """PA_DECODE_EARLY_COPIES only together with PA_DECODE_EARLY_PROLOGUE: the
+    binding refuses it alone (the library returns PA_ERR_INVALID_ARG)."""
+    from paged_kv_cache_179_gb300 import _abi
+    assert _abi._flags(True, True) == _abi.PA_DECODE_EARLY_PROLOGUE | _abi.PA_DECODE_EARLY_COPIES
+    assert _abi._flags(True) == _abi.PA_DECODE_EARLY_PROLOGUE
+    assert _abi._flags(False) == 0
+    with pytest.raises(ValueError):
+        _abi._flags(False, True)

@@ -1,8 +1,12 @@
 """PA_DECODE_EARLY_PROLOGUE: the attention launch is a programmatic dependent
 launch whose prologue may overlap the kernel before it on the stream.  That
 kernel here writes what the decode reads after its wait (the appended rows
-of the pools, q), so a read made too early would show.  Results must equal
-those of the plain launch bit for bit, step after step."""
+of the pools, q), so a read made too early would show.  With
+PA_DECODE_EARLY_COPIES as well, the first K/V copies of blocks before each
+sequence's last two start before the wait; the kernels before write the
+pools only in the last block (the appends, E4M3 page re-scales included),
+as the flag requires.  Results must equal those of the plain launch bit for
+bit, step after step."""
 import numpy as np
 import pytest
 import torch
@@ -17,10 +21,16 @@ from _helpers import TOL, max_err, to_cuda, to_np16
 pytestmark = pytest.mark.gpu
 
 
-def _steps(w, kc, vc, early, **kw):
+# (early_prologue, early_copies)
+MODES = {"plain": (False, False), "prologue": (True, False), "copies": (True, True)}
+
+
+def _steps(w, kc, vc, mode, **kw):
+    early, copies = MODES[mode]
     return DecodeStep(k_cache=kc, v_cache=vc, block_tables=w.block_tables,
                       context_lens=w.context_lens, max_context_len=w.max_context_len,
-                      scale=w.scale, num_q_heads=w.Hq, early_prologue=early, **kw)
+                      scale=w.scale, num_q_heads=w.Hq, early_prologue=early,
+                      early_copies=copies, **kw)
 
 
 @pytest.mark.parametrize("config,window", [("qwen2_5_1_5b", 0), ("smollm2_360m", 0),
@@ -33,9 +43,9 @@ def test_early_prologue_matches_plain_launch(config, window):
     kns = [torch.randn(w.k_new.shape, generator=g, device="cuda").to(w.q.dtype) for _ in range(n)]
     vns = [torch.randn(w.k_new.shape, generator=g, device="cuda").to(w.q.dtype) for _ in range(n)]
     outs = {}
-    for early in (False, True):
+    for mode in MODES:
         kc, vc = w.k_cache.clone(), w.v_cache.clone()
-        st = _steps(w, kc, vc, early, window=window)
+        st = _steps(w, kc, vc, mode, window=window)
         q_buf = torch.empty_like(w.q)
         got = []
         for i in range(n):
@@ -50,12 +60,14 @@ def test_early_prologue_matches_plain_launch(config, window):
             got += [o1, o2]
         torch.cuda.synchronize()
         assert _abi.pa_get_status() == (0, 0)
-        outs[early] = ([o.clone() for o in got], kc.clone(), vc.clone())
-    plain, early = outs[False], outs[True]
-    for a, b in zip(plain[0], early[0]):
-        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
-    assert torch.equal(plain[1].view(torch.int16), early[1].view(torch.int16))
-    assert torch.equal(plain[2].view(torch.int16), early[2].view(torch.int16))
+        outs[mode] = ([o.clone() for o in got], kc.clone(), vc.clone())
+    plain = outs["plain"]
+    for mode in ("prologue", "copies"):
+        early = outs[mode]
+        for a, b in zip(plain[0], early[0]):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), mode
+        assert torch.equal(plain[1].view(torch.int16), early[1].view(torch.int16)), mode
+        assert torch.equal(plain[2].view(torch.int16), early[2].view(torch.int16)), mode
     # and the last fused step against the oracle
     kp, vp = to_np16(plain[1]), to_np16(plain[2])
     ref = oracle.decode(to_np16(qs[0]), kp, vp, w.block_tables.cpu().numpy(),
@@ -72,15 +84,26 @@ def test_early_prologue_fp8_and_noalloc():
     vs = torch.empty_like(ks)
     _abi.pa_quantize_fp8(w.k_cache, w.v_cache, kc, vc, ks, vs)
     res = {}
-    for early in (False, True):
+    g = torch.Generator(device="cuda").manual_seed(6)
+    # new rows of growing size: later appends re-scale their (last) page
+    news = [(torch.randn(w.k_new.shape, generator=g, device="cuda") * 4 ** i).to(w.q.dtype)
+            for i in range(3)]
+    for mode in MODES:
+        early, copies = MODES[mode]
         kc2, vc2, ks2, vs2 = kc.clone(), vc.clone(), ks.clone(), vs.clone()
-        st = _steps(w, kc2, vc2, early, k_scale=ks2, v_scale=vs2)
-        o1, o2 = torch.empty_like(w.q), torch.empty_like(w.q)
-        st(w.q, w.k_new, w.v_new, w.slot_mapping, o1)          # append_fp8, then decode
+        st = _steps(w, kc2, vc2, mode, k_scale=ks2, v_scale=vs2)
+        got = []
+        for kn in news:
+            o1 = torch.empty_like(w.q)
+            st(w.q, kn, kn.flip(-1), w.slot_mapping, o1)       # append (E4M3), then decode
+            got.append(o1)
+        o2 = torch.empty_like(w.q)
         _abi.pa_decode_noalloc(o2, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
-                               w.max_context_len, w.scale, 0, early_prologue=early)
+                               w.max_context_len, w.scale, 0, early_prologue=early,
+                               early_copies=copies)
         torch.cuda.synchronize()
         assert _abi.pa_get_status() == (0, 0)
-        res[early] = (o1, o2, kc2, ks2)
-    for a, b in zip(res[False], res[True]):
-        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+        res[mode] = (*got, o2, kc2, ks2, vc2, vs2)
+    for mode in ("prologue", "copies"):
+        for a, b in zip(res["plain"], res[mode]):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), mode
